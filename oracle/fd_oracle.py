@@ -1,0 +1,271 @@
+"""Plain, slow, unfused CPU oracle for the SwiGLU-prologue W4A16 GEMV and fused
+residual-add + RMSNorm.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline legs of ``bench.py``, never by the product path. It shares no code,
+constants or helpers with the CUDA library; it reads the same input bytes.
+
+Every floating-point step is done in float64 unless a page fixes a narrower
+precision (the residual add is fp32-then-bf16, as the pages' kernel does). Each
+function cites the passage it follows, by page title and section:
+
+* [FIX]   "PyTorch Community Proposes Fusion Fix as Large Intermediate Buffers May Slow
+          Single-Token Decoding in Quantized LLMs" - "Reproduction and analysis",
+          "Fix proposal".
+* [SGL13] "Chapter 13 - torch.compile" (learning-sglang) - "The two halves of one tool,
+          and what each is worth".
+* [FUSE]  "09 - Operator fusion" (inference engineering, part IV) - section 5 "Technical
+          explanation": "The taxonomy of fusions", "The fusion boundary problem".
+* [KFM]   "Kernel Fusion, torch.compile and CUDA Graphs, Measured" - "Step 1: why
+          elementwise kernels are memory-bound", "Step 2: fusing them by hand in
+          Triton", "Step 3: what torch.compile generates".
+
+Where the pages are silent the plainest reading is taken (symmetric two's-complement
+int4, eight nibbles per 32-bit word along K, nibble j of word p holding k = 8p + j,
+bf16 scales [N, K/group] with w = q * s). Every function here is pinned by
+``tests/test_oracle_pins.py`` to something other than itself; none is "parity
+unpinned".
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "bf16_to_f32",
+    "f32_to_bf16_rne",
+    "silu",
+    "swiglu_activation",
+    "unpack_int4",
+    "dequant_w4",
+    "swiglu_w4a16_gemv",
+    "add_rmsnorm",
+    "decode_mlp_step",
+    "unfused_product_bytes",
+    "eager_add_rmsnorm_kernels",
+    "eager_add_rmsnorm_bytes_per_elem",
+    "eager_swiglu_bytes_per_elem",
+    "fused_swiglu_bytes_per_elem",
+]
+
+
+# --------------------------------------------------------------------------------------
+# bfloat16 <-> float32 (bit level)
+# --------------------------------------------------------------------------------------
+
+def bf16_to_f32(bits) -> np.ndarray:
+    """Widen bf16 bit patterns (uint16) to float32. Exact: a bf16 value is the top
+    half of the float32 with the same value."""
+    b = np.asarray(bits).astype(np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def f32_to_bf16_rne(x) -> np.ndarray:
+    """Round float32 values to bf16 (round to nearest, ties to even), returned as
+    uint16 bit patterns. NaN stays NaN (quiet bit set); +-inf stays inf.
+
+    [KFM] Step 2: every bf16 value the pages' kernel stores is a float32 rounded to
+    bf16 (`.to(tl.bfloat16)`), which rounds to nearest-even.
+    """
+    f = np.asarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    upper = u >> np.uint64(16)
+    lower = u & np.uint64(0xFFFF)
+    half = np.uint64(0x8000)
+    round_up = (lower > half) | ((lower == half) & ((upper & np.uint64(1)) == np.uint64(1)))
+    out = upper + round_up.astype(np.uint64)
+    is_nan = np.isnan(f)
+    out = np.where(is_nan, upper | np.uint64(0x0040), out)
+    return out.astype(np.uint16)
+
+
+# --------------------------------------------------------------------------------------
+# SwiGLU prologue
+# --------------------------------------------------------------------------------------
+
+def silu(x) -> np.ndarray:
+    """silu(x) = x * sigmoid(x) = x / (1 + exp(-x)), in float64.
+
+    [KFM] Step 1: SwiGLU's activation "computes g / (1 + exp(-g)) * u".
+    """
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def swiglu_activation(gate_bits, up_bits) -> np.ndarray:
+    """a = silu(g) * u in float64 from bf16 gate and up (uint16 bits), unrounded.
+
+    [KFM] Step 1 (silu(g) * u); [FUSE] "The fusion boundary problem" (act = silu(gate) *
+    up feeding the down projection). The fused kernel never stores `a`; the oracle keeps
+    it in float64.
+    """
+    g = bf16_to_f32(gate_bits).astype(np.float64)
+    u = bf16_to_f32(up_bits).astype(np.float64)
+    return silu(g) * u
+
+
+# --------------------------------------------------------------------------------------
+# int4 weights
+# --------------------------------------------------------------------------------------
+
+def unpack_int4(qweight) -> np.ndarray:
+    """Unpack int32 words [N, K/8] into int8 q [N, K] with q in [-8, 7].
+
+    Nibble j (bits 4j..4j+3) of word p in row n is q[n, 8p + j], a 4-bit two's
+    complement integer. [FUSE] taxonomy item 4 ("GEMM prologue fusion": the INT4 form is
+    what crosses HBM); the bit layout is this library's reading, the pages give none.
+    """
+    w = np.ascontiguousarray(qweight).view(np.uint32)
+    n_rows, n_words = w.shape
+    q = np.empty((n_rows, n_words * 8), dtype=np.int8)
+    for j in range(8):
+        nib = ((w >> np.uint32(4 * j)) & np.uint32(0xF)).astype(np.int16)
+        nib = np.where(nib >= 8, nib - 16, nib)
+        q[:, j::8] = nib.astype(np.int8)
+    return q
+
+
+def dequant_w4(qweight, scale_bits, group: int) -> np.ndarray:
+    """Dequantised weights W[n, k] = q[n, k] * s[n, k // group] as float32 [N, K].
+
+    [FUSE] taxonomy item 4 (dequantize weights -> matmul). The product of a 4-bit integer
+    and a bf16 scale has at most 12 significant bits, so the float32 result is exact; it
+    is computed in float64 and then narrowed.
+    """
+    q = unpack_int4(qweight).astype(np.float64)
+    s = bf16_to_f32(scale_bits).astype(np.float64)
+    n_rows, k = q.shape
+    if k % group != 0 or s.shape != (n_rows, k // group):
+        raise ValueError("scales must be [N, K/group]")
+    w = q * np.repeat(s, group, axis=1)
+    return w.astype(np.float32)
+
+
+def swiglu_w4a16_gemv(gate_bits, up_bits, qweight, scale_bits, group: int) -> np.ndarray:
+    """y[m, n] = sum_k a[m, k] * W[n, k] with a = silu(g) * u, as float64 [M, N].
+
+    Unfused on purpose: the activation, the dequantised weight matrix and the product
+    are each formed in full before the next step. [FIX] "Reproduction and analysis"
+    (single-row matmul y = x @ W with a SwiGLU pre-operation and int4 weights);
+    [FUSE] "The fusion boundary problem" (out = act @ W_down). The contraction uses a
+    float64 library matmul.
+    """
+    a = swiglu_activation(gate_bits, up_bits)
+    if a.ndim == 1:
+        a = a[None, :]
+    w = dequant_w4(qweight, scale_bits, group).astype(np.float64)
+    if a.shape[1] != w.shape[1]:
+        raise ValueError("gate/up K does not match the weights")
+    return a @ w.T
+
+
+# --------------------------------------------------------------------------------------
+# Residual add + RMSNorm
+# --------------------------------------------------------------------------------------
+
+def add_rmsnorm(x_bits, residual_bits, weight_bits, eps: float):
+    """Residual add followed by RMSNorm over the last axis.
+
+    Follows the order of [KFM] Step 2's hand-written kernel:
+      h = bf16(f32(x) + f32(r))              (float32 add, rounded to bf16; stored)
+      rstd = 1 / sqrt(mean_j f32(h_j)^2 + eps)   (here in float64)
+      y = h * rstd * w
+
+    Returns ``(h_bits, y_ref, y_eager_bits)``:
+      * ``h_bits``      uint16, the new residual (bit-exact target);
+      * ``y_ref``       float64, h * rstd * w with no rounding;
+      * ``y_eager_bits`` uint16, bf16(bf16(h * rstd) * w), the page's two roundings
+                        (normalised value rounded to bf16, then scaled by w).
+    The mean divides by the row length ([KFM] Step 3 divides by 4096.0 for hidden 4096).
+    """
+    x = bf16_to_f32(x_bits)
+    r = bf16_to_f32(residual_bits)
+    h_bits = f32_to_bf16_rne(x + r)  # numpy float32 + float32 -> float32 (IEEE RNE)
+    h = bf16_to_f32(h_bits).astype(np.float64)
+    w = bf16_to_f32(weight_bits).astype(np.float64)
+    ms = np.mean(h * h, axis=-1, keepdims=True)
+    rstd = 1.0 / np.sqrt(ms + float(eps))
+    normed = h * rstd
+    y_ref = normed * w
+    t_bits = f32_to_bf16_rne(normed.astype(np.float32))
+    prod = bf16_to_f32(t_bits).astype(np.float64) * w  # exact: 8-bit x 8-bit significands
+    y_eager_bits = f32_to_bf16_rne(prod.astype(np.float32))
+    return h_bits, y_ref, y_eager_bits
+
+
+# --------------------------------------------------------------------------------------
+# The decode MLP step (add-RMSNorm, then the SwiGLU-prologue down projection)
+# --------------------------------------------------------------------------------------
+
+def decode_mlp_step(x_bits, residual_bits, layers, eps: float, group: int):
+    """Run L layers of: (normed, residual) = add_rmsnorm(x, residual); y = down(g, u);
+    x_next = bf16(y).
+
+    ``layers`` is a sequence of dicts with keys ``rms_weight``, ``gate``, ``up``,
+    ``qweight``, ``scales`` (bf16 bits / int32 words). [FUSE] "The fusion boundary
+    problem": kernel 1 is add_rmsnorm(residual, attn_out) -> (x, h) with two outputs and
+    the down projection's output joins the residual stream at the next add. The gate/up
+    projection between them is not part of this path, so each layer's g and u are given
+    inputs. The value handed to the next layer is the bf16-rounded GEMV output, as the
+    bf16 layer output of a model would be.
+
+    Returns per-layer lists of (h_bits, y_norm_ref, y_norm_eager_bits, y_gemv_ref) and
+    the final (x_bits, residual_bits).
+    """
+    x = np.asarray(x_bits, dtype=np.uint16)
+    res = np.asarray(residual_bits, dtype=np.uint16)
+    record = []
+    for layer in layers:
+        h_bits, y_norm, y_norm_eager = add_rmsnorm(x, res, layer["rms_weight"], eps)
+        y = swiglu_w4a16_gemv(layer["gate"], layer["up"], layer["qweight"], layer["scales"], group)
+        record.append((h_bits, y_norm, y_norm_eager, y))
+        res = h_bits
+        x = f32_to_bf16_rne(y.astype(np.float32)).reshape(x.shape)
+    return record, x, res
+
+
+# --------------------------------------------------------------------------------------
+# Byte models of the unfused forms the fused kernels replace
+# --------------------------------------------------------------------------------------
+
+def unfused_product_bytes(m: int, k: int, n: int, elem_bytes: int = 4) -> int:
+    """Size of the (M, K, N) broadcast product an M=1 matmul decomposed into a
+    multiply and a sum materialises. [FIX] "Reproduction and analysis": K=9216, N=2560
+    writes and reads back about 94 MB."""
+    return m * k * n * elem_bytes
+
+
+def eager_add_rmsnorm_kernels():
+    """The eager residual add + Qwen2-style RMSNorm chain, one entry per kernel:
+    (name, bytes read per element, bytes written per element). [KFM] "Why it matters"
+    and Step 1 (9 kernels, 42 bytes per element on bf16; the page's per-element table
+    did not survive, so the split is reconstructed from the listed operations: add,
+    cast to fp32, square, mean, add eps, rsqrt, multiply, cast to bf16, multiply by w;
+    the eps add and rsqrt touch one value per row and the mean writes one per row)."""
+    return [
+        ("add", 4, 2),
+        ("to_fp32", 2, 4),
+        ("pow", 4, 4),
+        ("mean", 4, 0),
+        ("add_eps", 0, 0),
+        ("rsqrt", 0, 0),
+        ("mul_rstd", 4, 4),
+        ("to_bf16", 4, 2),
+        ("mul_weight", 2, 2),
+    ]
+
+
+def eager_add_rmsnorm_bytes_per_elem() -> int:
+    return sum(r + w for _, r, w in eager_add_rmsnorm_kernels())
+
+
+def eager_swiglu_bytes_per_elem() -> int:
+    """silu then multiply as two bf16 kernels: read g, write s; read s and u, write a.
+    [KFM] Step 1: 10 bytes per element."""
+    return (2 + 2) + (2 + 2 + 2)
+
+
+def fused_swiglu_bytes_per_elem() -> int:
+    """One kernel: read g and u, write a. [KFM] Step 1: 6 bytes per element."""
+    return 2 + 2 + 2

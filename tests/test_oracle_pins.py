@@ -1,0 +1,367 @@
+"""Pins for the CPU oracle: each check ties an oracle function to something other than
+itself - closed forms, identities, exhaustive tables, library routines on special
+cases, brute force on tiny inputs, and the figures the source pages print
+(tests/golden/page_figures.json). A plausible slip (dropped term, wrong sign, swapped
+index, transposed operand, wrong nibble order or group index) fails at least one."""
+
+import json
+import math
+from pathlib import Path
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from memory_bound_decode_fd_gb300 import inputs, pack_int4
+
+GOLDEN = json.loads((Path(__file__).parent / "golden" / "page_figures.json").read_text())
+
+
+def bits_to_torch_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+# ------------------------------------------------------------------------------ bf16
+
+def test_bf16_rne_matches_torch_on_random_and_ties():
+    rng = np.random.default_rng(123)
+    x = np.concatenate([
+        rng.normal(0, 1, 200_000).astype(np.float32),
+        (rng.normal(0, 1, 200_000) * 1e30).astype(np.float32),
+        (rng.normal(0, 1, 200_000) * 1e-35).astype(np.float32),  # subnormal region
+        rng.integers(0, 2**32, 400_000, dtype=np.uint32).view(np.float32),
+    ])
+    # exact ties: low half == 0x8000 with both parities of the kept LSB
+    ties = (rng.integers(0, 2**16, 1000, dtype=np.uint32) << 16 | 0x8000).view(np.float32)
+    x = np.concatenate([x, ties, np.array([0.0, -0.0, np.inf, -np.inf, 3.3895314e38], np.float32)])
+    finite = ~np.isnan(x)
+    ours = oracle.f32_to_bf16_rne(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours[finite], ref[finite])
+    # NaN stays NaN
+    nan_bits = oracle.f32_to_bf16_rne(np.array([np.nan], np.float32))
+    assert np.isnan(oracle.bf16_to_f32(nan_bits))[0]
+
+
+def test_bf16_widen_is_exact():
+    bits = np.arange(0, 2**16, dtype=np.uint32).astype(np.uint16)
+    f = oracle.bf16_to_f32(bits)
+    ref = bits_to_torch_bf16(bits).float().numpy()
+    same = (f.view(np.uint32) == ref.view(np.uint32)) | (np.isnan(f) & np.isnan(ref))
+    assert same.all()
+
+
+# ------------------------------------------------------------------------------ silu
+
+def test_silu_closed_forms():
+    ln3 = math.log(3.0)
+    # sigmoid(ln 3) = 3/4, sigmoid(-ln 3) = 1/4, sigmoid(0) = 1/2
+    got = oracle.silu(np.array([ln3, -ln3, 0.0, 2 * math.log(2.0)]))
+    want = np.array([0.75 * ln3, -0.25 * ln3, 0.0, 0.8 * 2 * math.log(2.0)])
+    np.testing.assert_allclose(got, want, rtol=1e-15, atol=0)
+    assert oracle.silu(np.array([0.0]))[0] == 0.0
+
+
+def test_silu_odd_part_and_tails():
+    x = np.linspace(-30, 30, 20001)
+    # silu(x) - silu(-x) = x * (sigmoid(x) + sigmoid(-x)) = x
+    np.testing.assert_allclose(oracle.silu(x) - oracle.silu(-x), x, rtol=1e-13, atol=1e-13)
+    assert oracle.silu(np.array([50.0]))[0] == 50.0
+    assert abs(oracle.silu(np.array([-50.0]))[0]) < 1e-19
+    assert oracle.silu(np.array([-1e4]))[0] == 0.0  # exp overflow -> -0.0, not NaN
+
+
+def test_swiglu_activation_is_silu_gate_times_up():
+    g = inputs.to_bf16_bits(np.array([[0.0, math.log(3.0), -2.5, 1.0]]))
+    u = inputs.to_bf16_bits(np.array([[7.0, 2.0, -4.0, 0.0]]))
+    a = oracle.swiglu_activation(g, u)
+    gf = oracle.bf16_to_f32(g).astype(np.float64)
+    assert a[0, 0] == 0.0 and a[0, 3] == 0.0
+    np.testing.assert_allclose(a[0, 1], 2.0 * gf[0, 1] * 0.75, rtol=1e-2)  # ln3 rounded to bf16
+    np.testing.assert_allclose(a[0, 2], -4.0 * -2.5 / (1 + math.exp(2.5)), rtol=1e-15)
+
+
+# ------------------------------------------------------------------------------ int4
+
+def test_unpack_nibble_order_and_sign():
+    w = np.array([[0x76543210, 0x89ABCDEF - 2**32, 0x0000000F, 0x80000000 - 2**32]], np.int64).astype(np.int32)
+    q = oracle.unpack_int4(w)
+    assert q[0, 0:8].tolist() == [0, 1, 2, 3, 4, 5, 6, 7]
+    assert q[0, 8:16].tolist() == [-1, -2, -3, -4, -5, -6, -7, -8]
+    assert q[0, 16:24].tolist() == [-1, 0, 0, 0, 0, 0, 0, 0]
+    assert q[0, 24:32].tolist() == [0, 0, 0, 0, 0, 0, 0, -8]
+
+
+def test_unpack_exhaustive_table():
+    # Every nibble value at every position: two's complement table.
+    table = [v if v < 8 else v - 16 for v in range(16)]
+    words = []
+    for j in range(8):
+        for v in range(16):
+            words.append((v << (4 * j)) & 0xFFFFFFFF)
+    w = np.array(words, dtype=np.uint32).view(np.int32).reshape(-1, 1)
+    q = oracle.unpack_int4(w)
+    for idx, (j, v) in enumerate((j, v) for j in range(8) for v in range(16)):
+        expect = [0] * 8
+        expect[j] = table[v]
+        assert q[idx].tolist() == expect
+
+
+def test_pack_then_unpack_roundtrip():
+    rng = np.random.default_rng(5)
+    q = rng.integers(-8, 8, size=(7, 64)).astype(np.int8)
+    assert np.array_equal(oracle.unpack_int4(pack_int4(q)), q)
+
+
+def test_generator_nibbles_are_uniform_on_minus8_to_7():
+    rng = np.random.default_rng(0)
+    q = oracle.unpack_int4(inputs.int4_words(rng, 64, 4096))
+    counts = np.bincount((q.astype(np.int64) + 8).ravel(), minlength=16)
+    assert q.min() == -8 and q.max() == 7
+    expected = q.size / 16
+    assert np.all(np.abs(counts - expected) < 6 * math.sqrt(expected))
+
+
+def test_dequant_group_indexing_and_exactness():
+    N, K, group = 3, 256, 64
+    q = np.ones((N, K), np.int8)
+    q[1] = -8
+    q[2] = 7
+    s = np.array([[2.0**-i for i in range(4)], [0.5, 0.25, 0.125, 0.0625], [0.01, 0.02, 0.005, 0.015]])
+    sb = inputs.to_bf16_bits(s)
+    w = oracle.dequant_w4(pack_int4(q), sb, group)
+    sf = oracle.bf16_to_f32(sb)
+    for n in range(N):
+        for k in (0, 63, 64, 127, 128, 191, 192, 255):
+            assert w[n, k] == np.float32(q[n, k]) * sf[n, k // group]
+    assert w.dtype == np.float32
+
+
+# ------------------------------------------------------------------------------ GEMV
+
+def _a(g, u):
+    return oracle.swiglu_activation(g, u)
+
+
+def test_gemv_one_hot_pins_indices():
+    rng = np.random.default_rng(7)
+    M, K, N, group = 3, 256, 40, 64
+    g = inputs.normal_bf16(rng, (M, K))
+    u = inputs.normal_bf16(rng, (M, K))
+    for (n_star, k_star, qv) in [(0, 0, 3), (39, 255, -8), (17, 129, 7), (5, 64, -1)]:
+        q = np.zeros((N, K), np.int8)
+        q[n_star, k_star] = qv
+        s = np.full((N, K // group), 0.5)
+        s[n_star, k_star // group] = 0.25
+        y = oracle.swiglu_w4a16_gemv(g, u, pack_int4(q), inputs.to_bf16_bits(s), group)
+        a = _a(g, u)
+        expect = np.zeros((M, N))
+        expect[:, n_star] = a[:, k_star] * qv * 0.25
+        assert np.array_equal(y, expect)
+
+
+def test_gemv_constant_weights_closed_form():
+    rng = np.random.default_rng(8)
+    M, K, N, group = 2, 512, 6, 128
+    g = inputs.normal_bf16(rng, (M, K))
+    u = inputs.normal_bf16(rng, (M, K))
+    q = np.full((N, K), -3, np.int8)
+    s = np.full((N, K // group), 0.015625)
+    y = oracle.swiglu_w4a16_gemv(g, u, pack_int4(q), inputs.to_bf16_bits(s), group)
+    a_sum = _a(g, u).sum(axis=1)
+    for n in range(N):
+        np.testing.assert_allclose(y[:, n], -3 * 0.015625 * a_sum, rtol=1e-12)
+
+
+def test_gemv_group_scales_pin_k_over_group():
+    rng = np.random.default_rng(9)
+    M, K, N, group = 1, 512, 3, 128
+    g = inputs.normal_bf16(rng, (M, K))
+    u = inputs.normal_bf16(rng, (M, K))
+    q = np.ones((N, K), np.int8)
+    s = np.array([[1.0, 2.0, 4.0, 8.0], [8.0, 4.0, 2.0, 1.0], [1.0, 0.0, 0.0, 0.0]])
+    y = oracle.swiglu_w4a16_gemv(g, u, pack_int4(q), inputs.to_bf16_bits(s), group)
+    a = _a(g, u)[0]
+    part = [a[i * group:(i + 1) * group].sum() for i in range(4)]
+    np.testing.assert_allclose(y[0, 0], part[0] + 2 * part[1] + 4 * part[2] + 8 * part[3], rtol=1e-12)
+    np.testing.assert_allclose(y[0, 1], 8 * part[0] + 4 * part[1] + 2 * part[2] + part[3], rtol=1e-12)
+    np.testing.assert_allclose(y[0, 2], part[0], rtol=1e-12)
+
+
+def test_gemv_brute_force_tiny():
+    rng = np.random.default_rng(10)
+    M, K, N, group = 2, 64, 5, 32
+    d = inputs.gemv_inputs(M, K, N, group, rng=rng)
+    y = oracle.swiglu_w4a16_gemv(d["gate"], d["up"], d["qweight"], d["scales"], group)
+    g = oracle.bf16_to_f32(d["gate"]).astype(float)
+    u = oracle.bf16_to_f32(d["up"]).astype(float)
+    s = oracle.bf16_to_f32(d["scales"]).astype(float)
+    words = d["qweight"].view(np.uint32)
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                nib = (int(words[n, k // 8]) >> (4 * (k % 8))) & 0xF
+                qk = nib - 16 if nib & 0x8 else nib
+                gk = g[m, k]
+                acc += gk / (1.0 + math.exp(-gk)) * u[m, k] * qk * s[n, k // group]
+            assert abs(acc - y[m, n]) <= 1e-12 * max(1.0, abs(acc))
+
+
+def test_gemv_rows_independent_and_linear_in_up():
+    rng = np.random.default_rng(11)
+    M, K, N, group = 4, 256, 9, 128
+    d = inputs.gemv_inputs(M, K, N, group, rng=rng)
+    y = oracle.swiglu_w4a16_gemv(d["gate"], d["up"], d["qweight"], d["scales"], group)
+    y1 = oracle.swiglu_w4a16_gemv(d["gate"][2:3], d["up"][2:3], d["qweight"], d["scales"], group)
+    np.testing.assert_allclose(y[2:3], y1, rtol=1e-13, atol=1e-13)
+    # flipping the sign of up flips y exactly (bf16 negation is exact)
+    neg_up = d["up"] ^ np.uint16(0x8000)
+    yn = oracle.swiglu_w4a16_gemv(d["gate"], neg_up, d["qweight"], d["scales"], group)
+    np.testing.assert_allclose(yn, -y, rtol=1e-13, atol=1e-13)
+    # a subset of weight rows gives the same outputs for those rows
+    ys = oracle.swiglu_w4a16_gemv(d["gate"], d["up"], d["qweight"][[1, 7]], d["scales"][[1, 7]], group)
+    np.testing.assert_allclose(ys, y[:, [1, 7]], rtol=1e-13)
+
+
+def test_gemv_matches_torch_linear_fp64():
+    d = inputs.gemv_inputs(3, 1024, 64, 128, seed=12)
+    y = oracle.swiglu_w4a16_gemv(d["gate"], d["up"], d["qweight"], d["scales"], 128)
+    g = bits_to_torch_bf16(d["gate"]).double()
+    u = bits_to_torch_bf16(d["up"]).double()
+    a = torch.nn.functional.silu(g) * u
+    w32 = torch.from_numpy(d["qweight"].astype(np.int64) & 0xFFFFFFFF)
+    shifts = torch.arange(0, 32, 4, dtype=torch.int64)
+    nib = (w32.unsqueeze(-1) >> shifts) & 0xF
+    q = torch.where(nib >= 8, nib - 16, nib).reshape(64, 1024).double()
+    s = bits_to_torch_bf16(d["scales"]).double().repeat_interleave(128, dim=1)
+    ref = torch.nn.functional.linear(a, q * s).numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-11, atol=1e-11)
+
+
+# ------------------------------------------------------------------------------ RMSNorm
+
+def test_add_rmsnorm_residual_matches_torch_bit_exact():
+    d = inputs.rmsnorm_inputs(64, 1024, seed=20)
+    h, _, _ = oracle.add_rmsnorm(d["x"], d["residual"], d["weight"], 1e-6)
+    ref = (bits_to_torch_bf16(d["x"]).float() + bits_to_torch_bf16(d["residual"]).float()).to(torch.bfloat16)
+    assert np.array_equal(h, ref.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_add_rmsnorm_matches_torch_rms_norm_fp64():
+    d = inputs.rmsnorm_inputs(32, 512, seed=21)
+    h, y, _ = oracle.add_rmsnorm(d["x"], d["residual"], d["weight"], 1e-5)
+    hd = bits_to_torch_bf16(h).double()
+    wd = bits_to_torch_bf16(d["weight"]).double()
+    ref = torch.nn.functional.rms_norm(hd, (512,), wd, eps=1e-5).numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_add_rmsnorm_unit_rms_before_weight():
+    d = inputs.rmsnorm_inputs(16, 4096, seed=22)
+    eps = 1e-6
+    ones = inputs.to_bf16_bits(np.ones(4096))
+    h, y, _ = oracle.add_rmsnorm(d["x"], d["residual"], ones, eps)
+    hf = oracle.bf16_to_f32(h).astype(float)
+    ms = np.mean(hf * hf, axis=1)
+    np.testing.assert_allclose(np.mean(y * y, axis=1), ms / (ms + eps), rtol=1e-12)
+
+
+def test_add_rmsnorm_constant_row_closed_form():
+    hidden, eps = 256, 1e-5
+    x = inputs.to_bf16_bits(np.full((2, hidden), 0.5))
+    r = inputs.to_bf16_bits(np.stack([np.full(hidden, 1.0), np.full(hidden, -2.5)]))
+    w = inputs.to_bf16_bits(np.linspace(0.5, 1.5, hidden))
+    h, y, _ = oracle.add_rmsnorm(x, r, w, eps)
+    wf = oracle.bf16_to_f32(w).astype(float)
+    for i, c in enumerate([1.5, -2.0]):
+        np.testing.assert_allclose(y[i], c / math.sqrt(c * c + eps) * wf, rtol=1e-14)
+
+
+def test_add_rmsnorm_eager_variant_matches_torch_eager_chain():
+    # The eager chain written with torch ops (fp32 variance and rsqrt; round to bf16;
+    # multiply by the bf16 weight) agrees with the oracle's two-rounding variant to one
+    # bf16 step everywhere, and exactly almost everywhere.
+    d = inputs.rmsnorm_inputs(256, 1024, seed=23)
+    eps = 1e-6
+    h, _, ye = oracle.add_rmsnorm(d["x"], d["residual"], d["weight"], eps)
+    ht = bits_to_torch_bf16(h).float()
+    var = ht.pow(2).mean(-1, keepdim=True)
+    t = (ht * torch.rsqrt(var + eps)).to(torch.bfloat16)
+    ref = (bits_to_torch_bf16(d["weight"]) * t).view(torch.int16).numpy().view(np.uint16)
+    a = oracle.bf16_to_f32(ye).astype(float)
+    b = oracle.bf16_to_f32(ref).astype(float)
+    step = np.abs(oracle.bf16_to_f32(oracle.f32_to_bf16_rne(np.abs(b) * (1 + 2.0**-7))) - np.abs(b))
+    assert np.all(np.abs(a - b) <= np.maximum(step, 1e-30) * 1.0001)
+    assert np.mean(ye == ref) > 0.99
+
+
+def test_rmsnorm_output_step_matches_page_0031():
+    # The page's "one BF16 rounding step (0.031)" is the bf16 spacing 2^-5 of values in
+    # [4, 8): the largest normalised outputs of the 8192 x 4096 workload land there.
+    d = inputs.rmsnorm_inputs(1024, 4096, seed=1)
+    _, y, _ = oracle.add_rmsnorm(d["x"], d["residual"], d["weight"], 1e-6)
+    top = np.max(np.abs(y))
+    assert 4.0 <= top < 8.0
+    assert abs(2.0 ** (math.floor(math.log2(top)) - 7) - GOLDEN["add_rmsnorm_parity"]["y_step_value"]) < 5e-4
+
+
+# ------------------------------------------------------------------------------ decode step
+
+def test_decode_step_zero_weights_pass_residual_through():
+    hidden, inter, group = 64, 128, 32
+    rng = np.random.default_rng(30)
+    x0 = inputs.normal_bf16(rng, (1, hidden))
+    r0 = inputs.normal_bf16(rng, (1, hidden))
+    layers = []
+    for _ in range(2):
+        layers.append({
+            "rms_weight": inputs.normal_bf16(rng, (hidden,), 1.0, 0.1),
+            "gate": inputs.normal_bf16(rng, (1, inter)),
+            "up": inputs.normal_bf16(rng, (1, inter)),
+            "qweight": np.zeros((hidden, inter // 8), np.int32),
+            "scales": inputs.to_bf16_bits(np.full((hidden, inter // group), 0.01)),
+        })
+    rec, x_last, res = oracle.decode_mlp_step(x0, r0, layers, 1e-5, group)
+    h1 = oracle.f32_to_bf16_rne(oracle.bf16_to_f32(x0) + oracle.bf16_to_f32(r0))
+    assert np.array_equal(rec[0][0], h1)
+    assert np.array_equal(rec[1][0], h1)  # x_1 = 0, so h_2 = h_1
+    assert np.all(rec[0][3] == 0) and np.all(oracle.bf16_to_f32(x_last) == 0)
+    assert np.array_equal(res, h1)
+
+
+# ------------------------------------------------------------------------------ page figures
+
+def test_byte_model_unfused_product_is_94mb():
+    f = GOLDEN["unfused_product"]
+    b = oracle.unfused_product_bytes(f["M"], f["K"], f["N"], f["dtype_bytes"])
+    assert b == 94_371_840
+    assert round(b / 1e6) == f["approx_MB"]
+
+
+def test_byte_model_silu_traffic_llama3():
+    f = GOLDEN["silu_traffic_llama3_8b"]
+    per = f["inter"] * f["dtype_bytes"]
+    assert round(per / 1024) == f["silu_output_KB_per_token_per_layer"]
+    assert round(2 * per / 1024) == f["saved_KB_per_token_per_layer"]
+    assert round(2 * per * f["layers"] / 1e6, 1) == f["saved_MB_per_token"]
+
+
+def test_byte_model_eager_rmsnorm_42_vs_8():
+    f = GOLDEN["add_rmsnorm_eager_vs_fused"]
+    assert len(oracle.eager_add_rmsnorm_kernels()) == f["eager_kernels"]
+    assert oracle.eager_add_rmsnorm_bytes_per_elem() == f["eager_bytes_per_elem"]
+    elems = f["rows"] * f["hidden"]
+    bw = f["mixed_rw_GBps"] * 1e9
+    assert round(elems * f["eager_bytes_per_elem"] / bw * 1e3, 1) == f["eager_ms"]
+    assert round(elems * f["fused_bytes_per_elem"] / bw * 1e3, 2) == f["fused_ms"]
+    assert round(f["eager_ms"] / f["fused_ms"], 1) == f["speedup"]
+
+
+def test_byte_model_swiglu_10_vs_6():
+    f = GOLDEN["swiglu_eager_vs_fused"]
+    assert oracle.eager_swiglu_bytes_per_elem() == f["eager_bytes_per_elem"]
+    assert oracle.fused_swiglu_bytes_per_elem() == f["fused_bytes_per_elem"]
+    assert round(f["flops_per_elem"] / oracle.fused_swiglu_bytes_per_elem(), 1) == f["flops_per_byte"]
+    assert round(100 * (1 - 6 / 10)) == f["time_cut_pct"]
