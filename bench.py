@@ -1,0 +1,557 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused decode kernels on GB300 (prints ONE JSON line on rank 0).
+
+Default workload (one "step" = one pass of the whole hot path): the 32-layer decode MLP
+step - per layer add-RMSNorm on [1, 4096] bf16 (eps 1e-5) then the SwiGLU-prologue
+W4A16 down projection K=14336 N=4096 (group 128), seeded synthetic inputs (seed 3). Its
+weights (972 MB) exceed the 129 MB L2, so no flush is needed between steps. The step
+is captured once in a CUDA graph and replayed.
+
+Reported:
+  value      achieved GB/s = algorithmic bytes per step / device time per step
+             (CUDA events around K replays on the launching stream, max over ranks)
+  e2e        the same metric through the public API with the per-token inputs in
+             pinned host memory: H2D of x, residual and every layer's gate/up, the
+             replay, D2H of x_L and the residual, all inside the timed region
+  roofline   the dominant kernel (the GEMV) - its average launch duration from CUDA
+             events bracketing each launch in a separate eager pass queued behind a
+             GPU sleep (so the events time the kernel, not the launch latency)
+  cpu_baseline  the CPU oracle, single-threaded, on a bounded sample of the workload
+  --impl reference  times the CPU oracle alone (the reference arm of this benchmark)
+
+Other workloads (--workload gemv_94mb | rmsnorm_big | gemv_small | batched_m64) time
+one call per step and rotate ceil(3 x L2 / bytes) input sets so every step reads HBM.
+"""
+
+from __future__ import annotations
+
+import os
+
+# The CPU oracle legs run single-threaded (set before numpy loads a BLAS).
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import math
+import re
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import numpy as np
+import torch
+
+REPO = Path(__file__).resolve().parent
+METRIC = "µs/call and achieved HBM GB/s (% of GB300 peak) for SwiGLU-W4A16 GEMV + add-RMSNorm"
+FALLBACK_HBM_GBS = 6800.0
+SPEC_HBM_GBS = 8000.0
+KERNEL_SOURCES = {
+    "swiglu_w4a16_gemv": ["csrc/fd_gemv_cc.cu", "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
+    "add_rmsnorm": ["csrc/fd_add_rmsnorm.cu", "csrc/fd_internal.h"],
+}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def read_peaks():
+    p = REPO / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured", d
+    return FALLBACK_HBM_GBS, "fallback", {}
+
+
+def kernel_hash(name: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[name]:
+        h.update((REPO / "memory_bound_decode_fd_gb300" / rel).read_bytes())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(name: str, tag: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this kernel
+    source (hash match); else None."""
+    p = REPO / "profiles" / "traffic.md"
+    if not p.exists():
+        return None
+    pat = re.compile(rf"^\|\s*{re.escape(name)}\s*\|\s*{re.escape(tag)}\s*\|\s*([0-9a-f]+)\s*\|\s*([0-9]+)\s*\|", re.M)
+    m = pat.search(p.read_text())
+    if not m or m.group(1) != kernel_hash(name):
+        return None
+    return int(m.group(2))
+
+
+def smi_index() -> int:
+    """nvidia-smi index of this rank's GPU (CUDA_VISIBLE_DEVICES remaps device ids)."""
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(ids) and ids[local].isdigit():
+            return int(ids[local])
+    return local
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while the GPU is loaded."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def time_region(stream, fn, iters: int) -> float:
+    """ms for `iters` calls of fn on `stream`, CUDA events, synchronized on both sides."""
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(iters):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def per_launch_times(stream, launches, sleep_cycles=50_000_000):
+    """Average device duration (ms) of each named launch: the GPU is held by a sleep
+    kernel while every (event, launch, event) triple is queued, so each event pair
+    brackets only its kernel. `launches` is a list of (name, callable)."""
+    evs = []
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(sleep_cycles)
+        for name, fn in launches:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((name, a, b))
+    torch.cuda.synchronize()
+    acc = {}
+    for name, a, b in evs:
+        acc.setdefault(name, []).append(a.elapsed_time(b))
+    return {k: (sum(v) / len(v), len(v)) for k, v in acc.items()}
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def to_dev(bits_or_words, device):
+    arr = np.ascontiguousarray(bits_or_words)
+    if arr.dtype == np.uint16:
+        return torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(arr).to(device)
+
+
+def build_decode(device, seed=3, layers=32):
+    import memory_bound_decode_fd_gb300 as fd
+    from memory_bound_decode_fd_gb300 import inputs
+    from memory_bound_decode_fd_gb300.step import DecodeStep
+
+    spec = inputs.WORKLOADS["decode_step"]
+    d = inputs.decode_step_inputs(layers=layers, hidden=spec["hidden"], inter=spec["inter"],
+                                  group=spec["group"], seed=seed)
+    dev_layers = [{"rms_weight": to_dev(L["rms_weight"], device),
+                   "qweight": to_dev(L["qweight"], device),
+                   "scales": to_dev(L["scales"], device)} for L in d["layers"]]
+    step = DecodeStep(dev_layers, spec["hidden"], spec["inter"], spec["group"], spec["eps"], device)
+    step.x.copy_(to_dev(d["x"], device))
+    step.residual.copy_(to_dev(d["residual"], device))
+    for i, L in enumerate(d["layers"]):
+        step.gate[i].copy_(to_dev(L["gate"], device))
+        step.up[i].copy_(to_dev(L["up"], device))
+    step.capture()
+    bytes_per_step = fd.decode_step_bytes(layers, spec["hidden"], spec["inter"], spec["group"])
+    return d, step, bytes_per_step
+
+
+def bench_decode(args, device, rank, world):
+    import memory_bound_decode_fd_gb300 as fd
+
+    spec = {"layers": 32, "hidden": 4096, "inter": 14336, "group": 128, "eps": 1e-5}
+    d, step, bytes_per_step = build_decode(device)
+    stream = step.stream
+    hbm_peak, peak_kind, peaks = read_peaks()
+
+    sampler = ClockSampler(smi_index())
+    sampler.start()
+    # clocks settle + warm-up (untimed)
+    settle_until = time.time() + 1.0
+    while time.time() < settle_until:
+        time_region(stream, step.replay, 200)
+    time_region(stream, step.replay, max(args.warmup, 3))
+
+    barrier(world)
+    ms = time_region(stream, step.replay, args.steps)
+    ms = max_over_ranks(ms, world)
+    clocks = sampler.stop()
+    ms_per_step = ms / args.steps
+    value_gbs = world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+    # Per-kernel durations (eager launches of the same kernels on the same stream).
+    hidden = spec["hidden"]
+    launches = []
+    for i, L in enumerate(step.layers):
+        launches.append(("add_rmsnorm", lambda L=L, i=i: fd.add_rmsnorm(
+            step.y[i - 1] if i else step.x, step.residual, L["rms_weight"], spec["eps"],
+            out=step.normed[i], residual_out=step.residual, stream=stream)))
+        launches.append(("swiglu_w4a16_gemv", lambda L=L, i=i: fd.swiglu_w4a16_gemv(
+            L["gate"], L["up"], L["qweight"], L["scales"], out=step.y[i], group=spec["group"],
+            stream=stream)))
+    kt = {}
+    for _ in range(3):
+        for k, (t, n) in per_launch_times(stream, launches).items():
+            kt.setdefault(k, []).append((t, n))
+    kernels = {}
+    for k, v in kt.items():
+        t_ms = sum(t * n for t, n in v) / sum(n for _, n in v)
+        kernels[k] = {"us": t_ms * 1e3, "launches_sampled": sum(n for _, n in v)}
+    gemv_bytes = fd.gemv_bytes(1, spec["inter"], hidden, spec["group"])
+    rms_bytes = fd.add_rmsnorm_bytes(1, hidden)
+    kernels["swiglu_w4a16_gemv"]["bytes"] = gemv_bytes
+    kernels["add_rmsnorm"]["bytes"] = rms_bytes
+    for k in kernels.values():
+        k["gbs"] = k["bytes"] / (k["us"] * 1e-6) / 1e9
+    gemv_us = kernels["swiglu_w4a16_gemv"]["us"]
+    achieved = gemv_bytes / (gemv_us * 1e-6) / 1e9
+    traffic = recorded_traffic("swiglu_w4a16_gemv", "K14336_N4096_M1")
+
+    # End to end: pinned host inputs -> device, replay, device -> pinned host.
+    pin = dict(dtype=torch.bfloat16, pin_memory=True)
+    xh = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    rh = torch.from_numpy(d["residual"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    gh = torch.from_numpy(np.stack([L["gate"] for L in d["layers"]]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    uh = torch.from_numpy(np.stack([L["up"] for L in d["layers"]]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    ox = torch.empty((1, hidden), **pin)
+    orr = torch.empty((1, hidden), **pin)
+    e2e_call = lambda: step(xh, rh, gh, uh, ox, orr)  # noqa: E731
+    time_region(stream, e2e_call, max(args.warmup, 3))
+    barrier(world)
+    e2e_ms = max_over_ranks(time_region(stream, e2e_call, args.steps), world) / args.steps
+    h2d = (xh.numel() + rh.numel() + gh.numel() + uh.numel()) * 2
+    d2h = (ox.numel() + orr.numel()) * 2
+
+    line = {
+        "metric": METRIC,
+        "value": round(value_gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "us_per_step": round(ms_per_step * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 (int4 weights, fp32 accumulation)",
+        "data": "synthetic (seeded: int4 weights uniform on [-8,7], bf16 scales U[0.005,0.02], activations and residual N(0,1), norm weights N(1,0.1))",
+        "config": {
+            "workload": "decode_step: 32 x [add-RMSNorm 1x4096 eps 1e-5 + SwiGLU-W4A16 GEMV M=1 K=14336 N=4096 group 128], seed 3",
+            "bytes_per_step": bytes_per_step,
+            "l2": "inputs larger than L2 (972 MB of weights per step vs 129 MB L2); no flush",
+            "launch": "one CUDA graph replay per step (64 kernels)",
+            "parallelism": f"replicas x{world}",
+        },
+        "pct_of_measured_hbm": round(100 * value_gbs / world / hbm_peak, 1),
+        "pct_of_spec_8tbs": round(100 * value_gbs / world / SPEC_HBM_GBS, 1),
+        "kernels": {k: {kk: (round(vv, 3) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                    for k, v in kernels.items()},
+        "roofline": {
+            "kernel": "swiglu_w4a16_gemv (M=1 K=14336 N=4096)",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": hbm_peak,
+            "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": gemv_bytes,
+        },
+        "e2e": {
+            "value": round(world * bytes_per_step / (e2e_ms * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "ms_per_step": round(e2e_ms, 6),
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "api": "memory_bound_decode_fd_gb300.step.DecodeStep.__call__ (pinned host in/out)",
+        },
+        "gpu_launches": 2 * spec["layers"] * args.steps,
+        "clocks": clocks,
+    }
+    return line, d
+
+
+def cpu_baseline_decode(d, budget_s=12.0):
+    """The oracle as it stands on this host's cores, on a bounded sample of the decode
+    step: whole layers, in order, until `budget_s` of CPU time is spent."""
+    import oracle
+    from memory_bound_decode_fd_gb300 import traffic
+
+    t0 = time.perf_counter()
+    n = 0
+    x, res = d["x"], d["residual"]
+    for L in d["layers"]:
+        rec, x, res = oracle.decode_mlp_step(x, res, [L], 1e-5, d["group"])
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    b = n * (traffic.add_rmsnorm_bytes(1, d["hidden"]) + traffic.gemv_bytes(1, d["inter"], d["hidden"], d["group"]))
+    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} of 32 decode-step layers (add-RMSNorm 1x4096 + GEMV 14336x4096 each), {dt:.1f} s, float64 numpy, 1 thread"}
+
+
+def reference_arm(args):
+    """`--impl reference`: the CPU oracle, as it stands, timed on the host cores (one
+    thread). Each step is a bounded sample of the decode step: the add-RMSNorm of one
+    layer and that layer's GEMV over a slice of its output rows, sized so the whole
+    run ends within a few minutes."""
+    import oracle
+    from memory_bound_decode_fd_gb300 import inputs, traffic
+
+    d = inputs.decode_step_inputs(layers=32, seed=3)
+    hidden, inter, group = d["hidden"], d["inter"], d["group"]
+    total = args.steps + args.warmup
+    target_s = min(2.0, max(0.02, 150.0 / max(total, 1)))
+
+    def sample(i, rows):
+        L = d["layers"][i % 32]
+        lo = (i * 97) % (hidden - rows + 1)
+        t0 = time.perf_counter()
+        h, _, _ = oracle.add_rmsnorm(d["x"], d["residual"], L["rms_weight"], 1e-5)
+        oracle.swiglu_w4a16_gemv(L["gate"], L["up"], L["qweight"][lo:lo + rows],
+                                 L["scales"][lo:lo + rows], group)
+        return time.perf_counter() - t0
+
+    # calibrate the slice so one sample takes about target_s
+    probe = 64
+    t_probe = min(sample(0, probe) for _ in range(2))
+    rows = int(max(8, min(hidden, probe * target_s / max(t_probe, 1e-6))))
+    sample_bytes = traffic.add_rmsnorm_bytes(1, hidden) + traffic.gemv_bytes(1, inter, rows, group)
+    times = []
+    for i in range(total):
+        dt = sample(i, rows)
+        if i >= args.warmup:
+            times.append(dt)
+    per = sum(times) / len(times)
+    value = sample_bytes / per / 1e9
+    step_bytes = traffic.decode_step_bytes(32, hidden, inter, group)
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_bytes / (value * 1e9) * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": "decode_step: 32 x [add-RMSNorm 1x4096 eps 1e-5 + SwiGLU-W4A16 GEMV M=1 K=14336 N=4096 group 128], seed 3",
+                   "sample": f"per step: one layer's add-RMSNorm + its GEMV over {rows} of 4096 output rows ({sample_bytes} B); ms_per_step scales the rate to the 32-layer step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{len(times)} samples of one layer's add-RMSNorm + GEMV over {rows} output rows, float64 numpy, 1 thread"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- single-call workloads
+
+def bench_single(args, device, rank, world):
+    import memory_bound_decode_fd_gb300 as fd
+    from memory_bound_decode_fd_gb300 import inputs
+
+    spec = dict(inputs.WORKLOADS[args.workload])
+    kind = spec.pop("kind")
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    calls = []
+    if kind in ("gemv", "batched"):
+        M, K, N, g = spec["M"], spec["K"], spec["N"], spec["group"]
+        nbytes = fd.gemv_bytes(M, K, N, g)
+        nsets = max(1, min(4096, math.ceil(3 * l2 / nbytes)))
+        base = inputs.gemv_inputs(M, K, N, g, seed=spec["seed"])
+        gate, up = to_dev(base["gate"], device), to_dev(base["up"], device)
+        rng = np.random.default_rng(spec["seed"] + 1)
+        qs = [to_dev(base["qweight"], device)] + [to_dev(inputs.int4_words(rng, N, K), device) for _ in range(nsets - 1)]
+        ss = [to_dev(base["scales"], device)] + [to_dev(inputs.scales_bf16(rng, N, K, g), device) for _ in range(nsets - 1)]
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        for q, s in zip(qs, ss):
+            calls.append(lambda q=q, s=s: fd.swiglu_w4a16_gemv(gate, up, q, s, out=out, group=g))
+        kname, desc = "swiglu_w4a16_gemv", f"GEMV M={M} K={K} N={N} group {g}, seed {spec['seed']}"
+    else:
+        rows, hidden = spec["rows"], spec["hidden"]
+        nbytes = fd.add_rmsnorm_bytes(rows, hidden)
+        nsets = max(1, min(64, math.ceil(3 * l2 / nbytes)))
+        d = inputs.rmsnorm_inputs(rows, hidden, seed=spec["seed"])
+        w = to_dev(d["weight"], device)
+        sets = [(to_dev(d["x"], device), to_dev(d["residual"], device)) for _ in range(nsets)]
+        y = torch.empty((rows, hidden), dtype=torch.bfloat16, device=device)
+        h = torch.empty_like(y)
+        for x, r in sets:
+            calls.append(lambda x=x, r=r: fd.add_rmsnorm(x, r, w, spec["eps"], out=y, residual_out=h))
+        kname, desc = "add_rmsnorm", f"add-RMSNorm rows={rows} hidden={hidden} eps {spec['eps']}, seed {spec['seed']}"
+
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for c in calls:
+            c()
+    replay = lambda: graph.replay()  # noqa: E731
+    reps = max(1, math.ceil(args.steps / len(calls)))
+    hbm_peak, peak_kind, _ = read_peaks()
+    sampler = ClockSampler(smi_index())
+    sampler.start()
+    settle_until = time.time() + 1.0
+    with torch.cuda.stream(stream):
+        while time.time() < settle_until:
+            time_region(stream, replay, 10)
+        time_region(stream, replay, max(args.warmup, 3))
+        barrier(world)
+        ms = max_over_ranks(time_region(stream, replay, reps), world)
+    clocks = sampler.stop()
+    n_calls = reps * len(calls)
+    us_call = ms * 1e3 / n_calls
+    with torch.cuda.stream(stream):
+        kt = per_launch_times(stream, [(kname, c) for c in calls[:256]])
+    k_us = kt[kname][0] * 1e3
+    gbs = world * nbytes / (us_call * 1e-6) / 1e9
+    return {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": n_calls, "warmup": args.warmup, "ms_per_step": round(us_call / 1e3, 6),
+        "us_per_call": round(us_call, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (int4 weights, fp32 accumulation)" if kname.startswith("swiglu") else "bf16 (fp32 reduction)",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"{args.workload}: {desc}", "bytes_per_call": nbytes,
+                   "l2": f"{len(calls)} rotating input sets ({len(calls)} x {nbytes} B vs L2 {l2} B)",
+                   "launch": f"CUDA graph of {len(calls)} calls"},
+        "pct_of_measured_hbm": round(100 * gbs / world / hbm_peak, 1),
+        "pct_of_spec_8tbs": round(100 * gbs / world / SPEC_HBM_GBS, 1),
+        "roofline": {"kernel": kname, "bound": "hbm", "achieved": round(nbytes / (k_us * 1e-6) / 1e9, 1),
+                     "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(nbytes / (k_us * 1e-6) / 1e9 / hbm_peak, 4),
+                     "kernel_us": round(k_us, 3), "traffic": None},
+        "e2e": None,
+        "gpu_launches": n_calls,
+        "clocks": clocks,
+    }
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
+    ap.add_argument("--workload", default="decode_step",
+                    choices=["decode_step", "gemv_94mb", "rmsnorm_big", "gemv_small", "batched_m64"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)), flush=True)
+        return 0
+
+    from memory_bound_decode_fd_gb300 import build
+
+    build.build()  # no-op when libfd.so is up to date
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}), flush=True)
+        return 1
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    if args.workload == "decode_step":
+        line, d = bench_decode(args, device, rank, world)
+        if rank == 0 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline_decode(d)
+    else:
+        line = bench_single(args, device, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,129 @@
+/*
+ * fd.h - C ABI of the fused memory-bound decode kernels for GB300 (sm_103a).
+ *
+ * Two operations of an LLM decode layer, each one kernel launch:
+ *
+ *   fd_swiglu_w4a16_gemv   y = (silu(g) * u) . dequant(W_int4)^T   ("GEMM prologue
+ *                          fusion": the activation and the int4 dequantisation are done
+ *                          as the weights stream in; the (M, K, N) product and the
+ *                          silu/mul intermediate never exist in memory).
+ *   fd_add_rmsnorm         h = x + residual; out = RMSNorm(h) * weight  (one kernel, two
+ *                          outputs: the new residual h and the normalised row).
+ *
+ * Sources (web pages, cited by title and section):
+ *   [FIX]  "PyTorch Community Proposes Fusion Fix as Large Intermediate Buffers May Slow
+ *          Single-Token Decoding in Quantized LLMs" - "Reproduction and analysis" (the
+ *          (1, K, N) product an M=1 matmul must not materialise), "Fix proposal" (int4
+ *          weights with a SwiGLU pre-operation).
+ *   [FUSE] "09 - Operator fusion" - section 5, "The taxonomy of fusions" (items 2 and 4:
+ *          reduction + elementwise; GEMM prologue dequantisation for W4A16) and "The
+ *          fusion boundary problem" (add_rmsnorm with two outputs; act @ W_down).
+ *   [KFM]  "Kernel Fusion, torch.compile and CUDA Graphs, Measured" - "Step 1" (silu(g) *
+ *          u), "Step 2: fusing them by hand in Triton" (add + RMSNorm order and roundings).
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer (cudaMalloc / PyTorch CUDA memory) on the
+ *     current device, contiguous, row-major, 16-byte aligned. The caller allocates and
+ *     owns every buffer. The library allocates no memory and keeps no state beyond a
+ *     per-device cache of the SM count.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *     asynchronous and stream-ordered: no host synchronisation, no host<->device copy.
+ *   - bf16 is IEEE bfloat16 stored as 16-bit words.
+ *   - Arguments are checked on the host before anything is launched. A bad call
+ *     returns a nonzero fd_status and launches nothing. A failed launch returns
+ *     FD_ERR_CUDA (from cudaGetLastError); faults inside a kernel surface, as in CUDA,
+ *     at the caller's next synchronisation.
+ *   - All entry points are thread-safe.
+ */
+#ifndef FD_H_
+#define FD_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA header. */
+typedef struct CUstream_st *fd_stream_t;
+
+typedef enum fd_status {
+    FD_OK = 0,
+    FD_ERR_NULL = 1,        /* a required pointer is NULL */
+    FD_ERR_SHAPE = 2,       /* a size is <= 0 or breaks a divisibility rule */
+    FD_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+    FD_ERR_UNSUPPORTED = 4, /* a size is above the supported maximum */
+    FD_ERR_CUDA = 5,        /* the CUDA runtime reported an error */
+    FD_ERR_OVERLAP = 6      /* outputs overlap inputs in a way the kernel does not allow */
+} fd_status;
+
+/* Largest supported sizes (checked, FD_ERR_UNSUPPORTED above them). */
+#define FD_MAX_K 32768        /* gemv: reduction length */
+#define FD_MAX_M 256          /* gemv: activation rows (batched decode) */
+#define FD_MAX_HIDDEN 32768   /* add_rmsnorm: row length */
+
+/*
+ * fd_swiglu_w4a16_gemv - SwiGLU-prologue W4A16 matrix-vector / skinny-matrix product.
+ *
+ *   a[m, k]  = silu(gate[m, k]) * up[m, k],   silu(x) = x / (1 + exp(-x))      [KFM Step 1]
+ *   W[n, k]  = q[n, k] * scales[n, k / group]                                 [FUSE item 4]
+ *   out[m, n] = bf16( sum_k a[m, k] * W[n, k] )   (fp32 accumulation, one RNE rounding)
+ *
+ * gate, up  bf16 [M, K] row-major.
+ * qweight   int32 [N, K/8] row-major (nn.Linear [out, in] orientation). Nibble j
+ *           (bits 4j..4j+3) of word p in row n holds q[n, 8p + j] as a 4-bit two's
+ *           complement integer in [-8, 7] (symmetric, no zero point).
+ * scales    bf16 [N, K/group] row-major; group consecutive k share one scale.
+ * out       bf16 [M, N] row-major. Must not overlap any input.
+ * Requires  1 <= M <= FD_MAX_M, 32 <= K <= FD_MAX_K, N >= 1, K % 32 == 0,
+ *           group % 32 == 0, K % group == 0.
+ * The silu/mul intermediate and the dequantised weights are kept on chip; the kernel
+ * reads each packed weight word from HBM once per call.
+ */
+int fd_swiglu_w4a16_gemv(const void *gate, const void *up, const void *qweight,
+                         const void *scales, void *out, int M, int K, int N, int group,
+                         fd_stream_t stream);
+
+/*
+ * fd_add_rmsnorm - fused residual add + RMSNorm, one pass over HBM.     [KFM Step 2]
+ *
+ *   h[i, j]   = bf16( f32(x[i, j]) + f32(residual[i, j]) )            -> residual_out
+ *   rstd[i]   = 1 / sqrt( (1/hidden) * sum_j f32(h[i, j])^2 + eps )   (fp32)
+ *   out[i, j] = bf16( f32(bf16( f32(h[i, j]) * rstd[i] )) * f32(weight[j]) )
+ *
+ * The two roundings of out follow the page's kernel (normalised value rounded to bf16,
+ * then multiplied by the weight).
+ * x, residual         bf16 [rows, hidden] row-major.
+ * weight              bf16 [hidden].
+ * out, residual_out   bf16 [rows, hidden] row-major.
+ * Aliasing            residual_out == residual and/or out == x (exactly the same pointer)
+ *                     are allowed; any other overlap returns FD_ERR_OVERLAP.
+ * Requires            rows >= 1, 8 <= hidden <= FD_MAX_HIDDEN, hidden % 8 == 0,
+ *                     eps >= 0 and finite.
+ * Reads 4 bytes and writes 4 bytes per element (plus the weight row once per CTA).
+ */
+int fd_add_rmsnorm(const void *x, const void *residual, const void *weight, float eps,
+                   void *out, void *residual_out, int rows, int hidden,
+                   fd_stream_t stream);
+
+/*
+ * fd_w4_dequant_debug - write the dequantised weights W[n, k] = q[n, k] * s[n, k/group]
+ * as fp32 [N, K] (test support: the unpack and scale of the GEMV prologue, checked bit
+ * for bit). Same layouts and size rules as fd_swiglu_w4a16_gemv; `out` is fp32 [N, K].
+ */
+int fd_w4_dequant_debug(const void *qweight, const void *scales, float *out, int K, int N,
+                        int group, fd_stream_t stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char *fd_status_string(int status);
+
+/* The cudaError_t value behind the calling thread's most recent FD_ERR_CUDA (0 if none).
+ * Thread-local; not reset by successful calls. */
+int fd_last_cuda_error(void);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int fd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FD_H_ */

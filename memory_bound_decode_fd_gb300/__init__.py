@@ -1,0 +1,33 @@
+"""fd - fused memory-bound decode kernels for GB300 (sm_103a).
+
+* ``swiglu_w4a16_gemv``: y = (silu(g) * u) . dequant(W_int4)^T, one kernel, int4 in HBM only.
+* ``add_rmsnorm``: residual add + RMSNorm, one pass, two outputs.
+* ``decode_mlp_step``: L layers of the two, in stream order.
+
+The compute runs in ``libfd.so`` (C ABI in ``include/fd.h``); this package marshals
+PyTorch CUDA tensors into it. Build the library with ``build.build()``. There is no CPU
+fallback: calling a kernel without the library raises ``FdLibraryMissing``.
+"""
+
+from ._lib import (  # noqa: F401
+    FD_ERR_ALIGN,
+    FD_ERR_CUDA,
+    FD_ERR_NULL,
+    FD_ERR_OVERLAP,
+    FD_ERR_SHAPE,
+    FD_ERR_UNSUPPORTED,
+    FD_MAX_HIDDEN,
+    FD_MAX_K,
+    FD_MAX_M,
+    FD_OK,
+    LIB_PATH,
+    FdError,
+    FdLibraryMissing,
+    status_string,
+)
+from ._lib import load as load_library  # noqa: F401
+from .kernels import add_rmsnorm, decode_mlp_step, swiglu_w4a16_gemv, w4_dequant_debug  # noqa: F401
+from .packing import pack_int4  # noqa: F401
+from .traffic import add_rmsnorm_bytes, decode_step_bytes, gemv_bytes, gemv_flops  # noqa: F401
+
+__version__ = "1.0.0"

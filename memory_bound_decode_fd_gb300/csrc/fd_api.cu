@@ -1,0 +1,152 @@
+// fd_api.cu - the C ABI (include/fd.h): argument checks, dispatch, status strings.
+//
+// Every check runs on the host before any CUDA call, so a rejected call launches nothing
+// and touches no device state (it also works on a machine without a GPU).
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "fd_internal.h"
+
+namespace fd {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_info_ready[kMaxDevices];
+DeviceInfo g_info[kMaxDevices];
+thread_local int g_last_cuda_error = 0;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t a_bytes, const void *b, size_t b_bytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
+}
+
+int from_cuda(cudaError_t err) {
+    if (err == cudaSuccess) return FD_OK;
+    g_last_cuda_error = static_cast<int>(err);
+    return FD_ERR_CUDA;
+}
+
+int check_w4_layout(const void *qweight, const void *scales, int K, int N, int group) {
+    if (!qweight || !scales) return FD_ERR_NULL;
+    if (K <= 0 || N <= 0 || group <= 0) return FD_ERR_SHAPE;
+    if (K % 32 != 0 || group % 32 != 0 || K % group != 0) return FD_ERR_SHAPE;
+    if (K > FD_MAX_K) return FD_ERR_UNSUPPORTED;
+    if (!aligned16(qweight) || !aligned16(scales)) return FD_ERR_ALIGN;
+    return FD_OK;
+}
+
+}  // namespace
+
+cudaError_t device_info(DeviceInfo *info) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const int slot = dev % kMaxDevices;
+    if (g_info_ready[slot].load(std::memory_order_acquire) == dev + 1) {
+        *info = g_info[slot];
+        return cudaSuccess;
+    }
+    DeviceInfo di{};
+    err = cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                 dev);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&di.l2_bytes, cudaDevAttrL2CacheSize, dev);
+    if (err != cudaSuccess) return err;
+    // Benign race: concurrent first calls write identical values.
+    g_info[slot] = di;
+    g_info_ready[slot].store(dev + 1, std::memory_order_release);
+    *info = di;
+    return cudaSuccess;
+}
+
+}  // namespace fd
+
+using namespace fd;
+
+extern "C" {
+
+int fd_swiglu_w4a16_gemv(const void *gate, const void *up, const void *qweight,
+                         const void *scales, void *out, int M, int K, int N, int group,
+                         fd_stream_t stream) {
+    if (!gate || !up || !out) return FD_ERR_NULL;
+    int st = check_w4_layout(qweight, scales, K, N, group);
+    if (st != FD_OK) return st;
+    if (M <= 0) return FD_ERR_SHAPE;
+    if (M > FD_MAX_M) return FD_ERR_UNSUPPORTED;
+    if (!aligned16(gate) || !aligned16(up) || !aligned16(out)) return FD_ERR_ALIGN;
+    const size_t act_bytes = (size_t)M * K * 2;
+    const size_t out_bytes = (size_t)M * N * 2;
+    const size_t w_bytes = (size_t)N * K / 2;
+    const size_t s_bytes = (size_t)N * (K / group) * 2;
+    if (overlaps(out, out_bytes, gate, act_bytes) || overlaps(out, out_bytes, up, act_bytes) ||
+        overlaps(out, out_bytes, qweight, w_bytes) || overlaps(out, out_bytes, scales, s_bytes))
+        return FD_ERR_OVERLAP;
+    return from_cuda(launch_gemv_cc(gate, up, qweight, scales, out, M, K, N, group,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fd_add_rmsnorm(const void *x, const void *residual, const void *weight, float eps,
+                   void *out, void *residual_out, int rows, int hidden, fd_stream_t stream) {
+    if (!x || !residual || !weight || !out || !residual_out) return FD_ERR_NULL;
+    if (rows <= 0 || hidden <= 0 || hidden % 8 != 0 || hidden < 8) return FD_ERR_SHAPE;
+    if (!(eps >= 0.0f) || !std::isfinite(eps)) return FD_ERR_SHAPE;
+    if (hidden > FD_MAX_HIDDEN) return FD_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(residual) || !aligned16(weight) || !aligned16(out) ||
+        !aligned16(residual_out))
+        return FD_ERR_ALIGN;
+    const size_t bytes = (size_t)rows * hidden * 2;
+    const size_t w_bytes = (size_t)hidden * 2;
+    // Allowed aliasing: out == x, residual_out == residual (same pointer, in place).
+    if (overlaps(out, bytes, residual_out, bytes)) return FD_ERR_OVERLAP;
+    if (out != x && (overlaps(out, bytes, x, bytes) || overlaps(out, bytes, residual, bytes)))
+        return FD_ERR_OVERLAP;
+    if (out == x && overlaps(out, bytes, residual, bytes)) return FD_ERR_OVERLAP;
+    if (residual_out != residual && (overlaps(residual_out, bytes, residual, bytes) ||
+                                     overlaps(residual_out, bytes, x, bytes)))
+        return FD_ERR_OVERLAP;
+    if (residual_out == residual && overlaps(residual_out, bytes, x, bytes))
+        return FD_ERR_OVERLAP;
+    if (overlaps(weight, w_bytes, out, bytes) || overlaps(weight, w_bytes, residual_out, bytes))
+        return FD_ERR_OVERLAP;
+    return from_cuda(launch_add_rmsnorm(x, residual, weight, eps, out, residual_out, rows,
+                                        hidden, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fd_w4_dequant_debug(const void *qweight, const void *scales, float *out, int K, int N,
+                        int group, fd_stream_t stream) {
+    if (!out) return FD_ERR_NULL;
+    int st = check_w4_layout(qweight, scales, K, N, group);
+    if (st != FD_OK) return st;
+    if (!aligned16(out)) return FD_ERR_ALIGN;
+    const size_t out_bytes = (size_t)N * K * 4;
+    if (overlaps(out, out_bytes, qweight, (size_t)N * K / 2) ||
+        overlaps(out, out_bytes, scales, (size_t)N * (K / group) * 2))
+        return FD_ERR_OVERLAP;
+    return from_cuda(launch_w4_dequant_debug(qweight, scales, out, K, N, group,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char *fd_status_string(int status) {
+    switch (status) {
+        case FD_OK: return "FD_OK: success";
+        case FD_ERR_NULL: return "FD_ERR_NULL: a required pointer is NULL";
+        case FD_ERR_SHAPE: return "FD_ERR_SHAPE: a size is invalid (<= 0 or breaks a divisibility rule)";
+        case FD_ERR_ALIGN: return "FD_ERR_ALIGN: a pointer is not 16-byte aligned";
+        case FD_ERR_UNSUPPORTED: return "FD_ERR_UNSUPPORTED: a size is above the supported maximum";
+        case FD_ERR_CUDA: return "FD_ERR_CUDA: the CUDA runtime reported an error";
+        case FD_ERR_OVERLAP: return "FD_ERR_OVERLAP: an output overlaps an input in a way the kernel does not allow";
+        default: return "fd: unknown status";
+    }
+}
+
+int fd_last_cuda_error(void) { return g_last_cuda_error; }
+
+int fd_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+}  // extern "C"

@@ -1,0 +1,391 @@
+// fd_gemv_cc.cu - SwiGLU-prologue W4A16 GEMV on the CUDA cores (any M, tuned for M = 1).
+//
+// y[m, n] = bf16( sum_k silu(g[m, k]) * u[m, k] * q[n, k] * s[n, k / group] )
+//
+// Sources: "09 - Operator fusion", section 5 (taxonomy item 4, GEMM prologue fusion: the
+// dequantisation happens as the weights are loaded, so only int4 crosses HBM; "The fusion
+// boundary problem": act = silu(gate) * up feeds out = act @ W_down). "PyTorch Community
+// Proposes Fusion Fix ..." ("Reproduction and analysis": an M = 1 matmul must not
+// materialise its (1, K, N) product; "Fix proposal": materialise the small input first -
+// here that input, a = silu(g) * u, lives in registers).
+//
+// Work decomposition (one CTA per SM, persistent):
+//   * Thread t of a CTA owns the weight vector positions p = t + v * T (v < VPT) of every
+//     row: each position is 16 bytes = 4 words = 32 consecutive k, inside one scale group.
+//     So thread t needs a[m, k] only for its own k, and computes silu(g) * u once per
+//     m-chunk straight into registers (fp32). Nothing is staged through HBM.
+//   * The CTA owns a contiguous range of output rows n; it walks them in chunks of R rows.
+//     Each thread streams its own 16-byte slot of each row (and the 2-byte scale that
+//     belongs to it) with cp.async into a private ring of S stages in shared memory, S - 1
+//     chunks ahead of the math. Slots are thread-private, so the ring needs no barriers:
+//     cp.async.wait_group orders each thread's own copies.
+//   * Math per 32-bit word: 8 lop3 + 1 shift + 4 packed fp32x2 adds (exact int4 -> fp32,
+//     see fd_w4_unpack.cuh) + 4 packed fp32x2 FMAs; fp32 accumulation; the group scale
+//     multiplies the 32-k partial.
+//   * Reduction: each lane holds R x MB partials per chunk; a butterfly reduce-scatter
+//     over the warp (V - 1 + log2(32 / V) shuffles for V values) leaves one warp sum per
+//     (row, m) in shared memory; the CTA sums over warps and stores bf16 once per output.
+//   * M > MB: the CTA repeats its rows for each chunk of MB activation rows (weights are
+//     then read with an evict-last L2 policy so the repeats hit L2).
+#include <atomic>
+
+#include "fd_internal.h"
+#include "fd_w4_unpack.cuh"
+
+namespace fd {
+namespace {
+
+constexpr int kWindowRows = 64;  // rows whose per-warp partials are held before a flush
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src, int src_bytes,
+                                            uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;"
+                 :
+                 : "r"(smem_addr(dst)), "l"(src), "r"(src_bytes), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
+                 :
+                 : "r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// a = silu(g) * u for the 32 k of one weight vector position, as 16 float2 pairs
+// ordered (k0,k1) (k2,k3) ... to match unpack_w4_f32x2.
+__device__ __forceinline__ void load_activation(const uint16_t *__restrict__ gate,
+                                                const uint16_t *__restrict__ up,
+                                                size_t offset, float2 a[16]) {
+    const uint4 *g4 = reinterpret_cast<const uint4 *>(gate + offset);
+    const uint4 *u4 = reinterpret_cast<const uint4 *>(up + offset);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 gv = g4[i];
+        const uint4 uv = u4[i];
+        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+        const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float g0 = bf16lo(gw[j]), g1 = bf16hi(gw[j]);
+            const float s0 = g0 / (1.0f + expf(-g0));
+            const float s1 = g1 / (1.0f + expf(-g1));
+            a[4 * i + j] = make_float2(s0 * bf16lo(uw[j]), s1 * bf16hi(uw[j]));
+        }
+    }
+}
+
+// For MB activation rows: d[mb] = sum over the 32 k of one vector position of
+// a[mb][k] * q[k] (fp32, two packed chains per row). The word is unpacked once.
+template <int MB>
+__device__ __forceinline__ void dot32(const float2 (*a)[16], uint4 wv, float d[MB]) {
+    const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+    float2 acc0[MB], acc1[MB];
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb) {
+        acc0[mb] = make_float2(0.f, 0.f);
+        acc1[mb] = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 q[4];
+        unpack_w4_f32x2(w[i], q);
+#pragma unroll
+        for (int mb = 0; mb < MB; ++mb) {
+            acc0[mb] = ffma2(a[mb][4 * i + 0], q[0], acc0[mb]);
+            acc1[mb] = ffma2(a[mb][4 * i + 1], q[1], acc1[mb]);
+            acc0[mb] = ffma2(a[mb][4 * i + 2], q[2], acc0[mb]);
+            acc1[mb] = ffma2(a[mb][4 * i + 3], q[3], acc1[mb]);
+        }
+    }
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb) {
+        const float2 s = fadd2(acc0[mb], acc1[mb]);
+        d[mb] = s.x + s.y;
+    }
+}
+
+__host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v >> 1); }
+
+// Butterfly reduce-scatter of V values over a warp. On return, lane l holds in v[0] the
+// warp-wide sum of value index (l >> (5 - log2 V)).
+template <int V>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[V], int lane) {
+#pragma unroll
+    for (int width = V; width > 1; width >>= 1) {
+        const int half = width >> 1;
+        // offset for this stage: 16, 8, ... (one bit of the lane index per halving)
+        const int offset = 16 >> (ilog2(V) - ilog2(width));
+        const bool upper = (lane & offset) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, offset);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int offset = 16 >> ilog2(V); offset > 0; offset >>= 1)
+        r += __shfl_xor_sync(0xFFFFFFFFu, r, offset);
+    return r;
+}
+
+// Shared memory layout (dynamic):
+//   wring  uint4    [S][R][VPT][T]   weight slots
+//   sring  uint32_t [S][R][VPT][T]   scale slots (the bf16 scale in the low or high half)
+//   red    float    [nwarps][kWindowRows][MB]
+template <int VPT, int MB, int R, int S>
+__global__ void __launch_bounds__(512, 1)
+    gemv_cc_kernel(const uint16_t *__restrict__ gate, const uint16_t *__restrict__ up,
+                   const uint4 *__restrict__ qweight, const uint16_t *__restrict__ scales,
+                   uint16_t *__restrict__ out, int M, int K, int N, int group, int rows_base,
+                   int rows_extra, int weights_evict_first) {
+    static_assert(R * MB <= 32 && (R * MB & (R * MB - 1)) == 0, "R*MB: power of 2, <= 32");
+    static_assert(kWindowRows % R == 0, "window must hold whole chunks");
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int T = blockDim.x;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = T >> 5;
+    const int nvec = K >> 5;           // 16-byte weight vectors per row
+    const int ngroups = K / group;
+
+    uint4 *wring = reinterpret_cast<uint4 *>(smem_raw);
+    uint32_t *sring = reinterpret_cast<uint32_t *>(wring + (size_t)S * R * VPT * T);
+    float *red = reinterpret_cast<float *>(sring + (size_t)S * R * VPT * T);
+
+    const int b = blockIdx.x;
+    const int n_begin = b * rows_base + min(b, rows_extra);
+    const int n_cnt = rows_base + (b < rows_extra ? 1 : 0);
+    const int n_chunks = (n_cnt + R - 1) / R;
+    const int m_chunks = (M + MB - 1) / MB;
+    const int total = n_chunks * m_chunks;
+
+    const uint64_t pol = weights_evict_first ? policy_evict_first() : policy_evict_last();
+
+    int pos[VPT];
+    bool active[VPT];
+    int sidx_col[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        pos[v] = tid + v * T;
+        active[v] = pos[v] < nvec;
+        sidx_col[v] = active[v] ? (pos[v] * 32) / group : 0;
+    }
+
+    // Issue the copies of work item c (m-chunk major: c = mc * n_chunks + nc) into ring
+    // stage c % S. Rows past the CTA's range are zero-filled (no bytes read).
+    auto issue = [&](int c) {
+        if (c < total) {
+            const int nc = c % n_chunks;
+            const int stage = c % S;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int n_local = nc * R + r;
+                const bool row_ok = n_local < n_cnt;
+                const int n = n_begin + (row_ok ? n_local : 0);
+#pragma unroll
+                for (int v = 0; v < VPT; ++v) {
+                    if (!active[v]) continue;
+                    const size_t slot = ((size_t)(stage * R + r) * VPT + v) * T + tid;
+                    const uint4 *src = qweight + (size_t)n * nvec + pos[v];
+                    cp_async_16(&wring[slot], src, row_ok ? 16 : 0, pol);
+                    const size_t sidx = (size_t)n * ngroups + sidx_col[v];
+                    const uint16_t *ssrc = scales + (sidx & ~(size_t)1);
+                    const int sbytes = row_ok ? ((sidx & 1) ? 4 : 2) : 0;
+                    cp_async_4(&sring[slot], ssrc, sbytes);
+                }
+            }
+        }
+        cp_async_commit();  // always commit (possibly empty) so group counting is uniform
+    };
+
+#pragma unroll
+    for (int c = 0; c < S - 1; ++c) issue(c);
+
+    float2 a[VPT][MB][16];
+    int window_base = 0;  // first local row of the current flush window
+
+    for (int c = 0; c < total; ++c) {
+        issue(c + S - 1);
+        const int mc = c / n_chunks;
+        const int nc = c % n_chunks;
+        const int m0 = mc * MB;
+
+        if (nc == 0) {
+            // New m-chunk: build a = silu(g) * u for this thread's k and rows m0..m0+MB-1.
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb) {
+#pragma unroll
+                for (int v = 0; v < VPT; ++v) {
+                    if (active[v] && m0 + mb < M) {
+                        load_activation(gate, up, (size_t)(m0 + mb) * K + (size_t)pos[v] * 32,
+                                        a[v][mb]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) a[v][mb][i] = make_float2(0.f, 0.f);
+                    }
+                }
+            }
+        }
+
+        cp_async_wait<S - 1>();  // this thread's copies for item c have landed
+
+        const int stage = c % S;
+        float part[R * MB];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb) part[r * MB + mb] = 0.f;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                if (!active[v]) continue;
+                const size_t slot = ((size_t)(stage * R + r) * VPT + v) * T + tid;
+                const uint4 wv = wring[slot];
+                const uint32_t sw = sring[slot];
+                const size_t sidx = (size_t)(n_begin + nc * R + r) * ngroups + sidx_col[v];
+                const float s = (sidx & 1) ? bf16hi(sw) : bf16lo(sw);
+                float d[MB];
+                dot32<MB>(a[v], wv, d);
+#pragma unroll
+                for (int mb = 0; mb < MB; ++mb)
+                    part[r * MB + mb] = fmaf(s, d[mb], part[r * MB + mb]);
+            }
+        }
+
+        const float wsum = warp_reduce_scatter<R * MB>(part, lane);
+        constexpr int kLanesPerValue = 32 / (R * MB);
+        if ((lane & (kLanesPerValue - 1)) == 0) {
+            const int idx = lane / kLanesPerValue;  // = r * MB + mb
+            const int r = idx / MB, mb = idx % MB;
+            const int row_in_window = nc * R + r - window_base;
+            red[((size_t)warp * kWindowRows + row_in_window) * MB + mb] = wsum;
+        }
+
+        const int rows_done = (nc + 1) * R;
+        const bool last_chunk = (nc == n_chunks - 1);
+        if (rows_done - window_base == kWindowRows || last_chunk) {
+            __syncthreads();
+            const int rows_in_window = min(rows_done, n_cnt) - window_base;
+            for (int i = tid; i < rows_in_window * MB; i += T) {
+                const int row = i / MB, mb = i % MB;
+                float acc = 0.f;
+                for (int w = 0; w < nwarps; ++w)
+                    acc += red[((size_t)w * kWindowRows + row) * MB + mb];
+                if (m0 + mb < M) {
+                    const int n = n_begin + window_base + row;
+                    __nv_bfloat16 y = __float2bfloat16_rn(acc);
+                    out[(size_t)(m0 + mb) * N + n] = *reinterpret_cast<uint16_t *>(&y);
+                }
+            }
+            __syncthreads();
+            window_base = last_chunk ? 0 : rows_done;
+        }
+    }
+    cp_async_wait<0>();
+}
+
+template <int VPT, int MB, int R, int S>
+size_t gemv_smem_bytes(int T) {
+    return (size_t)S * R * VPT * T * (16 + 4) + (size_t)(T / 32) * kWindowRows * MB * 4;
+}
+
+int threads_for(int K, int VPT) {
+    const int nvec = K / 32;
+    const int T = (nvec + VPT - 1) / VPT;
+    return (T + 31) / 32 * 32;
+}
+
+// Raises the kernel's dynamic shared memory limit once per device.
+template <typename Kern>
+cudaError_t ensure_smem_attr(Kern kern, size_t smem, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    int max_optin = 0;
+    err = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+    if (err != cudaSuccess) return err;
+    (void)smem;
+    done.fetch_or(bit, std::memory_order_acq_rel);
+    return cudaSuccess;
+}
+
+template <int VPT, int MB, int R, int S>
+cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
+                       const void *qweight, const void *scales, void *out, int M, int K,
+                       int N, int group, cudaStream_t stream) {
+    static std::atomic<uint64_t> attr_done{0};
+    const int T = threads_for(K, VPT);
+    const size_t smem = gemv_smem_bytes<VPT, MB, R, S>(T);
+    auto kern = gemv_cc_kernel<VPT, MB, R, S>;
+    cudaError_t err = ensure_smem_attr(kern, smem, attr_done);
+    if (err != cudaSuccess) return err;
+    // One CTA per SM; fewer when there are not enough rows for a chunk each.
+    int grid = di.sm_count;
+    if ((long long)grid * R > N) grid = (N + R - 1) / R;
+    if (grid < 1) grid = 1;
+    const int rows_base = N / grid;
+    const int rows_extra = N % grid;
+    const int evict_first = (M <= MB) ? 1 : 0;
+    kern<<<grid, T, smem, stream>>>(
+        static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up),
+        static_cast<const uint4 *>(qweight), static_cast<const uint16_t *>(scales),
+        static_cast<uint16_t *>(out), M, K, N, group, rows_base, rows_extra, evict_first);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Picks the deepest ring that fits the SM's shared memory, for the M = 1 kernel (MB = 1)
+// or the M > 1 kernel (MB = 2), with one (K <= 16384) or two (K <= 32768) weight vector
+// positions per thread.
+cudaError_t launch_gemv_cc(const void *gate, const void *up, const void *qweight,
+                           const void *scales, void *out, int M, int K, int N, int group,
+                           cudaStream_t stream) {
+    DeviceInfo di;
+    cudaError_t err = device_info(&di);
+    if (err != cudaSuccess) return err;
+    const size_t limit = (size_t)di.max_smem_optin;
+#define FD_TRY(VPT, MB, R, S)                                                              \
+    if (gemv_smem_bytes<VPT, MB, R, S>(threads_for(K, VPT)) <= limit)                      \
+        return launch_cfg<VPT, MB, R, S>(di, gate, up, qweight, scales, out, M, K, N, group, \
+                                         stream);
+    const bool wide = K / 32 > 512;  // more than 512 vector positions: two per thread
+    if (!wide && M == 1) {
+        FD_TRY(1, 1, 8, 4)
+        FD_TRY(1, 1, 8, 3)
+        FD_TRY(1, 1, 4, 3)
+        FD_TRY(1, 1, 4, 2)
+    } else if (!wide) {
+        FD_TRY(1, 2, 8, 3)
+        FD_TRY(1, 2, 4, 3)
+        FD_TRY(1, 2, 4, 2)
+    } else {
+        FD_TRY(2, 1, 4, 3)
+        FD_TRY(2, 1, 4, 2)
+        FD_TRY(2, 1, 2, 2)
+    }
+#undef FD_TRY
+    return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace fd

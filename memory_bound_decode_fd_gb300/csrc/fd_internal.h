@@ -1,0 +1,105 @@
+// fd_internal.h - device helpers and launcher prototypes shared by the CUDA sources of
+// the fd library (not part of the public ABI; see include/fd.h for that).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/fd.h"
+
+namespace fd {
+
+// ------------------------------------------------------------------------------------
+// Host-side device facts (cached per device; thread-safe).
+// ------------------------------------------------------------------------------------
+struct DeviceInfo {
+    int sm_count;
+    int max_smem_optin;   // bytes of dynamic shared memory a CTA may opt in to
+    int l2_bytes;
+};
+// Returns cudaSuccess and fills `info` for the current device.
+cudaError_t device_info(DeviceInfo *info);
+
+// ------------------------------------------------------------------------------------
+// Launchers (host). Arguments are validated by the C-ABI layer before these run.
+// ------------------------------------------------------------------------------------
+cudaError_t launch_gemv_cc(const void *gate, const void *up, const void *qweight,
+                           const void *scales, void *out, int M, int K, int N, int group,
+                           cudaStream_t stream);
+cudaError_t launch_add_rmsnorm(const void *x, const void *residual, const void *weight,
+                               float eps, void *out, void *residual_out, int rows,
+                               int hidden, cudaStream_t stream);
+cudaError_t launch_w4_dequant_debug(const void *qweight, const void *scales, float *out,
+                                    int K, int N, int group, cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------
+// Device helpers.
+// ------------------------------------------------------------------------------------
+
+// L2 policy for data touched once per call (activations, streamed weights, outputs).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// L2 policy for data every CTA re-reads (the RMSNorm weight row).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 16-byte read-only load that bypasses L1 and carries an L2 eviction policy.
+__device__ __forceinline__ uint4 ld_nc_v4(const void *p, uint64_t pol) {
+    uint4 v;
+    asm volatile(
+        "ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p), "l"(pol));
+    return v;
+}
+
+// 16-byte store with an L2 eviction policy.
+__device__ __forceinline__ void st_v4(void *p, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
+                 :
+                 : "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
+// Two bf16 in one 32-bit word -> two floats (exact).
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two floats -> two bf16 (round to nearest even) packed low/high.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Packed fp32x2 arithmetic (one instruction for two lanes of work on sm_100+).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)),
+          "l"(*reinterpret_cast<uint64_t *>(&c)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+
+// lop3 with truth table 0x6A: (a & b) ^ c.
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+}  // namespace fd

@@ -1,0 +1,176 @@
+"""Python binding of the fd C ABI (include/fd.h) for PyTorch CUDA tensors.
+
+Argument marshalling only: every step of the computation runs in libfd.so's CUDA
+kernels, launched on the caller's current PyTorch stream. PyTorch provides the device
+memory and the stream; nothing here computes.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+
+def _stream_handle(stream: torch.cuda.Stream | None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(int(s.cuda_stream))
+
+
+def _check_tensor(name: str, t: torch.Tensor, dtype: torch.dtype, shape: tuple | None = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the fd kernels have no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def swiglu_w4a16_gemv(
+    gate: torch.Tensor,
+    up: torch.Tensor,
+    qweight: torch.Tensor,
+    scales: torch.Tensor,
+    out: torch.Tensor | None = None,
+    group: int = 128,
+    stream: torch.cuda.Stream | None = None,
+) -> torch.Tensor:
+    """out[m, n] = bf16(sum_k silu(gate[m, k]) * up[m, k] * q[n, k] * scales[n, k // group]).
+
+    gate, up: bf16 [M, K]; qweight: int32 [N, K/8] (nibble j of word p = q[n, 8p + j]);
+    scales: bf16 [N, K/group]; out: bf16 [M, N] (allocated if None).
+    """
+    if gate.dim() == 1:
+        gate = gate.unsqueeze(0)
+        up = up.unsqueeze(0)
+    if gate.dim() != 2 or qweight.dim() != 2 or scales.dim() != 2:
+        raise ValueError("gate/up must be [M, K]; qweight [N, K/8]; scales [N, K/group]")
+    M, K = gate.shape
+    N = qweight.shape[0]
+    _check_tensor("gate", gate, torch.bfloat16)
+    _check_tensor("up", up, torch.bfloat16, (M, K))
+    _check_tensor("qweight", qweight, torch.int32, (N, K // 8))
+    if group <= 0 or K % group != 0:
+        raise ValueError(f"K={K} must be a multiple of group={group}")
+    _check_tensor("scales", scales, torch.bfloat16, (N, K // group))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=gate.device)
+    _check_tensor("out", out, torch.bfloat16, (M, N))
+    lib = _lib.load()
+    st = lib.fd_swiglu_w4a16_gemv(
+        _ptr(gate), _ptr(up), _ptr(qweight), _ptr(scales), _ptr(out),
+        int(M), int(K), int(N), int(group), _stream_handle(stream),
+    )
+    _lib.check(st)
+    return out
+
+
+def add_rmsnorm(
+    x: torch.Tensor,
+    residual: torch.Tensor,
+    weight: torch.Tensor,
+    eps: float,
+    out: torch.Tensor | None = None,
+    residual_out: torch.Tensor | None = None,
+    stream: torch.cuda.Stream | None = None,
+) -> tuple[torch.Tensor, torch.Tensor]:
+    """(out, residual_out) with residual_out = bf16(x + residual) and
+    out = bf16(bf16(h * rstd) * weight), rstd = 1/sqrt(mean(h^2) + eps) per row.
+
+    x, residual: bf16 [rows, hidden] (a 1-D tensor is one row); weight: bf16 [hidden].
+    out may be x and residual_out may be residual (in place).
+    """
+    squeeze = x.dim() == 1
+    if squeeze:
+        x = x.unsqueeze(0)
+        residual = residual.unsqueeze(0)
+    if x.dim() != 2:
+        raise ValueError("x must be [rows, hidden]")
+    rows, hidden = x.shape
+    _check_tensor("x", x, torch.bfloat16)
+    _check_tensor("residual", residual, torch.bfloat16, (rows, hidden))
+    _check_tensor("weight", weight, torch.bfloat16, (hidden,))
+    if out is None:
+        out = torch.empty_like(x)
+    elif squeeze and out.dim() == 1:
+        out = out.unsqueeze(0)
+    if residual_out is None:
+        residual_out = torch.empty_like(x)
+    elif squeeze and residual_out.dim() == 1:
+        residual_out = residual_out.unsqueeze(0)
+    _check_tensor("out", out, torch.bfloat16, (rows, hidden))
+    _check_tensor("residual_out", residual_out, torch.bfloat16, (rows, hidden))
+    lib = _lib.load()
+    st = lib.fd_add_rmsnorm(
+        _ptr(x), _ptr(residual), _ptr(weight), ctypes.c_float(float(eps)), _ptr(out),
+        _ptr(residual_out), int(rows), int(hidden), _stream_handle(stream),
+    )
+    _lib.check(st)
+    if squeeze:
+        return out.squeeze(0), residual_out.squeeze(0)
+    return out, residual_out
+
+
+def w4_dequant_debug(
+    qweight: torch.Tensor,
+    scales: torch.Tensor,
+    group: int = 128,
+    out: torch.Tensor | None = None,
+    stream: torch.cuda.Stream | None = None,
+) -> torch.Tensor:
+    """fp32 [N, K] dequantised weights from the GEMV prologue's unpack (test support)."""
+    N, K8 = qweight.shape
+    K = K8 * 8
+    _check_tensor("qweight", qweight, torch.int32)
+    if group <= 0 or K % group != 0:
+        raise ValueError(f"K={K} must be a multiple of group={group}")
+    _check_tensor("scales", scales, torch.bfloat16, (N, K // group))
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=qweight.device)
+    _check_tensor("out", out, torch.float32, (N, K))
+    lib = _lib.load()
+    st = lib.fd_w4_dequant_debug(
+        _ptr(qweight), _ptr(scales), _ptr(out), int(K), int(N), int(group),
+        _stream_handle(stream),
+    )
+    _lib.check(st)
+    return out
+
+
+def decode_mlp_step(
+    x: torch.Tensor,
+    residual: torch.Tensor,
+    layers: list[dict],
+    eps: float,
+    group: int = 128,
+    normed: list[torch.Tensor] | None = None,
+    y: list[torch.Tensor] | None = None,
+    stream: torch.cuda.Stream | None = None,
+) -> tuple[torch.Tensor, torch.Tensor]:
+    """One decode step over L layers of ("09 - Operator fusion", "The fusion boundary
+    problem"): (normed_l, residual) = add_rmsnorm(x_l, residual); y_l = down(g_l, u_l);
+    x_{l+1} = y_l. Two kernel launches per layer, in stream order; ``residual`` is
+    updated in place. ``layers`` holds per-layer device tensors ``rms_weight``, ``gate``,
+    ``up``, ``qweight``, ``scales``. ``normed``/``y`` are optional preallocated outputs
+    (one [1, hidden] tensor per layer) so the step allocates nothing and can be captured
+    in a CUDA graph. Returns (x_L, residual).
+    """
+    cur = x
+    for i, layer in enumerate(layers):
+        n_out = normed[i] if normed is not None else None
+        n_out, _ = add_rmsnorm(cur, residual, layer["rms_weight"], eps, out=n_out,
+                               residual_out=residual, stream=stream)
+        y_out = y[i] if y is not None else None
+        cur = swiglu_w4a16_gemv(layer["gate"], layer["up"], layer["qweight"], layer["scales"],
+                                out=y_out, group=group, stream=stream)
+    return cur, residual

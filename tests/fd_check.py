@@ -1,0 +1,121 @@
+"""Shared helpers of the GPU parity tests: host<->device marshalling of bf16 bit patterns
+and the comparisons against the oracle.
+
+Tolerances
+  * Stated bar (both kernels): max |y - ref| <= 2e-2 * max |ref| and mean relative error
+    sum |y - ref| / sum |ref| <= 4e-3, per output tensor (ref in float64).
+  * GEMV, elementwise bound derived from the kernel's arithmetic: the fp32 result differs
+    from the exact sum by at most delta = 64 * 2^-24 * sum_k |a_k| |W_nk| (silu and the
+    product a = silu(g) * u within ~5 ulp, at most ~41 dependent fp32 roundings in the
+    per-vector chains, the scale FMA, the 5-level warp butterfly and the cross-warp sum,
+    rounded up to 64); the single bf16 rounding adds at most 2^-8 of the value. So
+    |y - ref| <= 2^-8 * |ref| + 1.01 * delta.
+  * add-RMSNorm: residual_out bit-exact; out within one bf16 step of the oracle's
+    two-rounding form (the page's criterion), and within the stated bar of the unrounded
+    float64 form.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+
+def dev_bf16(bits, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def dev_i32(words, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(words)).to(device)
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def bf16_f64(bits) -> np.ndarray:
+    return oracle.bf16_to_f32(bits).astype(np.float64)
+
+
+def stated_bar(y: np.ndarray, ref: np.ndarray, max_abs_rel=2e-2, mean_rel=4e-3) -> dict:
+    err = np.abs(y - ref)
+    scale = np.max(np.abs(ref))
+    res = {
+        "max_abs_err": float(err.max(initial=0.0)),
+        "max_abs_ref": float(scale),
+        "mean_rel_err": float(err.sum() / max(np.abs(ref).sum(), 1e-300)),
+    }
+    assert res["max_abs_err"] <= max_abs_rel * scale, res
+    assert res["mean_rel_err"] <= mean_rel, res
+    return res
+
+
+def gemv_reference(gate, up, qweight, scales, group, rows=None):
+    """(ref [M, n], abs_sum [M, n]) for all or the selected weight rows."""
+    if rows is not None:
+        qweight = qweight[rows]
+        scales = scales[rows]
+    ref = oracle.swiglu_w4a16_gemv(gate, up, qweight, scales, group)
+    a = np.abs(oracle.swiglu_activation(gate, up))
+    if a.ndim == 1:
+        a = a[None, :]
+    w = np.abs(oracle.dequant_w4(qweight, scales, group).astype(np.float64))
+    return ref, a @ w.T
+
+
+def check_gemv(y_bits, gate, up, qweight, scales, group, rows=None) -> dict:
+    ref, abs_sum = gemv_reference(gate, up, qweight, scales, group, rows)
+    y = bf16_f64(y_bits)
+    if rows is not None:
+        y = y[:, rows]
+    res = stated_bar(y, ref)
+    delta = 64 * 2.0**-24 * abs_sum
+    bound = 2.0**-8 * np.abs(ref) + 1.01 * delta
+    err = np.abs(y - ref)
+    bad = err > bound
+    assert not bad.any(), (
+        f"{int(bad.sum())} outputs outside the derived bound; worst excess "
+        f"{float((err - bound).max())}"
+    )
+    res["n_checked"] = int(y.size)
+    return res
+
+
+def ordered_key(bits) -> np.ndarray:
+    """bf16 bit patterns -> integers whose order is the numeric order (adjacent values
+    differ by 1; +0 and -0 both map to 0)."""
+    b = np.asarray(bits).astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def check_add_rmsnorm(out_bits, res_bits, x, residual, weight, eps) -> dict:
+    h_ref, y_ref, y_eager = oracle.add_rmsnorm(x, residual, weight, eps)
+    assert np.array_equal(res_bits, h_ref), "residual_out is not bit-exact"
+    res = stated_bar(bf16_f64(out_bits), y_ref)
+    steps = np.abs(ordered_key(out_bits) - ordered_key(y_eager))
+    res["max_bf16_steps"] = int(steps.max(initial=0))
+    res["frac_exact"] = float(np.mean(steps == 0))
+    assert res["max_bf16_steps"] <= 1, res
+    return res
+
+
+class GuardedBuffer:
+    """A device buffer with sentinel-filled guard bands before and after the payload."""
+
+    GUARD = 256  # elements on each side (512 bytes for bf16)
+
+    def __init__(self, shape, dtype=torch.bfloat16, device="cuda", sentinel=-12345):
+        n = int(np.prod(shape))
+        self.raw = torch.empty(n + 2 * self.GUARD, dtype=dtype, device=device)
+        self.raw.view(torch.int16 if dtype == torch.bfloat16 else dtype).fill_(sentinel)
+        self.sentinel = sentinel
+        self.tensor = self.raw[self.GUARD:self.GUARD + n].view(shape)
+
+    def guards_intact(self) -> bool:
+        v = self.raw.view(torch.int16) if self.raw.dtype == torch.bfloat16 else self.raw
+        head = v[: self.GUARD]
+        tail = v[-self.GUARD:]
+        return bool((head == self.sentinel).all() and (tail == self.sentinel).all())

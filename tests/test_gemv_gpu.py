@@ -1,0 +1,204 @@
+"""GPU parity of fd_swiglu_w4a16_gemv and fd_w4_dequant_debug against the CPU oracle,
+called through the C ABI (via the ctypes binding) on seeded synthetic inputs."""
+
+import numpy as np
+import pytest
+import torch
+
+import memory_bound_decode_fd_gb300 as fd
+import oracle
+from memory_bound_decode_fd_gb300 import inputs
+from fd_check import GuardedBuffer, check_gemv, dev_bf16, dev_i32, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gemv(d, out=None):
+    g, u = dev_bf16(d["gate"]), dev_bf16(d["up"])
+    q, s = dev_i32(d["qweight"]), dev_bf16(d["scales"])
+    y = fd.swiglu_w4a16_gemv(g, u, q, s, out=out, group=d["group"])
+    torch.cuda.synchronize()
+    return host_bits(y)
+
+
+# ------------------------------------------------------------------ dequant (bit-exact)
+
+@pytest.mark.parametrize("K,N,group,seed", [
+    (1024, 256, 128, 0),        # GEMV M=1 K=1024 N=256
+    (9216, 2560, 128, 2),       # GEMV M=1 K=9216 N=2560
+    (14336, 4096, 128, 3),      # down projection K=14336 N=4096
+    (96, 7, 32, 40),
+    (2048, 33, 2048, 41),
+])
+def test_dequant_bit_exact(cuda_device, K, N, group, seed):
+    d = inputs.gemv_inputs(1, K, N, group, seed=seed)
+    w = fd.w4_dequant_debug(dev_i32(d["qweight"]), dev_bf16(d["scales"]), group=group)
+    torch.cuda.synchronize()
+    ref = oracle.dequant_w4(d["qweight"], d["scales"], group)
+    got = w.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequant_every_nibble_every_position(cuda_device):
+    words = [(v << (4 * j)) & 0xFFFFFFFF for j in range(8) for v in range(16)]
+    qw = np.array(words, np.uint32).view(np.int32).reshape(32, 4)  # N=32, K=32
+    sc = inputs.to_bf16_bits(np.full((32, 1), 0.375))
+    w = fd.w4_dequant_debug(dev_i32(qw), dev_bf16(sc), group=32).cpu().numpy()
+    ref = oracle.dequant_w4(qw, sc, 32)
+    assert np.array_equal(w.view(np.uint32), ref.view(np.uint32))
+
+
+# ------------------------------------------------------------------ the workloads
+
+@pytest.mark.parametrize("M,K,N,seed", [
+    (1, 1024, 256, 0),      # GEMV M=1 K=1024 N=256, seed 0
+    (1, 9216, 2560, 2),     # GEMV M=1 K=9216 N=2560, seed 2 (94 MB unfused product)
+    (1, 14336, 4096, 3),    # down projection of the decode step
+])
+def test_gemv_workloads_full(cuda_device, M, K, N, seed):
+    d = inputs.gemv_inputs(M, K, N, 128, seed=seed)
+    y = run_gemv(d)
+    res = check_gemv(y, d["gate"], d["up"], d["qweight"], d["scales"], 128)
+    assert res["n_checked"] == M * N
+
+
+def test_gemv_batched_m64_sampled(cuda_device):
+    # Batched decode M=64, K=14336, N=4096 (seed 4): every output of 256 sampled rows.
+    d = inputs.batched_inputs()["gemv"]
+    y = run_gemv(d)
+    rows = np.sort(np.random.default_rng(99).choice(4096, 256, replace=False))
+    rows = np.unique(np.concatenate([rows, [0, 1, 4095]]))
+    check_gemv(y, d["gate"], d["up"], d["qweight"], d["scales"], 128, rows=rows)
+
+
+# ------------------------------------------------------------------ shapes and edges
+
+EDGE_SHAPES = [
+    # M, K, N, group
+    (1, 32, 1, 32),          # smallest: one vector position, one row
+    (1, 64, 3, 32),
+    (1, 1056, 1001, 32),     # 33 vector positions: a partial last warp; ragged rows
+    (1, 1024, 151, 128),     # fewer rows than SMs x chunk
+    (1, 1024, 153, 128),
+    (1, 4096, 1217, 64),     # rows not a multiple of 8 per CTA
+    (1, 9216, 2561, 128),
+    (1, 16384, 700, 128),    # largest K with one vector position per thread
+    (1, 16416, 300, 32),     # two vector positions per thread, partial
+    (1, 32768, 200, 128),    # largest K
+    (1, 2048, 64, 2048),     # one group spans K
+    (1, 1024, 64, 256),
+    (2, 1024, 300, 128),
+    (3, 1024, 300, 128),
+    (5, 2048, 257, 64),
+    (15, 1024, 300, 128),
+    (16, 1024, 300, 128),
+    (17, 4096, 300, 128),
+    (33, 1056, 99, 32),
+    (64, 2048, 512, 128),
+    (256, 1024, 128, 128),   # largest M
+    (3, 32768, 64, 128),     # M > 1 with two vector positions per thread
+]
+
+
+@pytest.mark.parametrize("M,K,N,group", EDGE_SHAPES)
+def test_gemv_edge_shapes(cuda_device, M, K, N, group):
+    d = inputs.gemv_inputs(M, K, N, group, seed=1000 + M + K + N)
+    y = run_gemv(d)
+    check_gemv(y, d["gate"], d["up"], d["qweight"], d["scales"], group)
+
+
+@pytest.mark.parametrize("n_star,k_star,qv", [(0, 0, 3), (2559, 9215, -8), (1234, 4097, 7), (77, 31, -1)])
+def test_gemv_one_hot_layout(cuda_device, n_star, k_star, qv):
+    # A single nonzero weight: every other output is exactly zero and the hot one is
+    # a[k*] * q * s rounded once (index mapping, nibble order and scale index).
+    M, K, N, group = 2, 9216, 2560, 128
+    rng = np.random.default_rng(5)
+    gate = inputs.normal_bf16(rng, (M, K))
+    up = inputs.normal_bf16(rng, (M, K))
+    q = np.zeros((N, K), np.int8)
+    q[n_star, k_star] = qv
+    s = np.full((N, K // group), 0.5)
+    s[n_star, k_star // group] = 0.75
+    d = {"gate": gate, "up": up, "qweight": fd.pack_int4(q), "scales": inputs.to_bf16_bits(s),
+         "group": group}
+    y = run_gemv(d)
+    yf = oracle.bf16_to_f32(y)
+    mask = np.ones((M, N), bool)
+    mask[:, n_star] = False
+    assert np.all(yf[mask] == 0.0)
+    check_gemv(y, gate, up, d["qweight"], d["scales"], group)
+
+
+def test_gemv_guard_bands_untouched(cuda_device):
+    d = inputs.gemv_inputs(3, 9216, 2561, 128, seed=7)
+    buf = GuardedBuffer((3, 2561))
+    run_gemv(d, out=buf.tensor)
+    assert buf.guards_intact()
+    check_gemv(host_bits(buf.tensor), d["gate"], d["up"], d["qweight"], d["scales"], 128)
+
+
+def test_gemv_allocates_nothing(cuda_device):
+    d = inputs.gemv_inputs(1, 9216, 2560, 128, seed=2)
+    g, u = dev_bf16(d["gate"]), dev_bf16(d["up"])
+    q, s = dev_i32(d["qweight"]), dev_bf16(d["scales"])
+    out = torch.empty((1, 2560), dtype=torch.bfloat16, device="cuda")
+    fd.swiglu_w4a16_gemv(g, u, q, s, out=out)  # first call loads the module
+    torch.cuda.synchronize()
+    before = torch.cuda.memory_allocated()
+    free_before, _ = torch.cuda.mem_get_info()
+    torch.cuda.reset_peak_memory_stats()
+    for _ in range(5):
+        fd.swiglu_w4a16_gemv(g, u, q, s, out=out)
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == before
+    assert torch.cuda.max_memory_allocated() == before
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before
+
+
+def test_gemv_deterministic_and_stream_ordered(cuda_device):
+    d = inputs.gemv_inputs(4, 4096, 1000, 128, seed=8)
+    g, u = dev_bf16(d["gate"]), dev_bf16(d["up"])
+    q, s = dev_i32(d["qweight"]), dev_bf16(d["scales"])
+    side = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            outs.append(fd.swiglu_w4a16_gemv(g, u, q, s))
+    side.synchronize()
+    base = host_bits(outs[0])
+    for o in outs[1:]:
+        assert np.array_equal(host_bits(o), base)
+    check_gemv(base, d["gate"], d["up"], d["qweight"], d["scales"], 128)
+
+
+def test_gemv_cuda_graph_replay_matches_eager(cuda_device):
+    d = inputs.gemv_inputs(1, 14336, 4096, 128, seed=3)
+    g, u = dev_bf16(d["gate"]), dev_bf16(d["up"])
+    q, s = dev_i32(d["qweight"]), dev_bf16(d["scales"])
+    eager = fd.swiglu_w4a16_gemv(g, u, q, s)
+    out = torch.empty_like(eager)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fd.swiglu_w4a16_gemv(g, u, q, s, out=out)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    out.zero_()
+    with torch.cuda.graph(graph):
+        fd.swiglu_w4a16_gemv(g, u, q, s, out=out)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(out), host_bits(eager))
+
+
+def test_gemv_rejects_misaligned_and_overlapping(cuda_device):
+    d = inputs.gemv_inputs(1, 1024, 256, 128, seed=0)
+    g = dev_bf16(np.concatenate([d["gate"].ravel(), np.zeros(8, np.uint16)]))
+    u, q, s = dev_bf16(d["up"]), dev_i32(d["qweight"]), dev_bf16(d["scales"])
+    with pytest.raises(fd.FdError) as e:
+        fd.swiglu_w4a16_gemv(g[1:1025].view(1, 1024), u, q, s)
+    assert e.value.status == fd.FD_ERR_ALIGN
+    with pytest.raises(fd.FdError) as e:
+        fd.swiglu_w4a16_gemv(g[:1024].view(1, 1024), u, q, s, out=u[:, :256])
+    assert e.value.status == fd.FD_ERR_OVERLAP
