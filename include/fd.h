@@ -105,6 +105,22 @@ int fd_add_rmsnorm(const void *x, const void *residual, const void *weight, floa
                    fd_stream_t stream);
 
 /*
+ * Kernel selection for fd_swiglu_w4a16_gemv (process-wide, thread-safe; default AUTO).
+ *   FD_GEMV_AUTO     the bulk-copy kernel where its layout rules hold (K % 1024 == 0,
+ *                    K <= 15360, (K / group) % 8 == 0), else the CUDA-core ring kernel.
+ *   FD_GEMV_CUDA_CORE  always the per-thread cp.async ring kernel (any valid shape).
+ *   FD_GEMV_BULK     the bulk-copy kernel where it applies, else the ring kernel.
+ * Results of every path meet the same accuracy bound; the choice exists for tests and
+ * for measuring one kernel against another. Returns FD_ERR_UNSUPPORTED for an unknown
+ * value.
+ */
+#define FD_GEMV_AUTO 0
+#define FD_GEMV_CUDA_CORE 1
+#define FD_GEMV_BULK 2
+int fd_set_gemv_path(int path);
+int fd_get_gemv_path(void);
+
+/*
  * fd_w4_dequant_debug - write the dequantised weights W[n, k] = q[n, k] * s[n, k/group]
  * as fp32 [N, K] (test support: the unpack and scale of the GEMV prologue, checked bit
  * for bit). Same layouts and size rules as fd_swiglu_w4a16_gemv; `out` is fp32 [N, K].

@@ -26,7 +26,14 @@ from ._lib import (  # noqa: F401
     status_string,
 )
 from ._lib import load as load_library  # noqa: F401
-from .kernels import add_rmsnorm, decode_mlp_step, swiglu_w4a16_gemv, w4_dequant_debug  # noqa: F401
+from .kernels import (  # noqa: F401
+    GEMV_PATHS,
+    add_rmsnorm,
+    decode_mlp_step,
+    set_gemv_path,
+    swiglu_w4a16_gemv,
+    w4_dequant_debug,
+)
 from .packing import pack_int4  # noqa: F401
 from .traffic import add_rmsnorm_bytes, decode_step_bytes, gemv_bytes, gemv_flops  # noqa: F401
 

@@ -16,6 +16,10 @@ FD_ERR_UNSUPPORTED = 4
 FD_ERR_CUDA = 5
 FD_ERR_OVERLAP = 6
 
+FD_GEMV_AUTO = 0
+FD_GEMV_CUDA_CORE = 1
+FD_GEMV_BULK = 2
+
 FD_MAX_K = 32768
 FD_MAX_M = 256
 FD_MAX_HIDDEN = 32768
@@ -30,6 +34,8 @@ SIGNATURES = {
     "fd_status_string": (ctypes.c_char_p, [_I]),
     "fd_last_cuda_error": (_I, []),
     "fd_version": (_I, []),
+    "fd_set_gemv_path": (_I, [_I]),
+    "fd_get_gemv_path": (_I, []),
 }
 
 

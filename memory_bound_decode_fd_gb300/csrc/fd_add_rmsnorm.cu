@@ -50,6 +50,17 @@ __global__ void __launch_bounds__(VPT >= 8 ? 512 : 256)
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
     int parity = 0;
+    // Every row is scaled by the same weight: with up to 4 vectors per thread the weight
+    // lives in registers for the whole kernel, loaded once, alongside the first row.
+    constexpr bool kWeightInRegs = VPT <= 4;
+    uint4 wreg[kWeightInRegs ? VPT : 1];
+    if (kWeightInRegs) {
+#pragma unroll
+        for (int i = 0; i < (kWeightInRegs ? VPT : 1); ++i) {
+            const int v = tid + i * T;
+            if (v < nvec) wreg[i] = ld_v4(weight + v, pol_keep);
+        }
+    }
 
     for (int row = blockIdx.x; row < rows; row += gridDim.x) {
         const size_t base = (size_t)row * nvec;
@@ -95,7 +106,7 @@ __global__ void __launch_bounds__(VPT >= 8 ? 512 : 256)
         for (int i = 0; i < VPT; ++i) {
             const int v = tid + i * T;
             if (v < nvec) {
-                const uint4 wv = ld_v4(weight + v, pol_keep);
+                const uint4 wv = kWeightInRegs ? wreg[kWeightInRegs ? i : 0] : ld_v4(weight + v, pol_keep);
                 const uint32_t hw[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
                 const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
                 uint32_t yw[4];

@@ -16,6 +16,7 @@ constexpr int kMaxDevices = 64;
 std::atomic<int> g_info_ready[kMaxDevices];
 DeviceInfo g_info[kMaxDevices];
 thread_local int g_last_cuda_error = 0;
+std::atomic<int> g_gemv_path{FD_GEMV_AUTO};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -87,9 +88,24 @@ int fd_swiglu_w4a16_gemv(const void *gate, const void *up, const void *qweight,
     if (overlaps(out, out_bytes, gate, act_bytes) || overlaps(out, out_bytes, up, act_bytes) ||
         overlaps(out, out_bytes, qweight, w_bytes) || overlaps(out, out_bytes, scales, s_bytes))
         return FD_ERR_OVERLAP;
-    return from_cuda(launch_gemv_cc(gate, up, qweight, scales, out, M, K, N, group,
-                                    reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+    const int path = g_gemv_path.load(std::memory_order_relaxed);
+    if (path == FD_GEMV_AUTO || path == FD_GEMV_BULK) {
+        bool launched = false;
+        cudaError_t err = launch_gemv_tma(gate, up, qweight, scales, out, M, K, N, group, st_,
+                                          &launched);
+        if (err != cudaSuccess || launched) return from_cuda(err);
+    }
+    return from_cuda(launch_gemv_cc(gate, up, qweight, scales, out, M, K, N, group, st_));
 }
+
+int fd_set_gemv_path(int path) {
+    if (path < FD_GEMV_AUTO || path > FD_GEMV_BULK) return FD_ERR_UNSUPPORTED;
+    g_gemv_path.store(path, std::memory_order_relaxed);
+    return FD_OK;
+}
+
+int fd_get_gemv_path(void) { return g_gemv_path.load(std::memory_order_relaxed); }
 
 int fd_add_rmsnorm(const void *x, const void *residual, const void *weight, float eps,
                    void *out, void *residual_out, int rows, int hidden, fd_stream_t stream) {

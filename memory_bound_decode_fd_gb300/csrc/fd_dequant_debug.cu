@@ -1,7 +1,8 @@
-// fd_dequant_debug.cu - writes W[n, k] = q[n, k] * s[n, k / group] as fp32, using the
-// same int4 -> fp32 conversion as the GEMV prologue ("09 - Operator fusion", section 5,
-// taxonomy item 4: dequantize weights -> matmul). Test support: the result is compared
-// bit for bit with the CPU oracle's dequantised weights.
+// fd_dequant_debug.cu - writes W[n, k] = q[n, k] * s[n, k / group] as fp32, reading the
+// nibbles through the same byte split the GEMV kernels feed to their dot-product unit
+// ("09 - Operator fusion", section 5, taxonomy item 4: dequantize weights -> matmul).
+// Test support: the result is compared bit for bit with the CPU oracle's dequantised
+// weights, which pins nibble order, sign handling and scale indexing of the GEMV.
 #include "fd_internal.h"
 #include "fd_w4_unpack.cuh"
 
@@ -15,6 +16,7 @@ __global__ void w4_dequant_kernel(const uint32_t *__restrict__ qweight,
     const size_t words_per_row = (size_t)K / 8;
     const size_t total = words_per_row * (size_t)N;
     const int ngroups = K / group;
+    const W4Keys keys = w4_keys();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
         const size_t n = i / words_per_row;
@@ -22,11 +24,14 @@ __global__ void w4_dequant_kernel(const uint32_t *__restrict__ qweight,
         const size_t k0 = p * 8;
         const uint16_t sbits = scales[n * ngroups + k0 / group];
         const float s = __uint_as_float((uint32_t)sbits << 16);
-        float2 q[4];
-        unpack_w4_f32x2(qweight[i], q);
+        uint32_t L, H;
+        split_w4(qweight[i], keys, L, H);
+        float q[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) q[j] = (float)q_from_split(L, H, j) * s;
         float4 *dst = reinterpret_cast<float4 *>(out + n * (size_t)K + k0);
-        dst[0] = make_float4(q[0].x * s, q[0].y * s, q[1].x * s, q[1].y * s);
-        dst[1] = make_float4(q[2].x * s, q[2].y * s, q[3].x * s, q[3].y * s);
+        dst[0] = make_float4(q[0], q[1], q[2], q[3]);
+        dst[1] = make_float4(q[4], q[5], q[6], q[7]);
     }
 }
 

@@ -13,15 +13,15 @@
 //   * Thread t of a CTA owns the weight vector positions p = t + v * T (v < VPT) of every
 //     row: each position is 16 bytes = 4 words = 32 consecutive k, inside one scale group.
 //     So thread t needs a[m, k] only for its own k, and computes silu(g) * u once per
-//     m-chunk straight into registers (fp32). Nothing is staged through HBM.
+//     m-chunk straight into registers. Nothing is staged through HBM.
 //   * The CTA owns a contiguous range of output rows n; it walks them in chunks of R rows.
 //     Each thread streams its own 16-byte slot of each row (and the 2-byte scale that
 //     belongs to it) with cp.async into a private ring of S stages in shared memory, S - 1
 //     chunks ahead of the math. Slots are thread-private, so the ring needs no barriers:
 //     cp.async.wait_group orders each thread's own copies.
-//   * Math per 32-bit word: 8 lop3 + 1 shift + 4 packed fp32x2 adds (exact int4 -> fp32,
-//     see fd_w4_unpack.cuh) + 4 packed fp32x2 FMAs; fp32 accumulation; the group scale
-//     multiplies the 32-k partial.
+//   * Math per 32-bit word: 2 lop3 (even/odd nibble bytes, fd_w4_unpack.cuh) + 4 dp2a
+//     against the block-scaled int16 activations (fd_gemv_common.cuh), exact int32 sums
+//     per 32-k slice; the activation and group scales multiply the slice's sum.
 //   * Reduction: each lane holds R x MB partials per chunk; a butterfly reduce-scatter
 //     over the warp (V - 1 + log2(32 / V) shuffles for V values) leaves one warp sum per
 //     (row, m) in shared memory; the CTA sums over warps and stores bf16 once per output.
@@ -30,12 +30,10 @@
 #include <atomic>
 
 #include "fd_internal.h"
-#include "fd_w4_unpack.cuh"
+#include "fd_gemv_common.cuh"
 
 namespace fd {
 namespace {
-
-constexpr int kWindowRows = 64;  // rows whose per-warp partials are held before a flush
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -63,85 +61,6 @@ __device__ __forceinline__ void cp_async_commit() {
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// a = silu(g) * u for the 32 k of one weight vector position, as 16 float2 pairs
-// ordered (k0,k1) (k2,k3) ... to match unpack_w4_f32x2.
-__device__ __forceinline__ void load_activation(const uint16_t *__restrict__ gate,
-                                                const uint16_t *__restrict__ up,
-                                                size_t offset, float2 a[16]) {
-    const uint4 *g4 = reinterpret_cast<const uint4 *>(gate + offset);
-    const uint4 *u4 = reinterpret_cast<const uint4 *>(up + offset);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint4 gv = g4[i];
-        const uint4 uv = u4[i];
-        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-        const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float g0 = bf16lo(gw[j]), g1 = bf16hi(gw[j]);
-            const float s0 = g0 / (1.0f + expf(-g0));
-            const float s1 = g1 / (1.0f + expf(-g1));
-            a[4 * i + j] = make_float2(s0 * bf16lo(uw[j]), s1 * bf16hi(uw[j]));
-        }
-    }
-}
-
-// For MB activation rows: d[mb] = sum over the 32 k of one vector position of
-// a[mb][k] * q[k] (fp32, two packed chains per row). The word is unpacked once.
-template <int MB>
-__device__ __forceinline__ void dot32(const float2 (*a)[16], uint4 wv, float d[MB]) {
-    const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-    float2 acc0[MB], acc1[MB];
-#pragma unroll
-    for (int mb = 0; mb < MB; ++mb) {
-        acc0[mb] = make_float2(0.f, 0.f);
-        acc1[mb] = make_float2(0.f, 0.f);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 q[4];
-        unpack_w4_f32x2(w[i], q);
-#pragma unroll
-        for (int mb = 0; mb < MB; ++mb) {
-            acc0[mb] = ffma2(a[mb][4 * i + 0], q[0], acc0[mb]);
-            acc1[mb] = ffma2(a[mb][4 * i + 1], q[1], acc1[mb]);
-            acc0[mb] = ffma2(a[mb][4 * i + 2], q[2], acc0[mb]);
-            acc1[mb] = ffma2(a[mb][4 * i + 3], q[3], acc1[mb]);
-        }
-    }
-#pragma unroll
-    for (int mb = 0; mb < MB; ++mb) {
-        const float2 s = fadd2(acc0[mb], acc1[mb]);
-        d[mb] = s.x + s.y;
-    }
-}
-
-__host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v >> 1); }
-
-// Butterfly reduce-scatter of V values over a warp. On return, lane l holds in v[0] the
-// warp-wide sum of value index (l >> (5 - log2 V)).
-template <int V>
-__device__ __forceinline__ float warp_reduce_scatter(float (&v)[V], int lane) {
-#pragma unroll
-    for (int width = V; width > 1; width >>= 1) {
-        const int half = width >> 1;
-        // offset for this stage: 16, 8, ... (one bit of the lane index per halving)
-        const int offset = 16 >> (ilog2(V) - ilog2(width));
-        const bool upper = (lane & offset) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float send = upper ? v[i] : v[i + half];
-            const float keep = upper ? v[i + half] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, offset);
-        }
-    }
-    float r = v[0];
-#pragma unroll
-    for (int offset = 16 >> ilog2(V); offset > 0; offset >>= 1)
-        r += __shfl_xor_sync(0xFFFFFFFFu, r, offset);
-    return r;
 }
 
 // Shared memory layout (dynamic):
@@ -218,7 +137,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
     for (int c = 0; c < S - 1; ++c) issue(c);
 
-    float2 a[VPT][MB][16];
+    const W4Keys keys = w4_keys();
+    Act16 act[VPT][MB];
     int window_base = 0;  // first local row of the current flush window
 
     for (int c = 0; c < total; ++c) {
@@ -233,13 +153,11 @@ __global__ void __launch_bounds__(512, 1)
             for (int mb = 0; mb < MB; ++mb) {
 #pragma unroll
                 for (int v = 0; v < VPT; ++v) {
-                    if (active[v] && m0 + mb < M) {
-                        load_activation(gate, up, (size_t)(m0 + mb) * K + (size_t)pos[v] * 32,
-                                        a[v][mb]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) a[v][mb][i] = make_float2(0.f, 0.f);
-                    }
+                    if (active[v] && m0 + mb < M)
+                        load_activation_q16(gate, up, (size_t)(m0 + mb) * K + (size_t)pos[v] * 32,
+                                            act[v][mb]);
+                    else
+                        zero_activation(act[v][mb]);
                 }
             }
         }
@@ -261,10 +179,9 @@ __global__ void __launch_bounds__(512, 1)
                 const size_t sidx = (size_t)(n_begin + nc * R + r) * ngroups + sidx_col[v];
                 const float s = (sidx & 1) ? bf16hi(sw) : bf16lo(sw);
                 float d[MB];
-                dot32<MB>(a[v], wv, d);
+                dot32<MB>(act[v], wv, keys, s, d);
 #pragma unroll
-                for (int mb = 0; mb < MB; ++mb)
-                    part[r * MB + mb] = fmaf(s, d[mb], part[r * MB + mb]);
+                for (int mb = 0; mb < MB; ++mb) part[r * MB + mb] += d[mb];
             }
         }
 
@@ -311,7 +228,8 @@ int threads_for(int K, int VPT) {
     return (T + 31) / 32 * 32;
 }
 
-// Raises the kernel's dynamic shared memory limit once per device.
+// Raises the kernel's dynamic shared memory limit once per device (to the opt-in limit
+// less the kernel's static shared memory).
 template <typename Kern>
 cudaError_t ensure_smem_attr(Kern kern, size_t smem, std::atomic<uint64_t> &done) {
     int dev = 0;
@@ -322,9 +240,13 @@ cudaError_t ensure_smem_attr(Kern kern, size_t smem, std::atomic<uint64_t> &done
     int max_optin = 0;
     err = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, kern);
     if (err != cudaSuccess) return err;
-    (void)smem;
+    const int limit = max_optin - (int)fa.sharedSizeBytes;
+    if ((size_t)limit < smem) return cudaErrorInvalidConfiguration;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+    if (err != cudaSuccess) return err;
     done.fetch_or(bit, std::memory_order_acq_rel);
     return cudaSuccess;
 }

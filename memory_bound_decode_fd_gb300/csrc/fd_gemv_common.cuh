@@ -1,0 +1,193 @@
+// fd_gemv_common.cuh - device pieces shared by the two SwiGLU-W4A16 GEMV kernels: the
+// SwiGLU prologue into registers, the 32-k integer dot product, and the warp
+// reduce-scatter.
+//
+// Numerics of one 32-k slice (one 16-byte weight vector position, inside one scale
+// group):
+//   a_k = silu(g_k) * u_k in fp32 (fast exp, Newton reciprocal), k in the slice;
+//   a_k is encoded as a16_k = rint(a_k * 32767 / amax) with amax = max |a_k| over the
+//   slice (a block-scaled 16-bit integer: 15 magnitude bits against bf16's 8), and
+//   a_k ~= a16_k * scale, scale = amax / 32767;
+//   sum_k a16_k q_k is formed EXACTLY in int32 with the dp2a integer dot-product
+//   instruction (16-bit x 8-bit products), from the byte split of fd_w4_unpack.cuh;
+//   the slice's contribution to y[n] is float(that sum) * (scale * s[n, group]).
+// The only error beyond fp32 rounding is the 16-bit encoding of a, at most
+// amax / 65534 per element.
+#pragma once
+
+#include "fd_internal.h"
+#include "fd_w4_unpack.cuh"
+
+namespace fd {
+
+constexpr int kWindowRows = 64;  // rows whose per-warp partials are held before a flush
+
+// One thread's activation slice (32 k) for one activation row, in the operand layout of
+// dp2a: for word i (k = 8i .. 8i+7 of the slice),
+//   e[i] = (a16[8i+0], a16[8i+2]), f[i] = (a16[8i+4], a16[8i+6])  pair with L's bytes
+//   g[i] = (a16[8i+1], a16[8i+3]), h[i] = (a16[8i+5], a16[8i+7])  pair with H's bytes
+// init_lo / init_hi remove the +8 offset of the nibbles (u = q + 8):
+//   sum a16 u_even = sum a16 q_even + 8 S_even;  sum a16 16 u_odd = 16 sum a16 q_odd + 128 S_odd.
+struct Act16 {
+    uint32_t e[4], f[4], g[4], h[4];
+    int init_lo, init_hi;
+    float scale;
+};
+
+__device__ __forceinline__ uint32_t pack16(int lo, int hi) {
+    return __byte_perm((uint32_t)lo, (uint32_t)hi, 0x5410);
+}
+
+// Round-to-nearest-even float -> int for |x| < 2^22 with two fast-pipe instructions.
+__device__ __forceinline__ int rint_small(float x) {
+    return (int)(__float_as_uint(x + 12582912.0f) - 0x4B400000u);
+}
+
+// Raw bf16 gate/up of one 32-element slice (issued early so the loads overlap set-up).
+struct GateUp {
+    uint4 g[4], u[4];
+};
+
+__device__ __forceinline__ void load_gate_up(const uint16_t *__restrict__ gate,
+                                             const uint16_t *__restrict__ up, size_t offset,
+                                             GateUp &gu) {
+    const uint4 *g4 = reinterpret_cast<const uint4 *>(gate + offset);
+    const uint4 *u4 = reinterpret_cast<const uint4 *>(up + offset);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        gu.g[i] = g4[i];
+        gu.u[i] = u4[i];
+    }
+}
+
+// silu(g) * u in fp32. exp runs on the MUFU unit; r = 1 / (1 + e) is computed on the
+// FMA/ALU pipes by Newton's iteration r' = r (2 - d r), seeded from the bit pattern of d
+// (an integer subtraction from 0x7EF311C7 gives a seed within 5.1% of 1/d in every
+// binade; each step squares the relative error: 5.1e-2 -> 2.6e-3 -> 6.7e-6 -> ~5e-11,
+// below fp32 rounding), so the prologue issues one MUFU operation per element, not two.
+// g is clamped at -60 so 1 + e stays finite (silu(-60) is below 1e-24).
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    const float gc = fmaxf(g, -60.0f);
+    const float d = 1.0f + __expf(-gc);
+    float r = __uint_as_float(0x7EF311C7u - __float_as_uint(d));
+    r = r * fmaf(-d, r, 2.0f);
+    r = r * fmaf(-d, r, 2.0f);
+    r = r * fmaf(-d, r, 2.0f);
+    return g * r * u;
+}
+
+// Encodes one slice (see Act16).
+__device__ __forceinline__ void encode_q16(const GateUp &gu, Act16 &act) {
+    float a[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t gw[4] = {gu.g[i].x, gu.g[i].y, gu.g[i].z, gu.g[i].w};
+        const uint32_t uw[4] = {gu.u[i].x, gu.u[i].y, gu.u[i].z, gu.u[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            a[8 * i + 2 * j] = silu_mul(bf16lo(gw[j]), bf16lo(uw[j]));
+            a[8 * i + 2 * j + 1] = silu_mul(bf16hi(gw[j]), bf16hi(uw[j]));
+        }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(a[k]));
+    const float s_inv = amax > 0.f ? 32767.0f / amax : 0.f;
+    act.scale = amax * (1.0f / 32767.0f);
+    int q[32];
+    int s_even = 0, s_odd = 0;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        q[k] = rint_small(a[k] * s_inv);
+        if (k & 1) s_odd += q[k]; else s_even += q[k];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        act.e[i] = pack16(q[8 * i + 0], q[8 * i + 2]);
+        act.f[i] = pack16(q[8 * i + 4], q[8 * i + 6]);
+        act.g[i] = pack16(q[8 * i + 1], q[8 * i + 3]);
+        act.h[i] = pack16(q[8 * i + 5], q[8 * i + 7]);
+    }
+    act.init_lo = -8 * s_even;
+    act.init_hi = -128 * s_odd;
+}
+
+// Builds the slice's Act16 from bf16 gate/up at element `offset` (32 elements).
+__device__ __forceinline__ void load_activation_q16(const uint16_t *__restrict__ gate,
+                                                    const uint16_t *__restrict__ up,
+                                                    size_t offset, Act16 &act) {
+    GateUp gu;
+    load_gate_up(gate, up, offset, gu);
+    encode_q16(gu, act);
+}
+
+__device__ __forceinline__ void zero_activation(Act16 &act) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) act.e[i] = act.f[i] = act.g[i] = act.h[i] = 0u;
+    act.init_lo = act.init_hi = 0;
+    act.scale = 0.f;
+}
+
+__device__ __forceinline__ int dp2a_lo(uint32_t a16x2, uint32_t bytes, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a16x2), "r"(bytes), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a16x2, uint32_t bytes, int c) {
+    int d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a16x2), "r"(bytes), "r"(c));
+    return d;
+}
+
+// Exact sum over the 32 k of one weight vector of a16_k * q_k.
+__device__ __forceinline__ int dot32_q16(const Act16 &act, uint4 wv, const W4Keys &keys) {
+    const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+    int lo = act.init_lo, hi = act.init_hi;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t L, H;
+        split_w4(w[i], keys, L, H);
+        lo = dp2a_lo(act.e[i], L, lo);
+        hi = dp2a_lo(act.g[i], H, hi);
+        lo = dp2a_hi(act.f[i], L, lo);
+        hi = dp2a_hi(act.h[i], H, hi);
+    }
+    return lo + (hi >> 4);
+}
+
+// For MB activation rows: d[mb] = fp32 contribution of this vector position.
+template <int MB>
+__device__ __forceinline__ void dot32(const Act16 *act, uint4 wv, const W4Keys &keys,
+                                      float group_scale, float d[MB]) {
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb)
+        d[mb] = (float)dot32_q16(act[mb], wv, keys) * (act[mb].scale * group_scale);
+}
+
+__host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v >> 1); }
+
+// Butterfly reduce-scatter of V values over a warp. On return, lane l holds in v[0] the
+// warp-wide sum of value index (l >> (5 - log2 V)).
+template <int V>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[V], int lane) {
+#pragma unroll
+    for (int width = V; width > 1; width >>= 1) {
+        const int half = width >> 1;
+        // offset for this stage: 16, 8, ... (one bit of the lane index per halving)
+        const int offset = 16 >> (ilog2(V) - ilog2(width));
+        const bool upper = (lane & offset) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, offset);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int offset = 16 >> ilog2(V); offset > 0; offset >>= 1)
+        r += __shfl_xor_sync(0xFFFFFFFFu, r, offset);
+    return r;
+}
+
+}  // namespace fd

@@ -1,0 +1,358 @@
+// fd_gemv_tma.cu - SwiGLU-prologue W4A16 GEMV, bulk-copy (TMA) weight stream.
+//
+// y[m, n] = bf16( sum_k silu(g[m, k]) * u[m, k] * q[n, k] * s[n, k / group] )
+//
+// Sources: "09 - Operator fusion", section 5 (taxonomy item 4: dequantisation as the
+// weights are loaded, only int4 crosses HBM; "The fusion boundary problem": act =
+// silu(gate) * up feeds act @ W_down); "PyTorch Community Proposes Fusion Fix ..."
+// ("Reproduction and analysis", "Fix proposal": the M = 1 product is never materialised,
+// the small input a = silu(g) * u is formed first - here in registers).
+//
+// The fast path for K % 1024 == 0, K <= 15360 and (K / group) % 8 == 0 (every
+// decode shape of interest). Design for GB300:
+//   * One persistent CTA per SM owning a contiguous range of output rows n.
+//   * Warp specialisation: the last warp is a producer whose lane 0 streams chunks of 4
+//     consecutive weight rows (4 * K/2 bytes, one contiguous bulk copy) and their scales
+//     (4 * K/group * 2 bytes, a second bulk copy) into an S-stage (up to 8) shared-memory
+//     ring, completion tracked by "full" mbarriers; consumers release a stage through an
+//     "empty" mbarrier (one arrival per consumer warp). At the decode shapes the ring
+//     holds every row the CTA owns (~200 KB per SM), so the whole weight stream is in
+//     flight from the first cycle and no refill waits on the math.
+//   * Consumer thread t (K/32 of them) owns 32 consecutive k: a = silu(g) * u for its k
+//     lives in registers as block-scaled int16 (fd_gemv_common.cuh); per row it reads its
+//     16-byte slot (conflict-free), splits each word into even/odd nibble bytes (2 lop3)
+//     and accumulates exactly in int32 with 4 dp2a per word; the 32-k sum is converted
+//     once and scaled by the activation and group scales.
+//   * Per chunk a butterfly reduce-scatter leaves one warp sum per (row, m) in shared
+//     memory; every 64 rows the consumers sum over warps and store bf16 once per output.
+//   * Every mbarrier wait is bounded (fd_tma.cuh). If one gives up, the CTA stops
+//     computing, waits (bounded) for the copies it issued, writes NaN to all of its
+//     outputs (so the failure is visible to the caller) and exits.
+#include <atomic>
+
+#include "fd_gemv_common.cuh"
+#include "fd_tma.cuh"
+
+namespace fd {
+namespace {
+
+constexpr int kMaxStages = 8;
+constexpr int kChunkRows = 4;  // rows per bulk-copy chunk
+
+// NVEC_C / NG_C: compile-time K/32 and K/group for the common shapes (0 = runtime), so
+// the per-row shared-memory offsets fold into instruction immediates.
+//
+// Shared memory: S ring stages of R weight rows + their scales, then the per-warp
+// partial sums. With one activation row (M == 1) the producer first bulk-copies gate and
+// up (2 * K * 2 bytes) into the space of the last ring stages, ahead of the weight
+// stream, so the consumers' activation reads do not queue behind it; those stages are
+// filled with weights only after every consumer warp has encoded its slice.
+template <int MB, int R, int NVEC_C, int NG_C>
+__global__ void __launch_bounds__(512, 1)
+    gemv_tma_kernel(const uint16_t *__restrict__ gate, const uint16_t *__restrict__ up,
+                    const unsigned char *__restrict__ qweight,
+                    const uint16_t *__restrict__ scales, uint16_t *__restrict__ out, int M,
+                    int K, int N, int group, int rows_base, int rows_extra, int S,
+                    int act_stages, int weights_evict_first) {
+    static_assert(R * MB <= 32 && (R * MB & (R * MB - 1)) == 0, "R*MB: power of 2, <= 32");
+    static_assert(kWindowRows % R == 0, "window must hold whole chunks");
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t act_full_bar;
+    __shared__ __align__(8) uint64_t act_free_bar;
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nvec = NVEC_C ? NVEC_C : (K >> 5);  // consumer threads, a multiple of 32
+    const int ncw = nvec >> 5;                     // consumer warps
+    const int ngroups = NG_C ? NG_C : K / group;
+    const uint32_t w_row_bytes = (uint32_t)nvec * 16;
+    const uint32_t s_row_bytes = (uint32_t)ngroups * 2;
+    const uint32_t stage_bytes = (uint32_t)R * (w_row_bytes + s_row_bytes);
+    float *red = reinterpret_cast<float *>(smem + (size_t)S * stage_bytes);
+    // gate then up, each K bf16, in the last act_stages stages (M == 1 only)
+    const bool act_in_smem = (M == 1);
+    uint16_t *act_smem = reinterpret_cast<uint16_t *>(smem + (size_t)(S - act_stages) * stage_bytes);
+
+    const int b = blockIdx.x;
+    const int n_begin = b * rows_base + min(b, rows_extra);
+    const int n_cnt = rows_base + (b < rows_extra ? 1 : 0);
+    const int n_chunks = (n_cnt + R - 1) / R;
+    const int m_chunks = (M + MB - 1) / MB;
+    const int total = n_chunks * m_chunks;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], ncw);
+        }
+        mbar_init(&act_full_bar, 1);
+        mbar_init(&act_free_bar, ncw);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == ncw) {
+        // ------------------------------------------------------------ producer warp
+        if (lane == 0) {
+            const uint64_t pol_w = weights_evict_first ? policy_evict_first() : policy_evict_last();
+            const uint64_t pol_s = policy_evict_first();
+            if (act_in_smem) {
+                const uint32_t ab = (uint32_t)K * 2;
+                mbar_arrive_expect_tx(&act_full_bar, 2 * ab);
+                bulk_g2s(act_smem, gate, ab, &act_full_bar, pol_s);
+                bulk_g2s(act_smem + K, up, ab, &act_full_bar, pol_s);
+            }
+            int issued = 0;
+            int s = 0, round = 0, nc = 0;
+            bool ok = true;
+            for (int c = 0; c < total; ++c) {
+                if (act_in_smem && c == S - act_stages)
+                    ok = mbar_wait_bounded(&act_free_bar, 0, &abort_flag);
+                if (ok && round > 0)
+                    ok = mbar_wait_bounded(&empty_bar[s], (round - 1) & 1, &abort_flag);
+                if (!ok) break;
+                const int rows = min(R, n_cnt - nc * R);
+                const size_t n0 = (size_t)n_begin + (size_t)nc * R;
+                unsigned char *st = smem + (size_t)s * stage_bytes;
+                const uint32_t wb = (uint32_t)rows * w_row_bytes;
+                const uint32_t sb = (uint32_t)rows * s_row_bytes;
+                mbar_arrive_expect_tx(&full_bar[s], wb + sb);
+                bulk_g2s(st, qweight + n0 * w_row_bytes, wb, &full_bar[s], pol_w);
+                bulk_g2s(st + (size_t)R * w_row_bytes, scales + n0 * ngroups, sb, &full_bar[s],
+                         pol_s);
+                issued = c + 1;
+                if (++s == S) { s = 0; ++round; }
+                if (++nc == n_chunks) nc = 0;
+            }
+            // Every issued copy must land before the CTA exits: wait (bounded) on the
+            // last phase of each stage that was used, and on the activation copy.
+            for (int c = max(0, issued - S); c < issued; ++c) {
+                const int st_idx = c % S;
+                const long long t0 = clock64();
+                while (!mbar_test_parity(&full_bar[st_idx], (c / S) & 1) &&
+                       clock64() - t0 < kWaitLimitCycles) {
+                    __nanosleep(64);
+                }
+            }
+            if (act_in_smem) {
+                const long long t0 = clock64();
+                while (!mbar_test_parity(&act_full_bar, 0) && clock64() - t0 < kWaitLimitCycles)
+                    __nanosleep(64);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumer warps
+        const int col = (tid * 32) / group;  // this thread's scale column
+        const W4Keys keys = w4_keys();
+        Act16 act[MB];
+        int window_base = 0;
+        int s = 0, phase = 0, nc = 0, m0 = 0;
+        for (int c = 0; c < total; ++c) {
+            if (nc == 0) {
+#pragma unroll
+                for (int mb = 0; mb < MB; ++mb) {
+                    if (m0 + mb < M) {
+                        GateUp gu;
+                        if (act_in_smem) {
+                            if (mbar_wait_bounded(&act_full_bar, 0, &abort_flag)) {
+                                const uint4 *g4 = reinterpret_cast<const uint4 *>(act_smem + tid * 32);
+                                const uint4 *u4 = reinterpret_cast<const uint4 *>(act_smem + K + tid * 32);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    gu.g[i] = g4[i];
+                                    gu.u[i] = u4[i];
+                                }
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) gu.g[i] = gu.u[i] = make_uint4(0, 0, 0, 0);
+                            }
+                            // The area is released only after its values are consumed, and
+                            // with a proxy fence: the producer's next bulk copy writes it.
+                            encode_q16(gu, act[mb]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&act_free_bar);
+                        } else {
+                            load_gate_up(gate, up, (size_t)(m0 + mb) * K + (size_t)tid * 32, gu);
+                            encode_q16(gu, act[mb]);
+                        }
+                    } else {
+                        zero_activation(act[mb]);
+                    }
+                }
+            }
+            float part[R * MB];
+            const bool ok = mbar_wait_bounded(&full_bar[s], phase, &abort_flag);
+            const int rows_valid = min(R, n_cnt - nc * R);
+            const unsigned char *st = smem + (size_t)s * stage_bytes;
+            const uint4 *wst = reinterpret_cast<const uint4 *>(st) + tid;
+            const uint16_t *sst = reinterpret_cast<const uint16_t *>(st + (size_t)R * w_row_bytes) + col;
+            if (ok && rows_valid == R) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint4 wv = wst[r * nvec];
+                    const float sc = __uint_as_float((uint32_t)sst[r * ngroups] << 16);
+                    float d[MB];
+                    dot32<MB>(act, wv, keys, sc, d);
+#pragma unroll
+                    for (int mb = 0; mb < MB; ++mb) part[r * MB + mb] = d[mb];
+                }
+            } else {
+                // last, partial chunk (or a failed wait): rows past the range are skipped
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (ok && r < rows_valid) {
+                        const uint4 wv = wst[r * nvec];
+                        const float sc = __uint_as_float((uint32_t)sst[r * ngroups] << 16);
+                        float d[MB];
+                        dot32<MB>(act, wv, keys, sc, d);
+#pragma unroll
+                        for (int mb = 0; mb < MB; ++mb) part[r * MB + mb] = d[mb];
+                    } else {
+#pragma unroll
+                        for (int mb = 0; mb < MB; ++mb) part[r * MB + mb] = 0.f;
+                    }
+                }
+            }
+            fence_proxy_async_smem();  // this stage's reads before its next bulk copy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[s]);
+
+            const float wsum = warp_reduce_scatter<R * MB>(part, lane);
+            constexpr int kLanesPerValue = 32 / (R * MB);
+            if ((lane & (kLanesPerValue - 1)) == 0) {
+                const int idx = lane / kLanesPerValue;
+                const int r = idx / MB, mb = idx % MB;
+                red[((size_t)warp * kWindowRows + (nc * R + r - window_base)) * MB + mb] = wsum;
+            }
+            const int rows_done = (nc + 1) * R;
+            const bool last_chunk = (nc == n_chunks - 1);
+            if (rows_done - window_base == kWindowRows || last_chunk) {
+                named_bar_sync(1, nvec);
+                const int rows_in_window = min(rows_done, n_cnt) - window_base;
+                for (int i = tid; i < rows_in_window * MB; i += nvec) {
+                    const int row = i / MB, mb = i % MB;
+                    float acc = 0.f;
+                    for (int w = 0; w < ncw; ++w) acc += red[((size_t)w * kWindowRows + row) * MB + mb];
+                    if (m0 + mb < M) {
+                        __nv_bfloat16 y = __float2bfloat16_rn(acc);
+                        out[(size_t)(m0 + mb) * N + n_begin + window_base + row] =
+                            *reinterpret_cast<uint16_t *>(&y);
+                    }
+                }
+                named_bar_sync(1, nvec);
+                window_base = last_chunk ? 0 : rows_done;
+            }
+            if (++s == S) { s = 0; phase ^= 1; }
+            if (++nc == n_chunks) { nc = 0; m0 += MB; }
+        }
+    }
+
+    __syncthreads();
+    if (abort_flag) {
+        // A wait gave up: make the failure visible in every output this CTA owns.
+        for (int i = tid; i < n_cnt * M; i += blockDim.x) {
+            const int m = i / n_cnt, r = i % n_cnt;
+            out[(size_t)m * N + n_begin + r] = 0x7FC0;  // bf16 quiet NaN
+        }
+    }
+}
+
+template <int MB, int R, int NVEC_C, int NG_C>
+cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
+                       const void *qweight, const void *scales, void *out, int M, int K,
+                       int N, int group, cudaStream_t stream, bool *launched) {
+    static std::atomic<uint64_t> attr_done{0};
+    static std::atomic<int> static_smem_cache{-1};
+    auto kern = gemv_tma_kernel<MB, R, NVEC_C, NG_C>;
+    int static_smem = static_smem_cache.load(std::memory_order_relaxed);
+    if (static_smem < 0) {
+        cudaFuncAttributes fa;
+        cudaError_t err = cudaFuncGetAttributes(&fa, kern);
+        if (err != cudaSuccess) return err;
+        static_smem = (int)fa.sharedSizeBytes;
+        static_smem_cache.store(static_smem, std::memory_order_relaxed);
+    }
+    const int nvec = K / 32;
+    const int ngroups = K / group;
+    const size_t stage = (size_t)R * ((size_t)K / 2 + (size_t)ngroups * 2);
+    const size_t red = (size_t)(nvec / 32) * kWindowRows * MB * 4;
+    const size_t budget = (size_t)di.max_smem_optin - (size_t)static_smem;
+    if (red + 2 * stage > budget) return cudaSuccess;  // not launched: ring too small
+    int S = (int)((budget - red) / stage);
+    if (S > kMaxStages) S = kMaxStages;
+    // With M == 1 the gate/up copy (2 * K * 2 bytes) borrows the last stages; keep at
+    // least two stages free for weights.
+    const size_t act_bytes = (size_t)K * 4;
+    const int act_stages = (int)((act_bytes + stage - 1) / stage);
+    if (M == 1 && S - act_stages < 2) return cudaSuccess;  // not launched
+    const size_t smem = (size_t)S * stage + red;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)budget);
+        if (err != cudaSuccess) return err;
+        attr_done.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    int grid = di.sm_count;
+    if ((long long)grid * R > N) grid = (N + R - 1) / R;
+    if (grid < 1) grid = 1;
+    const int rows_base = N / grid;
+    const int rows_extra = N % grid;
+    kern<<<grid, nvec + 32, smem, stream>>>(
+        static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up),
+        static_cast<const unsigned char *>(qweight), static_cast<const uint16_t *>(scales),
+        static_cast<uint16_t *>(out), M, K, N, group, rows_base, rows_extra, S, act_stages,
+        M <= MB ? 1 : 0);
+    *launched = true;
+    return cudaGetLastError();
+}
+
+template <int MB>
+cudaError_t launch_mb(const DeviceInfo &di, const void *gate, const void *up,
+                      const void *qweight, const void *scales, void *out, int M, int K, int N,
+                      int group, cudaStream_t stream, bool *launched) {
+    constexpr int R = kChunkRows;
+#define FD_SHAPE(KK, GG)                                                                      \
+    if (K == KK && group == GG)                                                               \
+        return launch_cfg<MB, R, KK / 32, KK / GG>(di, gate, up, qweight, scales, out, M, K, N, \
+                                                  group, stream, launched);
+    FD_SHAPE(14336, 128)
+    FD_SHAPE(9216, 128)
+    FD_SHAPE(4096, 128)
+    FD_SHAPE(1024, 128)
+#undef FD_SHAPE
+    return launch_cfg<MB, R, 0, 0>(di, gate, up, qweight, scales, out, M, K, N, group, stream,
+                                   launched);
+}
+
+}  // namespace
+
+bool gemv_tma_supported(int M, int K, int group) {
+    (void)M;
+    const int nvec = K / 32;
+    return K % 1024 == 0 && nvec + 32 <= 512 && (K / group) % 8 == 0;
+}
+
+cudaError_t launch_gemv_tma(const void *gate, const void *up, const void *qweight,
+                            const void *scales, void *out, int M, int K, int N, int group,
+                            cudaStream_t stream, bool *launched) {
+    *launched = false;
+    if (!gemv_tma_supported(M, K, group)) return cudaSuccess;
+    DeviceInfo di;
+    cudaError_t err = device_info(&di);
+    if (err != cudaSuccess) return err;
+    if (M == 1)
+        return launch_mb<1>(di, gate, up, qweight, scales, out, M, K, N, group, stream, launched);
+    return launch_mb<2>(di, gate, up, qweight, scales, out, M, K, N, group, stream, launched);
+}
+
+}  // namespace fd

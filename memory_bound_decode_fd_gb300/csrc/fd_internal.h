@@ -24,6 +24,9 @@ cudaError_t device_info(DeviceInfo *info);
 // ------------------------------------------------------------------------------------
 // Launchers (host). Arguments are validated by the C-ABI layer before these run.
 // ------------------------------------------------------------------------------------
+cudaError_t launch_gemv_tma(const void *gate, const void *up, const void *qweight,
+                            const void *scales, void *out, int M, int K, int N, int group,
+                            cudaStream_t stream, bool *launched);
 cudaError_t launch_gemv_cc(const void *gate, const void *up, const void *qweight,
                            const void *scales, void *out, int M, int K, int N, int group,
                            cudaStream_t stream);
@@ -79,27 +82,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Packed fp32x2 arithmetic (one instruction for two lanes of work on sm_100+).
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;"
-        : "=l"(d)
-        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)),
-          "l"(*reinterpret_cast<uint64_t *>(&c)));
-    return *reinterpret_cast<float2 *>(&d);
-}
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;"
-        : "=l"(d)
-        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)));
-    return *reinterpret_cast<float2 *>(&d);
-}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
-// lop3 with truth table 0x6A: (a & b) ^ c.
+// (a & b) ^ c: one lop3 (the compiler folds the constant operands).
 __device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
+    return (a & b) ^ c;
 }
 
 }  // namespace fd

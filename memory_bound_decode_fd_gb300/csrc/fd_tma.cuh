@@ -1,0 +1,92 @@
+// fd_tma.cuh - mbarrier and bulk-copy (TMA, non-tensor) wrappers in inline PTX, and a
+// bounded wait. Every wait in this library gives up after kWaitLimitCycles SM clocks
+// (about a second) or as soon as another thread of the CTA has given up, so a lost
+// completion can never hang the GPU; the caller then records the failure and exits.
+#pragma once
+
+#include "fd_internal.h"
+
+namespace fd {
+
+constexpr long long kWaitLimitCycles = 1ll << 31;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// Makes the initialised barriers visible to the async (bulk copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// True once the phase with parity `parity` has completed.
+__device__ __forceinline__ bool mbar_test_parity(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for the phase with parity `parity`. Returns false if the wait ran past the
+// cycle limit or `*abort_flag` became nonzero (another thread gave up); in the first
+// case it also sets `*abort_flag`.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort_flag) {
+    if (mbar_test_parity(bar, parity)) return true;
+    const long long t0 = clock64();
+    unsigned spins = 0;
+    while (true) {
+        if (mbar_test_parity(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (++spins > 64) __nanosleep(32);
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// Bulk copy global -> shared (this CTA), completion counted in bytes on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to shared memory (plain loads and
+// stores) before later async-proxy accesses (bulk copies) to the same memory. Issued
+// before releasing a buffer that a bulk copy will overwrite.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Barrier over the first `threads` threads of the CTA (named barrier `id`, id != 0).
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+}  // namespace fd

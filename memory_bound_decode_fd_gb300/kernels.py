@@ -14,6 +14,19 @@ import torch
 from . import _lib
 
 
+GEMV_PATHS = {"auto": _lib.FD_GEMV_AUTO, "cuda_core": _lib.FD_GEMV_CUDA_CORE,
+              "bulk": _lib.FD_GEMV_BULK}
+
+
+def set_gemv_path(path: str) -> str:
+    """Select the GEMV kernel process-wide ("auto", "cuda_core" or "bulk"); returns the
+    previous selection. See fd_set_gemv_path in include/fd.h."""
+    lib = _lib.load()
+    prev = {v: k for k, v in GEMV_PATHS.items()}[lib.fd_get_gemv_path()]
+    _lib.check(lib.fd_set_gemv_path(GEMV_PATHS[path]))
+    return prev
+
+
 def _stream_handle(stream: torch.cuda.Stream | None) -> ctypes.c_void_p:
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(int(s.cuda_stream))

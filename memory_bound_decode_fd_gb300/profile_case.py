@@ -1,0 +1,71 @@
+"""Run one fd kernel a few times on seeded inputs, nothing else (for ncu captures).
+
+    python -m memory_bound_decode_fd_gb300.profile_case gemv --M 1 --K 14336 --N 4096
+    python -m memory_bound_decode_fd_gb300.profile_case rmsnorm --rows 8192 --hidden 4096
+
+Each iteration uses the next of --sets input sets, so that consecutive launches do not
+find their weights in L2. Exits 0 after a final synchronize.
+"""
+
+from __future__ import annotations
+
+import argparse
+
+import numpy as np
+import torch
+
+
+def _dev(a, device):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(a).to(device)
+
+
+def main(argv=None) -> int:
+    import memory_bound_decode_fd_gb300 as fd
+    from memory_bound_decode_fd_gb300 import build, inputs
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["gemv", "rmsnorm"])
+    ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--K", type=int, default=14336)
+    ap.add_argument("--N", type=int, default=4096)
+    ap.add_argument("--group", type=int, default=128)
+    ap.add_argument("--rows", type=int, default=8192)
+    ap.add_argument("--hidden", type=int, default=4096)
+    ap.add_argument("--eps", type=float, default=1e-6)
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--sets", type=int, default=2)
+    args = ap.parse_args(argv)
+
+    build.build()
+    dev = torch.device("cuda:0")
+    if args.case == "gemv":
+        rng = np.random.default_rng(0)
+        d = inputs.gemv_inputs(args.M, args.K, args.N, args.group, rng=rng)
+        g, u = _dev(d["gate"], dev), _dev(d["up"], dev)
+        sets = [(_dev(inputs.int4_words(rng, args.N, args.K), dev),
+                 _dev(inputs.scales_bf16(rng, args.N, args.K, args.group), dev))
+                for _ in range(args.sets)]
+        out = torch.empty((args.M, args.N), dtype=torch.bfloat16, device=dev)
+        for i in range(args.iters):
+            q, s = sets[i % len(sets)]
+            fd.swiglu_w4a16_gemv(g, u, q, s, out=out, group=args.group)
+    else:
+        sets = []
+        for i in range(args.sets):
+            d = inputs.rmsnorm_inputs(args.rows, args.hidden, seed=i)
+            sets.append((_dev(d["x"], dev), _dev(d["residual"], dev), _dev(d["weight"], dev)))
+        y = torch.empty((args.rows, args.hidden), dtype=torch.bfloat16, device=dev)
+        h = torch.empty_like(y)
+        for i in range(args.iters):
+            x, r, w = sets[i % len(sets)]
+            fd.add_rmsnorm(x, r, w, args.eps, out=y, residual_out=h)
+    torch.cuda.synchronize()
+    print("profile_case done", flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())

@@ -13,6 +13,15 @@ from fd_check import GuardedBuffer, check_gemv, dev_bf16, dev_i32, host_bits
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["auto", "cuda_core"])
+def gemv_path(request, cuda_device):
+    """Run the test once with the default kernel choice (the bulk-copy kernel where its
+    layout rules hold) and once forcing the CUDA-core ring kernel."""
+    prev = fd.set_gemv_path(request.param)
+    yield request.param
+    fd.set_gemv_path(prev)
+
+
 def run_gemv(d, out=None):
     g, u = dev_bf16(d["gate"]), dev_bf16(d["up"])
     q, s = dev_i32(d["qweight"]), dev_bf16(d["scales"])
@@ -55,14 +64,14 @@ def test_dequant_every_nibble_every_position(cuda_device):
     (1, 9216, 2560, 2),     # GEMV M=1 K=9216 N=2560, seed 2 (94 MB unfused product)
     (1, 14336, 4096, 3),    # down projection of the decode step
 ])
-def test_gemv_workloads_full(cuda_device, M, K, N, seed):
+def test_gemv_workloads_full(gemv_path, M, K, N, seed):
     d = inputs.gemv_inputs(M, K, N, 128, seed=seed)
     y = run_gemv(d)
     res = check_gemv(y, d["gate"], d["up"], d["qweight"], d["scales"], 128)
     assert res["n_checked"] == M * N
 
 
-def test_gemv_batched_m64_sampled(cuda_device):
+def test_gemv_batched_m64_sampled(gemv_path):
     # Batched decode M=64, K=14336, N=4096 (seed 4): every output of 256 sampled rows.
     d = inputs.batched_inputs()["gemv"]
     y = run_gemv(d)
@@ -82,6 +91,7 @@ EDGE_SHAPES = [
     (1, 1024, 153, 128),
     (1, 4096, 1217, 64),     # rows not a multiple of 8 per CTA
     (1, 9216, 2561, 128),
+    (1, 15360, 700, 128),    # largest K of the bulk-copy kernel
     (1, 16384, 700, 128),    # largest K with one vector position per thread
     (1, 16416, 300, 32),     # two vector positions per thread, partial
     (1, 32768, 200, 128),    # largest K
@@ -101,14 +111,14 @@ EDGE_SHAPES = [
 
 
 @pytest.mark.parametrize("M,K,N,group", EDGE_SHAPES)
-def test_gemv_edge_shapes(cuda_device, M, K, N, group):
+def test_gemv_edge_shapes(gemv_path, M, K, N, group):
     d = inputs.gemv_inputs(M, K, N, group, seed=1000 + M + K + N)
     y = run_gemv(d)
     check_gemv(y, d["gate"], d["up"], d["qweight"], d["scales"], group)
 
 
 @pytest.mark.parametrize("n_star,k_star,qv", [(0, 0, 3), (2559, 9215, -8), (1234, 4097, 7), (77, 31, -1)])
-def test_gemv_one_hot_layout(cuda_device, n_star, k_star, qv):
+def test_gemv_one_hot_layout(gemv_path, n_star, k_star, qv):
     # A single nonzero weight: every other output is exactly zero and the hot one is
     # a[k*] * q * s rounded once (index mapping, nibble order and scale index).
     M, K, N, group = 2, 9216, 2560, 128
@@ -129,7 +139,7 @@ def test_gemv_one_hot_layout(cuda_device, n_star, k_star, qv):
     check_gemv(y, gate, up, d["qweight"], d["scales"], group)
 
 
-def test_gemv_guard_bands_untouched(cuda_device):
+def test_gemv_guard_bands_untouched(gemv_path):
     d = inputs.gemv_inputs(3, 9216, 2561, 128, seed=7)
     buf = GuardedBuffer((3, 2561))
     run_gemv(d, out=buf.tensor)
@@ -137,7 +147,7 @@ def test_gemv_guard_bands_untouched(cuda_device):
     check_gemv(host_bits(buf.tensor), d["gate"], d["up"], d["qweight"], d["scales"], 128)
 
 
-def test_gemv_allocates_nothing(cuda_device):
+def test_gemv_allocates_nothing(gemv_path):
     d = inputs.gemv_inputs(1, 9216, 2560, 128, seed=2)
     g, u = dev_bf16(d["gate"]), dev_bf16(d["up"])
     q, s = dev_i32(d["qweight"]), dev_bf16(d["scales"])
@@ -172,7 +182,7 @@ def test_gemv_deterministic_and_stream_ordered(cuda_device):
     check_gemv(base, d["gate"], d["up"], d["qweight"], d["scales"], 128)
 
 
-def test_gemv_cuda_graph_replay_matches_eager(cuda_device):
+def test_gemv_cuda_graph_replay_matches_eager(gemv_path):
     d = inputs.gemv_inputs(1, 14336, 4096, 128, seed=3)
     g, u = dev_bf16(d["gate"]), dev_bf16(d["up"])
     q, s = dev_i32(d["qweight"]), dev_bf16(d["scales"])
@@ -202,3 +212,40 @@ def test_gemv_rejects_misaligned_and_overlapping(cuda_device):
     with pytest.raises(fd.FdError) as e:
         fd.swiglu_w4a16_gemv(g[:1024].view(1, 1024), u, q, s, out=u[:, :256])
     assert e.value.status == fd.FD_ERR_OVERLAP
+
+
+def test_gemv_paths_agree_within_bound(cuda_device):
+    # The two kernels sum in different orders; both meet the bound, and they agree to
+    # within one bf16 step almost everywhere.
+    d = inputs.gemv_inputs(1, 14336, 4096, 128, seed=3)
+    outs = {}
+    for p in ("bulk", "cuda_core"):
+        prev = fd.set_gemv_path(p)
+        try:
+            outs[p] = run_gemv(d)
+        finally:
+            fd.set_gemv_path(prev)
+    from fd_check import ordered_key
+    steps = np.abs(ordered_key(outs["bulk"]) - ordered_key(outs["cuda_core"]))
+    assert steps.max() <= 1 and np.mean(steps == 0) > 0.95
+
+
+def test_gemv_path_selector_rejects_unknown(cuda_device):
+    assert fd.load_library().fd_set_gemv_path(7) == fd.FD_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("K,N", [(14336, 4096), (9216, 2560), (1024, 256)])
+def test_gemv_back_to_back_calls_identical(cuda_device, K, N):
+    # Many launches in a row on one stream: every call must reproduce the first bit for
+    # bit (the bulk-copy kernel's shared-memory reuse and release order are exercised on
+    # every call), and the first must meet the parity bound.
+    d = inputs.gemv_inputs(1, K, N, 128, seed=11)
+    g, u = dev_bf16(d["gate"]), dev_bf16(d["up"])
+    q, s = dev_i32(d["qweight"]), dev_bf16(d["scales"])
+    outs = torch.empty((64, 1, N), dtype=torch.bfloat16, device="cuda")
+    for i in range(64):
+        fd.swiglu_w4a16_gemv(g, u, q, s, out=outs[i])
+    torch.cuda.synchronize()
+    bits = host_bits(outs)
+    assert all(np.array_equal(bits[i], bits[0]) for i in range(1, 64))
+    check_gemv(bits[0], d["gate"], d["up"], d["qweight"], d["scales"], 128)
