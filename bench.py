@@ -14,8 +14,7 @@ Reported:
              pinned host memory: H2D of x, residual and every layer's gate/up, the
              replay, D2H of x_L and the residual, all inside the timed region
   roofline   the dominant kernel (the GEMV) - its average launch duration from CUDA
-             events bracketing each launch in a separate eager pass queued behind a
-             GPU sleep (so the events time the kernel, not the launch latency)
+             events around replays of a graph of the step's 32 GEMV launches alone
   cpu_baseline  the CPU oracle, single-threaded, on a bounded sample of the workload
   --impl reference  times the CPU oracle alone (the reference arm of this benchmark)
 
@@ -157,27 +156,6 @@ def time_region(stream, fn, iters: int) -> float:
     return start.elapsed_time(end)
 
 
-def per_launch_times(stream, launches, sleep_cycles=50_000_000):
-    """Average device duration (ms) of each named launch: the GPU is held by a sleep
-    kernel while every (event, launch, event) triple is queued, so each event pair
-    brackets only its kernel. `launches` is a list of (name, callable)."""
-    evs = []
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(sleep_cycles)
-        for name, fn in launches:
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            evs.append((name, a, b))
-    torch.cuda.synchronize()
-    acc = {}
-    for name, a, b in evs:
-        acc.setdefault(name, []).append(a.elapsed_time(b))
-    return {k: (sum(v) / len(v), len(v)) for k, v in acc.items()}
-
-
 # ----------------------------------------------------------------------------- workloads
 
 def to_dev(bits_or_words, device):
@@ -230,26 +208,41 @@ def bench_decode(args, device, rank, world):
     ms = max_over_ranks(ms, world)
     clocks = sampler.stop()
     ms_per_step = ms / args.steps
-    value_gbs = world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+    value_gbs = job_throughput_gbs(world, bytes_per_step, ms_per_step)
 
-    # Per-kernel durations (eager launches of the same kernels on the same stream).
+    # Per-kernel durations: each kernel's 32 launches of the step, captured alone in a
+    # CUDA graph (same buffers and weights, programmatic dependent launch as in the
+    # step) and replayed on the same stream; average launch duration = event time /
+    # launches. Includes the small inter-kernel gap, so it is conservative.
     hidden = spec["hidden"]
-    launches = []
-    for i, L in enumerate(step.layers):
-        launches.append(("add_rmsnorm", lambda L=L, i=i: fd.add_rmsnorm(
+    kern_launch = {
+        "add_rmsnorm": [lambda L=L, i=i: fd.add_rmsnorm(
             step.y[i - 1] if i else step.x, step.residual, L["rms_weight"], spec["eps"],
-            out=step.normed[i], residual_out=step.residual, stream=stream)))
-        launches.append(("swiglu_w4a16_gemv", lambda L=L, i=i: fd.swiglu_w4a16_gemv(
+            out=step.normed[i], residual_out=step.residual, stream=stream)
+            for i, L in enumerate(step.layers)],
+        "swiglu_w4a16_gemv": [lambda L=L, i=i: fd.swiglu_w4a16_gemv(
             L["gate"], L["up"], L["qweight"], L["scales"], out=step.y[i], group=spec["group"],
-            stream=stream)))
-    kt = {}
-    for _ in range(3):
-        for k, (t, n) in per_launch_times(stream, launches).items():
-            kt.setdefault(k, []).append((t, n))
+            stream=stream) for i, L in enumerate(step.layers)],
+    }
     kernels = {}
-    for k, v in kt.items():
-        t_ms = sum(t * n for t, n in v) / sum(n for _, n in v)
-        kernels[k] = {"us": t_ms * 1e3, "launches_sampled": sum(n for _, n in v)}
+    prev_pdl = fd.set_pdl(step.pdl)
+    try:
+        for name, calls in kern_launch.items():
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                for c in calls:
+                    c()
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for c in calls:
+                    c()
+            reps = max(10, args.steps // 10)
+            with torch.cuda.stream(stream):
+                time_region(stream, g.replay, 3)
+                ms_k = time_region(stream, g.replay, reps)
+            kernels[name] = {"us": ms_k * 1e3 / (reps * len(calls)), "launches_timed": reps * len(calls)}
+    finally:
+        fd.set_pdl(prev_pdl)
     gemv_bytes = fd.gemv_bytes(1, spec["inter"], hidden, spec["group"])
     rms_bytes = fd.add_rmsnorm_bytes(1, hidden)
     kernels["swiglu_w4a16_gemv"]["bytes"] = gemv_bytes
@@ -312,7 +305,7 @@ def bench_decode(args, device, rank, world):
             "algorithmic_bytes_per_launch": gemv_bytes,
         },
         "e2e": {
-            "value": round(world * bytes_per_step / (e2e_ms * 1e-3) / 1e9, 2),
+            "value": round(job_throughput_gbs(world, bytes_per_step, e2e_ms), 2),
             "unit": "GB/s",
             "ms_per_step": round(e2e_ms, 6),
             "h2d_bytes_per_step": h2d,
@@ -462,9 +455,7 @@ def bench_single(args, device, rank, world):
     clocks = sampler.stop()
     n_calls = reps * len(calls)
     us_call = ms * 1e3 / n_calls
-    with torch.cuda.stream(stream):
-        kt = per_launch_times(stream, [(kname, c) for c in calls[:256]])
-    k_us = kt[kname][0] * 1e3
+    k_us = us_call  # the graph holds only this kernel's launches
     gbs = world * nbytes / (us_call * 1e-6) / 1e9
     return {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
@@ -497,6 +488,7 @@ def barrier(world):
 
 
 def max_over_ranks(value: float, world: int) -> float:
+    """The slowest rank's time: every rank gets the maximum of `value` over all ranks."""
     if world <= 1:
         return value
     import torch.distributed as dist
@@ -504,6 +496,12 @@ def max_over_ranks(value: float, world: int) -> float:
                      device="cuda" if dist.get_backend() == "nccl" else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput_gbs(world: int, bytes_per_step: int, ms_per_step: float) -> float:
+    """Whole-job GB/s of N independent replicas: every rank moves `bytes_per_step` per
+    step, and the job's step time is the slowest rank's (max over ranks)."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
 
 
 def main(argv=None):

@@ -121,6 +121,22 @@ int fd_set_gemv_path(int path);
 int fd_get_gemv_path(void);
 
 /*
+ * Launch options (process-wide, thread-safe; default 0).
+ *   FD_LAUNCH_PDL  launch with programmatic dependent launch: a kernel may begin while
+ *                  the previous kernel in the same stream is still running. Each fd
+ *                  kernel waits (griddepcontrol.wait) before it reads activations or
+ *                  writes any output, but the GEMV starts streaming qweight/scales, and
+ *                  add-RMSNorm loads its weight row, BEFORE that wait. Set this only
+ *                  when no kernel that may still be running in the stream writes those
+ *                  weight tensors (true for model weights during decode). Works inside
+ *                  CUDA graph capture (the edges become programmatic dependencies).
+ * fd_set_launch_flags returns FD_ERR_UNSUPPORTED for unknown bits.
+ */
+#define FD_LAUNCH_PDL 1u
+int fd_set_launch_flags(unsigned flags);
+unsigned fd_get_launch_flags(void);
+
+/*
  * fd_w4_dequant_debug - write the dequantised weights W[n, k] = q[n, k] * s[n, k/group]
  * as fp32 [N, K] (test support: the unpack and scale of the GEMV prologue, checked bit
  * for bit). Same layouts and size rules as fd_swiglu_w4a16_gemv; `out` is fp32 [N, K].

@@ -31,6 +31,7 @@ from .kernels import (  # noqa: F401
     add_rmsnorm,
     decode_mlp_step,
     set_gemv_path,
+    set_pdl,
     swiglu_w4a16_gemv,
     w4_dequant_debug,
 )

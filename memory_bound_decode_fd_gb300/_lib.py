@@ -20,6 +20,8 @@ FD_GEMV_AUTO = 0
 FD_GEMV_CUDA_CORE = 1
 FD_GEMV_BULK = 2
 
+FD_LAUNCH_PDL = 1
+
 FD_MAX_K = 32768
 FD_MAX_M = 256
 FD_MAX_HIDDEN = 32768
@@ -36,6 +38,8 @@ SIGNATURES = {
     "fd_version": (_I, []),
     "fd_set_gemv_path": (_I, [_I]),
     "fd_get_gemv_path": (_I, []),
+    "fd_set_launch_flags": (_I, [ctypes.c_uint]),
+    "fd_get_launch_flags": (ctypes.c_uint, []),
 }
 
 

@@ -62,6 +62,11 @@ __global__ void __launch_bounds__(VPT >= 8 ? 512 : 256)
         }
     }
 
+    // x and residual may come from the previous kernel in the stream (programmatic
+    // dependent launch): wait for it only now, after the weight row has been requested.
+    grid_dep_wait();
+    grid_dep_launch();
+
     for (int row = blockIdx.x; row < rows; row += gridDim.x) {
         const size_t base = (size_t)row * nvec;
         uint4 xv[VPT], rv[VPT];
@@ -149,10 +154,12 @@ cudaError_t launch_vpt(const DeviceInfo &di, const void *x, const void *residual
     }
     long long grid = (long long)di.sm_count * occ;
     if (grid > rows) grid = rows;
-    add_rmsnorm_kernel<VPT><<<(int)grid, T, 0, stream>>>(
-        static_cast<const uint4 *>(x), static_cast<const uint4 *>(residual),
-        static_cast<const uint4 *>(weight), static_cast<uint4 *>(out),
-        static_cast<uint4 *>(residual_out), rows, nvec, 1.0f / (float)hidden, eps);
+    err = launch_kernel(add_rmsnorm_kernel<VPT>, dim3((unsigned)grid), dim3(T), 0, stream, 1,
+                        static_cast<const uint4 *>(x), static_cast<const uint4 *>(residual),
+                        static_cast<const uint4 *>(weight), static_cast<uint4 *>(out),
+                        static_cast<uint4 *>(residual_out), rows, nvec, 1.0f / (float)hidden,
+                        eps);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

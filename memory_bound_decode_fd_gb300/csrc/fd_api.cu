@@ -17,6 +17,7 @@ std::atomic<int> g_info_ready[kMaxDevices];
 DeviceInfo g_info[kMaxDevices];
 thread_local int g_last_cuda_error = 0;
 std::atomic<int> g_gemv_path{FD_GEMV_AUTO};
+std::atomic<unsigned> g_launch_flags{0u};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -66,6 +67,8 @@ cudaError_t device_info(DeviceInfo *info) {
     return cudaSuccess;
 }
 
+unsigned launch_flags() { return g_launch_flags.load(std::memory_order_relaxed); }
+
 }  // namespace fd
 
 using namespace fd;
@@ -106,6 +109,14 @@ int fd_set_gemv_path(int path) {
 }
 
 int fd_get_gemv_path(void) { return g_gemv_path.load(std::memory_order_relaxed); }
+
+int fd_set_launch_flags(unsigned flags) {
+    if (flags & ~FD_LAUNCH_PDL) return FD_ERR_UNSUPPORTED;
+    g_launch_flags.store(flags, std::memory_order_relaxed);
+    return FD_OK;
+}
+
+unsigned fd_get_launch_flags(void) { return g_launch_flags.load(std::memory_order_relaxed); }
 
 int fd_add_rmsnorm(const void *x, const void *residual, const void *weight, float eps,
                    void *out, void *residual_out, int rows, int hidden, fd_stream_t stream) {

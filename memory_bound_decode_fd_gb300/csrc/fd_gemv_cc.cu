@@ -134,6 +134,11 @@ __global__ void __launch_bounds__(512, 1)
         cp_async_commit();  // always commit (possibly empty) so group counting is uniform
     };
 
+    // gate/up may come from the previous kernel in the stream (programmatic dependent
+    // launch); the weights are read only after this wait too.
+    grid_dep_wait();
+    grid_dep_launch();
+
 #pragma unroll
     for (int c = 0; c < S - 1; ++c) issue(c);
 
@@ -247,6 +252,9 @@ cudaError_t ensure_smem_attr(Kern kern, size_t smem, std::atomic<uint64_t> &done
     if ((size_t)limit < smem) return cudaErrorInvalidConfiguration;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
     if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (err != cudaSuccess) return err;
     done.fetch_or(bit, std::memory_order_acq_rel);
     return cudaSuccess;
 }
@@ -268,10 +276,12 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
     const int rows_base = N / grid;
     const int rows_extra = N % grid;
     const int evict_first = (M <= MB) ? 1 : 0;
-    kern<<<grid, T, smem, stream>>>(
-        static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up),
-        static_cast<const uint4 *>(qweight), static_cast<const uint16_t *>(scales),
-        static_cast<uint16_t *>(out), M, K, N, group, rows_base, rows_extra, evict_first);
+    err = launch_kernel(kern, dim3(grid), dim3(T), smem, stream, 1,
+                        static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up),
+                        static_cast<const uint4 *>(qweight),
+                        static_cast<const uint16_t *>(scales), static_cast<uint16_t *>(out), M,
+                        K, N, group, rows_base, rows_extra, evict_first);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

@@ -4,7 +4,7 @@
 //
 // Numerics of one 32-k slice (one 16-byte weight vector position, inside one scale
 // group):
-//   a_k = silu(g_k) * u_k in fp32 (fast exp, Newton reciprocal), k in the slice;
+//   a_k = silu(g_k) * u_k in fp32 (fast exp and divide intrinsics), k in the slice;
 //   a_k is encoded as a16_k = rint(a_k * 32767 / amax) with amax = max |a_k| over the
 //   slice (a block-scaled 16-bit integer: 15 magnitude bits against bf16's 8), and
 //   a_k ~= a16_k * scale, scale = amax / 32767;
@@ -60,20 +60,12 @@ __device__ __forceinline__ void load_gate_up(const uint16_t *__restrict__ gate,
     }
 }
 
-// silu(g) * u in fp32. exp runs on the MUFU unit; r = 1 / (1 + e) is computed on the
-// FMA/ALU pipes by Newton's iteration r' = r (2 - d r), seeded from the bit pattern of d
-// (an integer subtraction from 0x7EF311C7 gives a seed within 5.1% of 1/d in every
-// binade; each step squares the relative error: 5.1e-2 -> 2.6e-3 -> 6.7e-6 -> ~5e-11,
-// below fp32 rounding), so the prologue issues one MUFU operation per element, not two.
-// g is clamped at -60 so 1 + e stays finite (silu(-60) is below 1e-24).
+// silu(g) * u in fp32 with the fast exp and divide intrinsics (two MUFU operations per
+// element; relative error within a few ulp, far below the 16-bit encoding step). g is
+// clamped at -60 so 1 + e stays finite (silu(-60) is below 1e-24).
 __device__ __forceinline__ float silu_mul(float g, float u) {
     const float gc = fmaxf(g, -60.0f);
-    const float d = 1.0f + __expf(-gc);
-    float r = __uint_as_float(0x7EF311C7u - __float_as_uint(d));
-    r = r * fmaf(-d, r, 2.0f);
-    r = r * fmaf(-d, r, 2.0f);
-    r = r * fmaf(-d, r, 2.0f);
-    return g * r * u;
+    return __fdividef(g, 1.0f + __expf(-gc)) * u;
 }
 
 // Encodes one slice (see Act16).

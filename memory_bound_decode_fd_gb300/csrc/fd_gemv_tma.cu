@@ -37,7 +37,7 @@ namespace fd {
 namespace {
 
 constexpr int kMaxStages = 8;
-constexpr int kChunkRows = 4;  // rows per bulk-copy chunk
+constexpr int kChunkRows = 8;  // rows per bulk-copy chunk
 
 // NVEC_C / NG_C: compile-time K/32 and K/group for the common shapes (0 = runtime), so
 // the per-row shared-memory offsets fold into instruction immediates.
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(512, 1)
                     const unsigned char *__restrict__ qweight,
                     const uint16_t *__restrict__ scales, uint16_t *__restrict__ out, int M,
                     int K, int N, int group, int rows_base, int rows_extra, int S,
-                    int act_stages, int weights_evict_first) {
+                    int act_stages, int pre_stages, int weights_evict_first) {
     static_assert(R * MB <= 32 && (R * MB & (R * MB - 1)) == 0, "R*MB: power of 2, <= 32");
     static_assert(kWindowRows % R == 0, "window must hold whole chunks");
     extern __shared__ __align__(128) unsigned char smem[];
@@ -98,24 +98,21 @@ __global__ void __launch_bounds__(512, 1)
 
     if (warp == ncw) {
         // ------------------------------------------------------------ producer warp
-        if (lane == 0) {
+        if (lane != 0) {
+            grid_dep_wait();
+            grid_dep_launch();
+        } else {
             const uint64_t pol_w = weights_evict_first ? policy_evict_first() : policy_evict_last();
             const uint64_t pol_s = policy_evict_first();
-            if (act_in_smem) {
-                const uint32_t ab = (uint32_t)K * 2;
-                mbar_arrive_expect_tx(&act_full_bar, 2 * ab);
-                bulk_g2s(act_smem, gate, ab, &act_full_bar, pol_s);
-                bulk_g2s(act_smem + K, up, ab, &act_full_bar, pol_s);
-            }
             int issued = 0;
             int s = 0, round = 0, nc = 0;
             bool ok = true;
-            for (int c = 0; c < total; ++c) {
+            auto issue_chunk = [&](int c) {
                 if (act_in_smem && c == S - act_stages)
                     ok = mbar_wait_bounded(&act_free_bar, 0, &abort_flag);
                 if (ok && round > 0)
                     ok = mbar_wait_bounded(&empty_bar[s], (round - 1) & 1, &abort_flag);
-                if (!ok) break;
+                if (!ok) return;
                 const int rows = min(R, n_cnt - nc * R);
                 const size_t n0 = (size_t)n_begin + (size_t)nc * R;
                 unsigned char *st = smem + (size_t)s * stage_bytes;
@@ -128,7 +125,21 @@ __global__ void __launch_bounds__(512, 1)
                 issued = c + 1;
                 if (++s == S) { s = 0; ++round; }
                 if (++nc == n_chunks) nc = 0;
+            };
+            // Weights never come from the previous kernel: with programmatic dependent
+            // launch the first `pre_stages` chunks stream before the dependency wait.
+            const int pre = min(pre_stages, min(total, S - act_stages));
+            int c = 0;
+            for (; c < pre && ok; ++c) issue_chunk(c);
+            grid_dep_wait();
+            grid_dep_launch();
+            if (act_in_smem) {
+                const uint32_t ab = (uint32_t)K * 2;
+                mbar_arrive_expect_tx(&act_full_bar, 2 * ab);
+                bulk_g2s(act_smem, gate, ab, &act_full_bar, pol_s);
+                bulk_g2s(act_smem + K, up, ab, &act_full_bar, pol_s);
             }
+            for (; c < total && ok; ++c) issue_chunk(c);
             // Every issued copy must land before the CTA exits: wait (bounded) on the
             // last phase of each stage that was used, and on the activation copy.
             for (int c = max(0, issued - S); c < issued; ++c) {
@@ -147,11 +158,15 @@ __global__ void __launch_bounds__(512, 1)
         }
     } else {
         // ------------------------------------------------------------ consumer warps
+        // gate/up and the output may be shared with the previous kernel in the stream.
+        grid_dep_wait();
+        grid_dep_launch();
         const int col = (tid * 32) / group;  // this thread's scale column
         const W4Keys keys = w4_keys();
         Act16 act[MB];
         int window_base = 0;
         int s = 0, phase = 0, nc = 0, m0 = 0;
+        constexpr int kLanesPerValue = 32 / (R * MB);
         for (int c = 0; c < total; ++c) {
             if (nc == 0) {
 #pragma unroll
@@ -160,12 +175,21 @@ __global__ void __launch_bounds__(512, 1)
                         GateUp gu;
                         if (act_in_smem) {
                             if (mbar_wait_bounded(&act_full_bar, 0, &abort_flag)) {
+                                // Each lane's slice is 64 contiguous bytes; rotating the order
+                                // of its four 16-byte reads by lane spreads a warp's reads over
+                                // the banks.
                                 const uint4 *g4 = reinterpret_cast<const uint4 *>(act_smem + tid * 32);
                                 const uint4 *u4 = reinterpret_cast<const uint4 *>(act_smem + K + tid * 32);
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
-                                    gu.g[i] = g4[i];
-                                    gu.u[i] = u4[i];
+                                    const int j = (i + (lane >> 1)) & 3;
+                                    const uint4 gv = g4[j], uv = u4[j];
+#pragma unroll
+                                    for (int t = 0; t < 4; ++t)
+                                        if (t == j) {
+                                            gu.g[t] = gv;
+                                            gu.u[t] = uv;
+                                        }
                                 }
                             } else {
 #pragma unroll
@@ -224,7 +248,6 @@ __global__ void __launch_bounds__(512, 1)
             if (lane == 0) mbar_arrive(&empty_bar[s]);
 
             const float wsum = warp_reduce_scatter<R * MB>(part, lane);
-            constexpr int kLanesPerValue = 32 / (R * MB);
             if ((lane & (kLanesPerValue - 1)) == 0) {
                 const int idx = lane / kLanesPerValue;
                 const int r = idx / MB, mb = idx % MB;
@@ -300,6 +323,9 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)budget);
         if (err != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   cudaSharedmemCarveoutMaxShared);
+        if (err != cudaSuccess) return err;
         attr_done.fetch_or(bit, std::memory_order_acq_rel);
     }
     int grid = di.sm_count;
@@ -307,12 +333,15 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
     if (grid < 1) grid = 1;
     const int rows_base = N / grid;
     const int rows_extra = N % grid;
-    kern<<<grid, nvec + 32, smem, stream>>>(
-        static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up),
-        static_cast<const unsigned char *>(qweight), static_cast<const uint16_t *>(scales),
-        static_cast<uint16_t *>(out), M, K, N, group, rows_base, rows_extra, S, act_stages,
-        M <= MB ? 1 : 0);
+    const int pre_stages = (launch_flags() & FD_LAUNCH_PDL) ? 2 : 0;
+    err = launch_kernel(kern, dim3(grid), dim3(nvec + 32), smem, stream, 1,
+                        static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up),
+                        static_cast<const unsigned char *>(qweight),
+                        static_cast<const uint16_t *>(scales), static_cast<uint16_t *>(out), M,
+                        K, N, group, rows_base, rows_extra, S, act_stages, pre_stages,
+                        M <= MB ? 1 : 0);
     *launched = true;
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

@@ -21,6 +21,40 @@ struct DeviceInfo {
 // Returns cudaSuccess and fills `info` for the current device.
 cudaError_t device_info(DeviceInfo *info);
 
+// Process-wide launch options (fd_set_launch_flags), FD_LAUNCH_* bits.
+unsigned launch_flags();
+
+// Launches `kern` on `stream`; with FD_LAUNCH_PDL set the launch allows programmatic
+// dependent launch (the kernel may start while the previous kernel in the stream is
+// finishing; each kernel waits on griddepcontrol before it touches data that a previous
+// kernel produces).
+// `cluster` > 1 launches thread-block clusters of that many CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, int cluster, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    cfg.attrs = attr;
+    cfg.numAttrs = 0;
+    if (launch_flags() & FD_LAUNCH_PDL) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        ++cfg.numAttrs;
+    }
+    if (cluster > 1) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = (unsigned)cluster;
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ------------------------------------------------------------------------------------
 // Launchers (host). Arguments are validated by the C-ABI layer before these run.
 // ------------------------------------------------------------------------------------
@@ -39,6 +73,14 @@ cudaError_t launch_w4_dequant_debug(const void *qweight, const void *scales, flo
 // ------------------------------------------------------------------------------------
 // Device helpers.
 // ------------------------------------------------------------------------------------
+
+// Programmatic dependent launch: wait until the previous kernel in the stream has
+// completed and its writes are visible (a no-op for an ordinary launch), and allow the
+// next kernel to begin launching.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // L2 policy for data touched once per call (activations, streamed weights, outputs).
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -27,6 +27,16 @@ def set_gemv_path(path: str) -> str:
     return prev
 
 
+def set_pdl(enabled: bool) -> bool:
+    """Turn programmatic dependent launch on or off for every later fd launch in this
+    process; returns the previous setting. See FD_LAUNCH_PDL in include/fd.h for the
+    condition under which it is safe (no in-flight kernel writes the weight tensors)."""
+    lib = _lib.load()
+    prev = bool(lib.fd_get_launch_flags() & _lib.FD_LAUNCH_PDL)
+    _lib.check(lib.fd_set_launch_flags(_lib.FD_LAUNCH_PDL if enabled else 0))
+    return prev
+
+
 def _stream_handle(stream: torch.cuda.Stream | None) -> ctypes.c_void_p:
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(int(s.cuda_stream))

@@ -11,7 +11,7 @@ from __future__ import annotations
 
 import torch
 
-from .kernels import decode_mlp_step
+from .kernels import decode_mlp_step, set_pdl
 
 
 class DecodeStep:
@@ -24,7 +24,7 @@ class DecodeStep:
     """
 
     def __init__(self, layers, hidden: int, inter: int, group: int, eps: float,
-                 device="cuda", stream: torch.cuda.Stream | None = None):
+                 device="cuda", stream: torch.cuda.Stream | None = None, pdl: bool = True):
         self.device = torch.device(device)
         self.eps = eps
         self.group = group
@@ -40,6 +40,9 @@ class DecodeStep:
         self.layers = [dict(rms_weight=l["rms_weight"], qweight=l["qweight"], scales=l["scales"],
                             gate=self.gate[i], up=self.up[i]) for i, l in enumerate(layers)]
         self.graph = None
+        # Programmatic dependent launch between the step's kernels: each GEMV starts
+        # streaming its (constant) weights while the add-RMSNorm before it runs.
+        self.pdl = pdl
 
     def _launch(self):
         return decode_mlp_step(self.x, self.residual, self.layers, self.eps, self.group,
@@ -49,12 +52,16 @@ class DecodeStep:
         """Warm up once outside capture (module load, cached launch facts), then record."""
         saved = (self.x.clone(), self.residual.clone())
         self.stream.wait_stream(torch.cuda.current_stream(self.device))
-        with torch.cuda.stream(self.stream):
-            self._launch()
-        self.stream.synchronize()
-        self.graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.graph, stream=self.stream):
-            self._launch()
+        prev = set_pdl(self.pdl)
+        try:
+            with torch.cuda.stream(self.stream):
+                self._launch()
+            self.stream.synchronize()
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=self.stream):
+                self._launch()
+        finally:
+            set_pdl(prev)
         self.x.copy_(saved[0])
         self.residual.copy_(saved[1])
         torch.cuda.synchronize(self.device)

@@ -96,3 +96,45 @@ def test_decode_step_graph_and_eager_agree_bitwise(cuda_device, step_data):
     b = run_step(step_data, graph=True)
     for ta, tb in zip(a[0] + a[1] + [a[2]], b[0] + b[1] + [b[2]]):
         assert np.array_equal(ta, tb)
+
+
+def _step_outputs(d, pdl: bool):
+    from memory_bound_decode_fd_gb300.step import DecodeStep
+
+    layers = device_layers(d)
+    step = DecodeStep([{k: L[k] for k in ("rms_weight", "qweight", "scales")} for L in layers],
+                      d["hidden"], d["layers"][0]["gate"].shape[1], d["group"], EPS, pdl=pdl)
+    step.x.copy_(dev_bf16(d["x"]))
+    step.residual.copy_(dev_bf16(d["residual"]))
+    for i, L in enumerate(layers):
+        step.gate[i].copy_(L["gate"])
+        step.up[i].copy_(L["up"])
+    step.capture()
+    step.replay()
+    torch.cuda.synchronize()
+    return [host_bits(t) for t in step.normed] + [host_bits(t) for t in step.y] + [host_bits(step.residual)]
+
+
+def test_decode_step_with_pdl_matches_plain_launches(cuda_device, step_data, oracle_chain):
+    # Programmatic dependent launch lets each kernel start while the previous one runs;
+    # the results must be identical to ordinary stream-ordered launches, and match the
+    # oracle's chain.
+    plain = _step_outputs(step_data, pdl=False)
+    pdl = _step_outputs(step_data, pdl=True)
+    for a, b in zip(plain, pdl):
+        assert np.array_equal(a, b)
+    record, _, res_ref = oracle_chain
+    L = len(record)
+    for layer, (h_ref, yn_ref, yn_eager, y_ref) in enumerate(record):
+        stated_bar(bf16_f64(pdl[layer]), yn_ref)
+        stated_bar(bf16_f64(pdl[L + layer]), y_ref)
+    stated_bar(bf16_f64(pdl[-1]), bf16_f64(res_ref))
+
+
+def test_pdl_flag_roundtrip(cuda_device):
+    prev = fd.set_pdl(True)
+    assert fd.load_library().fd_get_launch_flags() == 1
+    fd.set_pdl(False)
+    assert fd.load_library().fd_get_launch_flags() == 0
+    fd.set_pdl(prev)
+    assert fd.load_library().fd_set_launch_flags(4) == fd.FD_ERR_UNSUPPORTED

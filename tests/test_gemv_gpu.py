@@ -1,6 +1,8 @@
 """GPU parity of fd_swiglu_w4a16_gemv and fd_w4_dequant_debug against the CPU oracle,
 called through the C ABI (via the ctypes binding) on seeded synthetic inputs."""
 
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -153,6 +155,8 @@ def test_gemv_allocates_nothing(gemv_path):
     q, s = dev_i32(d["qweight"]), dev_bf16(d["scales"])
     out = torch.empty((1, 2560), dtype=torch.bfloat16, device="cuda")
     fd.swiglu_w4a16_gemv(g, u, q, s, out=out)  # first call loads the module
+    gc.collect()  # tensors of earlier tests are freed now, not during the measurement
+    gc.disable()
     torch.cuda.synchronize()
     before = torch.cuda.memory_allocated()
     free_before, _ = torch.cuda.mem_get_info()
@@ -160,6 +164,7 @@ def test_gemv_allocates_nothing(gemv_path):
     for _ in range(5):
         fd.swiglu_w4a16_gemv(g, u, q, s, out=out)
     torch.cuda.synchronize()
+    gc.enable()
     assert torch.cuda.memory_allocated() == before
     assert torch.cuda.max_memory_allocated() == before
     free_after, _ = torch.cuda.mem_get_info()

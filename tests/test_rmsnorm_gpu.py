@@ -1,5 +1,7 @@
 """GPU parity of fd_add_rmsnorm against the CPU oracle, through the C ABI."""
 
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -66,6 +68,8 @@ def test_rmsnorm_allocates_nothing(cuda_device):
     x, r, w = dev_bf16(d["x"]), dev_bf16(d["residual"]), dev_bf16(d["weight"])
     y, h = torch.empty_like(x), torch.empty_like(x)
     fd.add_rmsnorm(x, r, w, 1e-6, out=y, residual_out=h)
+    gc.collect()  # tensors of earlier tests are freed now, not during the measurement
+    gc.disable()
     torch.cuda.synchronize()
     before = torch.cuda.memory_allocated()
     free_before, _ = torch.cuda.mem_get_info()
@@ -73,6 +77,7 @@ def test_rmsnorm_allocates_nothing(cuda_device):
     for _ in range(5):
         fd.add_rmsnorm(x, r, w, 1e-6, out=y, residual_out=h)
     torch.cuda.synchronize()
+    gc.enable()
     assert torch.cuda.memory_allocated() == before
     assert torch.cuda.max_memory_allocated() == before
     assert torch.cuda.mem_get_info()[0] == free_before
