@@ -432,16 +432,41 @@ def bench_single(args, device, rank, world):
         kname, desc = "add_rmsnorm", f"add-RMSNorm rows={rows} hidden={hidden} eps {spec['eps']}, seed {spec['seed']}"
 
     stream = torch.cuda.Stream(device)
-    with torch.cuda.stream(stream):
-        for c in calls:
-            c()
-    stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for c in calls:
-            c()
+
+    def capture():
+        with torch.cuda.stream(stream):
+            for c in calls:
+                c()
+        stream.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for c in calls:
+                c()
+        return gr
+
+    graph = capture()
     replay = lambda: graph.replay()  # noqa: E731
     reps = max(1, math.ceil(args.steps / len(calls)))
+    compare = None
+    if kind == "batched":
+        # The batched shape runs on the tensor-core kernel; time the CUDA-core kernel on
+        # the same calls for comparison (a short run: it is compute bound).
+        M, K, N, g = spec["M"], spec["K"], spec["N"], spec["group"]
+        compare = {"selected": "tensor" if fd.gemv_uses_tensor_cores(M, K, N, g) else "cuda_core"}
+        for path in ("tensor", "cuda_core"):
+            prev = fd.set_gemv_path(path)
+            try:
+                gr = capture()
+            finally:
+                fd.set_gemv_path(prev)
+            with torch.cuda.stream(stream):
+                time_region(stream, gr.replay, 2)
+                n = 2 if path == "cuda_core" else max(2, reps // 4)
+                t_ms = time_region(stream, gr.replay, n)
+            us = t_ms * 1e3 / (n * len(calls))
+            compare[f"{path}_us_per_call"] = round(us, 3)
+            compare[f"{path}_tflops"] = round(fd.gemv_flops(M, K, N) / (us * 1e-6) / 1e12, 1)
+            del gr
     hbm_peak, peak_kind, _ = read_peaks()
     sampler = ClockSampler(smi_index())
     sampler.start()
@@ -475,6 +500,7 @@ def bench_single(args, device, rank, world):
         "e2e": None,
         "gpu_launches": n_calls,
         "clocks": clocks,
+        **({"paths": compare} if compare else {}),
     }
 
 

@@ -106,19 +106,32 @@ int fd_add_rmsnorm(const void *x, const void *residual, const void *weight, floa
 
 /*
  * Kernel selection for fd_swiglu_w4a16_gemv (process-wide, thread-safe; default AUTO).
- *   FD_GEMV_AUTO     the bulk-copy kernel where its layout rules hold (K % 1024 == 0,
- *                    K <= 15360, (K / group) % 8 == 0), else the CUDA-core ring kernel.
+ *   FD_GEMV_AUTO     M >= 16: the tensor-core kernel where its layout rules hold
+ *                    (K % 1024 == 0, N % 128 == 0, group % 64 == 0, (K / group) % 8 == 0);
+ *                    otherwise the CUDA-core bulk-copy kernel where its rules hold
+ *                    (K % 1024 == 0, K <= 15360, (K / group) % 8 == 0), else the
+ *                    CUDA-core ring kernel.
  *   FD_GEMV_CUDA_CORE  always the per-thread cp.async ring kernel (any valid shape).
  *   FD_GEMV_BULK     the bulk-copy kernel where it applies, else the ring kernel.
- * Results of every path meet the same accuracy bound; the choice exists for tests and
- * for measuring one kernel against another. Returns FD_ERR_UNSUPPORTED for an unknown
- * value.
+ *   FD_GEMV_TENSOR   the tensor-core kernel where its rules hold (any M), else as AUTO
+ *                    for M < 16.
+ * The CUDA-core paths compute the activation in fp32 and the weights exactly; the
+ * tensor-core path rounds both MMA operands, silu(g) * u and q * s, to bf16 (fp32
+ * accumulation). Every path meets the documented tolerance; the choice exists for tests
+ * and for measuring one kernel against another. Returns FD_ERR_UNSUPPORTED for an
+ * unknown value.
  */
 #define FD_GEMV_AUTO 0
 #define FD_GEMV_CUDA_CORE 1
 #define FD_GEMV_BULK 2
+#define FD_GEMV_TENSOR 3
 int fd_set_gemv_path(int path);
 int fd_get_gemv_path(void);
+
+/* 1 if fd_swiglu_w4a16_gemv, under the current kernel selection, runs this shape on the
+ * tensor-core kernel (whose operands are rounded to bf16), else 0. Host-only; no CUDA
+ * call. */
+int fd_gemv_uses_tensor_cores(int M, int K, int N, int group);
 
 /*
  * Launch options (process-wide, thread-safe; default 0).

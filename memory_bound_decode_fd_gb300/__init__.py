@@ -30,6 +30,7 @@ from .kernels import (  # noqa: F401
     GEMV_PATHS,
     add_rmsnorm,
     decode_mlp_step,
+    gemv_uses_tensor_cores,
     set_gemv_path,
     set_pdl,
     swiglu_w4a16_gemv,

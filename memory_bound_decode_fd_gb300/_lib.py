@@ -19,6 +19,7 @@ FD_ERR_OVERLAP = 6
 FD_GEMV_AUTO = 0
 FD_GEMV_CUDA_CORE = 1
 FD_GEMV_BULK = 2
+FD_GEMV_TENSOR = 3
 
 FD_LAUNCH_PDL = 1
 
@@ -38,6 +39,7 @@ SIGNATURES = {
     "fd_version": (_I, []),
     "fd_set_gemv_path": (_I, [_I]),
     "fd_get_gemv_path": (_I, []),
+    "fd_gemv_uses_tensor_cores": (_I, [_I, _I, _I, _I]),
     "fd_set_launch_flags": (_I, [ctypes.c_uint]),
     "fd_get_launch_flags": (ctypes.c_uint, []),
 }

@@ -13,6 +13,8 @@ namespace fd {
 namespace {
 
 constexpr int kMaxDevices = 64;
+// Smallest M that FD_GEMV_AUTO sends to the tensor-core path.
+constexpr int kTensorCoreMinM = 16;
 std::atomic<int> g_info_ready[kMaxDevices];
 DeviceInfo g_info[kMaxDevices];
 thread_local int g_last_cuda_error = 0;
@@ -93,6 +95,12 @@ int fd_swiglu_w4a16_gemv(const void *gate, const void *up, const void *qweight,
         return FD_ERR_OVERLAP;
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
     const int path = g_gemv_path.load(std::memory_order_relaxed);
+    if (fd_gemv_uses_tensor_cores(M, K, N, group)) {
+        bool launched = false;
+        cudaError_t err = launch_gemv_tc(gate, up, qweight, scales, out, M, K, N, group, st_,
+                                         &launched);
+        if (err != cudaSuccess || launched) return from_cuda(err);
+    }
     if (path == FD_GEMV_AUTO || path == FD_GEMV_BULK) {
         bool launched = false;
         cudaError_t err = launch_gemv_tma(gate, up, qweight, scales, out, M, K, N, group, st_,
@@ -102,8 +110,15 @@ int fd_swiglu_w4a16_gemv(const void *gate, const void *up, const void *qweight,
     return from_cuda(launch_gemv_cc(gate, up, qweight, scales, out, M, K, N, group, st_));
 }
 
+int fd_gemv_uses_tensor_cores(int M, int K, int N, int group) {
+    if (M <= 0 || K <= 0 || N <= 0 || group <= 0) return 0;
+    const int path = g_gemv_path.load(std::memory_order_relaxed);
+    const bool wanted = (path == FD_GEMV_AUTO && M >= kTensorCoreMinM) || path == FD_GEMV_TENSOR;
+    return wanted && gemv_tc_supported(M, K, N, group) ? 1 : 0;
+}
+
 int fd_set_gemv_path(int path) {
-    if (path < FD_GEMV_AUTO || path > FD_GEMV_BULK) return FD_ERR_UNSUPPORTED;
+    if (path < FD_GEMV_AUTO || path > FD_GEMV_TENSOR) return FD_ERR_UNSUPPORTED;
     g_gemv_path.store(path, std::memory_order_relaxed);
     return FD_OK;
 }

@@ -1,0 +1,524 @@
+// fd_gemv_tc.cu - SwiGLU-prologue W4A16 product for batched decode (M >= 16) on the
+// fifth-generation tensor cores (tcgen05.mma, accumulator in tensor memory).
+//
+// y[m, n] = bf16( sum_k a[m, k] * w[n, k] ),  a = silu(g) * u,  w = q * s[n, k / group]
+//
+// Sources: "09 - Operator fusion", section 5 (taxonomy item 4, GEMM prologue fusion:
+// the int4 weights are dequantised on chip as they stream in; "The fusion boundary
+// problem": act = silu(gate) * up feeds act @ W_down); "PyTorch Community Proposes Fusion
+// Fix ..." ("Fix proposal": the activation and the dequantised weights are never written
+// to memory).
+//
+// At M = 64 a weight byte feeds 256 flops, at the tensor-core ridge of this GPU, so the
+// product runs on the tensor cores while the CUDA cores do the two prologues:
+//   * A CTA owns 128 weight rows (the MMA's M) and a quarter of K; the four CTAs of a
+//     thread-block cluster hold the four quarters of the same rows and combine their
+//     fp32 partial sums through distributed shared memory at the end (no global
+//     scratch, one bf16 store per output).
+//   * Warp 0 streams int4 weight tiles (128 rows x 64 k, 4 KB) and the CTA's scales with
+//     tensor-map bulk copies; warp 1 streams the matching gate/up tiles (M rows x 64 k).
+//   * Eight worker warps turn each step into MMA operands in shared memory:
+//       A = bf16(q * s) for the 128 x 64 weight tile (packed bf16x2 arithmetic: the
+//           nibble is placed in the mantissa of 128.0, 136 is subtracted exactly and the
+//           product with the group scale is rounded once), and
+//       B = bf16(silu(g) * u) for the M x 64 activation tile (fp32, tanh form of silu).
+//     Both use the same order of k inside each 8-k core matrix (k0 k4 k1 k5 k2 k6 k3 k7),
+//     which leaves the dot product unchanged.
+//   * Warp 2 lane 0 issues four tcgen05.mma (M = 128, N = M padded, K = 16) per step
+//     into one TMEM accumulator and returns the operand stage through tcgen05.commit.
+//   * Every wait is bounded (fd_tma.cuh); a CTA that gives up still takes part in both
+//     cluster barriers, frees its TMEM, and its cluster writes NaN to the outputs.
+#include <atomic>
+
+#include <cudaTypedefs.h>
+
+#include "fd_gemv_common.cuh"
+#include "fd_tc.cuh"
+
+namespace fd {
+namespace {
+
+constexpr int kTcRows = 128;                 // weight rows per CTA (MMA M)
+constexpr int kTcStepK = 64;                 // k per pipeline step
+constexpr int kTcSplit = 4;                  // CTAs per cluster (K quarters)
+constexpr int kTcWorkerWarps = 8;
+constexpr int kTcFirstWorker = 3;            // warps 0, 1, 2: weights, gate/up, MMA
+constexpr int kTcThreads = (kTcFirstWorker + kTcWorkerWarps) * 32;
+constexpr int kTcWorkers = kTcWorkerWarps * 32;
+constexpr int kTcMaxStages = 16;
+constexpr uint32_t kWStageBytes = kTcRows * kTcStepK / 2;  // int4 tile: 4096
+constexpr uint32_t kATileBytes = kTcRows * kTcStepK * 2;   // bf16 A tile: 16384
+constexpr uint32_t kCoreBytes = 128;                       // 8 rows x 16 bytes
+constexpr uint32_t kGroupBytes = 8 * kCoreBytes;           // 8-row group of a 64-k tile
+
+// Bias of the nibble trick: bf16 0x4300 | u is 128 + u, and u = q + 8.
+constexpr uint32_t kMagic136x2 = 0x43084308u;
+
+__device__ __forceinline__ float silu_mul_tanh(float g, float u) {
+    // silu(g) * u = (g u / 2) (1 + tanh(g / 2)); one MUFU operation per element.
+    const float h = 0.5f * g;
+    const float p = h * u;
+    return fmaf(p, tanh_approx(h), p);
+}
+
+// Bounded wait that ignores the abort flag: used where the CTA must not go on before the
+// hardware is done (copies landing, MMAs completing), even after a failure.
+__device__ __forceinline__ void wait_parity_hw(uint64_t *bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_test_parity(bar, parity) && clock64() - t0 < kWaitLimitCycles) __nanosleep(64);
+}
+
+template <int NPAD>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemv_tc_kernel(const __grid_constant__ CUtensorMap map_w,
+                   const __grid_constant__ CUtensorMap map_s,
+                   const __grid_constant__ CUtensorMap map_g,
+                   const __grid_constant__ CUtensorMap map_u, uint16_t *__restrict__ out,
+                   int M, int N, int group, int k_cta, int s_w, int s_gu, int s_op,
+                   uint32_t off_gu, uint32_t off_op, uint32_t off_sc, int sg) {
+    static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 128, "N of the MMA");
+    constexpr int kCols = NPAD < 32 ? 32 : NPAD;  // TMEM columns (power of two)
+    constexpr uint32_t kGuTile = NPAD * 128;      // one gate or up tile (NPAD x 64 bf16)
+    constexpr uint32_t kGuStage = 2 * kGuTile;
+    constexpr uint32_t kOpStage = kATileBytes + NPAD * 128;
+    constexpr int kHalf = NPAD / 2;               // accumulator columns per epilogue warp
+
+    __shared__ __align__(8) uint64_t w_full[kTcMaxStages], w_empty[kTcMaxStages];
+    __shared__ __align__(8) uint64_t gu_full[kTcMaxStages], gu_empty[kTcMaxStages];
+    __shared__ __align__(8) uint64_t op_full[kTcMaxStages], op_empty[kTcMaxStages];
+    __shared__ __align__(8) uint64_t sc_full, acc_full;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ uint32_t peer_abort[kTcSplit];
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte aligned base (swizzled tensor-map destinations need it).
+    unsigned char *smem = smem_raw + (((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw));
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int n0 = blockIdx.y * kTcRows;
+    const int k0 = (int)rank * k_cta;
+    const int n_steps = k_cta / kTcStepK;
+    const int x0_scale = (k0 / group) & ~7;
+
+    if (tid == 0) {
+        for (int s = 0; s < kTcMaxStages; ++s) {
+            mbar_init(&w_full[s], 1);
+            mbar_init(&w_empty[s], kTcWorkerWarps);
+            mbar_init(&gu_full[s], 1);
+            mbar_init(&gu_empty[s], kTcWorkerWarps);
+            mbar_init(&op_full[s], kTcWorkerWarps);
+            mbar_init(&op_empty[s], 1);
+        }
+        mbar_init(&sc_full, 1);
+        mbar_init(&acc_full, 1);
+        abort_flag = 0;
+        for (int p = 0; p < kTcSplit; ++p) peer_abort[p] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(&tmem_slot, kCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    grid_dep_launch();
+
+    if (warp == 0) {
+        // -------------------------------------------------- weights + scales (constant)
+        if (lane == 0) {
+            prefetch_tensormap(&map_w);
+            prefetch_tensormap(&map_s);
+            const uint64_t pol_w = policy_evict_first();
+            mbar_arrive_expect_tx(&sc_full, (uint32_t)kTcRows * sg * 2);
+            tma_load_2d(smem + off_sc, &map_s, x0_scale, n0, &sc_full, pol_w);
+            int s = 0, round = 0, issued = 0;
+            for (int t = 0; t < n_steps; ++t) {
+                if (round > 0 && !mbar_wait_bounded(&w_empty[s], (round - 1) & 1, &abort_flag))
+                    break;
+                mbar_arrive_expect_tx(&w_full[s], kWStageBytes);
+                tma_load_2d(smem + (size_t)s * kWStageBytes, &map_w, (k0 + t * kTcStepK) / 2, n0,
+                            &w_full[s], pol_w);
+                issued = t + 1;
+                if (++s == s_w) { s = 0; ++round; }
+            }
+            for (int t = issued > s_w ? issued - s_w : 0; t < issued; ++t)
+                wait_parity_hw(&w_full[t % s_w], (t / s_w) & 1);
+            wait_parity_hw(&sc_full, 0);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // -------------------------------------------------- gate / up tiles
+        if (lane == 0) {
+            prefetch_tensormap(&map_g);
+            prefetch_tensormap(&map_u);
+            grid_dep_wait();  // gate/up may be written by the previous kernel
+            const uint64_t pol = policy_evict_last();  // every n-tile re-reads them
+            int s = 0, round = 0, issued = 0;
+            for (int t = 0; t < n_steps; ++t) {
+                if (round > 0 && !mbar_wait_bounded(&gu_empty[s], (round - 1) & 1, &abort_flag))
+                    break;
+                unsigned char *st = smem + off_gu + (size_t)s * kGuStage;
+                mbar_arrive_expect_tx(&gu_full[s], kGuStage);
+                tma_load_2d(st, &map_g, k0 + t * kTcStepK, 0, &gu_full[s], pol);
+                tma_load_2d(st + kGuTile, &map_u, k0 + t * kTcStepK, 0, &gu_full[s], pol);
+                issued = t + 1;
+                if (++s == s_gu) { s = 0; ++round; }
+            }
+            for (int t = issued > s_gu ? issued - s_gu : 0; t < issued; ++t)
+                wait_parity_hw(&gu_full[t % s_gu], (t / s_gu) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // -------------------------------------------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kTcRows, NPAD);
+            int s = 0, phase = 0;
+            for (int t = 0; t < n_steps; ++t) {
+                if (!mbar_wait_bounded(&op_full[s], phase, &abort_flag)) break;
+                tc_fence_after();
+                const uint32_t a_base = smem_u32(smem + off_op + (size_t)s * kOpStage);
+                const uint32_t b_base = a_base + kATileBytes;
+#pragma unroll
+                for (int j = 0; j < kTcStepK / 16; ++j) {
+                    const uint64_t ad = smem_desc_interleaved(a_base + j * 2 * kCoreBytes,
+                                                              kCoreBytes, kGroupBytes);
+                    const uint64_t bd = smem_desc_interleaved(b_base + j * 2 * kCoreBytes,
+                                                              kCoreBytes, kGroupBytes);
+                    tc_mma_f16(tmem, ad, bd, idesc, (t | j) != 0);
+                }
+                tc_commit(&op_empty[s]);
+                if (++s == s_op) { s = 0; phase ^= 1; }
+            }
+            tc_commit(&acc_full);  // fires once every MMA issued above has completed
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------- workers: operand prologues
+        const int wt = tid - kTcFirstWorker * 32;
+        const uint32_t key = opaque_u32(kMagic136x2);
+        const uint32_t magic = opaque_u32(kMagic136x2);
+        const int row = wt & (kTcRows - 1);  // dequant: weight row and 32-k half
+        const int h = wt >> 7;
+        const int steps_per_group = group / kTcStepK;
+        int gcol = k0 / group - x0_scale;
+        int gstep = (k0 % group) / kTcStepK;
+        const uint16_t *sc_row = reinterpret_cast<const uint16_t *>(smem + off_sc) + row * sg;
+        bool ok = mbar_wait_bounded(&sc_full, 0, &abort_flag);
+        int ws = 0, wph = 0, gs = 0, gph = 0, os = 0, oround = 0;
+        for (int t = 0; t < n_steps && ok; ++t) {
+            ok = mbar_wait_bounded(&w_full[ws], wph, &abort_flag) &&
+                 mbar_wait_bounded(&gu_full[gs], gph, &abort_flag) &&
+                 (oround == 0 || mbar_wait_bounded(&op_empty[os], (oround - 1) & 1, &abort_flag));
+            if (!ok) break;
+            unsigned char *A = smem + off_op + (size_t)os * kOpStage;
+            // ---- A: dequantised weights, 128 rows x 64 k
+            {
+                const unsigned char *wst = smem + (size_t)ws * kWStageBytes;
+                // 32-byte swizzle of the tensor-map copy: 16-byte half h of row r sits at
+                // position h ^ bit 2 of r.
+                const uint4 wv = *reinterpret_cast<const uint4 *>(
+                    wst + row * 32 + ((h ^ ((row >> 2) & 1)) << 4));
+                const uint32_t sc = sc_row[gcol];
+                const uint32_t s2 = sc | (sc << 16);
+                uint4 *dst = reinterpret_cast<uint4 *>(A + (row >> 3) * kGroupBytes + (row & 7) * 16 +
+                                                       h * 4 * kCoreBytes);
+                const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    // pairs (k_j, k_j+4) of the word's 8 k: 136 + q as bf16, exact
+                    const uint32_t w = wd[i];
+                    const uint32_t t0 = mask_xor<0x000F000Fu>(w, key);
+                    const uint32_t t1 = mask_xor<0x000F000Fu>(w >> 4, key);
+                    const uint32_t t2 = mask_xor<0x000F000Fu>(w >> 8, key);
+                    const uint32_t t3 = mask_xor<0x000F000Fu>(w >> 12, key);
+                    uint4 o;
+                    o.x = bf16x2_mul(bf16x2_sub(t0, magic), s2);
+                    o.y = bf16x2_mul(bf16x2_sub(t1, magic), s2);
+                    o.z = bf16x2_mul(bf16x2_sub(t2, magic), s2);
+                    o.w = bf16x2_mul(bf16x2_sub(t3, magic), s2);
+                    dst[i * (kCoreBytes / 16)] = o;
+                }
+            }
+            // ---- B: activations, NPAD rows x 64 k
+            {
+                const unsigned char *G = smem + off_gu + (size_t)gs * kGuStage;
+                const unsigned char *U = G + kGuTile;
+                unsigned char *B = A + kATileBytes;
+#pragma unroll
+                for (int j = 0; j < (NPAD * 8 + kTcWorkers - 1) / kTcWorkers; ++j) {
+                    const int item = wt + j * kTcWorkers;
+                    if (item < NPAD * 8) {
+                        // lanes 0..7 take rows 0..7 of one core matrix: conflict-free reads
+                        // (128-byte swizzle: chunk c of row m at c ^ (m & 7)) and writes.
+                        const int m = (item & 7) | ((item >> 6) << 3);
+                        const int c = (item >> 3) & 7;
+                        const uint32_t soff = m * 128 + ((c ^ (m & 7)) << 4);
+                        const uint4 gv = *reinterpret_cast<const uint4 *>(G + soff);
+                        const uint4 uv = *reinterpret_cast<const uint4 *>(U + soff);
+                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                        const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+                        float a[8];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            a[2 * i] = silu_mul_tanh(bf16lo(gw[i]), bf16lo(uw[i]));
+                            a[2 * i + 1] = silu_mul_tanh(bf16hi(gw[i]), bf16hi(uw[i]));
+                        }
+                        uint4 o;
+                        o.x = pack_bf16x2(a[0], a[4]);
+                        o.y = pack_bf16x2(a[1], a[5]);
+                        o.z = pack_bf16x2(a[2], a[6]);
+                        o.w = pack_bf16x2(a[3], a[7]);
+                        *reinterpret_cast<uint4 *>(B + (m >> 3) * kGroupBytes + c * kCoreBytes +
+                                                   (m & 7) * 16) = o;
+                    }
+                }
+            }
+            // generic-proxy writes (A, B) before the tensor core reads them; generic reads
+            // of the input stages before the next bulk copy overwrites them
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&w_empty[ws]);
+                mbar_arrive(&gu_empty[gs]);
+                mbar_arrive(&op_full[os]);
+            }
+            if (++ws == s_w) { ws = 0; wph ^= 1; }
+            if (++gs == s_gu) { gs = 0; gph ^= 1; }
+            if (++os == s_op) { os = 0; ++oround; }
+            if (++gstep == steps_per_group) { gstep = 0; ++gcol; }
+        }
+        __syncwarp();
+    }
+
+    // ------------------------------------------------------ epilogue
+    uint32_t v[kHalf];
+    const bool worker = warp >= kTcFirstWorker;
+    const int quarter = warp & 3;                       // TMEM lanes 32q .. 32q + 31
+    const int col0 = ((warp - kTcFirstWorker) >> 2) * kHalf;
+    if (worker) {
+        wait_parity_hw(&acc_full, 0);
+        __syncwarp();
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kHalf / 8; ++c) {
+            uint32_t r[8];
+            tmem_ld_x8(tmem + ((uint32_t)(32 * quarter) << 16) + col0 + 8 * c, r);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[8 * c + i] = r[i];
+        }
+        tmem_ld_wait();
+    }
+    tc_fence_before();
+    __syncwarp();
+    // #1: every CTA of the cluster is done with its rings (copies landed, MMAs complete),
+    // so the ring memory can take the partial sums.
+    cluster_sync_all();
+    const uint32_t recv = smem_u32(smem + off_gu);  // [src rank][NPAD][32] fp32
+    if (worker) {
+        const uint32_t dst = map_to_rank(recv, (uint32_t)quarter);
+#pragma unroll
+        for (int j = 0; j < kHalf; ++j)
+            st_cluster_f32(dst + (((rank * NPAD) + col0 + j) * 32 + lane) * 4,
+                           __uint_as_float(v[j]));
+    }
+    if (tid == 0) {
+        for (int p = 0; p < kTcSplit; ++p)
+            st_cluster_u32(map_to_rank(smem_u32(&peer_abort[rank]), (uint32_t)p),
+                           (uint32_t)abort_flag);
+    }
+    __syncwarp();
+    // #2: all partial sums and failure flags have arrived.
+    cluster_sync_all();
+    if (worker) {
+        grid_dep_wait();  // the previous kernel in the stream may still use `out`
+        const float *rv = reinterpret_cast<const float *>(smem + off_gu);
+        const bool failed = (peer_abort[0] | peer_abort[1] | peer_abort[2] | peer_abort[3]) != 0;
+        const int wt = tid - kTcFirstWorker * 32;
+        for (int i = wt; i < M * 16; i += kTcWorkers) {
+            const int m = i >> 4, rp = (i & 15) * 2;
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int src = 0; src < kTcSplit; ++src) {
+                const float2 p = *reinterpret_cast<const float2 *>(rv + ((src * NPAD) + m) * 32 + rp);
+                s0 += p.x;
+                s1 += p.y;
+            }
+            const uint32_t o = failed ? 0x7FC07FC0u : pack_bf16x2(s0, s1);
+            *reinterpret_cast<uint32_t *>(out + (size_t)m * N + n0 + 32 * rank + rp) = o;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiled encode_fn() {
+    static std::atomic<void *> fn{nullptr};
+    void *f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !f)
+            return nullptr;
+        fn.store(f, std::memory_order_release);
+    }
+    return reinterpret_cast<EncodeTiled>(f);
+}
+
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base, uint64_t dim0,
+               uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1,
+               CUtensorMapSwizzle swizzle) {
+    EncodeTiled enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {dim0, dim1};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box0, box1};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, type, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct TcPlan {
+    int s_w, s_gu, s_op, sg;
+    uint32_t off_gu, off_op, off_sc, smem;
+};
+
+// Shared-memory plan: a deep ring of int4 weight tiles (the HBM stream), then as many
+// gate/up and operand stages as fit (2..4 each).
+bool make_plan(int npad, int k_cta, int group, size_t budget, TcPlan *p) {
+    const uint32_t gu_stage = 2u * npad * 128;
+    const uint32_t op_stage = kATileBytes + npad * 128u;
+    p->sg = ((k_cta + group - 1) / group + 7 + 7) & ~7;
+    if (p->sg > 256) return false;
+    p->s_w = 12;
+    const uint32_t w_bytes = p->s_w * kWStageBytes;
+    const uint32_t sc_bytes = ((uint32_t)kTcRows * p->sg * 2 + 1023u) & ~1023u;
+    if (budget < 1024 + w_bytes + sc_bytes) return false;
+    const size_t avail = budget - 1024 - w_bytes - sc_bytes;
+    int s_gu = 2, s_op = 2;
+    size_t used = 2 * (size_t)gu_stage + 2 * (size_t)op_stage;
+    if (used > avail) return false;
+    for (bool grew = true; grew;) {
+        grew = false;
+        if (s_op < 4 && used + op_stage <= avail) { ++s_op; used += op_stage; grew = true; }
+        if (s_gu < 4 && used + gu_stage <= avail) { ++s_gu; used += gu_stage; grew = true; }
+    }
+    p->s_gu = s_gu;
+    p->s_op = s_op;
+    p->off_gu = w_bytes;
+    p->off_op = p->off_gu + s_gu * gu_stage;
+    p->off_sc = p->off_op + s_op * op_stage;
+    p->smem = p->off_sc + sc_bytes + 1024;  // + alignment slack of the dynamic base
+    // the cluster reduction reuses the gate/up and operand rings
+    return (size_t)kTcSplit * npad * 32 * 4 <= (size_t)p->off_sc - p->off_gu;
+}
+
+template <int NPAD>
+cudaError_t launch_npad(const DeviceInfo &di, const void *gate, const void *up,
+                        const void *qweight, const void *scales, void *out, int mc, int K,
+                        int N, int group, cudaStream_t stream, bool *launched) {
+    static std::atomic<uint64_t> attr_done{0};
+    static std::atomic<int> static_smem_cache{-1};
+    auto kern = gemv_tc_kernel<NPAD>;
+    int static_smem = static_smem_cache.load(std::memory_order_relaxed);
+    if (static_smem < 0) {
+        cudaFuncAttributes fa;
+        cudaError_t err = cudaFuncGetAttributes(&fa, kern);
+        if (err != cudaSuccess) return err;
+        static_smem = (int)fa.sharedSizeBytes;
+        static_smem_cache.store(static_smem, std::memory_order_relaxed);
+    }
+    const int k_cta = K / kTcSplit;
+    TcPlan plan;
+    const size_t budget = (size_t)di.max_smem_optin - (size_t)static_smem;
+    if (!make_plan(NPAD, k_cta, group, budget, &plan)) return cudaSuccess;  // not launched
+
+    CUtensorMap mw, ms, mg, mu;
+    if (!encode_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, qweight, (uint64_t)K / 2, (uint64_t)N,
+                   (uint64_t)K / 2, kTcStepK / 2, kTcRows, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !encode_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, scales, (uint64_t)K / group,
+                   (uint64_t)N, (uint64_t)(K / group) * 2, (uint32_t)plan.sg, kTcRows,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, gate, (uint64_t)K, (uint64_t)mc,
+                   (uint64_t)K * 2, kTcStepK, NPAD, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, up, (uint64_t)K, (uint64_t)mc,
+                   (uint64_t)K * 2, kTcStepK, NPAD, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)budget);
+        if (err != cudaSuccess) return err;
+        attr_done.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    *launched = true;
+    err = launch_kernel(kern, dim3(kTcSplit, N / kTcRows), dim3(kTcThreads), plan.smem, stream,
+                        kTcSplit, mw, ms, mg, mu, static_cast<uint16_t *>(out), mc, N, group,
+                        k_cta, plan.s_w, plan.s_gu, plan.s_op, plan.off_gu, plan.off_op,
+                        plan.off_sc, plan.sg);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemv_tc_supported(int M, int K, int N, int group) {
+    if (M < 1 || K % (kTcSplit * 256) != 0 || N % kTcRows != 0) return false;
+    if (group % kTcStepK != 0 || K % group != 0 || (K / group) % 8 != 0) return false;
+    const int k_cta = K / kTcSplit;
+    return ((k_cta + group - 1) / group + 14) <= 256;
+}
+
+cudaError_t launch_gemv_tc(const void *gate, const void *up, const void *qweight,
+                           const void *scales, void *out, int M, int K, int N, int group,
+                           cudaStream_t stream, bool *launched) {
+    *launched = false;
+    if (!gemv_tc_supported(M, K, N, group)) return cudaSuccess;
+    DeviceInfo di;
+    cudaError_t err = device_info(&di);
+    if (err != cudaSuccess) return err;
+    const uint16_t *g = static_cast<const uint16_t *>(gate);
+    const uint16_t *u = static_cast<const uint16_t *>(up);
+    uint16_t *o = static_cast<uint16_t *>(out);
+    // Up to 128 activation rows per launch (the MMA's N); larger M runs in row blocks.
+    for (int m0 = 0; m0 < M; m0 += 128) {
+        const int mc = M - m0 < 128 ? M - m0 : 128;
+        const size_t ao = (size_t)m0 * K, oo = (size_t)m0 * N;
+        bool done = false;
+        if (mc <= 16)
+            err = launch_npad<16>(di, g + ao, u + ao, qweight, scales, o + oo, mc, K, N, group, stream, &done);
+        else if (mc <= 32)
+            err = launch_npad<32>(di, g + ao, u + ao, qweight, scales, o + oo, mc, K, N, group, stream, &done);
+        else if (mc <= 64)
+            err = launch_npad<64>(di, g + ao, u + ao, qweight, scales, o + oo, mc, K, N, group, stream, &done);
+        else
+            err = launch_npad<128>(di, g + ao, u + ao, qweight, scales, o + oo, mc, K, N, group, stream, &done);
+        if (err != cudaSuccess) return err;
+        if (!done) {
+            if (m0 == 0) return cudaSuccess;  // nothing launched: the caller falls back
+            return cudaErrorInvalidConfiguration;
+        }
+        *launched = true;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace fd

@@ -61,6 +61,12 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 cudaError_t launch_gemv_tma(const void *gate, const void *up, const void *qweight,
                             const void *scales, void *out, int M, int K, int N, int group,
                             cudaStream_t stream, bool *launched);
+// Tensor-core path (tcgen05) for batched decode; sets *launched = false when the shape
+// is outside its rules (K % 1024, N % 128, group % 64, (K / group) % 8).
+bool gemv_tc_supported(int M, int K, int N, int group);
+cudaError_t launch_gemv_tc(const void *gate, const void *up, const void *qweight,
+                           const void *scales, void *out, int M, int K, int N, int group,
+                           cudaStream_t stream, bool *launched);
 cudaError_t launch_gemv_cc(const void *gate, const void *up, const void *qweight,
                            const void *scales, void *out, int M, int K, int N, int group,
                            cudaStream_t stream);

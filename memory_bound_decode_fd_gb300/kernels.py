@@ -15,16 +15,22 @@ from . import _lib
 
 
 GEMV_PATHS = {"auto": _lib.FD_GEMV_AUTO, "cuda_core": _lib.FD_GEMV_CUDA_CORE,
-              "bulk": _lib.FD_GEMV_BULK}
+              "bulk": _lib.FD_GEMV_BULK, "tensor": _lib.FD_GEMV_TENSOR}
 
 
 def set_gemv_path(path: str) -> str:
-    """Select the GEMV kernel process-wide ("auto", "cuda_core" or "bulk"); returns the
+    """Select the GEMV kernel process-wide ("auto", "cuda_core", "bulk" or "tensor"); returns the
     previous selection. See fd_set_gemv_path in include/fd.h."""
     lib = _lib.load()
     prev = {v: k for k, v in GEMV_PATHS.items()}[lib.fd_get_gemv_path()]
     _lib.check(lib.fd_set_gemv_path(GEMV_PATHS[path]))
     return prev
+
+
+def gemv_uses_tensor_cores(M: int, K: int, N: int, group: int = 128) -> bool:
+    """Whether, under the current kernel selection, this GEMV shape runs on the
+    tensor-core kernel (bf16-rounded MMA operands). See fd_gemv_uses_tensor_cores."""
+    return bool(_lib.load().fd_gemv_uses_tensor_cores(M, K, N, group))
 
 
 def set_pdl(enabled: bool) -> bool:

@@ -13,6 +13,15 @@ Tolerances
     at most delta = 64 * 2^-24 * sum_k |a_k| |W_nk| + 1.05 * sum_k (amax_slice(k) / 65534) |W_nk|,
     and the single bf16 rounding adds at most 2^-8 of the value:
     |y - ref| <= 2^-8 * |ref| + 1.01 * delta.
+  * GEMV on the tensor-core path (fd_gemv_uses_tensor_cores): both MMA operands are
+    rounded to bf16, a' = bf16(silu(g) * u) with silu in its tanh form (tanh.approx.f32,
+    relative error below 2^-10.5 here; the error it leaves in a is at most
+    2^-10.5 * |g u / 2|) and w' = bf16(q * s); bf16 x bf16 products are exact in fp32
+    and the tensor core accumulates in fp32, one rounding per K = 16 step (allowed
+    2^-22 of the running magnitude each). So
+    delta = 1.01 * (2^-8 * sum_k |a_k| |W_nk| + 2^-10.5 * sum_k |g_k u_k / 2| |W_nk|)
+            + (K / 16 + 8) * 2^-22 * sum_k |a_k| |W_nk|,
+    |y - ref| <= 2^-8 * |ref| + delta.
   * add-RMSNorm: residual_out bit-exact. out against the oracle's two-rounding form
     t = bf16(h * rstd), y = bf16(t * w): the kernel's rstd is fp32, so where h * rstd sits
     next to a bf16 rounding boundary t can land one step (ulp(t)) away; that moves t * w
@@ -59,9 +68,13 @@ def stated_bar(y: np.ndarray, ref: np.ndarray, max_abs_rel=2e-2, mean_rel=4e-3) 
     return res
 
 
-def gemv_reference(gate, up, qweight, scales, group, rows=None):
-    """(ref [M, n], abs_sum [M, n], enc_err [M, n]) for all or the selected weight rows:
-    the float64 result, sum_k |a_k| |W_nk|, and sum_k (amax_slice(k) / 65534) |W_nk|."""
+TANH_REL = 2.0**-10.5
+
+
+def gemv_reference(gate, up, qweight, scales, group, rows=None, tensor_cores=False):
+    """(ref [M, n], abs_sum [M, n], extra [M, n]) for all or the selected weight rows:
+    the float64 result, sum_k |a_k| |W_nk|, and either sum_k (amax_slice(k) / 65534)
+    |W_nk| (CUDA-core paths) or sum_k |g_k u_k / 2| |W_nk| (tensor-core path)."""
     if rows is not None:
         qweight = qweight[rows]
         scales = scales[rows]
@@ -71,19 +84,36 @@ def gemv_reference(gate, up, qweight, scales, group, rows=None):
         a = a[None, :]
     w = np.abs(oracle.dequant_w4(qweight, scales, group).astype(np.float64))
     M, K = a.shape
+    if tensor_cores:
+        gu = 0.5 * np.abs(bf16_f64(gate) * bf16_f64(up)).reshape(M, K)
+        return ref, a @ w.T, gu @ w.T
     amax = a.reshape(M, K // 32, 32).max(axis=2)
     enc = np.repeat(amax / 65534.0, 32, axis=1)
     return ref, a @ w.T, enc @ w.T
 
 
-def check_gemv(y_bits, gate, up, qweight, scales, group, rows=None) -> dict:
-    ref, abs_sum, enc_err = gemv_reference(gate, up, qweight, scales, group, rows)
+def check_gemv(y_bits, gate, up, qweight, scales, group, rows=None, tensor_cores=None) -> dict:
+    """Stated bar plus the elementwise bound of the kernel that ran; by default the
+    library is asked which one that was (under the current kernel selection)."""
+    M = int(np.prod(np.shape(gate)[:-1])) if np.ndim(gate) > 1 else 1
+    K = np.shape(gate)[-1]
+    N = np.shape(qweight)[0]
+    if tensor_cores is None:
+        import memory_bound_decode_fd_gb300 as fd
+
+        tensor_cores = fd.gemv_uses_tensor_cores(M, K, N, group)
+    ref, abs_sum, extra = gemv_reference(gate, up, qweight, scales, group, rows, tensor_cores)
     y = bf16_f64(y_bits)
     if rows is not None:
         y = y[:, rows]
     res = stated_bar(y, ref)
-    delta = 64 * 2.0**-24 * abs_sum + 1.05 * enc_err
-    bound = 2.0**-8 * np.abs(ref) + 1.01 * delta
+    if tensor_cores:
+        delta = 1.01 * (2.0**-8 * abs_sum + TANH_REL * extra) + (K / 16 + 8) * 2.0**-22 * abs_sum
+        bound = 2.0**-8 * np.abs(ref) + delta
+    else:
+        delta = 64 * 2.0**-24 * abs_sum + 1.05 * extra
+        bound = 2.0**-8 * np.abs(ref) + 1.01 * delta
+    res["tensor_cores"] = bool(tensor_cores)
     err = np.abs(y - ref)
     bad = err > bound
     assert not bad.any(), (

@@ -15,10 +15,11 @@ from fd_check import GuardedBuffer, check_gemv, dev_bf16, dev_i32, host_bits
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["auto", "cuda_core"])
+@pytest.fixture(params=["auto", "cuda_core", "tensor"])
 def gemv_path(request, cuda_device):
-    """Run the test once with the default kernel choice (the bulk-copy kernel where its
-    layout rules hold) and once forcing the CUDA-core ring kernel."""
+    """Run the test with the default kernel choice (the tensor-core kernel for M >= 16,
+    else the bulk-copy kernel, where their layout rules hold), forcing the CUDA-core ring
+    kernel, and forcing the tensor-core kernel wherever its rules hold (any M)."""
     prev = fd.set_gemv_path(request.param)
     yield request.param
     fd.set_gemv_path(prev)
