@@ -15,9 +15,11 @@
 //     thread-block cluster hold the four quarters of the same rows and combine their
 //     fp32 partial sums through distributed shared memory at the end (no global
 //     scratch, one bf16 store per output).
-//   * Warp 0 streams int4 weight tiles (128 rows x 64 k, 4 KB) and the CTA's scales with
-//     tensor-map bulk copies; warp 1 streams the matching gate/up tiles (M rows x 64 k).
-//   * Eight worker warps turn each step into MMA operands in shared memory:
+//   * Warp 0 streams int4 weight tiles (128 rows x 256 k: one 128-byte line per row,
+//     16 KB) and the CTA's scales with tensor-map bulk copies; warp 1 streams the gate/up
+//     tiles (M rows x 64 k) of each 64-k step.
+//   * Sixteen worker warps turn each step into MMA operands in shared memory (eight
+//     for each operand, so the ALU-heavy and the MUFU-heavy work interleave):
 //       A = bf16(q * s) for the 128 x 64 weight tile (packed bf16x2 arithmetic: the
 //           nibble is placed in the mantissa of 128.0, 136 is subtracted exactly and the
 //           product with the group scale is rounded once), and
@@ -41,25 +43,23 @@ namespace {
 constexpr int kTcRows = 128;                 // weight rows per CTA (MMA M)
 constexpr int kTcStepK = 64;                 // k per pipeline step
 constexpr int kTcSplit = 4;                  // CTAs per cluster (K quarters)
-constexpr int kTcWorkerWarps = 8;
 constexpr int kTcFirstWorker = 3;            // warps 0, 1, 2: weights, gate/up, MMA
-constexpr int kTcThreads = (kTcFirstWorker + kTcWorkerWarps) * 32;
-constexpr int kTcWorkers = kTcWorkerWarps * 32;
+constexpr int kTcDequantWarps = 8;           // then the A-operand (weight) warps
+constexpr int kTcSiluWarps = 8;              // then the B-operand (activation) warps
+constexpr int kTcFirstSilu = kTcFirstWorker + kTcDequantWarps;
+constexpr int kTcThreads = (kTcFirstSilu + kTcSiluWarps) * 32;
+constexpr int kTcSiluThreads = kTcSiluWarps * 32;
+constexpr int kTcEpilogueThreads = kTcDequantWarps * 32;  // the dequant warps
 constexpr int kTcMaxStages = 16;
-constexpr uint32_t kWStageBytes = kTcRows * kTcStepK / 2;  // int4 tile: 4096
+constexpr int kTcWTileK = 256;               // k per weight tile (128 bytes of a row)
+constexpr int kTcStepsPerWTile = kTcWTileK / kTcStepK;
+constexpr uint32_t kWStageBytes = kTcRows * kTcWTileK / 2;  // int4 tile: 16384
 constexpr uint32_t kATileBytes = kTcRows * kTcStepK * 2;   // bf16 A tile: 16384
 constexpr uint32_t kCoreBytes = 128;                       // 8 rows x 16 bytes
 constexpr uint32_t kGroupBytes = 8 * kCoreBytes;           // 8-row group of a 64-k tile
 
 // Bias of the nibble trick: bf16 0x4300 | u is 128 + u, and u = q + 8.
 constexpr uint32_t kMagic136x2 = 0x43084308u;
-
-__device__ __forceinline__ float silu_mul_tanh(float g, float u) {
-    // silu(g) * u = (g u / 2) (1 + tanh(g / 2)); one MUFU operation per element.
-    const float h = 0.5f * g;
-    const float p = h * u;
-    return fmaf(p, tanh_approx(h), p);
-}
 
 // Bounded wait that ignores the abort flag: used where the CTA must not go on before the
 // hardware is done (copies landing, MMAs completing), even after a failure.
@@ -101,15 +101,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int n0 = blockIdx.y * kTcRows;
     const int k0 = (int)rank * k_cta;
     const int n_steps = k_cta / kTcStepK;
+    const int g_op = s_op / 2;  // operand stages per commit (the ring has two halves)
     const int x0_scale = (k0 / group) & ~7;
 
     if (tid == 0) {
         for (int s = 0; s < kTcMaxStages; ++s) {
             mbar_init(&w_full[s], 1);
-            mbar_init(&w_empty[s], kTcWorkerWarps);
+            mbar_init(&w_empty[s], kTcDequantWarps);
             mbar_init(&gu_full[s], 1);
-            mbar_init(&gu_empty[s], kTcWorkerWarps);
-            mbar_init(&op_full[s], kTcWorkerWarps);
+            mbar_init(&gu_empty[s], kTcSiluWarps);
+            mbar_init(&op_full[s], kTcDequantWarps + kTcSiluWarps);
             mbar_init(&op_empty[s], 1);
         }
         mbar_init(&sc_full, 1);
@@ -128,24 +129,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = tmem_slot;
     grid_dep_launch();
 
+    // The three single-issue roles run their loops with the whole warp (warp-uniform
+    // values, no divergent single-thread path); lane 0 waits and issues, and a shuffle
+    // keeps the warp's decision uniform.
     if (warp == 0) {
         // -------------------------------------------------- weights + scales (constant)
+        const uint64_t pol_w = policy_evict_first();
         if (lane == 0) {
             prefetch_tensormap(&map_w);
             prefetch_tensormap(&map_s);
-            const uint64_t pol_w = policy_evict_first();
             mbar_arrive_expect_tx(&sc_full, (uint32_t)kTcRows * sg * 2);
             tma_load_2d(smem + off_sc, &map_s, x0_scale, n0, &sc_full, pol_w);
-            int s = 0, round = 0, issued = 0;
-            for (int t = 0; t < n_steps; ++t) {
-                if (round > 0 && !mbar_wait_bounded(&w_empty[s], (round - 1) & 1, &abort_flag))
-                    break;
+        }
+        int s = 0, round = 0, issued = 0;
+        const int n_tiles = k_cta / kTcWTileK;
+        for (int t = 0; t < n_tiles; ++t) {
+            bool ok = true;
+            if (lane == 0 && round > 0) ok = mbar_wait_bounded(&w_empty[s], (round - 1) & 1, &abort_flag);
+            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+            if (lane == 0) {
                 mbar_arrive_expect_tx(&w_full[s], kWStageBytes);
-                tma_load_2d(smem + (size_t)s * kWStageBytes, &map_w, (k0 + t * kTcStepK) / 2, n0,
+                tma_load_2d(smem + (size_t)s * kWStageBytes, &map_w, (k0 + t * kTcWTileK) / 2, n0,
                             &w_full[s], pol_w);
-                issued = t + 1;
-                if (++s == s_w) { s = 0; ++round; }
             }
+            issued = t + 1;
+            if (++s == s_w) { s = 0; ++round; }
+        }
+        if (lane == 0) {
             for (int t = issued > s_w ? issued - s_w : 0; t < issued; ++t)
                 wait_parity_hw(&w_full[t % s_w], (t / s_w) & 1);
             wait_parity_hw(&sc_full, 0);
@@ -156,148 +166,207 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             prefetch_tensormap(&map_g);
             prefetch_tensormap(&map_u);
-            grid_dep_wait();  // gate/up may be written by the previous kernel
-            const uint64_t pol = policy_evict_last();  // every n-tile re-reads them
-            int s = 0, round = 0, issued = 0;
-            for (int t = 0; t < n_steps; ++t) {
-                if (round > 0 && !mbar_wait_bounded(&gu_empty[s], (round - 1) & 1, &abort_flag))
-                    break;
+        }
+        grid_dep_wait();  // gate/up may be written by the previous kernel
+        const uint64_t pol = policy_evict_last();  // every n-tile re-reads them
+        int s = 0, round = 0, issued = 0;
+        for (int t = 0; t < n_steps; ++t) {
+            bool ok = true;
+            if (lane == 0 && round > 0) ok = mbar_wait_bounded(&gu_empty[s], (round - 1) & 1, &abort_flag);
+            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+            if (lane == 0) {
                 unsigned char *st = smem + off_gu + (size_t)s * kGuStage;
                 mbar_arrive_expect_tx(&gu_full[s], kGuStage);
                 tma_load_2d(st, &map_g, k0 + t * kTcStepK, 0, &gu_full[s], pol);
                 tma_load_2d(st + kGuTile, &map_u, k0 + t * kTcStepK, 0, &gu_full[s], pol);
-                issued = t + 1;
-                if (++s == s_gu) { s = 0; ++round; }
             }
+            issued = t + 1;
+            if (++s == s_gu) { s = 0; ++round; }
+        }
+        if (lane == 0) {
             for (int t = issued > s_gu ? issued - s_gu : 0; t < issued; ++t)
                 wait_parity_hw(&gu_full[t % s_gu], (t / s_gu) & 1);
         }
         __syncwarp();
     } else if (warp == 2) {
         // -------------------------------------------------- MMA issue
+        // One thread (fastest measured issue loop). The operand ring is released in two
+        // halves of g_op stages: one tcgen05.commit per half instead of one per stage (a
+        // commit costs the issuing thread about as much as four MMAs).
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kTcRows, NPAD);
-            int s = 0, phase = 0;
+            // Descriptors of stage 0, first K = 16 step; the start-address field (bits 0-13,
+            // address / 16) advances by 2 core matrices per step and by a stage per stage.
+            const uint32_t a0 = smem_u32(smem + off_op);
+            const uint64_t adesc0 = smem_desc_interleaved(a0, kCoreBytes, kGroupBytes);
+            const uint64_t bdesc0 = smem_desc_interleaved(a0 + kATileBytes, kCoreBytes, kGroupBytes);
+            constexpr uint64_t kStepField = (2 * kCoreBytes) >> 4;
+            constexpr uint64_t kStageField = kOpStage >> 4;
+            uint64_t ad = adesc0, bd = bdesc0;
+            int s = 0, phase = 0, gpos = 0, gcount = 0;
             for (int t = 0; t < n_steps; ++t) {
                 if (!mbar_wait_bounded(&op_full[s], phase, &abort_flag)) break;
                 tc_fence_after();
-                const uint32_t a_base = smem_u32(smem + off_op + (size_t)s * kOpStage);
-                const uint32_t b_base = a_base + kATileBytes;
 #pragma unroll
-                for (int j = 0; j < kTcStepK / 16; ++j) {
-                    const uint64_t ad = smem_desc_interleaved(a_base + j * 2 * kCoreBytes,
-                                                              kCoreBytes, kGroupBytes);
-                    const uint64_t bd = smem_desc_interleaved(b_base + j * 2 * kCoreBytes,
-                                                              kCoreBytes, kGroupBytes);
-                    tc_mma_f16(tmem, ad, bd, idesc, (t | j) != 0);
+                for (int j = 0; j < kTcStepK / 16; ++j)
+                    tc_mma_f16(tmem, ad + j * kStepField, bd + j * kStepField, idesc, (t | j) != 0);
+                if (++gpos == g_op || t == n_steps - 1) {
+                    tc_commit(&op_empty[gcount & 1]);
+                    gpos = 0;
+                    ++gcount;
                 }
-                tc_commit(&op_empty[s]);
-                if (++s == s_op) { s = 0; phase ^= 1; }
+                if (++s == s_op) {
+                    s = 0;
+                    phase ^= 1;
+                    ad = adesc0;
+                    bd = bdesc0;
+                } else {
+                    ad += kStageField;
+                    bd += kStageField;
+                }
             }
             tc_commit(&acc_full);  // fires once every MMA issued above has completed
         }
         __syncwarp();
-    } else {
-        // -------------------------------------------------- workers: operand prologues
+    } else if (warp < kTcFirstSilu) {
+        // -------------------------------------------------- dequant warps: A operand
+        // Every shared-memory address below is a 32-bit shared-window address; the stage
+        // addresses advance with the ring instead of being recomputed.
         const int wt = tid - kTcFirstWorker * 32;
         const uint32_t key = opaque_u32(kMagic136x2);
         const uint32_t magic = opaque_u32(kMagic136x2);
-        const int row = wt & (kTcRows - 1);  // dequant: weight row and 32-k half
+        const int row = wt & (kTcRows - 1);  // weight row and 32-k half of each step
         const int h = wt >> 7;
         const int steps_per_group = group / kTcStepK;
-        int gcol = k0 / group - x0_scale;
         int gstep = (k0 % group) / kTcStepK;
-        const uint16_t *sc_row = reinterpret_cast<const uint16_t *>(smem + off_sc) + row * sg;
+        // 128-byte swizzle of the tensor-map copy: 16-byte chunk c of row r sits at c ^ (r & 7)
+        const uint32_t w_row0 = smem_u32(smem) + row * 128;
+        uint32_t chunk_off[kTcStepsPerWTile];
+#pragma unroll
+        for (int q = 0; q < kTcStepsPerWTile; ++q) chunk_off[q] = ((uint32_t)(2 * q + h) ^ (row & 7)) << 4;
+        const uint32_t a_row0 = smem_u32(smem + off_op) + (row >> 3) * kGroupBytes + (row & 7) * 16 +
+                                h * 4 * kCoreBytes;
+        uint32_t sc_at = smem_u32(smem + off_sc) + (uint32_t)(row * sg + (k0 / group - x0_scale)) * 2;
+        const uint32_t w_full0 = smem_u32(&w_full[0]), w_empty0 = smem_u32(&w_empty[0]);
+        const uint32_t op_full0 = smem_u32(&op_full[0]), op_empty0 = smem_u32(&op_empty[0]);
         bool ok = mbar_wait_bounded(&sc_full, 0, &abort_flag);
-        int ws = 0, wph = 0, gs = 0, gph = 0, os = 0, oround = 0;
+        int ws = 0, wph = 0, os = 0, gpos = 0, gcount = 0;
+        uint32_t w_at = w_row0, a_at = a_row0;
         for (int t = 0; t < n_steps && ok; ++t) {
-            ok = mbar_wait_bounded(&w_full[ws], wph, &abort_flag) &&
-                 mbar_wait_bounded(&gu_full[gs], gph, &abort_flag) &&
-                 (oround == 0 || mbar_wait_bounded(&op_empty[os], (oround - 1) & 1, &abort_flag));
+            const int wsub = t & (kTcStepsPerWTile - 1);
+            // entering a ring half: wait for the commit of its previous use
+            ok = (wsub != 0 || mbar_wait_bounded_at(w_full0 + 8 * ws, wph, &abort_flag)) &&
+                 (gpos != 0 || gcount < 2 ||
+                  mbar_wait_bounded_at(op_empty0 + 8 * (gcount & 1), ((gcount >> 1) - 1) & 1,
+                                       &abort_flag));
             if (!ok) break;
-            unsigned char *A = smem + off_op + (size_t)os * kOpStage;
-            // ---- A: dequantised weights, 128 rows x 64 k
-            {
-                const unsigned char *wst = smem + (size_t)ws * kWStageBytes;
-                // 32-byte swizzle of the tensor-map copy: 16-byte half h of row r sits at
-                // position h ^ bit 2 of r.
-                const uint4 wv = *reinterpret_cast<const uint4 *>(
-                    wst + row * 32 + ((h ^ ((row >> 2) & 1)) << 4));
-                const uint32_t sc = sc_row[gcol];
-                const uint32_t s2 = sc | (sc << 16);
-                uint4 *dst = reinterpret_cast<uint4 *>(A + (row >> 3) * kGroupBytes + (row & 7) * 16 +
-                                                       h * 4 * kCoreBytes);
-                const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+            const uint4 wv = lds_v4(w_at + chunk_off[wsub]);
+            const uint32_t sc = lds_u16(sc_at);
+            const uint32_t s2 = sc | (sc << 16);
+            const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    // pairs (k_j, k_j+4) of the word's 8 k: 136 + q as bf16, exact
-                    const uint32_t w = wd[i];
-                    const uint32_t t0 = mask_xor<0x000F000Fu>(w, key);
-                    const uint32_t t1 = mask_xor<0x000F000Fu>(w >> 4, key);
-                    const uint32_t t2 = mask_xor<0x000F000Fu>(w >> 8, key);
-                    const uint32_t t3 = mask_xor<0x000F000Fu>(w >> 12, key);
-                    uint4 o;
-                    o.x = bf16x2_mul(bf16x2_sub(t0, magic), s2);
-                    o.y = bf16x2_mul(bf16x2_sub(t1, magic), s2);
-                    o.z = bf16x2_mul(bf16x2_sub(t2, magic), s2);
-                    o.w = bf16x2_mul(bf16x2_sub(t3, magic), s2);
-                    dst[i * (kCoreBytes / 16)] = o;
-                }
+            for (int i = 0; i < 4; ++i) {
+                // pairs (k_j, k_j+4) of the word's 8 k: 136 + q as bf16, exact
+                const uint32_t w = wd[i];
+                const uint32_t t0 = mask_xor<0x000F000Fu>(w, key);
+                const uint32_t t1 = mask_xor<0x000F000Fu>(w >> 4, key);
+                const uint32_t t2 = mask_xor<0x000F000Fu>(w >> 8, key);
+                const uint32_t t3 = mask_xor<0x000F000Fu>(w >> 12, key);
+                uint4 o;
+                o.x = bf16x2_mul(bf16x2_sub(t0, magic), s2);
+                o.y = bf16x2_mul(bf16x2_sub(t1, magic), s2);
+                o.z = bf16x2_mul(bf16x2_sub(t2, magic), s2);
+                o.w = bf16x2_mul(bf16x2_sub(t3, magic), s2);
+                sts_v4(a_at + i * kCoreBytes, o);
             }
-            // ---- B: activations, NPAD rows x 64 k
-            {
-                const unsigned char *G = smem + off_gu + (size_t)gs * kGuStage;
-                const unsigned char *U = G + kGuTile;
-                unsigned char *B = A + kATileBytes;
+            // generic writes of A before the tensor core reads them; generic reads of the
+            // weight stage before the next bulk copy overwrites it
+            fence_proxy_async_smem();
+            __syncwarp();
+            const bool tile_done = (wsub == kTcStepsPerWTile - 1);
+            if (lane == 0) {
+                if (tile_done) mbar_arrive_at(w_empty0 + 8 * ws);
+                mbar_arrive_at(op_full0 + 8 * os);
+            }
+            if (tile_done) {
+                if (++ws == s_w) { ws = 0; wph ^= 1; w_at = w_row0; } else { w_at += kWStageBytes; }
+            }
+            if (++os == s_op) { os = 0; a_at = a_row0; } else { a_at += kOpStage; }
+            if (++gpos == g_op) { gpos = 0; ++gcount; }
+            if (++gstep == steps_per_group) { gstep = 0; sc_at += 2; }
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------- SwiGLU warps: B operand
+        constexpr int kItems = (NPAD * 8 + kTcSiluThreads - 1) / kTcSiluThreads;
+        const int st = tid - kTcFirstSilu * 32;
+        const float2 half2 = make_float2(0.5f, 0.5f);
+        // lanes 0..7 take rows 0..7 of one core matrix: conflict-free reads (128-byte
+        // swizzle: chunk c of row m at c ^ (m & 7)) and writes
+        uint32_t src_off[kItems], dst_off[kItems];
+        bool active[kItems];
 #pragma unroll
-                for (int j = 0; j < (NPAD * 8 + kTcWorkers - 1) / kTcWorkers; ++j) {
-                    const int item = wt + j * kTcWorkers;
-                    if (item < NPAD * 8) {
-                        // lanes 0..7 take rows 0..7 of one core matrix: conflict-free reads
-                        // (128-byte swizzle: chunk c of row m at c ^ (m & 7)) and writes.
-                        const int m = (item & 7) | ((item >> 6) << 3);
-                        const int c = (item >> 3) & 7;
-                        const uint32_t soff = m * 128 + ((c ^ (m & 7)) << 4);
-                        const uint4 gv = *reinterpret_cast<const uint4 *>(G + soff);
-                        const uint4 uv = *reinterpret_cast<const uint4 *>(U + soff);
-                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-                        const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
-                        float a[8];
+        for (int j = 0; j < kItems; ++j) {
+            const int item = st + j * kTcSiluThreads;
+            const int m = (item & 7) | ((item >> 6) << 3);
+            const int c = (item >> 3) & 7;
+            active[j] = item < NPAD * 8;
+            src_off[j] = m * 128 + ((c ^ (m & 7)) << 4);
+            dst_off[j] = (m >> 3) * kGroupBytes + c * kCoreBytes + (m & 7) * 16;
+        }
+        const uint32_t g_row0 = smem_u32(smem + off_gu);
+        const uint32_t b_row0 = smem_u32(smem + off_op) + kATileBytes;
+        const uint32_t gu_full0 = smem_u32(&gu_full[0]), gu_empty0 = smem_u32(&gu_empty[0]);
+        const uint32_t op_full0 = smem_u32(&op_full[0]), op_empty0 = smem_u32(&op_empty[0]);
+        bool ok = true;
+        int gs = 0, gph = 0, os = 0, gpos = 0, gcount = 0;
+        uint32_t g_at = g_row0, b_at = b_row0;
+        for (int t = 0; t < n_steps && ok; ++t) {
+            ok = mbar_wait_bounded_at(gu_full0 + 8 * gs, gph, &abort_flag) &&
+                 (gpos != 0 || gcount < 2 ||
+                  mbar_wait_bounded_at(op_empty0 + 8 * (gcount & 1), ((gcount >> 1) - 1) & 1,
+                                       &abort_flag));
+            if (!ok) break;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            a[2 * i] = silu_mul_tanh(bf16lo(gw[i]), bf16lo(uw[i]));
-                            a[2 * i + 1] = silu_mul_tanh(bf16hi(gw[i]), bf16hi(uw[i]));
-                        }
-                        uint4 o;
-                        o.x = pack_bf16x2(a[0], a[4]);
-                        o.y = pack_bf16x2(a[1], a[5]);
-                        o.z = pack_bf16x2(a[2], a[6]);
-                        o.w = pack_bf16x2(a[3], a[7]);
-                        *reinterpret_cast<uint4 *>(B + (m >> 3) * kGroupBytes + c * kCoreBytes +
-                                                   (m & 7) * 16) = o;
+            for (int j = 0; j < kItems; ++j) {
+                if (active[j]) {
+                    const uint4 gv = lds_v4(g_at + src_off[j]);
+                    const uint4 uv = lds_v4(g_at + kGuTile + src_off[j]);
+                    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                    const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+                    float2 a[4];  // a[i] = (element 2i, element 2i + 1)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        // silu(g) u = (g u / 2)(1 + tanh(g / 2)), two elements at a time
+                        const float2 hv = __fmul2_rn(make_float2(bf16lo(gw[i]), bf16hi(gw[i])), half2);
+                        const float2 p = __fmul2_rn(hv, make_float2(bf16lo(uw[i]), bf16hi(uw[i])));
+                        const float2 th = make_float2(tanh_approx(hv.x), tanh_approx(hv.y));
+                        a[i] = __ffma2_rn(p, th, p);
                     }
+                    uint4 o;  // k order 0 4 1 5 2 6 3 7, as the dequantised weights
+                    o.x = pack_bf16x2(a[0].x, a[2].x);
+                    o.y = pack_bf16x2(a[0].y, a[2].y);
+                    o.z = pack_bf16x2(a[1].x, a[3].x);
+                    o.w = pack_bf16x2(a[1].y, a[3].y);
+                    sts_v4(b_at + dst_off[j], o);
                 }
             }
-            // generic-proxy writes (A, B) before the tensor core reads them; generic reads
-            // of the input stages before the next bulk copy overwrites them
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&w_empty[ws]);
-                mbar_arrive(&gu_empty[gs]);
-                mbar_arrive(&op_full[os]);
+                mbar_arrive_at(gu_empty0 + 8 * gs);
+                mbar_arrive_at(op_full0 + 8 * os);
             }
-            if (++ws == s_w) { ws = 0; wph ^= 1; }
-            if (++gs == s_gu) { gs = 0; gph ^= 1; }
-            if (++os == s_op) { os = 0; ++oround; }
-            if (++gstep == steps_per_group) { gstep = 0; ++gcol; }
+            if (++gs == s_gu) { gs = 0; gph ^= 1; g_at = g_row0; } else { g_at += kGuStage; }
+            if (++os == s_op) { os = 0; b_at = b_row0; } else { b_at += kOpStage; }
+            if (++gpos == g_op) { gpos = 0; ++gcount; }
         }
         __syncwarp();
     }
 
     // ------------------------------------------------------ epilogue
     uint32_t v[kHalf];
-    const bool worker = warp >= kTcFirstWorker;
+    const bool worker = warp >= kTcFirstWorker && warp < kTcFirstSilu;
     const int quarter = warp & 3;                       // TMEM lanes 32q .. 32q + 31
     const int col0 = ((warp - kTcFirstWorker) >> 2) * kHalf;
     if (worker) {
@@ -339,7 +408,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float *rv = reinterpret_cast<const float *>(smem + off_gu);
         const bool failed = (peer_abort[0] | peer_abort[1] | peer_abort[2] | peer_abort[3]) != 0;
         const int wt = tid - kTcFirstWorker * 32;
-        for (int i = wt; i < M * 16; i += kTcWorkers) {
+        for (int i = wt; i < M * 16; i += kTcEpilogueThreads) {
             const int m = i >> 4, rp = (i & 15) * 2;
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -404,7 +473,7 @@ bool make_plan(int npad, int k_cta, int group, size_t budget, TcPlan *p) {
     const uint32_t op_stage = kATileBytes + npad * 128u;
     p->sg = ((k_cta + group - 1) / group + 7 + 7) & ~7;
     if (p->sg > 256) return false;
-    p->s_w = 12;
+    p->s_w = 4;
     const uint32_t w_bytes = p->s_w * kWStageBytes;
     const uint32_t sc_bytes = ((uint32_t)kTcRows * p->sg * 2 + 1023u) & ~1023u;
     if (budget < 1024 + w_bytes + sc_bytes) return false;
@@ -418,7 +487,7 @@ bool make_plan(int npad, int k_cta, int group, size_t budget, TcPlan *p) {
         if (s_gu < 4 && used + gu_stage <= avail) { ++s_gu; used += gu_stage; grew = true; }
     }
     p->s_gu = s_gu;
-    p->s_op = s_op;
+    p->s_op = s_op & ~1;  // two halves of equal size
     p->off_gu = w_bytes;
     p->off_op = p->off_gu + s_gu * gu_stage;
     p->off_sc = p->off_op + s_op * op_stage;
@@ -449,7 +518,7 @@ cudaError_t launch_npad(const DeviceInfo &di, const void *gate, const void *up,
 
     CUtensorMap mw, ms, mg, mu;
     if (!encode_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, qweight, (uint64_t)K / 2, (uint64_t)N,
-                   (uint64_t)K / 2, kTcStepK / 2, kTcRows, CU_TENSOR_MAP_SWIZZLE_32B) ||
+                   (uint64_t)K / 2, kTcWTileK / 2, kTcRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, scales, (uint64_t)K / group,
                    (uint64_t)N, (uint64_t)(K / group) * 2, (uint32_t)plan.sg, kTcRows,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||

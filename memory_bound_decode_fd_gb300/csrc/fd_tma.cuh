@@ -47,23 +47,66 @@ __device__ __forceinline__ bool mbar_test_parity(uint64_t *bar, uint32_t parity)
     return done != 0;
 }
 
-// Waits for the phase with parity `parity`. Returns false if the wait ran past the
-// cycle limit or `*abort_flag` became nonzero (another thread gave up); in the first
-// case it also sets `*abort_flag`.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
-                                                  volatile int *abort_flag) {
-    if (mbar_test_parity(bar, parity)) return true;
+// Like mbar_test_parity, but the hardware may suspend the thread for a short,
+// system-defined time while the phase is incomplete (no issue slots spent spinning).
+__device__ __forceinline__ bool mbar_try_parity(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Address (shared window, 32-bit) forms of mbar_try_parity and mbar_arrive.
+__device__ __forceinline__ bool mbar_try_parity_at(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ void mbar_arrive_at(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Slow path of mbar_wait_bounded (kept out of line so the fast path stays small):
+// several suspending polls between checks of the abort flag and the cycle budget.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity,
+                                            volatile int *abort_flag) {
     const long long t0 = clock64();
-    unsigned spins = 0;
     while (true) {
-        if (mbar_test_parity(bar, parity)) return true;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (mbar_try_parity(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (++spins > 64) __nanosleep(32);
         if (clock64() - t0 > kWaitLimitCycles) {
             *abort_flag = 1;
             return false;
         }
     }
+}
+
+// Waits for the phase with parity `parity`. Returns false if the wait ran past the
+// cycle limit or `*abort_flag` became nonzero (another thread gave up); in the first
+// case it also sets `*abort_flag`.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort_flag) {
+    if (mbar_try_parity(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag);
+}
+__device__ __forceinline__ bool mbar_wait_bounded_at(uint32_t bar, uint32_t parity,
+                                                     volatile int *abort_flag) {
+    if (mbar_try_parity_at(bar, parity)) return true;
+    return mbar_wait_slow(reinterpret_cast<uint64_t *>(__cvta_shared_to_generic(bar)), parity,
+                          abort_flag);
 }
 
 // Bulk copy global -> shared (this CTA), completion counted in bytes on `bar`.
@@ -82,6 +125,26 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 // before releasing a buffer that a bulk copy will overwrite.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 32-bit shared-memory (this CTA) loads and stores, volatile so that they stay ordered
+// with the barrier waits around them.
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
 }
 
 // Barrier over the first `threads` threads of the CTA (named barrier `id`, id != 0).

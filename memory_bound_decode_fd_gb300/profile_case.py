@@ -1,6 +1,7 @@
 """Run one fd kernel a few times on seeded inputs, nothing else (for ncu captures).
 
     python -m memory_bound_decode_fd_gb300.profile_case gemv --M 1 --K 14336 --N 4096
+    python -m memory_bound_decode_fd_gb300.profile_case gemv --M 64 --path tensor
     python -m memory_bound_decode_fd_gb300.profile_case rmsnorm --rows 8192 --hidden 4096
 
 Each iteration uses the next of --sets input sets, so that consecutive launches do not
@@ -37,9 +38,11 @@ def main(argv=None) -> int:
     ap.add_argument("--eps", type=float, default=1e-6)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--sets", type=int, default=2)
+    ap.add_argument("--path", choices=sorted(["auto", "cuda_core", "bulk", "tensor"]), default="auto")
     args = ap.parse_args(argv)
 
     build.build()
+    fd.set_gemv_path(args.path)
     dev = torch.device("cuda:0")
     if args.case == "gemv":
         rng = np.random.default_rng(0)
