@@ -49,7 +49,9 @@ METRIC = "µs/call and achieved HBM GB/s (% of GB300 peak) for SwiGLU-W4A16 GEMV
 FALLBACK_HBM_GBS = 6800.0
 SPEC_HBM_GBS = 8000.0
 KERNEL_SOURCES = {
-    "swiglu_w4a16_gemv": ["csrc/fd_gemv_cc.cu", "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
+    # the M = 1 kernel the decode step runs (bulk-copy kernel) and the headers it uses
+    "swiglu_w4a16_gemv": ["csrc/fd_gemv_tma.cu", "csrc/fd_gemv_common.cuh", "csrc/fd_tma.cuh",
+                          "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
     "add_rmsnorm": ["csrc/fd_add_rmsnorm.cu", "csrc/fd_internal.h"],
 }
 

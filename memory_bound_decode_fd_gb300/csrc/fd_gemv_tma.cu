@@ -11,13 +11,12 @@
 // The fast path for K % 1024 == 0, K <= 15360 and (K / group) % 8 == 0 (every
 // decode shape of interest). Design for GB300:
 //   * One persistent CTA per SM owning a contiguous range of output rows n.
-//   * Warp specialisation: the last warp is a producer whose lane 0 streams chunks of 4
-//     consecutive weight rows (4 * K/2 bytes, one contiguous bulk copy) and their scales
-//     (4 * K/group * 2 bytes, a second bulk copy) into an S-stage (up to 8) shared-memory
+//   * Warp specialisation: the last warp is a producer whose lane 0 streams chunks of 8
+//     consecutive weight rows (8 * K/2 bytes, one contiguous bulk copy) and their scales
+//     (8 * K/group * 2 bytes, a second bulk copy) into an S-stage (up to 8) shared-memory
 //     ring, completion tracked by "full" mbarriers; consumers release a stage through an
-//     "empty" mbarrier (one arrival per consumer warp). At the decode shapes the ring
-//     holds every row the CTA owns (~200 KB per SM), so the whole weight stream is in
-//     flight from the first cycle and no refill waits on the math.
+//     "empty" mbarrier (one arrival per consumer warp). The ring holds 3 stages (24
+//     rows) at K=14336 and 5 at K=9216, most of the ~27 and ~17 rows a CTA owns.
 //   * Consumer thread t (K/32 of them) owns 32 consecutive k: a = silu(g) * u for its k
 //     lives in registers as block-scaled int16 (fd_gemv_common.cuh); per row it reads its
 //     16-byte slot (conflict-free), splits each word into even/odd nibble bytes (2 lop3)
