@@ -4,15 +4,16 @@
 //
 // Numerics of one 32-k slice (one 16-byte weight vector position, inside one scale
 // group):
-//   a_k = silu(g_k) * u_k in fp32 (fast exp and divide intrinsics), k in the slice;
+//   a_k = silu(g_k) * u_k in fp32 through the identity silu(x) = (x/2)(1 + tanh(x/2))
+//   (one MUFU tanh per element; its error leaves a_k within 2^-10.5 |g_k u_k / 2|);
 //   a_k is encoded as a16_k = rint(a_k * 32767 / amax) with amax = max |a_k| over the
 //   slice (a block-scaled 16-bit integer: 15 magnitude bits against bf16's 8), and
 //   a_k ~= a16_k * scale, scale = amax / 32767;
 //   sum_k a16_k q_k is formed EXACTLY in int32 with the dp2a integer dot-product
 //   instruction (16-bit x 8-bit products), from the byte split of fd_w4_unpack.cuh;
 //   the slice's contribution to y[n] is float(that sum) * (scale * s[n, group]).
-// The only error beyond fp32 rounding is the 16-bit encoding of a, at most
-// amax / 65534 per element.
+// Beyond fp32 rounding, the errors are tanh's and the 16-bit encoding of a (at most
+// amax / 65534 per element).
 #pragma once
 
 #include "fd_internal.h"
@@ -60,50 +61,62 @@ __device__ __forceinline__ void load_gate_up(const uint16_t *__restrict__ gate,
     }
 }
 
-// silu(g) * u in fp32 with the fast exp and divide intrinsics (two MUFU operations per
-// element; relative error within a few ulp, far below the 16-bit encoding step). g is
-// clamped at -60 so 1 + e stays finite (silu(-60) is below 1e-24).
-__device__ __forceinline__ float silu_mul(float g, float u) {
-    const float gc = fmaxf(g, -60.0f);
-    return __fdividef(g, 1.0f + __expf(-gc)) * u;
+// tanh on MUFU (tanh.approx.f32: relative error about 2^-11).
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Encodes one slice (see Act16).
 __device__ __forceinline__ void encode_q16(const GateUp &gu, Act16 &act) {
-    float a[32];
+    // silu(g) u = (g u / 2)(1 + tanh(g / 2)), two elements per packed instruction;
+    // a[4i + j] holds elements 8i + 2j and 8i + 2j + 1
+    float2 a[16];
+    const float2 half2 = make_float2(0.5f, 0.5f);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t gw[4] = {gu.g[i].x, gu.g[i].y, gu.g[i].z, gu.g[i].w};
         const uint32_t uw[4] = {gu.u[i].x, gu.u[i].y, gu.u[i].z, gu.u[i].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            a[8 * i + 2 * j] = silu_mul(bf16lo(gw[j]), bf16lo(uw[j]));
-            a[8 * i + 2 * j + 1] = silu_mul(bf16hi(gw[j]), bf16hi(uw[j]));
+            const float2 h = __fmul2_rn(make_float2(bf16lo(gw[j]), bf16hi(gw[j])), half2);
+            const float2 p = __fmul2_rn(h, make_float2(bf16lo(uw[j]), bf16hi(uw[j])));
+            a[4 * i + j] = __ffma2_rn(p, make_float2(tanh_approx(h.x), tanh_approx(h.y)), p);
         }
     }
     float amax = 0.f;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(a[k]));
-    const float s_inv = amax > 0.f ? 32767.0f / amax : 0.f;
+    for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fmaxf(fabsf(a[k].x), fabsf(a[k].y)));
+    const float s_inv = amax > 0.f ? __fdividef(32767.0f, amax) : 0.f;
     act.scale = amax * (1.0f / 32767.0f);
-    int q[32];
-    int s_even = 0, s_odd = 0;
+    // round(a * s_inv) by one fma with 1.5 * 2^23: the low 16 bits of the result are the
+    // int16 code (two's complement), and the integer sum is the bit sum minus the bias
+    const float2 sv = make_float2(s_inv, s_inv);
+    const float2 mg = make_float2(12582912.0f, 12582912.0f);
+    uint32_t b[32];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        q[k] = rint_small(a[k] * s_inv);
-        if (k & 1) s_odd += q[k]; else s_even += q[k];
+    for (int k = 0; k < 16; ++k) {
+        const float2 r = __ffma2_rn(a[k], sv, mg);
+        b[2 * k] = __float_as_uint(r.x);
+        b[2 * k + 1] = __float_as_uint(r.y);
+    }
+    uint32_t s_even = 0u - 16u * 0x4B400000u, s_odd = 0u - 16u * 0x4B400000u;
+#pragma unroll
+    for (int k = 0; k < 32; k += 2) {
+        s_even += b[k];
+        s_odd += b[k + 1];
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        act.e[i] = pack16(q[8 * i + 0], q[8 * i + 2]);
-        act.f[i] = pack16(q[8 * i + 4], q[8 * i + 6]);
-        act.g[i] = pack16(q[8 * i + 1], q[8 * i + 3]);
-        act.h[i] = pack16(q[8 * i + 5], q[8 * i + 7]);
+        act.e[i] = __byte_perm(b[8 * i + 0], b[8 * i + 2], 0x5410);
+        act.f[i] = __byte_perm(b[8 * i + 4], b[8 * i + 6], 0x5410);
+        act.g[i] = __byte_perm(b[8 * i + 1], b[8 * i + 3], 0x5410);
+        act.h[i] = __byte_perm(b[8 * i + 5], b[8 * i + 7], 0x5410);
     }
-    act.init_lo = -8 * s_even;
-    act.init_hi = -128 * s_odd;
+    act.init_lo = -8 * (int)s_even;
+    act.init_hi = -128 * (int)s_odd;
 }
-
 // Builds the slice's Act16 from bf16 gate/up at element `offset` (32 elements).
 __device__ __forceinline__ void load_activation_q16(const uint16_t *__restrict__ gate,
                                                     const uint16_t *__restrict__ up,
