@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(512, 1)
                     const unsigned char *__restrict__ qweight,
                     const uint16_t *__restrict__ scales, uint16_t *__restrict__ out, int M,
                     int K, int N, int group, int rows_base, int rows_extra, int S,
-                    int act_stages, int pre_stages, int weights_evict_first) {
+                    int act_stages, int weights_evict_first) {
     static_assert(R * MB <= 32 && (R * MB & (R * MB - 1)) == 0, "R*MB: power of 2, <= 32");
     static_assert(kWindowRows % R == 0, "window must hold whole chunks");
     extern __shared__ __align__(128) unsigned char smem[];
@@ -125,18 +125,20 @@ __global__ void __launch_bounds__(512, 1)
                 if (++s == S) { s = 0; ++round; }
                 if (++nc == n_chunks) nc = 0;
             };
-            // Weights never come from the previous kernel: with programmatic dependent
-            // launch the first `pre_stages` chunks stream before the dependency wait.
-            const int pre = min(pre_stages, min(total, S - act_stages));
+            // Nothing is issued before the dependency wait, although the weights never come
+            // from the previous kernel: the activation copy is what every consumer waits for
+            // first, and weight traffic issued ahead of it (copies into the ring or L2
+            // prefetches) delayed it and cost the 32-layer decode step 15-25 % in
+            // measurements on GB300.
             int c = 0;
-            for (; c < pre && ok; ++c) issue_chunk(c);
             grid_dep_wait();
             grid_dep_launch();
             if (act_in_smem) {
                 const uint32_t ab = (uint32_t)K * 2;
                 mbar_arrive_expect_tx(&act_full_bar, 2 * ab);
-                bulk_g2s(act_smem, gate, ab, &act_full_bar, pol_s);
-                bulk_g2s(act_smem + K, up, ab, &act_full_bar, pol_s);
+                const uint64_t pol_a = policy_evict_last();  // every CTA reads it
+                bulk_g2s(act_smem, gate, ab, &act_full_bar, pol_a);
+                bulk_g2s(act_smem + K, up, ab, &act_full_bar, pol_a);
             }
             for (; c < total && ok; ++c) issue_chunk(c);
             // Every issued copy must land before the CTA exits: wait (bounded) on the
@@ -332,12 +334,11 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
     if (grid < 1) grid = 1;
     const int rows_base = N / grid;
     const int rows_extra = N % grid;
-    const int pre_stages = (launch_flags() & FD_LAUNCH_PDL) ? 2 : 0;
     err = launch_kernel(kern, dim3(grid), dim3(nvec + 32), smem, stream, 1,
                         static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up),
                         static_cast<const unsigned char *>(qweight),
                         static_cast<const uint16_t *>(scales), static_cast<uint16_t *>(out), M,
-                        K, N, group, rows_base, rows_extra, S, act_stages, pre_stages,
+                        K, N, group, rows_base, rows_extra, S, act_stages,
                         M <= MB ? 1 : 0);
     *launched = true;
     if (err != cudaSuccess) return err;
