@@ -436,14 +436,21 @@ def bench_single(args, device, rank, world):
     stream = torch.cuda.Stream(device)
 
     def capture():
-        with torch.cuda.stream(stream):
-            for c in calls:
-                c()
-        stream.synchronize()
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=stream):
-            for c in calls:
-                c()
+        # Back-to-back calls as a decode engine issues them: programmatic dependent launch
+        # between consecutive kernels (each still waits for its predecessor before it
+        # reads activations or writes outputs; results are bitwise those of plain launches).
+        prev_pdl = fd.set_pdl(True)
+        try:
+            with torch.cuda.stream(stream):
+                for c in calls:
+                    c()
+            stream.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                for c in calls:
+                    c()
+        finally:
+            fd.set_pdl(prev_pdl)
         return gr
 
     graph = capture()
@@ -492,7 +499,7 @@ def bench_single(args, device, rank, world):
         "data": "synthetic (seeded)",
         "config": {"workload": f"{args.workload}: {desc}", "bytes_per_call": nbytes,
                    "l2": f"{len(calls)} rotating input sets ({len(calls)} x {nbytes} B vs L2 {l2} B)",
-                   "launch": f"CUDA graph of {len(calls)} calls"},
+                   "launch": f"CUDA graph of {len(calls)} calls, programmatic dependent launch"},
         "pct_of_measured_hbm": round(100 * gbs / world / hbm_peak, 1),
         "pct_of_spec_8tbs": round(100 * gbs / world / SPEC_HBM_GBS, 1),
         "roofline": {"kernel": kname, "bound": "hbm", "achieved": round(nbytes / (k_us * 1e-6) / 1e9, 1),

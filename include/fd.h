@@ -139,10 +139,9 @@ int fd_gemv_uses_tensor_cores(int M, int K, int N, int group);
  *                  the previous kernel in the same stream is still running. Each fd
  *                  kernel waits (griddepcontrol.wait) before it reads activations or
  *                  writes any output; the GEMV kernels read their weights only after it,
- *                  but add-RMSNorm loads its weight row BEFORE that wait (the tensor-core
- *                  GEMV also reads qweight/scales early). Set this only when no kernel
- *                  that may still be running in the stream writes those weight tensors
- *                  (true for model weights during decode). Works inside CUDA graph
+ *                  but add-RMSNorm loads its weight row BEFORE that wait. Set this only
+ *                  when no kernel that may still be running in the stream writes that
+ *                  weight row (true for model weights during decode). Works inside CUDA graph
  *                  capture (the edges become programmatic dependencies).
  * fd_set_launch_flags returns FD_ERR_UNSUPPORTED for unknown bits.
  */

@@ -138,6 +138,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             prefetch_tensormap(&map_w);
             prefetch_tensormap(&map_s);
+        }
+        // Weight traffic ahead of the gate/up copies would delay them (measured on the
+        // decode step with the CUDA-core kernel), so the weights also wait for the previous
+        // kernel under programmatic dependent launch.
+        grid_dep_wait();
+        if (lane == 0) {
             mbar_arrive_expect_tx(&sc_full, (uint32_t)kTcRows * sg * 2);
             tma_load_2d(smem + off_sc, &map_s, x0_scale, n0, &sc_full, pol_w);
         }
