@@ -117,6 +117,72 @@ __device__ __forceinline__ void encode_q16(const GateUp &gu, Act16 &act) {
     act.init_lo = -8 * (int)s_even;
     act.init_hi = -128 * (int)s_odd;
 }
+// Paired-lane form of encode_q16 (lanes l and l ^ 16 share one 32-k slice): this lane
+// holds the slice's elements 16h .. 16h + 15 (h = half), computes their codes, and the
+// pair exchanges amax, codes and offset sums by shuffles, so that both lanes end with the
+// whole slice's Act16 (identical to encode_q16 on the 32 elements, up to the order of the
+// amax reduction, which max makes exact).
+struct GateUpHalf {
+    uint4 g[2], u[2];
+};
+
+__device__ __forceinline__ void encode_q16_pair(const GateUpHalf &gu, int h, Act16 &act) {
+    float2 a[8];  // a[4i + j] holds elements 8i + 2j, 8i + 2j + 1 of this half
+    const float2 half2 = make_float2(0.5f, 0.5f);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t gw[4] = {gu.g[i].x, gu.g[i].y, gu.g[i].z, gu.g[i].w};
+        const uint32_t uw[4] = {gu.u[i].x, gu.u[i].y, gu.u[i].z, gu.u[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 hh = __fmul2_rn(make_float2(bf16lo(gw[j]), bf16hi(gw[j])), half2);
+            const float2 p = __fmul2_rn(hh, make_float2(bf16lo(uw[j]), bf16hi(uw[j])));
+            a[4 * i + j] = __ffma2_rn(p, make_float2(tanh_approx(hh.x), tanh_approx(hh.y)), p);
+        }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fmaxf(fabsf(a[k].x), fabsf(a[k].y)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 16));
+    const float s_inv = amax > 0.f ? __fdividef(32767.0f, amax) : 0.f;
+    act.scale = amax * (1.0f / 32767.0f);
+    const float2 sv = make_float2(s_inv, s_inv);
+    const float2 mg = make_float2(12582912.0f, 12582912.0f);
+    uint32_t b[16];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float2 r = __ffma2_rn(a[k], sv, mg);
+        b[2 * k] = __float_as_uint(r.x);
+        b[2 * k + 1] = __float_as_uint(r.y);
+    }
+    uint32_t sum = 0u - 16u * 0x4B400000u;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) sum += b[k];
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 16);
+    // with accumulators started at 0, lo + (hi >> 4) exceeds the exact sum by 8 * sum(q)
+    act.init_lo = -8 * (int)sum;
+    act.init_hi = 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t mine[4] = {__byte_perm(b[8 * i + 0], b[8 * i + 2], 0x5410),
+                                  __byte_perm(b[8 * i + 4], b[8 * i + 6], 0x5410),
+                                  __byte_perm(b[8 * i + 1], b[8 * i + 3], 0x5410),
+                                  __byte_perm(b[8 * i + 5], b[8 * i + 7], 0x5410)};
+        uint32_t other[4];
+#pragma unroll
+        for (int f = 0; f < 4; ++f) other[f] = __shfl_xor_sync(0xFFFFFFFFu, mine[f], 16);
+        // words 0-1 of the slice come from half 0, words 2-3 from half 1
+        act.e[i] = h ? other[0] : mine[0];
+        act.f[i] = h ? other[1] : mine[1];
+        act.g[i] = h ? other[2] : mine[2];
+        act.h[i] = h ? other[3] : mine[3];
+        act.e[2 + i] = h ? mine[0] : other[0];
+        act.f[2 + i] = h ? mine[1] : other[1];
+        act.g[2 + i] = h ? mine[2] : other[2];
+        act.h[2 + i] = h ? mine[3] : other[3];
+    }
+}
+
 // Builds the slice's Act16 from bf16 gate/up at element `offset` (32 elements).
 __device__ __forceinline__ void load_activation_q16(const uint16_t *__restrict__ gate,
                                                     const uint16_t *__restrict__ up,
@@ -170,6 +236,29 @@ __device__ __forceinline__ void dot32(const Act16 *act, uint4 wv, const W4Keys &
 }
 
 __host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v >> 1); }
+
+// warp_reduce_scatter within each 16-lane half of the warp: on return, lane l holds in
+// v[0] the sum over its half of value index ((l & 15) >> (4 - log2 V)).
+template <int V>
+__device__ __forceinline__ float half_reduce_scatter(float (&v)[V], int lane) {
+#pragma unroll
+    for (int width = V; width > 1; width >>= 1) {
+        const int half = width >> 1;
+        const int offset = 8 >> (ilog2(V) - ilog2(width));
+        const bool upper = (lane & offset) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, offset);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int offset = 8 >> ilog2(V); offset > 0; offset >>= 1)
+        r += __shfl_xor_sync(0xFFFFFFFFu, r, offset);
+    return r;
+}
 
 // Butterfly reduce-scatter of V values over a warp. On return, lane l holds in v[0] the
 // warp-wide sum of value index (l >> (5 - log2 V)).

@@ -17,13 +17,19 @@
 //     ring, completion tracked by "full" mbarriers; consumers release a stage through an
 //     "empty" mbarrier (one arrival per consumer warp). The ring holds 3 stages (24
 //     rows) at K=14336 and 5 at K=9216, most of the ~27 and ~17 rows a CTA owns.
-//   * Consumer thread t (K/32 of them) owns 32 consecutive k: a = silu(g) * u for its k
-//     lives in registers as block-scaled int16 (fd_gemv_common.cuh); per row it reads its
-//     16-byte slot (conflict-free), splits each word into even/odd nibble bytes (2 lop3)
-//     and accumulates exactly in int32 with 4 dp2a per word; the 32-k sum is converted
-//     once and scaled by the activation and group scales.
-//   * Per chunk a butterfly reduce-scatter leaves one warp sum per (row, m) in shared
-//     memory; every 64 rows the consumers sum over warps and store bf16 once per output.
+//   * Each 32-k slice of K is owned by LPS consumer lanes (K/32 * LPS threads): a =
+//     silu(g) * u for its k lives in registers as block-scaled int16
+//     (fd_gemv_common.cuh); per row a lane reads its 16-byte slot (conflict-free), splits
+//     each word into even/odd nibble bytes (2 lop3) and accumulates exactly in int32 with
+//     4 dp2a per word; the 32-k sum is converted once and scaled by the activation and
+//     group scales.
+//   * LPS = 2 at M = 1: lanes l and l + 16 of a warp share a slice (16 slices per warp)
+//     and take alternate rows of each chunk, so K = 9216 runs 18 consumer warps instead of
+//     9 and every lane has half the rows; the encoding of the slice is split between them
+//     (each converts 16 of its 32 k and they swap halves with one shuffle).
+//   * Per chunk a butterfly reduce-scatter (over 16 lanes when LPS = 2) leaves one warp
+//     sum per (row, m) in shared memory; every 64 rows the consumers sum over warps and
+//     store bf16 once per output.
 //   * Every mbarrier wait is bounded (fd_tma.cuh). If one gives up, the CTA stops
 //     computing, waits (bounded) for the copies it issued, writes NaN to all of its
 //     outputs (so the failure is visible to the caller) and exits.
@@ -46,14 +52,15 @@ constexpr int kChunkRows = 8;  // rows per bulk-copy chunk
 // up (2 * K * 2 bytes) into the space of the last ring stages, ahead of the weight
 // stream, so the consumers' activation reads do not queue behind it; those stages are
 // filled with weights only after every consumer warp has encoded its slice.
-template <int MB, int R, int NVEC_C, int NG_C>
-__global__ void __launch_bounds__(512, 1)
+template <int MB, int R, int NVEC_C, int NG_C, int LPS>
+__global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
     gemv_tma_kernel(const uint16_t *__restrict__ gate, const uint16_t *__restrict__ up,
                     const unsigned char *__restrict__ qweight,
                     const uint16_t *__restrict__ scales, uint16_t *__restrict__ out, int M,
                     int K, int N, int group, int rows_base, int rows_extra, int S,
                     int act_stages, int weights_evict_first) {
     static_assert(R * MB <= 32 && (R * MB & (R * MB - 1)) == 0, "R*MB: power of 2, <= 32");
+    static_assert(LPS == 1 || (LPS == 2 && MB == 1 && R % 2 == 0), "paired lanes: M = 1 only");
     static_assert(kWindowRows % R == 0, "window must hold whole chunks");
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -65,8 +72,9 @@ __global__ void __launch_bounds__(512, 1)
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int nvec = NVEC_C ? NVEC_C : (K >> 5);  // consumer threads, a multiple of 32
-    const int ncw = nvec >> 5;                     // consumer warps
+    const int nvec = NVEC_C ? NVEC_C : (K >> 5);  // 32-k slices, a multiple of 32
+    const int ncons = LPS * nvec;                  // consumer threads (LPS lanes per slice)
+    const int ncw = ncons >> 5;                    // consumer warps
     const int ngroups = NG_C ? NG_C : K / group;
     const uint32_t w_row_bytes = (uint32_t)nvec * 16;
     const uint32_t s_row_bytes = (uint32_t)ngroups * 2;
@@ -161,8 +169,113 @@ __global__ void __launch_bounds__(512, 1)
                     __nanosleep(64);
             }
         }
+    } else if constexpr (LPS == 2) {
+        // ------------------------------------------------------ consumer warps, paired
+        // Lanes l and l ^ 16 share one 32-k slice: lane l owns slice 16 * warp + (l & 15)
+        // and, in every chunk, the rows r = 2i + h (h = l >> 4). So a CTA runs twice the
+        // warps of the one-lane form on the same rows, and each lane encodes 16 elements.
+        grid_dep_wait();
+        grid_dep_launch();
+        const int hh = lane >> 4;
+        const int slice = 16 * warp + (lane & 15);
+        const int col = (slice * 32) / group;  // this lane's scale column
+        const W4Keys keys = w4_keys();
+        Act16 act;
+        {
+            GateUpHalf gu;
+            bool act_ok = true;
+            if (act_in_smem) {
+                act_ok = mbar_wait_bounded(&act_full_bar, 0, &abort_flag);
+                if (act_ok) {
+                    const uint4 *g4 = reinterpret_cast<const uint4 *>(act_smem + slice * 32 + 16 * hh);
+                    const uint4 *u4 = reinterpret_cast<const uint4 *>(act_smem + K + slice * 32 + 16 * hh);
+                    gu.g[0] = g4[0];
+                    gu.g[1] = g4[1];
+                    gu.u[0] = u4[0];
+                    gu.u[1] = u4[1];
+                }
+            } else {
+                const uint4 *g4 = reinterpret_cast<const uint4 *>(gate + slice * 32 + 16 * hh);
+                const uint4 *u4 = reinterpret_cast<const uint4 *>(up + slice * 32 + 16 * hh);
+                gu.g[0] = g4[0];
+                gu.g[1] = g4[1];
+                gu.u[0] = u4[0];
+                gu.u[1] = u4[1];
+            }
+            if (!act_ok) gu.g[0] = gu.g[1] = gu.u[0] = gu.u[1] = make_uint4(0, 0, 0, 0);
+            encode_q16_pair(gu, hh, act);
+            if (act_in_smem) {
+                // released after its values are consumed, with a proxy fence: the
+                // producer's next bulk copy writes it
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&act_free_bar);
+            }
+        }
+        constexpr int kRowsPerLane = R / 2;
+        constexpr int kLanesPerValue = 16 / kRowsPerLane;
+        int window_base = 0;
+        int s = 0, phase = 0, nc = 0;
+        for (int c = 0; c < total; ++c) {
+            float part[kRowsPerLane];
+            const bool ok = mbar_wait_bounded(&full_bar[s], phase, &abort_flag);
+            const int rows_valid = min(R, n_cnt - nc * R);
+            const unsigned char *st = smem + (size_t)s * stage_bytes;
+            const uint4 *wst = reinterpret_cast<const uint4 *>(st) + slice + hh * nvec;
+            const uint16_t *sst = reinterpret_cast<const uint16_t *>(st + (size_t)R * w_row_bytes) + col + hh * ngroups;
+            if (ok && rows_valid == R) {
+#pragma unroll
+                for (int i = 0; i < kRowsPerLane; ++i) {
+                    const uint4 wv = wst[2 * i * nvec];
+                    const float sc = __uint_as_float((uint32_t)sst[2 * i * ngroups] << 16);
+                    float d[1];
+                    dot32<1>(&act, wv, keys, sc, d);
+                    part[i] = d[0];
+                }
+            } else {
+                // last, partial chunk (or a failed wait): rows past the range are skipped
+#pragma unroll
+                for (int i = 0; i < kRowsPerLane; ++i) {
+                    if (ok && 2 * i + hh < rows_valid) {
+                        const uint4 wv = wst[2 * i * nvec];
+                        const float sc = __uint_as_float((uint32_t)sst[2 * i * ngroups] << 16);
+                        float d[1];
+                        dot32<1>(&act, wv, keys, sc, d);
+                        part[i] = d[0];
+                    } else {
+                        part[i] = 0.f;
+                    }
+                }
+            }
+            fence_proxy_async_smem();  // this stage's reads before its next bulk copy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[s]);
+
+            const float wsum = half_reduce_scatter<kRowsPerLane>(part, lane);
+            if (((lane & 15) & (kLanesPerValue - 1)) == 0) {
+                const int r = 2 * ((lane & 15) / kLanesPerValue) + hh;
+                red[(size_t)warp * kWindowRows + (nc * R + r - window_base)] = wsum;
+            }
+            const int rows_done = (nc + 1) * R;
+            const bool last_chunk = (nc == n_chunks - 1);
+            if (rows_done - window_base == kWindowRows || last_chunk) {
+                named_bar_sync(1, ncons);
+                const int rows_in_window = min(rows_done, n_cnt) - window_base;
+                for (int i = tid; i < rows_in_window; i += ncons) {
+                    float acc = 0.f;
+                    for (int w = 0; w < ncw; ++w) acc += red[(size_t)w * kWindowRows + i];
+                    __nv_bfloat16 y = __float2bfloat16_rn(acc);
+                    out[(size_t)n_begin + window_base + i] = *reinterpret_cast<uint16_t *>(&y);
+                }
+                named_bar_sync(1, ncons);
+                window_base = last_chunk ? 0 : rows_done;
+            }
+            if (++s == S) { s = 0; phase ^= 1; }
+            if (++nc == n_chunks) nc = 0;
+        }
     } else {
         // ------------------------------------------------------------ consumer warps
+        // (one lane per 32-k slice)
         // gate/up and the output may be shared with the previous kernel in the stream.
         grid_dep_wait();
         grid_dep_launch();
@@ -256,9 +369,9 @@ __global__ void __launch_bounds__(512, 1)
             const int rows_done = (nc + 1) * R;
             const bool last_chunk = (nc == n_chunks - 1);
             if (rows_done - window_base == kWindowRows || last_chunk) {
-                named_bar_sync(1, nvec);
+                named_bar_sync(1, ncons);
                 const int rows_in_window = min(rows_done, n_cnt) - window_base;
-                for (int i = tid; i < rows_in_window * MB; i += nvec) {
+                for (int i = tid; i < rows_in_window * MB; i += ncons) {
                     const int row = i / MB, mb = i % MB;
                     float acc = 0.f;
                     for (int w = 0; w < ncw; ++w) acc += red[((size_t)w * kWindowRows + row) * MB + mb];
@@ -268,7 +381,7 @@ __global__ void __launch_bounds__(512, 1)
                             *reinterpret_cast<uint16_t *>(&y);
                     }
                 }
-                named_bar_sync(1, nvec);
+                named_bar_sync(1, ncons);
                 window_base = last_chunk ? 0 : rows_done;
             }
             if (++s == S) { s = 0; phase ^= 1; }
@@ -286,13 +399,13 @@ __global__ void __launch_bounds__(512, 1)
     }
 }
 
-template <int MB, int R, int NVEC_C, int NG_C>
+template <int MB, int R, int NVEC_C, int NG_C, int LPS>
 cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
                        const void *qweight, const void *scales, void *out, int M, int K,
                        int N, int group, cudaStream_t stream, bool *launched) {
     static std::atomic<uint64_t> attr_done{0};
     static std::atomic<int> static_smem_cache{-1};
-    auto kern = gemv_tma_kernel<MB, R, NVEC_C, NG_C>;
+    auto kern = gemv_tma_kernel<MB, R, NVEC_C, NG_C, LPS>;
     int static_smem = static_smem_cache.load(std::memory_order_relaxed);
     if (static_smem < 0) {
         cudaFuncAttributes fa;
@@ -304,7 +417,7 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
     const int nvec = K / 32;
     const int ngroups = K / group;
     const size_t stage = (size_t)R * ((size_t)K / 2 + (size_t)ngroups * 2);
-    const size_t red = (size_t)(nvec / 32) * kWindowRows * MB * 4;
+    const size_t red = (size_t)(LPS * nvec / 32) * kWindowRows * MB * 4;
     const size_t budget = (size_t)di.max_smem_optin - (size_t)static_smem;
     if (red + 2 * stage > budget) return cudaSuccess;  // not launched: ring too small
     int S = (int)((budget - red) / stage);
@@ -333,7 +446,7 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
     if (grid < 1) grid = 1;
     const int rows_base = N / grid;
     const int rows_extra = N % grid;
-    err = launch_kernel(kern, dim3(grid), dim3(nvec + 32), smem, stream, 1,
+    err = launch_kernel(kern, dim3(grid), dim3(LPS * nvec + 32), smem, stream, 1,
                         static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up),
                         static_cast<const unsigned char *>(qweight),
                         static_cast<const uint16_t *>(scales), static_cast<uint16_t *>(out), M,
@@ -344,22 +457,24 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
     return cudaGetLastError();
 }
 
+// LPS = 2 (two lanes per 32-k slice) for one activation row, else one lane per slice.
 template <int MB>
 cudaError_t launch_mb(const DeviceInfo &di, const void *gate, const void *up,
                       const void *qweight, const void *scales, void *out, int M, int K, int N,
                       int group, cudaStream_t stream, bool *launched) {
     constexpr int R = kChunkRows;
-#define FD_SHAPE(KK, GG)                                                                      \
-    if (K == KK && group == GG)                                                               \
-        return launch_cfg<MB, R, KK / 32, KK / GG>(di, gate, up, qweight, scales, out, M, K, N, \
-                                                  group, stream, launched);
+    constexpr int LPS = MB == 1 ? 2 : 1;
+#define FD_SHAPE(KK, GG)                                                                        \
+    if (K == KK && group == GG)                                                                 \
+        return launch_cfg<MB, R, KK / 32, KK / GG, LPS>(di, gate, up, qweight, scales, out, M, K, \
+                                                       N, group, stream, launched);
     FD_SHAPE(14336, 128)
     FD_SHAPE(9216, 128)
     FD_SHAPE(4096, 128)
     FD_SHAPE(1024, 128)
 #undef FD_SHAPE
-    return launch_cfg<MB, R, 0, 0>(di, gate, up, qweight, scales, out, M, K, N, group, stream,
-                                   launched);
+    return launch_cfg<MB, R, 0, 0, LPS>(di, gate, up, qweight, scales, out, M, K, N, group,
+                                        stream, launched);
 }
 
 }  // namespace
