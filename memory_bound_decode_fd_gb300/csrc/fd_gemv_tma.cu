@@ -13,10 +13,11 @@
 //   * One persistent CTA per SM owning a contiguous range of output rows n.
 //   * Warp specialisation: the last warp is a producer whose lane 0 streams chunks of 8
 //     consecutive weight rows (8 * K/2 bytes, one contiguous bulk copy) and their scales
-//     (8 * K/group * 2 bytes, a second bulk copy) into an S-stage (up to 8) shared-memory
-//     ring, completion tracked by "full" mbarriers; consumers release a stage through an
-//     "empty" mbarrier (one arrival per consumer warp). The ring holds 3 stages (24
-//     rows) at K=14336 and 5 at K=9216, most of the ~27 and ~17 rows a CTA owns.
+//     (8 * K/group * 2 bytes, a second bulk copy) into shared-memory stages, completion
+//     tracked by "full" mbarriers. When a CTA's whole share of rows fits (27 rows at
+//     K=14336 N=4096, 17 at K=9216 N=2560), every chunk has a stage of its own and all
+//     are in flight from the start; otherwise the stages form a ring (up to 8) and
+//     consumers release a stage through an "empty" mbarrier (one arrival per warp).
 //   * Each 32-k slice of K is owned by LPS consumer lanes (K/32 * LPS threads): a =
 //     silu(g) * u for its k lives in registers as block-scaled int16
 //     (fd_gemv_common.cuh); per row a lane reads its 16-byte slot (conflict-free), splits
@@ -47,18 +48,20 @@ constexpr int kChunkRows = 8;  // rows per bulk-copy chunk
 // NVEC_C / NG_C: compile-time K/32 and K/group for the common shapes (0 = runtime), so
 // the per-row shared-memory offsets fold into instruction immediates.
 //
-// Shared memory: S ring stages of R weight rows + their scales, then the per-warp
-// partial sums. With one activation row (M == 1) the producer first bulk-copies gate and
-// up (2 * K * 2 bytes) into the space of the last ring stages, ahead of the weight
-// stream, so the consumers' activation reads do not queue behind it; those stages are
-// filled with weights only after every consumer warp has encoded its slice.
+// Shared memory: w_rows weight rows (stage s holds rows [sR, sR + R)), the scales of S
+// stages, then the per-warp partial sums. With one activation row (M == 1) the producer
+// first bulk-copies gate and up (2 * K * 2 bytes = 8 weight rows) into the last 8 weight
+// rows, ahead of the weight stream, so the consumers' activation reads do not queue
+// behind it (loaded from global memory instead, they arrived behind the weights and the
+// call took 10-25 % longer on GB300); stages from act_first_stage on are filled only
+// after every consumer warp has read its slice.
 template <int MB, int R, int NVEC_C, int NG_C, int LPS>
 __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
     gemv_tma_kernel(const uint16_t *__restrict__ gate, const uint16_t *__restrict__ up,
                     const unsigned char *__restrict__ qweight,
                     const uint16_t *__restrict__ scales, uint16_t *__restrict__ out, int M,
                     int K, int N, int group, int rows_base, int rows_extra, int S,
-                    int act_stages, int weights_evict_first) {
+                    int w_rows, int act_first_stage, int weights_evict_first) {
     static_assert(R * MB <= 32 && (R * MB & (R * MB - 1)) == 0, "R*MB: power of 2, <= 32");
     static_assert(LPS == 1 || (LPS == 2 && MB == 1 && R % 2 == 0), "paired lanes: M = 1 only");
     static_assert(kWindowRows % R == 0, "window must hold whole chunks");
@@ -78,11 +81,15 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
     const int ngroups = NG_C ? NG_C : K / group;
     const uint32_t w_row_bytes = (uint32_t)nvec * 16;
     const uint32_t s_row_bytes = (uint32_t)ngroups * 2;
-    const uint32_t stage_bytes = (uint32_t)R * (w_row_bytes + s_row_bytes);
-    float *red = reinterpret_cast<float *>(smem + (size_t)S * stage_bytes);
-    // gate then up, each K bf16, in the last act_stages stages (M == 1 only)
+    const uint32_t w_stage_bytes = (uint32_t)R * w_row_bytes;
+    const uint32_t s_stage_bytes = (uint32_t)R * s_row_bytes;
+    unsigned char *s_region = smem + (size_t)w_rows * w_row_bytes;
+    float *red = reinterpret_cast<float *>(s_region + (size_t)S * s_stage_bytes);
+    // gate then up, each K bf16 (4K bytes = 8 weight rows), in the last 8 weight rows
+    // (M == 1 only); stages from act_first_stage on are filled only after its release
     const bool act_in_smem = (M == 1);
-    uint16_t *act_smem = reinterpret_cast<uint16_t *>(smem + (size_t)(S - act_stages) * stage_bytes);
+    uint16_t *act_smem =
+        reinterpret_cast<uint16_t *>(smem + (size_t)w_rows * w_row_bytes - (size_t)K * 4);
 
     const int b = blockIdx.x;
     const int n_begin = b * rows_base + min(b, rows_extra);
@@ -99,19 +106,20 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
     int issued = 0, ps = 0, pround = 0, pnc = 0, pc = 0;
     bool pok = true;
     auto issue_chunk = [&](int c) {
-        if (act_in_smem && c == S - act_stages)
+        if (act_in_smem && c == act_first_stage)
             pok = mbar_wait_bounded(&act_free_bar, 0, &abort_flag);
         if (pok && pround > 0)
             pok = mbar_wait_bounded(&empty_bar[ps], (pround - 1) & 1, &abort_flag);
         if (!pok) return;
         const int rows = min(R, n_cnt - pnc * R);
         const size_t n0 = (size_t)n_begin + (size_t)pnc * R;
-        unsigned char *st = smem + (size_t)ps * stage_bytes;
         const uint32_t wb = (uint32_t)rows * w_row_bytes;
         const uint32_t sb = (uint32_t)rows * s_row_bytes;
         mbar_arrive_expect_tx(&full_bar[ps], wb + sb);
-        bulk_g2s(st, qweight + n0 * w_row_bytes, wb, &full_bar[ps], pol_w);
-        bulk_g2s(st + (size_t)R * w_row_bytes, scales + n0 * ngroups, sb, &full_bar[ps], pol_s);
+        bulk_g2s(smem + (size_t)ps * w_stage_bytes, qweight + n0 * w_row_bytes, wb,
+                 &full_bar[ps], pol_w);
+        bulk_g2s(s_region + (size_t)ps * s_stage_bytes, scales + n0 * ngroups, sb,
+                 &full_bar[ps], pol_s);
         issued = c + 1;
         if (++ps == S) { ps = 0; ++pround; }
         if (++pnc == n_chunks) pnc = 0;
@@ -142,7 +150,7 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
             bulk_g2s(act_smem + K, up, ab, &act_full_bar, pol_a);
         }
         // stages that are free from the start: no waits
-        for (; pc < total && pc < S - act_stages; ++pc) issue_chunk(pc);
+        for (; pc < total && pc < act_first_stage; ++pc) issue_chunk(pc);
     }
     __syncthreads();
 
@@ -204,9 +212,11 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
             }
             if (!act_ok) gu.g[0] = gu.g[1] = gu.u[0] = gu.u[1] = make_uint4(0, 0, 0, 0);
             encode_q16_pair(gu, hh, act);
-            if (act_in_smem) {
-                // released after its values are consumed, with a proxy fence: the
-                // producer's next bulk copy writes it
+            // When weight chunks overlay the area, it is released after the encode (released
+            // before it, the encode ran ~0.4 us longer at K=14336 and the call gained
+            // nothing, the weight stream being the bound), with a proxy fence: the
+            // producer's bulk copy writes it next.
+            if (act_in_smem && act_first_stage < total) {
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&act_free_bar);
@@ -220,9 +230,10 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
             float part[kRowsPerLane];
             const bool ok = mbar_wait_bounded(&full_bar[s], phase, &abort_flag);
             const int rows_valid = min(R, n_cnt - nc * R);
-            const unsigned char *st = smem + (size_t)s * stage_bytes;
-            const uint4 *wst = reinterpret_cast<const uint4 *>(st) + slice + hh * nvec;
-            const uint16_t *sst = reinterpret_cast<const uint16_t *>(st + (size_t)R * w_row_bytes) + col + hh * ngroups;
+            const uint4 *wst =
+                reinterpret_cast<const uint4 *>(smem + (size_t)s * w_stage_bytes) + slice + hh * nvec;
+            const uint16_t *sst = reinterpret_cast<const uint16_t *>(s_region + (size_t)s * s_stage_bytes) +
+                                  col + hh * ngroups;
             if (ok && rows_valid == R) {
 #pragma unroll
                 for (int i = 0; i < kRowsPerLane; ++i) {
@@ -247,9 +258,11 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                     }
                 }
             }
-            fence_proxy_async_smem();  // this stage's reads before its next bulk copy
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[s]);
+            if (total > S) {  // the stage is reused: its reads before the next bulk copy
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_bar[s]);
+            }
 
             const float wsum = half_reduce_scatter<kRowsPerLane>(part, lane);
             if (((lane & 15) & (kLanesPerValue - 1)) == 0) {
@@ -308,12 +321,14 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) gu.g[i] = gu.u[i] = make_uint4(0, 0, 0, 0);
                             }
-                            // The area is released only after its values are consumed, and
-                            // with a proxy fence: the producer's next bulk copy writes it.
+                            // The area is released after the encode (when chunks overlay
+                            // it), with a proxy fence: the next bulk copy writes it.
                             encode_q16(gu, act[mb]);
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&act_free_bar);
+                            if (act_first_stage < total) {
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(&act_free_bar);
+                            }
                         } else {
                             load_gate_up(gate, up, (size_t)(m0 + mb) * K + (size_t)tid * 32, gu);
                             encode_q16(gu, act[mb]);
@@ -326,9 +341,9 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
             float part[R * MB];
             const bool ok = mbar_wait_bounded(&full_bar[s], phase, &abort_flag);
             const int rows_valid = min(R, n_cnt - nc * R);
-            const unsigned char *st = smem + (size_t)s * stage_bytes;
-            const uint4 *wst = reinterpret_cast<const uint4 *>(st) + tid;
-            const uint16_t *sst = reinterpret_cast<const uint16_t *>(st + (size_t)R * w_row_bytes) + col;
+            const uint4 *wst = reinterpret_cast<const uint4 *>(smem + (size_t)s * w_stage_bytes) + tid;
+            const uint16_t *sst =
+                reinterpret_cast<const uint16_t *>(s_region + (size_t)s * s_stage_bytes) + col;
             if (ok && rows_valid == R) {
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
@@ -356,9 +371,11 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                     }
                 }
             }
-            fence_proxy_async_smem();  // this stage's reads before its next bulk copy
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[s]);
+            if (total > S) {  // the stage is reused: its reads before the next bulk copy
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_bar[s]);
+            }
 
             const float wsum = warp_reduce_scatter<R * MB>(part, lane);
             if ((lane & (kLanesPerValue - 1)) == 0) {
@@ -416,18 +433,50 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
     }
     const int nvec = K / 32;
     const int ngroups = K / group;
-    const size_t stage = (size_t)R * ((size_t)K / 2 + (size_t)ngroups * 2);
+    const size_t w_row = (size_t)K / 2, s_row = (size_t)ngroups * 2;
     const size_t red = (size_t)(LPS * nvec / 32) * kWindowRows * MB * 4;
     const size_t budget = (size_t)di.max_smem_optin - (size_t)static_smem;
-    if (red + 2 * stage > budget) return cudaSuccess;  // not launched: ring too small
-    int S = (int)((budget - red) / stage);
-    if (S > kMaxStages) S = kMaxStages;
-    // With M == 1 the gate/up copy (2 * K * 2 bytes) borrows the last stages; keep at
-    // least two stages free for weights.
-    const size_t act_bytes = (size_t)K * 4;
-    const int act_stages = (int)((act_bytes + stage - 1) / stage);
-    if (M == 1 && S - act_stages < 2) return cudaSuccess;  // not launched
-    const size_t smem = (size_t)S * stage + red;
+    int grid = di.sm_count;
+    if ((long long)grid * R > N) grid = (N + R - 1) / R;
+    if (grid < 1) grid = 1;
+    const int rows_base = N / grid;
+    const int rows_extra = N % grid;
+    const int n_max = rows_base + (rows_extra > 0 ? 1 : 0);
+    const int n_chunks_max = (n_max + R - 1) / R;
+    // Shared memory: w_rows weight rows (stage s = rows [sR, sR + R)), S stages of scales,
+    // then the per-warp partial sums.
+    auto bytes = [&](int wr, int st) { return (size_t)wr * w_row + (size_t)st * R * s_row + red; };
+    constexpr int kActRows = 8;  // gate + up of one row: 4K bytes = 8 weight rows of K/2
+    int S = 0, w_rows = 0;
+    if (M <= MB) {
+        // One pass over the rows: when the CTA's share fits, every chunk gets a stage of
+        // its own and all are issued at once. The activation (M == 1) takes the stages
+        // after the chunks if there is room, else it overlays the last 8 weight rows and
+        // the chunks there are issued once the consumers have read it.
+        const int own = n_chunks_max + (M == 1 ? (kActRows + R - 1) / R : 0);
+        if (own <= kMaxStages && bytes(own * R, own) <= budget) {
+            S = own;
+            w_rows = own * R;
+        } else if (M == 1 && n_chunks_max <= kMaxStages && n_max >= kActRows &&
+                   bytes(n_max, n_chunks_max) <= budget) {
+            S = n_chunks_max;
+            w_rows = n_max;
+        }
+    }
+    const bool ring = (S == 0);
+    if (ring) {
+        // a ring of uniform stages, reused across chunks and activation-row passes
+        const size_t stage = (size_t)R * (w_row + s_row);
+        if (red + 2 * stage > budget) return cudaSuccess;  // not launched: ring too small
+        S = (int)((budget - red) / stage);
+        if (S > kMaxStages) S = kMaxStages;
+        w_rows = S * R;
+    }
+    // With M == 1 the gate/up copy borrows the last 8 weight rows: stages from
+    // act_first_stage on are filled after it is read. A ring keeps two stages for weights.
+    const int act_first_stage = (M == 1) ? (w_rows - kActRows) / R : S;
+    if (ring && M == 1 && act_first_stage < 2) return cudaSuccess;  // not launched
+    const size_t smem = bytes(w_rows, S);
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -441,16 +490,11 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
         if (err != cudaSuccess) return err;
         attr_done.fetch_or(bit, std::memory_order_acq_rel);
     }
-    int grid = di.sm_count;
-    if ((long long)grid * R > N) grid = (N + R - 1) / R;
-    if (grid < 1) grid = 1;
-    const int rows_base = N / grid;
-    const int rows_extra = N % grid;
     err = launch_kernel(kern, dim3(grid), dim3(LPS * nvec + 32), smem, stream, 1,
                         static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up),
                         static_cast<const unsigned char *>(qweight),
                         static_cast<const uint16_t *>(scales), static_cast<uint16_t *>(out), M,
-                        K, N, group, rows_base, rows_extra, S, act_stages,
+                        K, N, group, rows_base, rows_extra, S, w_rows, act_first_stage,
                         M <= MB ? 1 : 0);
     *launched = true;
     if (err != cudaSuccess) return err;
