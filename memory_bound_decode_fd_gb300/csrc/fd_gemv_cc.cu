@@ -206,9 +206,8 @@ __global__ void __launch_bounds__(512, 1)
             const int rows_in_window = min(rows_done, n_cnt) - window_base;
             for (int i = tid; i < rows_in_window * MB; i += T) {
                 const int row = i / MB, mb = i % MB;
-                float acc = 0.f;
-                for (int w = 0; w < nwarps; ++w)
-                    acc += red[((size_t)w * kWindowRows + row) * MB + mb];
+                const float acc =
+                    sum_partials(red + (size_t)row * MB + mb, nwarps, kWindowRows * MB);
                 if (m0 + mb < M) {
                     const int n = n_begin + window_base + row;
                     __nv_bfloat16 y = __float2bfloat16_rn(acc);

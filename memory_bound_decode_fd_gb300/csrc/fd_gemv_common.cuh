@@ -23,6 +23,23 @@ namespace fd {
 
 constexpr int kWindowRows = 64;  // rows whose per-warp partials are held before a flush
 
+// Sum of the n per-warp partials of one output (p[w * stride], w < n) in four
+// independent chains, so the loads overlap: a single chain waits on each load in turn,
+// which made the final flush of a CTA's outputs ~0.3 us long at 28 warps.
+__device__ __forceinline__ float sum_partials(const float *p, int n, int stride) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int w = 0;
+#pragma unroll 2
+    for (; w + 3 < n; w += 4) {
+        a0 += p[(size_t)w * stride];
+        a1 += p[(size_t)(w + 1) * stride];
+        a2 += p[(size_t)(w + 2) * stride];
+        a3 += p[(size_t)(w + 3) * stride];
+    }
+    for (; w < n; ++w) a0 += p[(size_t)w * stride];
+    return (a0 + a1) + (a2 + a3);
+}
+
 // One thread's activation slice (32 k) for one activation row, in the operand layout of
 // dp2a: for word i (k = 8i .. 8i+7 of the slice),
 //   e[i] = (a16[8i+0], a16[8i+2]), f[i] = (a16[8i+4], a16[8i+6])  pair with L's bytes

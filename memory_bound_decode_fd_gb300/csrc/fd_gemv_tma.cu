@@ -275,8 +275,7 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                 named_bar_sync(1, ncons);
                 const int rows_in_window = min(rows_done, n_cnt) - window_base;
                 for (int i = tid; i < rows_in_window; i += ncons) {
-                    float acc = 0.f;
-                    for (int w = 0; w < ncw; ++w) acc += red[(size_t)w * kWindowRows + i];
+                    const float acc = sum_partials(red + i, ncw, kWindowRows);
                     __nv_bfloat16 y = __float2bfloat16_rn(acc);
                     out[(size_t)n_begin + window_base + i] = *reinterpret_cast<uint16_t *>(&y);
                 }
@@ -390,8 +389,7 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                 const int rows_in_window = min(rows_done, n_cnt) - window_base;
                 for (int i = tid; i < rows_in_window * MB; i += ncons) {
                     const int row = i / MB, mb = i % MB;
-                    float acc = 0.f;
-                    for (int w = 0; w < ncw; ++w) acc += red[((size_t)w * kWindowRows + row) * MB + mb];
+                    const float acc = sum_partials(red + (size_t)row * MB + mb, ncw, kWindowRows * MB);
                     if (m0 + mb < M) {
                         __nv_bfloat16 y = __float2bfloat16_rn(acc);
                         out[(size_t)(m0 + mb) * N + n_begin + window_base + row] =
