@@ -18,8 +18,8 @@ Reported:
   cpu_baseline  the CPU oracle, single-threaded, on a bounded sample of the workload
   --impl reference  times the CPU oracle alone (the reference arm of this benchmark)
 
-Other workloads (--workload gemv_94mb | rmsnorm_big | gemv_small | batched_m64) time
-one call per step and rotate ceil(3 x L2 / bytes) input sets so every step reads HBM.
+Other workloads (--workload gemv_94mb | rmsnorm_big | gemv_small | batched_m64 |
+gemv_residual) time one call per step and rotate ceil(3 x L2 / bytes) input sets so every step reads HBM.
 """
 
 from __future__ import annotations
@@ -407,9 +407,10 @@ def bench_single(args, device, rank, world):
     kind = spec.pop("kind")
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     calls = []
-    if kind in ("gemv", "batched"):
+    if kind in ("gemv", "batched", "gemv_residual"):
         M, K, N, g = spec["M"], spec["K"], spec["N"], spec["group"]
-        nbytes = fd.gemv_bytes(M, K, N, g)
+        with_res = kind == "gemv_residual"
+        nbytes = fd.gemv_bytes(M, K, N, g) + (M * N * 2 if with_res else 0)
         nsets = max(1, min(4096, math.ceil(3 * l2 / nbytes)))
         base = inputs.gemv_inputs(M, K, N, g, seed=spec["seed"])
         gate, up = to_dev(base["gate"], device), to_dev(base["up"], device)
@@ -417,9 +418,17 @@ def bench_single(args, device, rank, world):
         qs = [to_dev(base["qweight"], device)] + [to_dev(inputs.int4_words(rng, N, K), device) for _ in range(nsets - 1)]
         ss = [to_dev(base["scales"], device)] + [to_dev(inputs.scales_bf16(rng, N, K, g), device) for _ in range(nsets - 1)]
         out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
-        for q, s in zip(qs, ss):
-            calls.append(lambda q=q, s=s: fd.swiglu_w4a16_gemv(gate, up, q, s, out=out, group=g))
-        kname, desc = "swiglu_w4a16_gemv", f"GEMV M={M} K={K} N={N} group {g}, seed {spec['seed']}"
+        if with_res:
+            # the residual stream x (read) and the new residual (written to `out`)
+            res = to_dev(inputs.normal_bf16(rng, (M, N)), device)
+            for q, s in zip(qs, ss):
+                calls.append(lambda q=q, s=s: fd.swiglu_w4a16_gemv_residual(gate, up, q, s, res, out=out, group=g))
+            kname = "swiglu_w4a16_gemv_residual"
+            desc = f"GEMV + residual-add epilogue M={M} K={K} N={N} group {g}, seed {spec['seed']}"
+        else:
+            for q, s in zip(qs, ss):
+                calls.append(lambda q=q, s=s: fd.swiglu_w4a16_gemv(gate, up, q, s, out=out, group=g))
+            kname, desc = "swiglu_w4a16_gemv", f"GEMV M={M} K={K} N={N} group {g}, seed {spec['seed']}"
     else:
         rows, hidden = spec["rows"], spec["hidden"]
         nbytes = fd.add_rmsnorm_bytes(rows, hidden)
@@ -546,7 +555,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--workload", default="decode_step",
-                    choices=["decode_step", "gemv_94mb", "rmsnorm_big", "gemv_small", "batched_m64"])
+                    choices=["decode_step", "gemv_94mb", "rmsnorm_big", "gemv_small", "batched_m64",
+                             "gemv_residual"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
 

@@ -9,6 +9,9 @@
  *                          silu/mul intermediate never exist in memory).
  *   fd_add_rmsnorm         h = x + residual; out = RMSNorm(h) * weight  (one kernel, two
  *                          outputs: the new residual h and the normalised row).
+ *   fd_swiglu_w4a16_gemv_residual
+ *                          the same GEMV with a residual-add epilogue: out = residual + y
+ *                          (the down projection of a fused layer writes the new residual).
  *
  * Sources (web pages, cited by title and section):
  *   [FIX]  "PyTorch Community Proposes Fusion Fix as Large Intermediate Buffers May Slow
@@ -16,8 +19,10 @@
  *          (1, K, N) product an M=1 matmul must not materialise), "Fix proposal" (int4
  *          weights with a SwiGLU pre-operation).
  *   [FUSE] "09 - Operator fusion" - section 5, "The taxonomy of fusions" (items 2 and 4:
- *          reduction + elementwise; GEMM prologue dequantisation for W4A16) and "The
- *          fusion boundary problem" (add_rmsnorm with two outputs; act @ W_down).
+ *          reduction + elementwise; GEMM prologue dequantisation for W4A16; item 3: GEMM
+ *          epilogue fusion) and "The fusion boundary problem" (add_rmsnorm with two
+ *          outputs; act @ W_down; kernel 3: the down projection with a residual-add
+ *          epilogue that writes new_residual = x + out).
  *   [KFM]  "Kernel Fusion, torch.compile and CUDA Graphs, Measured" - "Step 1" (silu(g) *
  *          u), "Step 2: fusing them by hand in Triton" (add + RMSNorm order and roundings).
  *
@@ -81,6 +86,26 @@ typedef enum fd_status {
 int fd_swiglu_w4a16_gemv(const void *gate, const void *up, const void *qweight,
                          const void *scales, void *out, int M, int K, int N, int group,
                          fd_stream_t stream);
+
+/*
+ * fd_swiglu_w4a16_gemv_residual - fd_swiglu_w4a16_gemv with a residual-add epilogue
+ * ("kernel 3" of a fused layer, [FUSE] "The fusion boundary problem"; GEMM epilogue
+ * fusion, [FUSE] item 3):
+ *
+ *   out[m, n] = bf16( f32(residual[m, n]) + sum_k a[m, k] * W[n, k] )   (one RNE rounding)
+ *
+ * The sum is the fp32 accumulator of fd_swiglu_w4a16_gemv: the product is not rounded to
+ * bf16 before the add (eager PyTorch would round twice, out = bf16(bf16(y) + residual)).
+ * residual  bf16 [M, N] row-major: x, the pre-norm residual stream of the layer (the
+ *           residual_out of fd_add_rmsnorm).
+ * out       bf16 [M, N]: the new residual. out == residual (exactly the same pointer, in
+ *           place) is allowed; any other overlap of out with an input, or of residual
+ *           with gate, up, qweight or scales, returns FD_ERR_OVERLAP.
+ * Other arguments, requirements and the kernels used are those of fd_swiglu_w4a16_gemv.
+ */
+int fd_swiglu_w4a16_gemv_residual(const void *gate, const void *up, const void *qweight,
+                                  const void *scales, const void *residual, void *out, int M,
+                                  int K, int N, int group, fd_stream_t stream);
 
 /*
  * fd_add_rmsnorm - fused residual add + RMSNorm, one pass over HBM.     [KFM Step 2]

@@ -1,6 +1,8 @@
 """fd - fused memory-bound decode kernels for GB300 (sm_103a).
 
 * ``swiglu_w4a16_gemv``: y = (silu(g) * u) . dequant(W_int4)^T, one kernel, int4 in HBM only.
+* ``swiglu_w4a16_gemv_residual``: the same GEMV with a residual-add epilogue (out =
+  residual + y, the new residual stream written by the down projection).
 * ``add_rmsnorm``: residual add + RMSNorm, one pass, two outputs.
 * ``decode_mlp_step``: L layers of the two, in stream order.
 
@@ -34,6 +36,7 @@ from .kernels import (  # noqa: F401
     set_gemv_path,
     set_pdl,
     swiglu_w4a16_gemv,
+    swiglu_w4a16_gemv_residual,
     w4_dequant_debug,
 )
 from .packing import pack_int4  # noqa: F401

@@ -75,17 +75,19 @@ unsigned launch_flags() { return g_launch_flags.load(std::memory_order_relaxed);
 
 using namespace fd;
 
-extern "C" {
+namespace {
 
-int fd_swiglu_w4a16_gemv(const void *gate, const void *up, const void *qweight,
-                         const void *scales, void *out, int M, int K, int N, int group,
-                         fd_stream_t stream) {
+// Validation and kernel choice shared by both GEMV entry points; `residual` may be null.
+int swiglu_gemv(const void *gate, const void *up, const void *qweight, const void *scales,
+                const void *residual, void *out, int M, int K, int N, int group,
+                fd_stream_t stream) {
     if (!gate || !up || !out) return FD_ERR_NULL;
     int st = check_w4_layout(qweight, scales, K, N, group);
     if (st != FD_OK) return st;
     if (M <= 0) return FD_ERR_SHAPE;
     if (M > FD_MAX_M) return FD_ERR_UNSUPPORTED;
     if (!aligned16(gate) || !aligned16(up) || !aligned16(out)) return FD_ERR_ALIGN;
+    if (residual && !aligned16(residual)) return FD_ERR_ALIGN;
     const size_t act_bytes = (size_t)M * K * 2;
     const size_t out_bytes = (size_t)M * N * 2;
     const size_t w_bytes = (size_t)N * K / 2;
@@ -93,21 +95,48 @@ int fd_swiglu_w4a16_gemv(const void *gate, const void *up, const void *qweight,
     if (overlaps(out, out_bytes, gate, act_bytes) || overlaps(out, out_bytes, up, act_bytes) ||
         overlaps(out, out_bytes, qweight, w_bytes) || overlaps(out, out_bytes, scales, s_bytes))
         return FD_ERR_OVERLAP;
+    // the residual may be the output itself (in place), or apart from every other buffer
+    if (residual && residual != out &&
+        (overlaps(residual, out_bytes, out, out_bytes) ||
+         overlaps(residual, out_bytes, gate, act_bytes) ||
+         overlaps(residual, out_bytes, up, act_bytes) ||
+         overlaps(residual, out_bytes, qweight, w_bytes) ||
+         overlaps(residual, out_bytes, scales, s_bytes)))
+        return FD_ERR_OVERLAP;
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
     const int path = g_gemv_path.load(std::memory_order_relaxed);
     if (fd_gemv_uses_tensor_cores(M, K, N, group)) {
         bool launched = false;
-        cudaError_t err = launch_gemv_tc(gate, up, qweight, scales, out, M, K, N, group, st_,
-                                         &launched);
+        cudaError_t err = launch_gemv_tc(gate, up, qweight, scales, residual, out, M, K, N,
+                                         group, st_, &launched);
         if (err != cudaSuccess || launched) return from_cuda(err);
     }
     if (path == FD_GEMV_AUTO || path == FD_GEMV_BULK) {
         bool launched = false;
-        cudaError_t err = launch_gemv_tma(gate, up, qweight, scales, out, M, K, N, group, st_,
-                                          &launched);
+        cudaError_t err = launch_gemv_tma(gate, up, qweight, scales, residual, out, M, K, N,
+                                          group, st_, &launched);
         if (err != cudaSuccess || launched) return from_cuda(err);
     }
-    return from_cuda(launch_gemv_cc(gate, up, qweight, scales, out, M, K, N, group, st_));
+    return from_cuda(
+        launch_gemv_cc(gate, up, qweight, scales, residual, out, M, K, N, group, st_));
+}
+
+}  // namespace
+
+extern "C" {
+
+
+int fd_swiglu_w4a16_gemv(const void *gate, const void *up, const void *qweight,
+                         const void *scales, void *out, int M, int K, int N, int group,
+                         fd_stream_t stream) {
+    return swiglu_gemv(gate, up, qweight, scales, nullptr, out, M, K, N, group, stream);
+}
+
+int fd_swiglu_w4a16_gemv_residual(const void *gate, const void *up, const void *qweight,
+                                  const void *scales, const void *residual, void *out, int M,
+                                  int K, int N, int group, fd_stream_t stream) {
+    if (!residual) return FD_ERR_NULL;
+    return swiglu_gemv(gate, up, qweight, scales, residual, out, M, K, N, group, stream);
 }
 
 int fd_gemv_uses_tensor_cores(int M, int K, int N, int group) {

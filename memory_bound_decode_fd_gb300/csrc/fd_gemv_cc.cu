@@ -71,7 +71,8 @@ template <int VPT, int MB, int R, int S>
 __global__ void __launch_bounds__(512, 1)
     gemv_cc_kernel(const uint16_t *__restrict__ gate, const uint16_t *__restrict__ up,
                    const uint4 *__restrict__ qweight, const uint16_t *__restrict__ scales,
-                   uint16_t *__restrict__ out, int M, int K, int N, int group, int rows_base,
+                   const uint16_t *residual, uint16_t *out, int M, int K, int N, int group,
+                   int rows_base,
                    int rows_extra, int weights_evict_first) {
     static_assert(R * MB <= 32 && (R * MB & (R * MB - 1)) == 0, "R*MB: power of 2, <= 32");
     static_assert(kWindowRows % R == 0, "window must hold whole chunks");
@@ -206,12 +207,13 @@ __global__ void __launch_bounds__(512, 1)
             const int rows_in_window = min(rows_done, n_cnt) - window_base;
             for (int i = tid; i < rows_in_window * MB; i += T) {
                 const int row = i / MB, mb = i % MB;
-                const float acc =
+                float acc =
                     sum_partials(red + (size_t)row * MB + mb, nwarps, kWindowRows * MB);
                 if (m0 + mb < M) {
-                    const int n = n_begin + window_base + row;
+                    const size_t o = (size_t)(m0 + mb) * N + n_begin + window_base + row;
+                    if (residual) acc += bf16lo(residual[o]);
                     __nv_bfloat16 y = __float2bfloat16_rn(acc);
-                    out[(size_t)(m0 + mb) * N + n] = *reinterpret_cast<uint16_t *>(&y);
+                    out[o] = *reinterpret_cast<uint16_t *>(&y);
                 }
             }
             __syncthreads();
@@ -260,8 +262,8 @@ cudaError_t ensure_smem_attr(Kern kern, size_t smem, std::atomic<uint64_t> &done
 
 template <int VPT, int MB, int R, int S>
 cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
-                       const void *qweight, const void *scales, void *out, int M, int K,
-                       int N, int group, cudaStream_t stream) {
+                       const void *qweight, const void *scales, const void *residual,
+                       void *out, int M, int K, int N, int group, cudaStream_t stream) {
     static std::atomic<uint64_t> attr_done{0};
     const int T = threads_for(K, VPT);
     const size_t smem = gemv_smem_bytes<VPT, MB, R, S>(T);
@@ -278,8 +280,9 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
     err = launch_kernel(kern, dim3(grid), dim3(T), smem, stream, 1,
                         static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up),
                         static_cast<const uint4 *>(qweight),
-                        static_cast<const uint16_t *>(scales), static_cast<uint16_t *>(out), M,
-                        K, N, group, rows_base, rows_extra, evict_first);
+                        static_cast<const uint16_t *>(scales),
+                        static_cast<const uint16_t *>(residual), static_cast<uint16_t *>(out),
+                        M, K, N, group, rows_base, rows_extra, evict_first);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
@@ -290,16 +293,16 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
 // or the M > 1 kernel (MB = 2), with one (K <= 16384) or two (K <= 32768) weight vector
 // positions per thread.
 cudaError_t launch_gemv_cc(const void *gate, const void *up, const void *qweight,
-                           const void *scales, void *out, int M, int K, int N, int group,
-                           cudaStream_t stream) {
+                           const void *scales, const void *residual, void *out, int M, int K,
+                           int N, int group, cudaStream_t stream) {
     DeviceInfo di;
     cudaError_t err = device_info(&di);
     if (err != cudaSuccess) return err;
     const size_t limit = (size_t)di.max_smem_optin;
 #define FD_TRY(VPT, MB, R, S)                                                              \
     if (gemv_smem_bytes<VPT, MB, R, S>(threads_for(K, VPT)) <= limit)                      \
-        return launch_cfg<VPT, MB, R, S>(di, gate, up, qweight, scales, out, M, K, N, group, \
-                                         stream);
+        return launch_cfg<VPT, MB, R, S>(di, gate, up, qweight, scales, residual, out, M, K, N, \
+                                         group, stream);
     const bool wide = K / 32 > 512;  // more than 512 vector positions: two per thread
     if (!wide && M == 1) {
         FD_TRY(1, 1, 8, 4)

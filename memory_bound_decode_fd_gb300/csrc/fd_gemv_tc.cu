@@ -73,8 +73,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap map_w,
                    const __grid_constant__ CUtensorMap map_s,
                    const __grid_constant__ CUtensorMap map_g,
-                   const __grid_constant__ CUtensorMap map_u, uint16_t *__restrict__ out,
-                   int M, int N, int group, int k_cta, int s_w, int s_gu, int s_op,
+                   const __grid_constant__ CUtensorMap map_u, const uint16_t *residual,
+                   uint16_t *out, int M, int N, int group, int k_cta, int s_w, int s_gu, int s_op,
                    uint32_t off_gu, uint32_t off_op, uint32_t off_sc, int sg) {
     static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 128, "N of the MMA");
     constexpr int kCols = NPAD < 32 ? 32 : NPAD;  // TMEM columns (power of two)
@@ -423,8 +423,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 s0 += p.x;
                 s1 += p.y;
             }
+            const size_t oi = (size_t)m * N + n0 + 32 * rank + rp;
+            if (residual) {
+                const uint32_t r = *reinterpret_cast<const uint32_t *>(residual + oi);
+                s0 += bf16lo(r);
+                s1 += bf16hi(r);
+            }
             const uint32_t o = failed ? 0x7FC07FC0u : pack_bf16x2(s0, s1);
-            *reinterpret_cast<uint32_t *>(out + (size_t)m * N + n0 + 32 * rank + rp) = o;
+            *reinterpret_cast<uint32_t *>(out + oi) = o;
         }
     }
     tc_fence_before();
@@ -504,8 +510,9 @@ bool make_plan(int npad, int k_cta, int group, size_t budget, TcPlan *p) {
 
 template <int NPAD>
 cudaError_t launch_npad(const DeviceInfo &di, const void *gate, const void *up,
-                        const void *qweight, const void *scales, void *out, int mc, int K,
-                        int N, int group, cudaStream_t stream, bool *launched) {
+                        const void *qweight, const void *scales, const void *residual,
+                        void *out, int mc, int K, int N, int group, cudaStream_t stream,
+                        bool *launched) {
     static std::atomic<uint64_t> attr_done{0};
     static std::atomic<int> static_smem_cache{-1};
     auto kern = gemv_tc_kernel<NPAD>;
@@ -546,7 +553,8 @@ cudaError_t launch_npad(const DeviceInfo &di, const void *gate, const void *up,
     }
     *launched = true;
     err = launch_kernel(kern, dim3(kTcSplit, N / kTcRows), dim3(kTcThreads), plan.smem, stream,
-                        kTcSplit, mw, ms, mg, mu, static_cast<uint16_t *>(out), mc, N, group,
+                        kTcSplit, mw, ms, mg, mu, static_cast<const uint16_t *>(residual),
+                        static_cast<uint16_t *>(out), mc, N, group,
                         k_cta, plan.s_w, plan.s_gu, plan.s_op, plan.off_gu, plan.off_op,
                         plan.off_sc, plan.sg);
     if (err != cudaSuccess) return err;
@@ -563,8 +571,8 @@ bool gemv_tc_supported(int M, int K, int N, int group) {
 }
 
 cudaError_t launch_gemv_tc(const void *gate, const void *up, const void *qweight,
-                           const void *scales, void *out, int M, int K, int N, int group,
-                           cudaStream_t stream, bool *launched) {
+                           const void *scales, const void *residual, void *out, int M, int K,
+                           int N, int group, cudaStream_t stream, bool *launched) {
     *launched = false;
     if (!gemv_tc_supported(M, K, N, group)) return cudaSuccess;
     DeviceInfo di;
@@ -573,19 +581,21 @@ cudaError_t launch_gemv_tc(const void *gate, const void *up, const void *qweight
     const uint16_t *g = static_cast<const uint16_t *>(gate);
     const uint16_t *u = static_cast<const uint16_t *>(up);
     uint16_t *o = static_cast<uint16_t *>(out);
+    const uint16_t *r = static_cast<const uint16_t *>(residual);
     // Up to 128 activation rows per launch (the MMA's N); larger M runs in row blocks.
     for (int m0 = 0; m0 < M; m0 += 128) {
         const int mc = M - m0 < 128 ? M - m0 : 128;
         const size_t ao = (size_t)m0 * K, oo = (size_t)m0 * N;
+        const uint16_t *ro = r ? r + oo : nullptr;
         bool done = false;
         if (mc <= 16)
-            err = launch_npad<16>(di, g + ao, u + ao, qweight, scales, o + oo, mc, K, N, group, stream, &done);
+            err = launch_npad<16>(di, g + ao, u + ao, qweight, scales, ro, o + oo, mc, K, N, group, stream, &done);
         else if (mc <= 32)
-            err = launch_npad<32>(di, g + ao, u + ao, qweight, scales, o + oo, mc, K, N, group, stream, &done);
+            err = launch_npad<32>(di, g + ao, u + ao, qweight, scales, ro, o + oo, mc, K, N, group, stream, &done);
         else if (mc <= 64)
-            err = launch_npad<64>(di, g + ao, u + ao, qweight, scales, o + oo, mc, K, N, group, stream, &done);
+            err = launch_npad<64>(di, g + ao, u + ao, qweight, scales, ro, o + oo, mc, K, N, group, stream, &done);
         else
-            err = launch_npad<128>(di, g + ao, u + ao, qweight, scales, o + oo, mc, K, N, group, stream, &done);
+            err = launch_npad<128>(di, g + ao, u + ao, qweight, scales, ro, o + oo, mc, K, N, group, stream, &done);
         if (err != cudaSuccess) return err;
         if (!done) {
             if (m0 == 0) return cudaSuccess;  // nothing launched: the caller falls back

@@ -59,8 +59,9 @@ template <int MB, int R, int NVEC_C, int NG_C, int LPS>
 __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
     gemv_tma_kernel(const uint16_t *__restrict__ gate, const uint16_t *__restrict__ up,
                     const unsigned char *__restrict__ qweight,
-                    const uint16_t *__restrict__ scales, uint16_t *__restrict__ out, int M,
-                    int K, int N, int group, int rows_base, int rows_extra, int S,
+                    const uint16_t *__restrict__ scales, const uint16_t *residual,
+                    uint16_t *out, int M, int K, int N, int group, int rows_base,
+                    int rows_extra, int S,
                     int w_rows, int act_first_stage, int weights_evict_first) {
     static_assert(R * MB <= 32 && (R * MB & (R * MB - 1)) == 0, "R*MB: power of 2, <= 32");
     static_assert(LPS == 1 || (LPS == 2 && MB == 1 && R % 2 == 0), "paired lanes: M = 1 only");
@@ -184,6 +185,10 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
         // warps of the one-lane form on the same rows, and each lane encodes 16 elements.
         grid_dep_wait();
         grid_dep_launch();
+        // The residual of the first window's rows (thread i stores row i, below), requested
+        // now so that the final store does not wait on its load.
+        float res0 = 0.f;
+        if (residual && tid < min(n_cnt, kWindowRows)) res0 = bf16lo(residual[n_begin + tid]);
         const int hh = lane >> 4;
         const int slice = 16 * warp + (lane & 15);
         const int col = (slice * 32) / group;  // this lane's scale column
@@ -275,9 +280,11 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                 named_bar_sync(1, ncons);
                 const int rows_in_window = min(rows_done, n_cnt) - window_base;
                 for (int i = tid; i < rows_in_window; i += ncons) {
-                    const float acc = sum_partials(red + i, ncw, kWindowRows);
+                    const size_t n = (size_t)n_begin + window_base + i;
+                    float acc = sum_partials(red + i, ncw, kWindowRows);
+                    if (residual) acc += window_base == 0 ? res0 : bf16lo(residual[n]);
                     __nv_bfloat16 y = __float2bfloat16_rn(acc);
-                    out[(size_t)n_begin + window_base + i] = *reinterpret_cast<uint16_t *>(&y);
+                    out[n] = *reinterpret_cast<uint16_t *>(&y);
                 }
                 named_bar_sync(1, ncons);
                 window_base = last_chunk ? 0 : rows_done;
@@ -389,11 +396,12 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                 const int rows_in_window = min(rows_done, n_cnt) - window_base;
                 for (int i = tid; i < rows_in_window * MB; i += ncons) {
                     const int row = i / MB, mb = i % MB;
-                    const float acc = sum_partials(red + (size_t)row * MB + mb, ncw, kWindowRows * MB);
+                    float acc = sum_partials(red + (size_t)row * MB + mb, ncw, kWindowRows * MB);
                     if (m0 + mb < M) {
+                        const size_t o = (size_t)(m0 + mb) * N + n_begin + window_base + row;
+                        if (residual) acc += bf16lo(residual[o]);
                         __nv_bfloat16 y = __float2bfloat16_rn(acc);
-                        out[(size_t)(m0 + mb) * N + n_begin + window_base + row] =
-                            *reinterpret_cast<uint16_t *>(&y);
+                        out[o] = *reinterpret_cast<uint16_t *>(&y);
                     }
                 }
                 named_bar_sync(1, ncons);
@@ -416,8 +424,9 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
 
 template <int MB, int R, int NVEC_C, int NG_C, int LPS>
 cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
-                       const void *qweight, const void *scales, void *out, int M, int K,
-                       int N, int group, cudaStream_t stream, bool *launched) {
+                       const void *qweight, const void *scales, const void *residual,
+                       void *out, int M, int K, int N, int group, cudaStream_t stream,
+                       bool *launched) {
     static std::atomic<uint64_t> attr_done{0};
     static std::atomic<int> static_smem_cache{-1};
     auto kern = gemv_tma_kernel<MB, R, NVEC_C, NG_C, LPS>;
@@ -491,8 +500,9 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
     err = launch_kernel(kern, dim3(grid), dim3(LPS * nvec + 32), smem, stream, 1,
                         static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up),
                         static_cast<const unsigned char *>(qweight),
-                        static_cast<const uint16_t *>(scales), static_cast<uint16_t *>(out), M,
-                        K, N, group, rows_base, rows_extra, S, w_rows, act_first_stage,
+                        static_cast<const uint16_t *>(scales),
+                        static_cast<const uint16_t *>(residual), static_cast<uint16_t *>(out),
+                        M, K, N, group, rows_base, rows_extra, S, w_rows, act_first_stage,
                         M <= MB ? 1 : 0);
     *launched = true;
     if (err != cudaSuccess) return err;
@@ -502,21 +512,21 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
 // LPS = 2 (two lanes per 32-k slice) for one activation row, else one lane per slice.
 template <int MB>
 cudaError_t launch_mb(const DeviceInfo &di, const void *gate, const void *up,
-                      const void *qweight, const void *scales, void *out, int M, int K, int N,
-                      int group, cudaStream_t stream, bool *launched) {
+                      const void *qweight, const void *scales, const void *residual, void *out,
+                      int M, int K, int N, int group, cudaStream_t stream, bool *launched) {
     constexpr int R = kChunkRows;
     constexpr int LPS = MB == 1 ? 2 : 1;
 #define FD_SHAPE(KK, GG)                                                                        \
     if (K == KK && group == GG)                                                                 \
-        return launch_cfg<MB, R, KK / 32, KK / GG, LPS>(di, gate, up, qweight, scales, out, M, K, \
-                                                       N, group, stream, launched);
+        return launch_cfg<MB, R, KK / 32, KK / GG, LPS>(di, gate, up, qweight, scales, residual, \
+                                                       out, M, K, N, group, stream, launched);
     FD_SHAPE(14336, 128)
     FD_SHAPE(9216, 128)
     FD_SHAPE(4096, 128)
     FD_SHAPE(1024, 128)
 #undef FD_SHAPE
-    return launch_cfg<MB, R, 0, 0, LPS>(di, gate, up, qweight, scales, out, M, K, N, group,
-                                        stream, launched);
+    return launch_cfg<MB, R, 0, 0, LPS>(di, gate, up, qweight, scales, residual, out, M, K, N,
+                                        group, stream, launched);
 }
 
 }  // namespace
@@ -528,16 +538,18 @@ bool gemv_tma_supported(int M, int K, int group) {
 }
 
 cudaError_t launch_gemv_tma(const void *gate, const void *up, const void *qweight,
-                            const void *scales, void *out, int M, int K, int N, int group,
-                            cudaStream_t stream, bool *launched) {
+                            const void *scales, const void *residual, void *out, int M, int K,
+                            int N, int group, cudaStream_t stream, bool *launched) {
     *launched = false;
     if (!gemv_tma_supported(M, K, group)) return cudaSuccess;
     DeviceInfo di;
     cudaError_t err = device_info(&di);
     if (err != cudaSuccess) return err;
     if (M == 1)
-        return launch_mb<1>(di, gate, up, qweight, scales, out, M, K, N, group, stream, launched);
-    return launch_mb<2>(di, gate, up, qweight, scales, out, M, K, N, group, stream, launched);
+        return launch_mb<1>(di, gate, up, qweight, scales, residual, out, M, K, N, group, stream,
+                            launched);
+    return launch_mb<2>(di, gate, up, qweight, scales, residual, out, M, K, N, group, stream,
+                        launched);
 }
 
 }  // namespace fd

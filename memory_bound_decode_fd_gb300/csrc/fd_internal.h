@@ -58,18 +58,20 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 // ------------------------------------------------------------------------------------
 // Launchers (host). Arguments are validated by the C-ABI layer before these run.
 // ------------------------------------------------------------------------------------
+// `residual` (bf16 [M, N], may equal `out`, or null) is added to the sum before the single
+// rounding to bf16 (the residual-add epilogue of the down projection).
 cudaError_t launch_gemv_tma(const void *gate, const void *up, const void *qweight,
-                            const void *scales, void *out, int M, int K, int N, int group,
-                            cudaStream_t stream, bool *launched);
+                            const void *scales, const void *residual, void *out, int M, int K,
+                            int N, int group, cudaStream_t stream, bool *launched);
 // Tensor-core path (tcgen05) for batched decode; sets *launched = false when the shape
 // is outside its rules (K % 1024, N % 128, group % 64, (K / group) % 8).
 bool gemv_tc_supported(int M, int K, int N, int group);
 cudaError_t launch_gemv_tc(const void *gate, const void *up, const void *qweight,
-                           const void *scales, void *out, int M, int K, int N, int group,
-                           cudaStream_t stream, bool *launched);
+                           const void *scales, const void *residual, void *out, int M, int K,
+                           int N, int group, cudaStream_t stream, bool *launched);
 cudaError_t launch_gemv_cc(const void *gate, const void *up, const void *qweight,
-                           const void *scales, void *out, int M, int K, int N, int group,
-                           cudaStream_t stream);
+                           const void *scales, const void *residual, void *out, int M, int K,
+                           int N, int group, cudaStream_t stream);
 cudaError_t launch_add_rmsnorm(const void *x, const void *residual, const void *weight,
                                float eps, void *out, void *residual_out, int rows,
                                int hidden, cudaStream_t stream);

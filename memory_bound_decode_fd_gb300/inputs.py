@@ -99,4 +99,6 @@ WORKLOADS = {
     "decode_step": dict(kind="decode", layers=32, hidden=4096, inter=14336, group=128,
                         eps=1e-5, seed=3),
     "batched_m64": dict(kind="batched", M=64, K=14336, N=4096, group=128, eps=1e-5, seed=4),
+    # the decode-step down projection with the residual-add epilogue (new_residual = x + out)
+    "gemv_residual": dict(kind="gemv_residual", M=1, K=14336, N=4096, group=128, seed=3),
 }

@@ -104,6 +104,52 @@ def swiglu_w4a16_gemv(
     return out
 
 
+def swiglu_w4a16_gemv_residual(
+    gate: torch.Tensor,
+    up: torch.Tensor,
+    qweight: torch.Tensor,
+    scales: torch.Tensor,
+    residual: torch.Tensor,
+    out: torch.Tensor | None = None,
+    group: int = 128,
+    stream: torch.cuda.Stream | None = None,
+) -> torch.Tensor:
+    """The GEMV with a residual-add epilogue: out[m, n] = bf16(f32(residual[m, n]) +
+    sum_k silu(gate[m, k]) * up[m, k] * q[n, k] * scales[n, k // group]), one rounding.
+
+    residual: bf16 [M, N] (a 1-D tensor is one row); out may be residual (in place).
+    Other arguments as ``swiglu_w4a16_gemv``.
+    """
+    if gate.dim() == 1:
+        gate = gate.unsqueeze(0)
+        up = up.unsqueeze(0)
+    if residual.dim() == 1:
+        residual = residual.unsqueeze(0)
+    if gate.dim() != 2 or qweight.dim() != 2 or scales.dim() != 2:
+        raise ValueError("gate/up must be [M, K]; qweight [N, K/8]; scales [N, K/group]")
+    M, K = gate.shape
+    N = qweight.shape[0]
+    _check_tensor("gate", gate, torch.bfloat16)
+    _check_tensor("up", up, torch.bfloat16, (M, K))
+    _check_tensor("qweight", qweight, torch.int32, (N, K // 8))
+    if group <= 0 or K % group != 0:
+        raise ValueError(f"K={K} must be a multiple of group={group}")
+    _check_tensor("scales", scales, torch.bfloat16, (N, K // group))
+    _check_tensor("residual", residual, torch.bfloat16, (M, N))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=gate.device)
+    elif out.dim() == 1:
+        out = out.unsqueeze(0)
+    _check_tensor("out", out, torch.bfloat16, (M, N))
+    lib = _lib.load()
+    st = lib.fd_swiglu_w4a16_gemv_residual(
+        _ptr(gate), _ptr(up), _ptr(qweight), _ptr(scales), _ptr(residual), _ptr(out),
+        int(M), int(K), int(N), int(group), _stream_handle(stream),
+    )
+    _lib.check(st)
+    return out
+
+
 def add_rmsnorm(
     x: torch.Tensor,
     residual: torch.Tensor,

@@ -39,6 +39,7 @@ __all__ = [
     "unpack_int4",
     "dequant_w4",
     "swiglu_w4a16_gemv",
+    "swiglu_w4a16_gemv_residual",
     "add_rmsnorm",
     "decode_mlp_step",
     "unfused_product_bytes",
@@ -158,6 +159,32 @@ def swiglu_w4a16_gemv(gate_bits, up_bits, qweight, scale_bits, group: int) -> np
     if a.shape[1] != w.shape[1]:
         raise ValueError("gate/up K does not match the weights")
     return a @ w.T
+
+
+def swiglu_w4a16_gemv_residual(gate_bits, up_bits, qweight, scale_bits, residual_bits,
+                               group: int):
+    """The down projection with a residual-add epilogue: new_residual = x + out.
+
+    [FUSE] "The fusion boundary problem": kernel 3 of a fused layer is GEMM(act, W_down)
+    with a residual-add epilogue writing new_residual = x + out, x being the pre-norm
+    residual stream (the first output of kernel 1, add_rmsnorm). [FUSE] "The taxonomy of
+    fusions", item 3: the elementwise op is applied to the accumulator before the output
+    is written.
+
+    Returns ``(ref, eager_bits)``:
+      * ``ref``        float64 [M, N], f32(residual) + y with y from swiglu_w4a16_gemv,
+                       nothing rounded;
+      * ``eager_bits`` uint16, the unfused chain's two roundings: out = bf16(y) is stored,
+                       then a separate add kernel stores bf16(f32(x) + f32(out)).
+    """
+    y = swiglu_w4a16_gemv(gate_bits, up_bits, qweight, scale_bits, group)
+    r = bf16_to_f32(np.asarray(residual_bits, dtype=np.uint16)).astype(np.float64)
+    r = r.reshape(y.shape)
+    ref = r + y
+    out_bits = f32_to_bf16_rne(y.astype(np.float32))
+    s32 = bf16_to_f32(out_bits) + r.astype(np.float32)  # float32 add, IEEE RNE
+    eager_bits = f32_to_bf16_rne(s32)
+    return ref, eager_bits
 
 
 # --------------------------------------------------------------------------------------

@@ -93,6 +93,15 @@ def gemv_reference(gate, up, qweight, scales, group, rows=None):
     return ref, a @ w.T, enc @ w.T, gu @ w.T
 
 
+def gemv_sum_error(K, abs_sum, enc_err, tanh_err, tensor_cores):
+    """Bound on |fp32 sum of the kernel - float64 sum| before the final bf16 rounding:
+    bf16 operands (tensor cores) or the 16-bit activation encoding (CUDA cores), the
+    tanh form of silu, and fp32 accumulation."""
+    if tensor_cores:
+        return 1.01 * (2.0**-8 * abs_sum + TANH_REL * tanh_err) + (K / 16 + 8) * 2.0**-22 * abs_sum
+    return 1.01 * (64 * 2.0**-24 * abs_sum + 1.05 * enc_err + 1.01 * TANH_REL * tanh_err)
+
+
 def check_gemv(y_bits, gate, up, qweight, scales, group, rows=None, tensor_cores=None) -> dict:
     """Stated bar plus the elementwise bound of the kernel that ran; by default the
     library is asked which one that was (under the current kernel selection)."""
@@ -108,12 +117,7 @@ def check_gemv(y_bits, gate, up, qweight, scales, group, rows=None, tensor_cores
     if rows is not None:
         y = y[:, rows]
     res = stated_bar(y, ref)
-    if tensor_cores:
-        delta = 1.01 * (2.0**-8 * abs_sum + TANH_REL * tanh_err) + (K / 16 + 8) * 2.0**-22 * abs_sum
-        bound = 2.0**-8 * np.abs(ref) + delta
-    else:
-        delta = 64 * 2.0**-24 * abs_sum + 1.05 * enc_err + 1.01 * TANH_REL * tanh_err
-        bound = 2.0**-8 * np.abs(ref) + 1.01 * delta
+    bound = 2.0**-8 * np.abs(ref) + gemv_sum_error(K, abs_sum, enc_err, tanh_err, tensor_cores)
     res["tensor_cores"] = bool(tensor_cores)
     err = np.abs(y - ref)
     bad = err > bound
@@ -122,6 +126,36 @@ def check_gemv(y_bits, gate, up, qweight, scales, group, rows=None, tensor_cores
         f"{float((err - bound).max())}"
     )
     res["n_checked"] = int(y.size)
+    return res
+
+
+def check_gemv_residual(y_bits, gate, up, qweight, scales, residual, group,
+                        tensor_cores=None) -> dict:
+    """The residual-add epilogue: y = bf16(f32(residual) + fp32 sum), one rounding, against
+    the oracle's float64 residual + sum. Same sum error as check_gemv; the final rounding
+    (and the fp32 add) act on |residual + sum|."""
+    M = int(np.prod(np.shape(gate)[:-1])) if np.ndim(gate) > 1 else 1
+    K = np.shape(gate)[-1]
+    N = np.shape(qweight)[0]
+    if tensor_cores is None:
+        import memory_bound_decode_fd_gb300 as fd
+
+        tensor_cores = fd.gemv_uses_tensor_cores(M, K, N, group)
+    ref, eager_bits = oracle.swiglu_w4a16_gemv_residual(gate, up, qweight, scales, residual, group)
+    _, abs_sum, enc_err, tanh_err = gemv_reference(gate, up, qweight, scales, group)
+    y = bf16_f64(y_bits).reshape(ref.shape)
+    res = stated_bar(y, ref)
+    bound = 2.0**-8 * np.abs(ref) + gemv_sum_error(K, abs_sum, enc_err, tanh_err, tensor_cores)
+    err = np.abs(y - ref)
+    bad = err > bound
+    assert not bad.any(), (
+        f"{int(bad.sum())} outputs outside the derived bound; worst excess "
+        f"{float((err - bound).max())}"
+    )
+    res["tensor_cores"] = bool(tensor_cores)
+    res["n_checked"] = int(y.size)
+    # how often the unfused chain's two roundings are farther from the unrounded value
+    res["eager_farther"] = float(np.mean(np.abs(bf16_f64(eager_bits).reshape(ref.shape) - ref) > err))
     return res
 
 

@@ -24,7 +24,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("fd_swiglu_w4a16_gemv", "fd_add_rmsnorm", "fd_status_string", "fd_w4_dequant_debug"):
+    for n in ("fd_swiglu_w4a16_gemv", "fd_swiglu_w4a16_gemv_residual", "fd_add_rmsnorm",
+              "fd_status_string", "fd_w4_dequant_debug"):
         assert n in names
 
 
@@ -90,6 +91,31 @@ def gemv(lib, gate=A, up=B, qw=C, sc=D, out=E, M=1, K=1024, N=256, group=128):
 ])
 def test_gemv_rejects_bad_arguments_without_launching(fdlib, kw, status):
     assert gemv(fdlib, **kw) == status
+
+
+F = 0x60000000
+
+
+def gemv_res(lib, gate=A, up=B, qw=C, sc=D, res=F, out=E, M=1, K=1024, N=256, group=128):
+    return lib.fd_swiglu_w4a16_gemv_residual(gate, up, qw, sc, res, out, M, K, N, group, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(res=None), _lib.FD_ERR_NULL),
+    (dict(gate=None), _lib.FD_ERR_NULL),
+    (dict(M=0), _lib.FD_ERR_SHAPE),
+    (dict(K=1000), _lib.FD_ERR_SHAPE),
+    (dict(M=257), _lib.FD_ERR_UNSUPPORTED),
+    (dict(res=F + 2), _lib.FD_ERR_ALIGN),
+    (dict(res=E + 16), _lib.FD_ERR_OVERLAP),   # partial overlap with out (== out is allowed)
+    (dict(res=A), _lib.FD_ERR_OVERLAP),        # residual over gate
+    (dict(res=B + 64), _lib.FD_ERR_OVERLAP),   # residual inside up
+    (dict(res=C + 32), _lib.FD_ERR_OVERLAP),   # residual inside qweight
+    (dict(res=D), _lib.FD_ERR_OVERLAP),        # residual over scales
+    (dict(out=A), _lib.FD_ERR_OVERLAP),        # out over gate
+])
+def test_gemv_residual_rejects_bad_arguments_without_launching(fdlib, kw, status):
+    assert gemv_res(fdlib, **kw) == status
 
 
 def rms(lib, x=A, r=B, w=C, eps=1e-6, out=D, rout=E, rows=4, hidden=4096):

@@ -242,6 +242,52 @@ def test_gemv_matches_torch_linear_fp64():
 
 # ------------------------------------------------------------------------------ RMSNorm
 
+def test_gemv_residual_zero_weights_pass_residual_through():
+    # q = 0: the epilogue adds exactly nothing, so the new residual is the residual.
+    rng = np.random.default_rng(40)
+    M, K, N, group = 2, 256, 7, 128
+    g = inputs.normal_bf16(rng, (M, K))
+    u = inputs.normal_bf16(rng, (M, K))
+    r = inputs.normal_bf16(rng, (M, N))
+    q = np.zeros((N, K), np.int8)
+    s = inputs.scales_bf16(rng, N, K, group)
+    ref, eager = oracle.swiglu_w4a16_gemv_residual(g, u, pack_int4(q), s, r, group)
+    assert np.array_equal(ref, oracle.bf16_to_f32(r).astype(np.float64))
+    assert np.array_equal(eager, r)
+
+
+def test_gemv_residual_one_hot_published_sigmoid():
+    # gate = 1, up = 2 everywhere; one weight q = 5 with scale 0.25 at (n*, k*): the new
+    # residual is r + 2 * silu(1) * 5 * 0.25 at n* (sigma(1) = 0.7310585786300049, the
+    # tabulated logistic value) and exactly r elsewhere.
+    M, K, N, group = 1, 128, 4, 64
+    g = inputs.to_bf16_bits(np.ones((M, K)))
+    u = inputs.to_bf16_bits(np.full((M, K), 2.0))
+    r = inputs.to_bf16_bits(np.array([[0.5, -1.25, 3.0, 0.0]]))
+    q = np.zeros((N, K), np.int8)
+    q[2, 77] = 5
+    s = inputs.to_bf16_bits(np.full((N, K // group), 0.25))
+    ref, eager = oracle.swiglu_w4a16_gemv_residual(g, u, pack_int4(q), s, r, group)
+    expect = np.array([[0.5, -1.25, 3.0 + 2 * 0.7310585786300049 * 5 * 0.25, 0.0]])
+    np.testing.assert_allclose(ref, expect, rtol=1e-15, atol=0)
+    # the unfused chain rounds y = 1.8276... to bf16 (1.828125) before the add
+    assert oracle.bf16_to_f32(eager)[0, 2] == np.float32(4.8125)
+    assert np.array_equal(eager[:, [0, 1, 3]], r[:, [0, 1, 3]])
+
+
+def test_gemv_residual_shift_by_residual_is_exact():
+    # Two residuals that differ by exactly representable amounts shift ref by exactly
+    # that difference (the epilogue is an add, nothing else).
+    rng = np.random.default_rng(41)
+    M, K, N, group = 3, 256, 5, 128
+    d = inputs.gemv_inputs(M, K, N, group, rng=rng)
+    r1 = inputs.to_bf16_bits(np.full((M, N), 1.0))
+    r2 = inputs.to_bf16_bits(np.full((M, N), -2.0))
+    a1, _ = oracle.swiglu_w4a16_gemv_residual(d["gate"], d["up"], d["qweight"], d["scales"], r1, group)
+    a2, _ = oracle.swiglu_w4a16_gemv_residual(d["gate"], d["up"], d["qweight"], d["scales"], r2, group)
+    np.testing.assert_allclose(a1 - a2, 3.0, rtol=0, atol=1e-12)
+
+
 def test_add_rmsnorm_residual_matches_torch_bit_exact():
     d = inputs.rmsnorm_inputs(64, 1024, seed=20)
     h, _, _ = oracle.add_rmsnorm(d["x"], d["residual"], d["weight"], 1e-6)
