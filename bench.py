@@ -19,7 +19,7 @@ Reported:
   --impl reference  times the CPU oracle alone (the reference arm of this benchmark)
 
 Other workloads (--workload gemv_94mb | rmsnorm_big | gemv_small | batched_m64 |
-gemv_residual) time one call per step and rotate ceil(3 x L2 / bytes) input sets so every step reads HBM.
+gemv_residual | gate_up) time one call per step and rotate ceil(3 x L2 / bytes) input sets so every step reads HBM.
 """
 
 from __future__ import annotations
@@ -429,6 +429,21 @@ def bench_single(args, device, rank, world):
             for q, s in zip(qs, ss):
                 calls.append(lambda q=q, s=s: fd.swiglu_w4a16_gemv(gate, up, q, s, out=out, group=g))
             kname, desc = "swiglu_w4a16_gemv", f"GEMV M={M} K={K} N={N} group {g}, seed {spec['seed']}"
+    elif kind == "gate_up":
+        M, K, inter, g = spec["M"], spec["K"], spec["I"], spec["group"]
+        # stacked int4 weights [2I, K] and scales, x once, g and u written
+        nbytes = fd.gate_up_bytes(M, K, inter, g)
+        nsets = max(1, min(4096, math.ceil(3 * l2 / nbytes)))
+        rng = np.random.default_rng(spec["seed"])
+        x = to_dev(inputs.normal_bf16(rng, (M, K)), device)
+        gout = torch.empty((M, inter), dtype=torch.bfloat16, device=device)
+        uout = torch.empty_like(gout)
+        for _ in range(nsets):
+            q = to_dev(inputs.int4_words(rng, 2 * inter, K), device)
+            s = to_dev(inputs.scales_bf16(rng, 2 * inter, K, g), device)
+            calls.append(lambda q=q, s=s: fd.w4a16_gate_up_gemv(x, q, s, gate_out=gout, up_out=uout, group=g))
+        kname = "w4a16_gate_up_gemv"
+        desc = f"gate/up GEMV (horizontal fusion) M={M} K={K} I={inter} (2I={2 * inter} rows) group {g}, seed {spec['seed']}"
     else:
         rows, hidden = spec["rows"], spec["hidden"]
         nbytes = fd.add_rmsnorm_bytes(rows, hidden)
@@ -504,7 +519,7 @@ def bench_single(args, device, rank, world):
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
         "steps": n_calls, "warmup": args.warmup, "ms_per_step": round(us_call / 1e3, 6),
         "us_per_call": round(us_call, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16 (int4 weights, fp32 accumulation)" if kname.startswith("swiglu") else "bf16 (fp32 reduction)",
+        "vs_baseline": None, "dtype": "bf16 (int4 weights, fp32 accumulation)" if "gemv" in kname else "bf16 (fp32 reduction)",
         "data": "synthetic (seeded)",
         "config": {"workload": f"{args.workload}: {desc}", "bytes_per_call": nbytes,
                    "l2": f"{len(calls)} rotating input sets ({len(calls)} x {nbytes} B vs L2 {l2} B)",
@@ -556,7 +571,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--workload", default="decode_step",
                     choices=["decode_step", "gemv_94mb", "rmsnorm_big", "gemv_small", "batched_m64",
-                             "gemv_residual"])
+                             "gemv_residual", "gate_up"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
 

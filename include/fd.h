@@ -12,6 +12,9 @@
  *   fd_swiglu_w4a16_gemv_residual
  *                          the same GEMV with a residual-add epilogue: out = residual + y
  *                          (the down projection of a fused layer writes the new residual).
+ *   fd_w4a16_gate_up_gemv  the horizontally fused gate and up projections of the MLP, one
+ *                          W4A16 GEMV over both weight matrices ("horizontal fusion"):
+ *                          one read of x, g and u written for the down projection.
  *
  * Sources (web pages, cited by title and section):
  *   [FIX]  "PyTorch Community Proposes Fusion Fix as Large Intermediate Buffers May Slow
@@ -20,7 +23,8 @@
  *          weights with a SwiGLU pre-operation).
  *   [FUSE] "09 - Operator fusion" - section 5, "The taxonomy of fusions" (items 2 and 4:
  *          reduction + elementwise; GEMM prologue dequantisation for W4A16; item 3: GEMM
- *          epilogue fusion) and "The fusion boundary problem" (add_rmsnorm with two
+ *          epilogue fusion; item 5: horizontal fusion, gate_proj and up_proj as one
+ *          gate_up_proj) and "The fusion boundary problem" (add_rmsnorm with two
  *          outputs; act @ W_down; kernel 3: the down projection with a residual-add
  *          epilogue that writes new_residual = x + out).
  *   [KFM]  "Kernel Fusion, torch.compile and CUDA Graphs, Measured" - "Step 1" (silu(g) *
@@ -106,6 +110,32 @@ int fd_swiglu_w4a16_gemv(const void *gate, const void *up, const void *qweight,
 int fd_swiglu_w4a16_gemv_residual(const void *gate, const void *up, const void *qweight,
                                   const void *scales, const void *residual, void *out, int M,
                                   int K, int N, int group, fd_stream_t stream);
+
+/*
+ * fd_w4a16_gate_up_gemv - the gate and up projections of the MLP as one W4A16 GEMV
+ * ([FUSE] item 5, horizontal fusion: gate_proj and up_proj become one gate_up_proj;
+ * "The fusion boundary problem": gate, up = h @ W_gate_up):
+ *
+ *   W[n, k]          = q[n, k] * scales[n, k / group],   n < 2I (rows 0..I-1: gate,
+ *                                                         rows I..2I-1: up)
+ *   gate_out[m, j]   = bf16( sum_k x[m, k] * W[j, k] )
+ *   up_out[m, j]     = bf16( sum_k x[m, k] * W[I + j, k] )   (fp32 accumulation)
+ *
+ * x          bf16 [M, K] row-major (the normalised row, out of fd_add_rmsnorm).
+ * qweight    int32 [2I, K/8], the gate projection's I rows followed by the up
+ *            projection's I rows, each in the nibble layout of fd_swiglu_w4a16_gemv.
+ * scales     bf16 [2I, K/group].
+ * gate_out, up_out  bf16 [M, I] row-major; they may not overlap each other or an input.
+ * Requires   1 <= M <= FD_MAX_M, 32 <= K <= FD_MAX_K, I >= 1, K % 32 == 0,
+ *            group % 32 == 0, K % group == 0.
+ * gate_out and up_out are the gate and up inputs of fd_swiglu_w4a16_gemv(_residual): the
+ * two calls are the whole MLP, and silu(g) * u exists only in the second kernel's
+ * registers. x is encoded per 32-k slice like the SwiGLU activation (block-scaled int16).
+ * No tensor-core kernel: every M runs on the CUDA-core kernels.
+ */
+int fd_w4a16_gate_up_gemv(const void *x, const void *qweight, const void *scales,
+                          void *gate_out, void *up_out, int M, int K, int I, int group,
+                          fd_stream_t stream);
 
 /*
  * fd_add_rmsnorm - fused residual add + RMSNorm, one pass over HBM.     [KFM Step 2]

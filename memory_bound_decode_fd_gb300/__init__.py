@@ -3,6 +3,8 @@
 * ``swiglu_w4a16_gemv``: y = (silu(g) * u) . dequant(W_int4)^T, one kernel, int4 in HBM only.
 * ``swiglu_w4a16_gemv_residual``: the same GEMV with a residual-add epilogue (out =
   residual + y, the new residual stream written by the down projection).
+* ``w4a16_gate_up_gemv``: the gate and up projections as one W4A16 GEMV (horizontal
+  fusion), writing the g and u that ``swiglu_w4a16_gemv`` consumes.
 * ``add_rmsnorm``: residual add + RMSNorm, one pass, two outputs.
 * ``decode_mlp_step``: L layers of the two, in stream order.
 
@@ -38,8 +40,9 @@ from .kernels import (  # noqa: F401
     swiglu_w4a16_gemv,
     swiglu_w4a16_gemv_residual,
     w4_dequant_debug,
+    w4a16_gate_up_gemv,
 )
 from .packing import pack_int4  # noqa: F401
-from .traffic import add_rmsnorm_bytes, decode_step_bytes, gemv_bytes, gemv_flops  # noqa: F401
+from .traffic import add_rmsnorm_bytes, decode_step_bytes, gate_up_bytes, gemv_bytes, gemv_flops  # noqa: F401
 
 __version__ = "1.0.0"

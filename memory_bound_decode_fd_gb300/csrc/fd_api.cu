@@ -111,14 +111,14 @@ int swiglu_gemv(const void *gate, const void *up, const void *qweight, const voi
                                          group, st_, &launched);
         if (err != cudaSuccess || launched) return from_cuda(err);
     }
+    const GemvOut o{out, nullptr, N, N};
     if (path == FD_GEMV_AUTO || path == FD_GEMV_BULK) {
         bool launched = false;
-        cudaError_t err = launch_gemv_tma(gate, up, qweight, scales, residual, out, M, K, N,
+        cudaError_t err = launch_gemv_tma(gate, up, qweight, scales, residual, o, M, K, N,
                                           group, st_, &launched);
         if (err != cudaSuccess || launched) return from_cuda(err);
     }
-    return from_cuda(
-        launch_gemv_cc(gate, up, qweight, scales, residual, out, M, K, N, group, st_));
+    return from_cuda(launch_gemv_cc(gate, up, qweight, scales, residual, o, M, K, N, group, st_));
 }
 
 }  // namespace
@@ -137,6 +137,40 @@ int fd_swiglu_w4a16_gemv_residual(const void *gate, const void *up, const void *
                                   int K, int N, int group, fd_stream_t stream) {
     if (!residual) return FD_ERR_NULL;
     return swiglu_gemv(gate, up, qweight, scales, residual, out, M, K, N, group, stream);
+}
+
+int fd_w4a16_gate_up_gemv(const void *x, const void *qweight, const void *scales,
+                          void *gate_out, void *up_out, int M, int K, int I, int group,
+                          fd_stream_t stream) {
+    if (!x || !gate_out || !up_out) return FD_ERR_NULL;
+    if (I <= 0) return FD_ERR_SHAPE;
+    if (I > (INT32_MAX - 1) / 2) return FD_ERR_UNSUPPORTED;
+    const int N = 2 * I;  // gate rows, then up rows
+    int st = check_w4_layout(qweight, scales, K, N, group);
+    if (st != FD_OK) return st;
+    if (M <= 0) return FD_ERR_SHAPE;
+    if (M > FD_MAX_M) return FD_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(gate_out) || !aligned16(up_out)) return FD_ERR_ALIGN;
+    const size_t x_bytes = (size_t)M * K * 2;
+    const size_t o_bytes = (size_t)M * I * 2;
+    const size_t w_bytes = (size_t)N * K / 2;
+    const size_t s_bytes = (size_t)N * (K / group) * 2;
+    for (const void *o : {static_cast<const void *>(gate_out), static_cast<const void *>(up_out)}) {
+        if (overlaps(o, o_bytes, x, x_bytes) || overlaps(o, o_bytes, qweight, w_bytes) ||
+            overlaps(o, o_bytes, scales, s_bytes))
+            return FD_ERR_OVERLAP;
+    }
+    if (overlaps(gate_out, o_bytes, up_out, o_bytes)) return FD_ERR_OVERLAP;
+    cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+    const GemvOut o{gate_out, up_out, I, I};
+    const int path = g_gemv_path.load(std::memory_order_relaxed);
+    if (path != FD_GEMV_CUDA_CORE) {  // the bulk-copy kernel where its layout rules hold
+        bool launched = false;
+        cudaError_t err = launch_gemv_tma(x, nullptr, qweight, scales, nullptr, o, M, K, N,
+                                          group, st_, &launched);
+        if (err != cudaSuccess || launched) return from_cuda(err);
+    }
+    return from_cuda(launch_gemv_cc(x, nullptr, qweight, scales, nullptr, o, M, K, N, group, st_));
 }
 
 int fd_gemv_uses_tensor_cores(int M, int K, int N, int group) {

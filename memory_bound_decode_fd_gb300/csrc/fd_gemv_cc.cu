@@ -71,8 +71,8 @@ template <int VPT, int MB, int R, int S>
 __global__ void __launch_bounds__(512, 1)
     gemv_cc_kernel(const uint16_t *__restrict__ gate, const uint16_t *__restrict__ up,
                    const uint4 *__restrict__ qweight, const uint16_t *__restrict__ scales,
-                   const uint16_t *residual, uint16_t *out, int M, int K, int N, int group,
-                   int rows_base,
+                   const uint16_t *residual, uint16_t *out, uint16_t *out2, int split, int ldo,
+                   int M, int K, int N, int group, int rows_base,
                    int rows_extra, int weights_evict_first) {
     static_assert(R * MB <= 32 && (R * MB & (R * MB - 1)) == 0, "R*MB: power of 2, <= 32");
     static_assert(kWindowRows % R == 0, "window must hold whole chunks");
@@ -159,11 +159,16 @@ __global__ void __launch_bounds__(512, 1)
             for (int mb = 0; mb < MB; ++mb) {
 #pragma unroll
                 for (int v = 0; v < VPT; ++v) {
-                    if (active[v] && m0 + mb < M)
-                        load_activation_q16(gate, up, (size_t)(m0 + mb) * K + (size_t)pos[v] * 32,
-                                            act[v][mb]);
-                    else
+                    const size_t off = (size_t)(m0 + mb) * K + (size_t)pos[v] * 32;
+                    if (!(active[v] && m0 + mb < M)) {
                         zero_activation(act[v][mb]);
+                    } else if (up) {
+                        load_activation_q16(gate, up, off, act[v][mb]);
+                    } else {  // a plain activation (no SwiGLU): gate holds x
+                        const uint4 *x4 = reinterpret_cast<const uint4 *>(gate + off);
+                        const uint4 x[4] = {x4[0], x4[1], x4[2], x4[3]};
+                        encode_plain(x, act[v][mb]);
+                    }
                 }
             }
         }
@@ -210,10 +215,10 @@ __global__ void __launch_bounds__(512, 1)
                 float acc =
                     sum_partials(red + (size_t)row * MB + mb, nwarps, kWindowRows * MB);
                 if (m0 + mb < M) {
-                    const size_t o = (size_t)(m0 + mb) * N + n_begin + window_base + row;
-                    if (residual) acc += bf16lo(residual[o]);
+                    const int n = n_begin + window_base + row;
+                    if (residual) acc += bf16lo(residual[(size_t)(m0 + mb) * N + n]);
                     __nv_bfloat16 y = __float2bfloat16_rn(acc);
-                    out[o] = *reinterpret_cast<uint16_t *>(&y);
+                    *out_at(out, out2, split, ldo, m0 + mb, n) = *reinterpret_cast<uint16_t *>(&y);
                 }
             }
             __syncthreads();
@@ -263,7 +268,7 @@ cudaError_t ensure_smem_attr(Kern kern, size_t smem, std::atomic<uint64_t> &done
 template <int VPT, int MB, int R, int S>
 cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
                        const void *qweight, const void *scales, const void *residual,
-                       void *out, int M, int K, int N, int group, cudaStream_t stream) {
+                       GemvOut o, int M, int K, int N, int group, cudaStream_t stream) {
     static std::atomic<uint64_t> attr_done{0};
     const int T = threads_for(K, VPT);
     const size_t smem = gemv_smem_bytes<VPT, MB, R, S>(T);
@@ -281,8 +286,9 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
                         static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up),
                         static_cast<const uint4 *>(qweight),
                         static_cast<const uint16_t *>(scales),
-                        static_cast<const uint16_t *>(residual), static_cast<uint16_t *>(out),
-                        M, K, N, group, rows_base, rows_extra, evict_first);
+                        static_cast<const uint16_t *>(residual), static_cast<uint16_t *>(o.out),
+                        static_cast<uint16_t *>(o.out2), o.split, o.ldo, M, K, N, group,
+                        rows_base, rows_extra, evict_first);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
@@ -293,7 +299,7 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
 // or the M > 1 kernel (MB = 2), with one (K <= 16384) or two (K <= 32768) weight vector
 // positions per thread.
 cudaError_t launch_gemv_cc(const void *gate, const void *up, const void *qweight,
-                           const void *scales, const void *residual, void *out, int M, int K,
+                           const void *scales, const void *residual, GemvOut o, int M, int K,
                            int N, int group, cudaStream_t stream) {
     DeviceInfo di;
     cudaError_t err = device_info(&di);
@@ -301,7 +307,7 @@ cudaError_t launch_gemv_cc(const void *gate, const void *up, const void *qweight
     const size_t limit = (size_t)di.max_smem_optin;
 #define FD_TRY(VPT, MB, R, S)                                                              \
     if (gemv_smem_bytes<VPT, MB, R, S>(threads_for(K, VPT)) <= limit)                      \
-        return launch_cfg<VPT, MB, R, S>(di, gate, up, qweight, scales, residual, out, M, K, N, \
+        return launch_cfg<VPT, MB, R, S>(di, gate, up, qweight, scales, residual, o, M, K, N, \
                                          group, stream);
     const bool wide = K / 32 > 512;  // more than 512 vector positions: two per thread
     if (!wide && M == 1) {

@@ -23,6 +23,14 @@ namespace fd {
 
 constexpr int kWindowRows = 64;  // rows whose per-warp partials are held before a flush
 
+// Address of output (m, n): rows n < split go to out (row stride ldo); rows n >= split go
+// to out2 at column n - split (the gate and up halves of a horizontal gate/up projection).
+// A plain GEMV has split = ldo = N.
+__device__ __forceinline__ uint16_t *out_at(uint16_t *out, uint16_t *out2, int split, int ldo,
+                                            int m, int n) {
+    return n < split ? out + (size_t)m * ldo + n : out2 + (size_t)m * ldo + (n - split);
+}
+
 // Sum of the n per-warp partials of one output (p[w * stride], w < n) in four
 // independent chains, so the loads overlap: a single chain waits on each load in turn,
 // which made the final flush of a CTA's outputs ~0.3 us long at 28 warps.
@@ -85,7 +93,9 @@ __device__ __forceinline__ float tanh_approx(float x) {
     return y;
 }
 
-// Encodes one slice (see Act16).
+__device__ __forceinline__ void encode_floats(const float2 (&a)[16], Act16 &act);
+
+// Encodes one slice of a = silu(g) * u (see Act16).
 __device__ __forceinline__ void encode_q16(const GateUp &gu, Act16 &act) {
     // silu(g) u = (g u / 2)(1 + tanh(g / 2)), two elements per packed instruction;
     // a[4i + j] holds elements 8i + 2j and 8i + 2j + 1
@@ -102,6 +112,23 @@ __device__ __forceinline__ void encode_q16(const GateUp &gu, Act16 &act) {
             a[4 * i + j] = __ffma2_rn(p, make_float2(tanh_approx(h.x), tanh_approx(h.y)), p);
         }
     }
+    encode_floats(a, act);
+}
+
+// Encodes one slice of a plain bf16 activation x (32 elements, four 16-byte words).
+__device__ __forceinline__ void encode_plain(const uint4 (&x)[4], Act16 &act) {
+    float2 a[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a[4 * i + j] = make_float2(bf16lo(w[j]), bf16hi(w[j]));
+    }
+    encode_floats(a, act);
+}
+
+// The block-scaled int16 encoding of a slice's 32 fp32 values (see Act16).
+__device__ __forceinline__ void encode_floats(const float2 (&a)[16], Act16 &act) {
     float amax = 0.f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fmaxf(fabsf(a[k].x), fabsf(a[k].y)));
@@ -143,6 +170,8 @@ struct GateUpHalf {
     uint4 g[2], u[2];
 };
 
+__device__ __forceinline__ void encode_floats_pair(const float2 (&a)[8], int h, Act16 &act);
+
 __device__ __forceinline__ void encode_q16_pair(const GateUpHalf &gu, int h, Act16 &act) {
     float2 a[8];  // a[4i + j] holds elements 8i + 2j, 8i + 2j + 1 of this half
     const float2 half2 = make_float2(0.5f, 0.5f);
@@ -157,6 +186,24 @@ __device__ __forceinline__ void encode_q16_pair(const GateUpHalf &gu, int h, Act
             a[4 * i + j] = __ffma2_rn(p, make_float2(tanh_approx(hh.x), tanh_approx(hh.y)), p);
         }
     }
+    encode_floats_pair(a, h, act);
+}
+
+// Paired-lane form of encode_plain: this lane holds elements 16h .. 16h + 15 of the slice
+// (two 16-byte words of a plain bf16 activation).
+__device__ __forceinline__ void encode_plain_pair(const uint4 (&x)[2], int h, Act16 &act) {
+    float2 a[8];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a[4 * i + j] = make_float2(bf16lo(w[j]), bf16hi(w[j]));
+    }
+    encode_floats_pair(a, h, act);
+}
+
+// The pair's block-scaled int16 encoding of its 32 fp32 values (16 per lane).
+__device__ __forceinline__ void encode_floats_pair(const float2 (&a)[8], int h, Act16 &act) {
     float amax = 0.f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fmaxf(fabsf(a[k].x), fabsf(a[k].y)));

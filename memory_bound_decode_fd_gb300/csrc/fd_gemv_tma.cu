@@ -55,13 +55,13 @@ constexpr int kChunkRows = 8;  // rows per bulk-copy chunk
 // behind it (loaded from global memory instead, they arrived behind the weights and the
 // call took 10-25 % longer on GB300); stages from act_first_stage on are filled only
 // after every consumer warp has read its slice.
-template <int MB, int R, int NVEC_C, int NG_C, int LPS>
+template <int MB, int R, int NVEC_C, int NG_C, int LPS, bool PLAIN>
 __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
     gemv_tma_kernel(const uint16_t *__restrict__ gate, const uint16_t *__restrict__ up,
                     const unsigned char *__restrict__ qweight,
                     const uint16_t *__restrict__ scales, const uint16_t *residual,
-                    uint16_t *out, int M, int K, int N, int group, int rows_base,
-                    int rows_extra, int S,
+                    uint16_t *out, uint16_t *out2, int split, int ldo, int M, int K, int N,
+                    int group, int rows_base, int rows_extra, int S,
                     int w_rows, int act_first_stage, int weights_evict_first) {
     static_assert(R * MB <= 32 && (R * MB & (R * MB - 1)) == 0, "R*MB: power of 2, <= 32");
     static_assert(LPS == 1 || (LPS == 2 && MB == 1 && R % 2 == 0), "paired lanes: M = 1 only");
@@ -86,11 +86,13 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
     const uint32_t s_stage_bytes = (uint32_t)R * s_row_bytes;
     unsigned char *s_region = smem + (size_t)w_rows * w_row_bytes;
     float *red = reinterpret_cast<float *>(s_region + (size_t)S * s_stage_bytes);
-    // gate then up, each K bf16 (4K bytes = 8 weight rows), in the last 8 weight rows
-    // (M == 1 only); stages from act_first_stage on are filled only after its release
+    // gate then up, each K bf16 (4K bytes = 8 weight rows; PLAIN: x alone, 2K bytes = 4
+    // rows), in the last weight rows (M == 1 only); stages from act_first_stage on are
+    // filled only after its release
     const bool act_in_smem = (M == 1);
+    const uint32_t act_bytes = (uint32_t)K * (PLAIN ? 2 : 4);
     uint16_t *act_smem =
-        reinterpret_cast<uint16_t *>(smem + (size_t)w_rows * w_row_bytes - (size_t)K * 4);
+        reinterpret_cast<uint16_t *>(smem + (size_t)w_rows * w_row_bytes - act_bytes);
 
     const int b = blockIdx.x;
     const int n_begin = b * rows_base + min(b, rows_extra);
@@ -145,10 +147,10 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
         grid_dep_launch();
         if (act_in_smem) {
             const uint32_t ab = (uint32_t)K * 2;
-            mbar_arrive_expect_tx(&act_full_bar, 2 * ab);
+            mbar_arrive_expect_tx(&act_full_bar, act_bytes);
             const uint64_t pol_a = policy_evict_last();  // every CTA reads it
             bulk_g2s(act_smem, gate, ab, &act_full_bar, pol_a);
-            bulk_g2s(act_smem + K, up, ab, &act_full_bar, pol_a);
+            if (!PLAIN) bulk_g2s(act_smem + K, up, ab, &act_full_bar, pol_a);
         }
         // stages that are free from the start: no waits
         for (; pc < total && pc < act_first_stage; ++pc) issue_chunk(pc);
@@ -201,22 +203,29 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                 act_ok = mbar_wait_bounded(&act_full_bar, 0, &abort_flag);
                 if (act_ok) {
                     const uint4 *g4 = reinterpret_cast<const uint4 *>(act_smem + slice * 32 + 16 * hh);
-                    const uint4 *u4 = reinterpret_cast<const uint4 *>(act_smem + K + slice * 32 + 16 * hh);
                     gu.g[0] = g4[0];
                     gu.g[1] = g4[1];
-                    gu.u[0] = u4[0];
-                    gu.u[1] = u4[1];
+                    if (!PLAIN) {
+                        const uint4 *u4 = reinterpret_cast<const uint4 *>(act_smem + K + slice * 32 + 16 * hh);
+                        gu.u[0] = u4[0];
+                        gu.u[1] = u4[1];
+                    }
                 }
             } else {
                 const uint4 *g4 = reinterpret_cast<const uint4 *>(gate + slice * 32 + 16 * hh);
-                const uint4 *u4 = reinterpret_cast<const uint4 *>(up + slice * 32 + 16 * hh);
                 gu.g[0] = g4[0];
                 gu.g[1] = g4[1];
-                gu.u[0] = u4[0];
-                gu.u[1] = u4[1];
+                if (!PLAIN) {
+                    const uint4 *u4 = reinterpret_cast<const uint4 *>(up + slice * 32 + 16 * hh);
+                    gu.u[0] = u4[0];
+                    gu.u[1] = u4[1];
+                }
             }
             if (!act_ok) gu.g[0] = gu.g[1] = gu.u[0] = gu.u[1] = make_uint4(0, 0, 0, 0);
-            encode_q16_pair(gu, hh, act);
+            if constexpr (PLAIN)
+                encode_plain_pair(gu.g, hh, act);
+            else
+                encode_q16_pair(gu, hh, act);
             // When weight chunks overlay the area, it is released after the encode (released
             // before it, the encode ran ~0.4 us longer at K=14336 and the call gained
             // nothing, the weight stream being the bound), with a proxy fence: the
@@ -280,11 +289,17 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                 named_bar_sync(1, ncons);
                 const int rows_in_window = min(rows_done, n_cnt) - window_base;
                 for (int i = tid; i < rows_in_window; i += ncons) {
-                    const size_t n = (size_t)n_begin + window_base + i;
+                    const int n = n_begin + window_base + i;
                     float acc = sum_partials(red + i, ncw, kWindowRows);
                     if (residual) acc += window_base == 0 ? res0 : bf16lo(residual[n]);
                     __nv_bfloat16 y = __float2bfloat16_rn(acc);
-                    out[n] = *reinterpret_cast<uint16_t *>(&y);
+                    // The split output (gate/up halves) only where it is used: in the SwiGLU
+                    // kernel the extra select changed the register allocation of the row
+                    // loop and cost 2.8 % per call at K=14336 on GB300.
+                    if constexpr (PLAIN)
+                        *out_at(out, out2, split, ldo, 0, n) = *reinterpret_cast<uint16_t *>(&y);
+                    else
+                        out[n] = *reinterpret_cast<uint16_t *>(&y);
                 }
                 named_bar_sync(1, ncons);
                 window_base = last_chunk ? 0 : rows_done;
@@ -321,7 +336,7 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
                                     gu.g[i] = g4[i];
-                                    gu.u[i] = u4[i];
+                                    if (!PLAIN) gu.u[i] = u4[i];
                                 }
                             } else {
 #pragma unroll
@@ -329,15 +344,26 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                             }
                             // The area is released after the encode (when chunks overlay
                             // it), with a proxy fence: the next bulk copy writes it.
-                            encode_q16(gu, act[mb]);
+                            if constexpr (PLAIN)
+                                encode_plain(gu.g, act[mb]);
+                            else
+                                encode_q16(gu, act[mb]);
                             if (act_first_stage < total) {
                                 fence_proxy_async_smem();
                                 __syncwarp();
                                 if (lane == 0) mbar_arrive(&act_free_bar);
                             }
                         } else {
-                            load_gate_up(gate, up, (size_t)(m0 + mb) * K + (size_t)tid * 32, gu);
-                            encode_q16(gu, act[mb]);
+                            const size_t off = (size_t)(m0 + mb) * K + (size_t)tid * 32;
+                            if constexpr (PLAIN) {
+                                const uint4 *x4 = reinterpret_cast<const uint4 *>(gate + off);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) gu.g[i] = x4[i];
+                                encode_plain(gu.g, act[mb]);
+                            } else {
+                                load_gate_up(gate, up, off, gu);
+                                encode_q16(gu, act[mb]);
+                            }
                         }
                     } else {
                         zero_activation(act[mb]);
@@ -398,10 +424,13 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                     const int row = i / MB, mb = i % MB;
                     float acc = sum_partials(red + (size_t)row * MB + mb, ncw, kWindowRows * MB);
                     if (m0 + mb < M) {
-                        const size_t o = (size_t)(m0 + mb) * N + n_begin + window_base + row;
-                        if (residual) acc += bf16lo(residual[o]);
+                        const int n = n_begin + window_base + row;
+                        if (residual) acc += bf16lo(residual[(size_t)(m0 + mb) * N + n]);
                         __nv_bfloat16 y = __float2bfloat16_rn(acc);
-                        out[o] = *reinterpret_cast<uint16_t *>(&y);
+                        if constexpr (PLAIN)
+                            *out_at(out, out2, split, ldo, m0 + mb, n) = *reinterpret_cast<uint16_t *>(&y);
+                        else
+                            out[(size_t)(m0 + mb) * N + n] = *reinterpret_cast<uint16_t *>(&y);
                     }
                 }
                 named_bar_sync(1, ncons);
@@ -417,19 +446,22 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
         // A wait gave up: make the failure visible in every output this CTA owns.
         for (int i = tid; i < n_cnt * M; i += blockDim.x) {
             const int m = i / n_cnt, r = i % n_cnt;
-            out[(size_t)m * N + n_begin + r] = 0x7FC0;  // bf16 quiet NaN
+            if constexpr (PLAIN)
+                *out_at(out, out2, split, ldo, m, n_begin + r) = 0x7FC0;  // bf16 quiet NaN
+            else
+                out[(size_t)m * N + n_begin + r] = 0x7FC0;
         }
     }
 }
 
-template <int MB, int R, int NVEC_C, int NG_C, int LPS>
+template <int MB, int R, int NVEC_C, int NG_C, int LPS, bool PLAIN>
 cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
                        const void *qweight, const void *scales, const void *residual,
-                       void *out, int M, int K, int N, int group, cudaStream_t stream,
+                       GemvOut o, int M, int K, int N, int group, cudaStream_t stream,
                        bool *launched) {
     static std::atomic<uint64_t> attr_done{0};
     static std::atomic<int> static_smem_cache{-1};
-    auto kern = gemv_tma_kernel<MB, R, NVEC_C, NG_C, LPS>;
+    auto kern = gemv_tma_kernel<MB, R, NVEC_C, NG_C, LPS, PLAIN>;
     int static_smem = static_smem_cache.load(std::memory_order_relaxed);
     if (static_smem < 0) {
         cudaFuncAttributes fa;
@@ -453,7 +485,8 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
     // Shared memory: w_rows weight rows (stage s = rows [sR, sR + R)), S stages of scales,
     // then the per-warp partial sums.
     auto bytes = [&](int wr, int st) { return (size_t)wr * w_row + (size_t)st * R * s_row + red; };
-    constexpr int kActRows = 8;  // gate + up of one row: 4K bytes = 8 weight rows of K/2
+    // gate + up of one row: 4K bytes = 8 weight rows of K/2 (PLAIN: x alone, 4 rows)
+    constexpr int kActRows = PLAIN ? 4 : 8;
     int S = 0, w_rows = 0;
     if (M <= MB) {
         // One pass over the rows: when the CTA's share fits, every chunk gets a stage of
@@ -501,8 +534,9 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
                         static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up),
                         static_cast<const unsigned char *>(qweight),
                         static_cast<const uint16_t *>(scales),
-                        static_cast<const uint16_t *>(residual), static_cast<uint16_t *>(out),
-                        M, K, N, group, rows_base, rows_extra, S, w_rows, act_first_stage,
+                        static_cast<const uint16_t *>(residual), static_cast<uint16_t *>(o.out),
+                        static_cast<uint16_t *>(o.out2), o.split, o.ldo, M, K, N, group,
+                        rows_base, rows_extra, S, w_rows, act_first_stage,
                         M <= MB ? 1 : 0);
     *launched = true;
     if (err != cudaSuccess) return err;
@@ -510,23 +544,30 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
 }
 
 // LPS = 2 (two lanes per 32-k slice) for one activation row, else one lane per slice.
-template <int MB>
+// The SwiGLU form is specialised for the down-projection widths, the plain form for the
+// model width (the gate/up projection's K).
+template <int MB, bool PLAIN>
 cudaError_t launch_mb(const DeviceInfo &di, const void *gate, const void *up,
-                      const void *qweight, const void *scales, const void *residual, void *out,
+                      const void *qweight, const void *scales, const void *residual, GemvOut o,
                       int M, int K, int N, int group, cudaStream_t stream, bool *launched) {
     constexpr int R = kChunkRows;
     constexpr int LPS = MB == 1 ? 2 : 1;
-#define FD_SHAPE(KK, GG)                                                                        \
-    if (K == KK && group == GG)                                                                 \
-        return launch_cfg<MB, R, KK / 32, KK / GG, LPS>(di, gate, up, qweight, scales, residual, \
-                                                       out, M, K, N, group, stream, launched);
-    FD_SHAPE(14336, 128)
-    FD_SHAPE(9216, 128)
-    FD_SHAPE(4096, 128)
-    FD_SHAPE(1024, 128)
+#define FD_SHAPE(KK, GG)                                                                          \
+    if (K == KK && group == GG)                                                                   \
+        return launch_cfg<MB, R, KK / 32, KK / GG, LPS, PLAIN>(di, gate, up, qweight, scales,      \
+                                                              residual, o, M, K, N, group, stream, \
+                                                              launched);
+    if constexpr (PLAIN) {
+        FD_SHAPE(4096, 128)
+    } else {
+        FD_SHAPE(14336, 128)
+        FD_SHAPE(9216, 128)
+        FD_SHAPE(4096, 128)
+        FD_SHAPE(1024, 128)
+    }
 #undef FD_SHAPE
-    return launch_cfg<MB, R, 0, 0, LPS>(di, gate, up, qweight, scales, residual, out, M, K, N,
-                                        group, stream, launched);
+    return launch_cfg<MB, R, 0, 0, LPS, PLAIN>(di, gate, up, qweight, scales, residual, o, M, K,
+                                               N, group, stream, launched);
 }
 
 }  // namespace
@@ -538,18 +579,25 @@ bool gemv_tma_supported(int M, int K, int group) {
 }
 
 cudaError_t launch_gemv_tma(const void *gate, const void *up, const void *qweight,
-                            const void *scales, const void *residual, void *out, int M, int K,
+                            const void *scales, const void *residual, GemvOut o, int M, int K,
                             int N, int group, cudaStream_t stream, bool *launched) {
     *launched = false;
     if (!gemv_tma_supported(M, K, group)) return cudaSuccess;
     DeviceInfo di;
     cudaError_t err = device_info(&di);
     if (err != cudaSuccess) return err;
+    if (up == nullptr) {
+        if (M == 1)
+            return launch_mb<1, true>(di, gate, up, qweight, scales, residual, o, M, K, N, group,
+                                      stream, launched);
+        return launch_mb<2, true>(di, gate, up, qweight, scales, residual, o, M, K, N, group,
+                                  stream, launched);
+    }
     if (M == 1)
-        return launch_mb<1>(di, gate, up, qweight, scales, residual, out, M, K, N, group, stream,
-                            launched);
-    return launch_mb<2>(di, gate, up, qweight, scales, residual, out, M, K, N, group, stream,
-                        launched);
+        return launch_mb<1, false>(di, gate, up, qweight, scales, residual, o, M, K, N, group,
+                                   stream, launched);
+    return launch_mb<2, false>(di, gate, up, qweight, scales, residual, o, M, K, N, group,
+                               stream, launched);
 }
 
 }  // namespace fd

@@ -58,10 +58,20 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 // ------------------------------------------------------------------------------------
 // Launchers (host). Arguments are validated by the C-ABI layer before these run.
 // ------------------------------------------------------------------------------------
+// Where a GEMV's outputs go: row n < split to out[m * ldo + n], row n >= split to
+// out2[m * ldo + n - split]. A plain output is {out, nullptr, N, N}.
+struct GemvOut {
+    void *out;
+    void *out2;
+    int split;
+    int ldo;
+};
+
+// `up` null: the activation is gate itself (a plain W4A16 GEMV), else silu(gate) * up.
 // `residual` (bf16 [M, N], may equal `out`, or null) is added to the sum before the single
 // rounding to bf16 (the residual-add epilogue of the down projection).
 cudaError_t launch_gemv_tma(const void *gate, const void *up, const void *qweight,
-                            const void *scales, const void *residual, void *out, int M, int K,
+                            const void *scales, const void *residual, GemvOut o, int M, int K,
                             int N, int group, cudaStream_t stream, bool *launched);
 // Tensor-core path (tcgen05) for batched decode; sets *launched = false when the shape
 // is outside its rules (K % 1024, N % 128, group % 64, (K / group) % 8).
@@ -70,7 +80,7 @@ cudaError_t launch_gemv_tc(const void *gate, const void *up, const void *qweight
                            const void *scales, const void *residual, void *out, int M, int K,
                            int N, int group, cudaStream_t stream, bool *launched);
 cudaError_t launch_gemv_cc(const void *gate, const void *up, const void *qweight,
-                           const void *scales, const void *residual, void *out, int M, int K,
+                           const void *scales, const void *residual, GemvOut o, int M, int K,
                            int N, int group, cudaStream_t stream);
 cudaError_t launch_add_rmsnorm(const void *x, const void *residual, const void *weight,
                                float eps, void *out, void *residual_out, int rows,

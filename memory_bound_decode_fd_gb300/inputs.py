@@ -101,4 +101,6 @@ WORKLOADS = {
     "batched_m64": dict(kind="batched", M=64, K=14336, N=4096, group=128, eps=1e-5, seed=4),
     # the decode-step down projection with the residual-add epilogue (new_residual = x + out)
     "gemv_residual": dict(kind="gemv_residual", M=1, K=14336, N=4096, group=128, seed=3),
+    # the gate and up projections of the same MLP as one horizontally fused W4A16 GEMV
+    "gate_up": dict(kind="gate_up", M=1, K=4096, I=14336, group=128, seed=3),
 }

@@ -150,6 +150,51 @@ def swiglu_w4a16_gemv_residual(
     return out
 
 
+def w4a16_gate_up_gemv(
+    x: torch.Tensor,
+    qweight: torch.Tensor,
+    scales: torch.Tensor,
+    gate_out: torch.Tensor | None = None,
+    up_out: torch.Tensor | None = None,
+    group: int = 128,
+    stream: torch.cuda.Stream | None = None,
+) -> tuple[torch.Tensor, torch.Tensor]:
+    """(gate, up) = the gate and up projections of x as one W4A16 GEMV over the stacked
+    weights: qweight int32 [2I, K/8] (gate rows, then up rows), scales bf16 [2I, K/group].
+
+    gate[m, j] = bf16(sum_k x[m, k] * W[j, k]), up[m, j] = bf16(sum_k x[m, k] * W[I + j, k]).
+    x: bf16 [M, K] (a 1-D tensor is one row); gate_out, up_out: bf16 [M, I] (allocated if
+    None). They are the gate and up inputs of ``swiglu_w4a16_gemv``.
+    """
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    if x.dim() != 2 or qweight.dim() != 2 or scales.dim() != 2:
+        raise ValueError("x must be [M, K]; qweight [2I, K/8]; scales [2I, K/group]")
+    M, K = x.shape
+    N = qweight.shape[0]
+    if N % 2 != 0:
+        raise ValueError(f"qweight has {N} rows: expected 2I (gate rows, then up rows)")
+    inter = N // 2
+    _check_tensor("x", x, torch.bfloat16)
+    _check_tensor("qweight", qweight, torch.int32, (N, K // 8))
+    if group <= 0 or K % group != 0:
+        raise ValueError(f"K={K} must be a multiple of group={group}")
+    _check_tensor("scales", scales, torch.bfloat16, (N, K // group))
+    if gate_out is None:
+        gate_out = torch.empty((M, inter), dtype=torch.bfloat16, device=x.device)
+    if up_out is None:
+        up_out = torch.empty((M, inter), dtype=torch.bfloat16, device=x.device)
+    _check_tensor("gate_out", gate_out, torch.bfloat16, (M, inter))
+    _check_tensor("up_out", up_out, torch.bfloat16, (M, inter))
+    lib = _lib.load()
+    st = lib.fd_w4a16_gate_up_gemv(
+        _ptr(x), _ptr(qweight), _ptr(scales), _ptr(gate_out), _ptr(up_out),
+        int(M), int(K), int(inter), int(group), _stream_handle(stream),
+    )
+    _lib.check(st)
+    return gate_out, up_out
+
+
 def add_rmsnorm(
     x: torch.Tensor,
     residual: torch.Tensor,

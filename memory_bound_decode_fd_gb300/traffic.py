@@ -14,6 +14,12 @@ def gemv_bytes(M: int, K: int, N: int, group: int) -> int:
     return N * K // 2 + N * (K // group) * 2 + 2 * M * K * 2 + M * N * 2
 
 
+def gate_up_bytes(M: int, K: int, inter: int, group: int) -> int:
+    """The stacked [2I, K] int4 weights and their bf16 scales, x once, g and u written."""
+    N = 2 * inter
+    return N * K // 2 + N * (K // group) * 2 + M * K * 2 + M * N * 2
+
+
 def gemv_flops(M: int, K: int, N: int) -> int:
     return 2 * M * K * N
 

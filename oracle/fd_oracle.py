@@ -40,6 +40,8 @@ __all__ = [
     "dequant_w4",
     "swiglu_w4a16_gemv",
     "swiglu_w4a16_gemv_residual",
+    "w4a16_gemv",
+    "gate_up_gemv",
     "add_rmsnorm",
     "decode_mlp_step",
     "unfused_product_bytes",
@@ -185,6 +187,37 @@ def swiglu_w4a16_gemv_residual(gate_bits, up_bits, qweight, scale_bits, residual
     s32 = bf16_to_f32(out_bits) + r.astype(np.float32)  # float32 add, IEEE RNE
     eager_bits = f32_to_bf16_rne(s32)
     return ref, eager_bits
+
+
+def w4a16_gemv(x_bits, qweight, scale_bits, group: int) -> np.ndarray:
+    """y[m, n] = sum_k x[m, k] * W[n, k] as float64 [M, N], x a plain bf16 activation.
+
+    [FUSE] "The taxonomy of fusions", item 4 (dequantise the int4 weights, then the
+    matmul) with no pre-operation on the activation. Unfused: W is formed in full, then a
+    float64 library matmul.
+    """
+    x = bf16_to_f32(np.asarray(x_bits, dtype=np.uint16)).astype(np.float64)
+    if x.ndim == 1:
+        x = x[None, :]
+    w = dequant_w4(qweight, scale_bits, group).astype(np.float64)
+    if x.shape[1] != w.shape[1]:
+        raise ValueError("x K does not match the weights")
+    return x @ w.T
+
+
+def gate_up_gemv(x_bits, qweight, scale_bits, group: int):
+    """(g, u), each float64 [M, I]: the gate and up projections of x as one GEMV.
+
+    [FUSE] "The taxonomy of fusions", item 5 (horizontal fusion: gate_proj and up_proj,
+    two matmuls on the same input, become one gate_up_proj) and "The fusion boundary
+    problem" (gate, up = h @ W_gate_up). The stacked weight holds the gate projection's I
+    rows, then the up projection's I rows.
+    """
+    y = w4a16_gemv(x_bits, qweight, scale_bits, group)
+    if y.shape[1] % 2 != 0:
+        raise ValueError("the stacked weight must have 2I rows")
+    inter = y.shape[1] // 2
+    return y[:, :inter], y[:, inter:]
 
 
 # --------------------------------------------------------------------------------------

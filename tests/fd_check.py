@@ -159,6 +159,41 @@ def check_gemv_residual(y_bits, gate, up, qweight, scales, residual, group,
     return res
 
 
+def w4a16_reference(x, qweight, scales, group, rows=None):
+    """(ref, abs_sum, enc_err) of the plain GEMV for all or the selected weight rows: the
+    float64 result, sum_k |x_k| |W_nk| and sum_k (amax_slice(k) / 65534) |W_nk|."""
+    if rows is not None:
+        qweight = qweight[rows]
+        scales = scales[rows]
+    ref = oracle.w4a16_gemv(x, qweight, scales, group)
+    M, K = ref.shape[0], np.shape(x)[-1]
+    xa = np.abs(bf16_f64(x)).reshape(M, K)
+    w = np.abs(oracle.dequant_w4(qweight, scales, group).astype(np.float64))
+    amax = xa.reshape(M, K // 32, 32).max(axis=2)
+    enc = np.repeat(amax / 65534.0, 32, axis=1)
+    return ref, xa @ w.T, enc @ w.T
+
+
+def check_w4a16(y_bits, x, qweight, scales, group, rows=None) -> dict:
+    """Stated bar plus the elementwise bound of the CUDA-core kernels for a plain
+    activation (its 16-bit slice encoding and fp32 accumulation; no tanh term)."""
+    K = np.shape(x)[-1]
+    ref, abs_sum, enc_err = w4a16_reference(x, qweight, scales, group, rows)
+    y = bf16_f64(y_bits).reshape(ref.shape[0], -1)
+    if rows is not None:
+        y = y[:, rows]
+    res = stated_bar(y, ref)
+    bound = 2.0**-8 * np.abs(ref) + gemv_sum_error(K, abs_sum, enc_err, 0.0, False)
+    err = np.abs(y - ref)
+    bad = err > bound
+    assert not bad.any(), (
+        f"{int(bad.sum())} outputs outside the derived bound; worst excess "
+        f"{float((err - bound).max())}"
+    )
+    res["n_checked"] = int(y.size)
+    return res
+
+
 def ordered_key(bits) -> np.ndarray:
     """bf16 bit patterns -> integers whose order is the numeric order (adjacent values
     differ by 1; +0 and -0 both map to 0)."""

@@ -118,6 +118,32 @@ def test_gemv_residual_rejects_bad_arguments_without_launching(fdlib, kw, status
     assert gemv_res(fdlib, **kw) == status
 
 
+def gate_up(lib, x=A, qw=C, sc=D, g=E, u=F, M=1, K=1024, I=128, group=128):
+    return lib.fd_w4a16_gate_up_gemv(x, qw, sc, g, u, M, K, I, group, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), _lib.FD_ERR_NULL),
+    (dict(g=None), _lib.FD_ERR_NULL),
+    (dict(u=None), _lib.FD_ERR_NULL),
+    (dict(qw=None), _lib.FD_ERR_NULL),
+    (dict(I=0), _lib.FD_ERR_SHAPE),
+    (dict(M=0), _lib.FD_ERR_SHAPE),
+    (dict(K=1000), _lib.FD_ERR_SHAPE),
+    (dict(group=48), _lib.FD_ERR_SHAPE),
+    (dict(M=257), _lib.FD_ERR_UNSUPPORTED),
+    (dict(I=2**30), _lib.FD_ERR_UNSUPPORTED),
+    (dict(x=A + 2), _lib.FD_ERR_ALIGN),
+    (dict(u=F + 8), _lib.FD_ERR_ALIGN),
+    (dict(u=E + 64), _lib.FD_ERR_OVERLAP),     # up over gate
+    (dict(g=A), _lib.FD_ERR_OVERLAP),          # gate over x
+    (dict(u=C + 16), _lib.FD_ERR_OVERLAP),     # up inside qweight
+    (dict(g=D), _lib.FD_ERR_OVERLAP),          # gate over scales
+])
+def test_gate_up_rejects_bad_arguments_without_launching(fdlib, kw, status):
+    assert gate_up(fdlib, **kw) == status
+
+
 def rms(lib, x=A, r=B, w=C, eps=1e-6, out=D, rout=E, rows=4, hidden=4096):
     return lib.fd_add_rmsnorm(x, r, w, ctypes.c_float(eps), out, rout, rows, hidden, None)
 
@@ -200,5 +226,8 @@ def test_ideal_bytes_of_the_workloads():
     assert traffic.add_rmsnorm_bytes(8192, 4096) == 268_443_648
     assert traffic.gemv_bytes(1, 9216, 2560, 128) == 12_207_104
     assert traffic.decode_step_bytes(32, 4096, 14336, 128) == 972_292_096
+    # gate/up of the same MLP: 28672 x 4096 int4 + scales + x + g and u
+    assert traffic.gate_up_bytes(1, 4096, 14336, 128) == (
+        28672 * 2048 + 28672 * 32 * 2 + 4096 * 2 + 28672 * 2)
     assert traffic.gemv_bytes(64, 14336, 4096, 128) == 34_471_936
     assert traffic.add_rmsnorm_bytes(64, 4096) == 2_105_344

@@ -288,6 +288,66 @@ def test_gemv_residual_shift_by_residual_is_exact():
     np.testing.assert_allclose(a1 - a2, 3.0, rtol=0, atol=1e-12)
 
 
+def test_w4a16_gemv_brute_force_tiny():
+    # y[m, n] = sum_k x q s written as loops over the packed words (nothing shared with
+    # the oracle's unpack or dequant).
+    rng = np.random.default_rng(42)
+    M, K, N, group = 2, 64, 5, 32
+    x = inputs.normal_bf16(rng, (M, K))
+    qw = inputs.int4_words(rng, N, K)
+    s = inputs.scales_bf16(rng, N, K, group)
+    y = oracle.w4a16_gemv(x, qw, s, group)
+    xf = oracle.bf16_to_f32(x).astype(float)
+    sf = oracle.bf16_to_f32(s).astype(float)
+    words = qw.view(np.uint32)
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                nib = (int(words[n, k // 8]) >> (4 * (k % 8))) & 0xF
+                acc += xf[m, k] * (nib - 16 if nib & 0x8 else nib) * sf[n, k // group]
+            assert abs(acc - y[m, n]) <= 1e-12 * max(1.0, abs(acc))
+
+
+def test_gate_up_split_one_hot_pins_halves():
+    # A one-hot weight in the up half (row I + j) appears in u[:, j] only; one in the gate
+    # half (row j) in g[:, j] only; each is exactly x[k*] * q * s.
+    M, K, inter, group = 2, 128, 6, 64
+    rng = np.random.default_rng(43)
+    x = inputs.normal_bf16(rng, (M, K))
+    q = np.zeros((2 * inter, K), np.int8)
+    q[inter + 4, 70] = -7
+    q[1, 3] = 2
+    s = inputs.to_bf16_bits(np.full((2 * inter, K // group), 0.5))
+    g, u = oracle.gate_up_gemv(x, pack_int4(q), s, group)
+    xf = oracle.bf16_to_f32(x).astype(float)
+    expect_u = np.zeros((M, inter))
+    expect_u[:, 4] = xf[:, 70] * -7 * 0.5
+    expect_g = np.zeros((M, inter))
+    expect_g[:, 1] = xf[:, 3] * 2 * 0.5
+    assert np.array_equal(u, expect_u) and np.array_equal(g, expect_g)
+
+
+def test_gate_up_matches_torch_linear_fp64():
+    # Each half equals torch's float64 linear with that half's dequantised weights, built
+    # here from torch's own bit ops on the packed words.
+    rng = np.random.default_rng(44)
+    M, K, inter, group = 3, 256, 10, 128
+    x = inputs.normal_bf16(rng, (M, K))
+    qw = inputs.int4_words(rng, 2 * inter, K)
+    s = inputs.scales_bf16(rng, 2 * inter, K, group)
+    g, u = oracle.gate_up_gemv(x, qw, s, group)
+    words = torch.from_numpy(qw.view(np.uint32).astype(np.int64))
+    shifts = torch.arange(8, dtype=torch.int64) * 4
+    nib = (words.unsqueeze(-1) >> shifts) & 0xF
+    qt = torch.where(nib >= 8, nib - 16, nib).reshape(2 * inter, K).double()
+    st = torch.from_numpy(oracle.bf16_to_f32(s).astype(np.float64)).repeat_interleave(group, dim=1)
+    xt = torch.from_numpy(oracle.bf16_to_f32(x).astype(np.float64))
+    full = torch.nn.functional.linear(xt, qt * st).numpy()
+    np.testing.assert_allclose(g, full[:, :inter], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(u, full[:, inter:], rtol=1e-13, atol=1e-13)
+
+
 def test_add_rmsnorm_residual_matches_torch_bit_exact():
     d = inputs.rmsnorm_inputs(64, 1024, seed=20)
     h, _, _ = oracle.add_rmsnorm(d["x"], d["residual"], d["weight"], 1e-6)
