@@ -60,6 +60,11 @@ cudaError_t device_info(DeviceInfo *info) {
     err = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
                                  dev);
     if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                 dev);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&di.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (err != cudaSuccess) return err;
     err = cudaDeviceGetAttribute(&di.l2_bytes, cudaDevAttrL2CacheSize, dev);
     if (err != cudaSuccess) return err;
     // Benign race: concurrent first calls write identical values.

@@ -16,6 +16,8 @@ namespace fd {
 struct DeviceInfo {
     int sm_count;
     int max_smem_optin;   // bytes of dynamic shared memory a CTA may opt in to
+    int smem_per_sm;      // bytes of shared memory per SM (all resident CTAs)
+    int smem_reserved;    // bytes of shared memory the system reserves per CTA
     int l2_bytes;
 };
 // Returns cudaSuccess and fills `info` for the current device.
