@@ -53,6 +53,9 @@ KERNEL_SOURCES = {
     "swiglu_w4a16_gemv": ["csrc/fd_gemv_tma.cu", "csrc/fd_gemv_common.cuh", "csrc/fd_tma.cuh",
                           "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
     "add_rmsnorm": ["csrc/fd_add_rmsnorm.cu", "csrc/fd_internal.h"],
+    # the horizontal gate/up GEMV runs the same kernel's plain-activation form
+    "w4a16_gate_up_gemv": ["csrc/fd_gemv_tma.cu", "csrc/fd_gemv_common.cuh", "csrc/fd_tma.cuh",
+                           "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
 }
 
 
@@ -407,6 +410,7 @@ def bench_single(args, device, rank, world):
     kind = spec.pop("kind")
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     calls = []
+    traffic_tag = None
     if kind in ("gemv", "batched", "gemv_residual"):
         M, K, N, g = spec["M"], spec["K"], spec["N"], spec["group"]
         with_res = kind == "gemv_residual"
@@ -443,6 +447,7 @@ def bench_single(args, device, rank, world):
             s = to_dev(inputs.scales_bf16(rng, 2 * inter, K, g), device)
             calls.append(lambda q=q, s=s: fd.w4a16_gate_up_gemv(x, q, s, gate_out=gout, up_out=uout, group=g))
         kname = "w4a16_gate_up_gemv"
+        traffic_tag = f"K{K}_I{inter}_M{M}"
         desc = f"gate/up GEMV (horizontal fusion) M={M} K={K} I={inter} (2I={2 * inter} rows) group {g}, seed {spec['seed']}"
     else:
         rows, hidden = spec["rows"], spec["hidden"]
@@ -529,11 +534,87 @@ def bench_single(args, device, rank, world):
         "roofline": {"kernel": kname, "bound": "hbm", "achieved": round(nbytes / (k_us * 1e-6) / 1e9, 1),
                      "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(nbytes / (k_us * 1e-6) / 1e9 / hbm_peak, 4),
-                     "kernel_us": round(k_us, 3), "traffic": None},
+                     "kernel_us": round(k_us, 3),
+                     "traffic": recorded_traffic(kname, traffic_tag) if traffic_tag else None},
         "e2e": None,
         "gpu_launches": n_calls,
         "clocks": clocks,
         **({"paths": compare} if compare else {}),
+    }
+
+
+def bench_fused_layer(args, device, rank, world):
+    """32 decode layers of the pages' fully fused form, one CUDA graph with programmatic
+    dependent launch: add_rmsnorm(x, h) -> (normed, h); g, u = gate_up(normed);
+    h = h + down(silu(g) * u) in place. Llama-3-8B shapes (hidden 4096, MLP 14336). The
+    2.9 GB of int4 weights are drawn on the device (seeded); x_next of a layer is the
+    normed row of the next (x is the same tensor), so the step is one residual stream."""
+    import memory_bound_decode_fd_gb300 as fd
+
+    L, hidden, inter, g, eps, seed = 32, 4096, 14336, 128, 1e-5, 3
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+
+    def words(n, k):
+        return torch.randint(-2**31, 2**31 - 1, (n, k // 8), generator=gen, device=device, dtype=torch.int32)
+
+    def scales(n, k):
+        return (0.005 + 0.015 * torch.rand((n, k // g), generator=gen, device=device)).to(torch.bfloat16)
+
+    layers = [dict(w=(1.0 + 0.1 * torch.randn(hidden, generator=gen, device=device)).to(torch.bfloat16),
+                   qgu=words(2 * inter, hidden), sgu=scales(2 * inter, hidden),
+                   qd=words(hidden, inter), sd=scales(hidden, inter)) for _ in range(L)]
+    x = torch.randn((1, hidden), generator=gen, device=device).to(torch.bfloat16)
+    h = torch.randn((1, hidden), generator=gen, device=device).to(torch.bfloat16)
+    normed = torch.empty_like(x)
+    gt = torch.empty((1, inter), dtype=torch.bfloat16, device=device)
+    ut = torch.empty_like(gt)
+    zero = torch.zeros_like(x)
+
+    def step():
+        for i, ly in enumerate(layers):
+            # layer 0 adds the incoming x; later layers' residual stream is h alone
+            fd.add_rmsnorm(x if i == 0 else zero, h, ly["w"], eps, out=normed, residual_out=h)
+            fd.w4a16_gate_up_gemv(normed, ly["qgu"], ly["sgu"], gate_out=gt, up_out=ut, group=g)
+            fd.swiglu_w4a16_gemv_residual(gt, ut, ly["qd"], ly["sd"], h, out=h, group=g)
+
+    stream = torch.cuda.Stream(device)
+    prev = fd.set_pdl(True)
+    try:
+        stream.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(stream):
+            step()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    finally:
+        fd.set_pdl(prev)
+    per_layer = (fd.add_rmsnorm_bytes(1, hidden) + fd.gate_up_bytes(1, hidden, inter, g)
+                 + fd.gemv_bytes(1, inter, hidden, g) + hidden * 2)
+    nbytes = L * per_layer
+    hbm_peak, peak_kind, _ = read_peaks()
+    sampler = ClockSampler(smi_index())
+    sampler.start()
+    with torch.cuda.stream(stream):
+        time_region(stream, graph.replay, max(args.warmup, 3))
+        barrier(world)
+        ms = max_over_ranks(time_region(stream, graph.replay, args.steps), world)
+    clocks = sampler.stop()
+    ms_step = ms / args.steps
+    gbs = job_throughput_gbs(world, nbytes, ms_step)
+    return {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
+        "us_per_step": round(ms_step * 1e3, 3), "us_per_layer": round(ms_step * 1e3 / L, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (int4 weights, fp32 accumulation)", "data": "synthetic (seeded, drawn on the device)",
+        "config": {"workload": f"fused_layer: {L} x [add-RMSNorm 1x{hidden} + gate/up GEMV K={hidden} I={inter} "
+                               f"+ down GEMV K={inter} N={hidden} with SwiGLU prologue and residual epilogue], seed {seed}",
+                   "bytes_per_step": nbytes, "l2": f"{nbytes} B of weights per step vs L2 (defeats it)",
+                   "launch": f"one CUDA graph of {3 * L} launches, programmatic dependent launch"},
+        "pct_of_measured_hbm": round(100 * gbs / world / hbm_peak, 1),
+        "roofline": None, "e2e": None, "gpu_launches": 3 * L * args.steps, "clocks": clocks,
     }
 
 
@@ -571,7 +652,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--workload", default="decode_step",
                     choices=["decode_step", "gemv_94mb", "rmsnorm_big", "gemv_small", "batched_m64",
-                             "gemv_residual", "gate_up"])
+                             "gemv_residual", "gate_up", "fused_layer"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
 
@@ -600,6 +681,8 @@ def main(argv=None):
         line, d = bench_decode(args, device, rank, world)
         if rank == 0 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline_decode(d)
+    elif args.workload == "fused_layer":
+        line = bench_fused_layer(args, device, rank, world)
     else:
         line = bench_single(args, device, rank, world)
     if rank == 0:

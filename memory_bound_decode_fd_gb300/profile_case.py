@@ -3,6 +3,7 @@
     python -m memory_bound_decode_fd_gb300.profile_case gemv --M 1 --K 14336 --N 4096
     python -m memory_bound_decode_fd_gb300.profile_case gemv --M 64 --path tensor
     python -m memory_bound_decode_fd_gb300.profile_case rmsnorm --rows 8192 --hidden 4096
+    python -m memory_bound_decode_fd_gb300.profile_case gate_up --K 4096 --N 14336
 
 Each iteration uses the next of --sets input sets, so that consecutive launches do not
 find their weights in L2. Exits 0 after a final synchronize.
@@ -28,10 +29,10 @@ def main(argv=None) -> int:
     from memory_bound_decode_fd_gb300 import build, inputs
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["gemv", "rmsnorm"])
+    ap.add_argument("case", choices=["gemv", "rmsnorm", "gate_up"])
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--K", type=int, default=14336)
-    ap.add_argument("--N", type=int, default=4096)
+    ap.add_argument("--N", type=int, default=4096, help="rows (gate_up: I, the stacked weight has 2I)")
     ap.add_argument("--group", type=int, default=128)
     ap.add_argument("--rows", type=int, default=8192)
     ap.add_argument("--hidden", type=int, default=4096)
@@ -55,6 +56,17 @@ def main(argv=None) -> int:
         for i in range(args.iters):
             q, s = sets[i % len(sets)]
             fd.swiglu_w4a16_gemv(g, u, q, s, out=out, group=args.group)
+    elif args.case == "gate_up":
+        rng = np.random.default_rng(0)
+        x = _dev(inputs.normal_bf16(rng, (args.M, args.K)), dev)
+        sets = [(_dev(inputs.int4_words(rng, 2 * args.N, args.K), dev),
+                 _dev(inputs.scales_bf16(rng, 2 * args.N, args.K, args.group), dev))
+                for _ in range(args.sets)]
+        g = torch.empty((args.M, args.N), dtype=torch.bfloat16, device=dev)
+        u = torch.empty_like(g)
+        for i in range(args.iters):
+            q, s = sets[i % len(sets)]
+            fd.w4a16_gate_up_gemv(x, q, s, gate_out=g, up_out=u, group=args.group)
     else:
         sets = []
         for i in range(args.sets):
