@@ -269,7 +269,19 @@ def bench_decode(args, device, rank, world):
     e2e_call = lambda: step(xh, rh, gh, uh, ox, orr)  # noqa: E731
     time_region(stream, e2e_call, max(args.warmup, 3))
     barrier(world)
-    e2e_ms = max_over_ranks(time_region(stream, e2e_call, args.steps), world) / args.steps
+    e2e_sep_ms = max_over_ranks(time_region(stream, e2e_call, args.steps), world) / args.steps
+    # the same through StepIO: one host->device copy of the step's inputs, one
+    # device->host copy of its outputs
+    io = step.pinned_io()
+    io.x.copy_(xh)
+    io.residual.copy_(rh)
+    io.gate.copy_(gh)
+    io.up.copy_(uh)
+    step.capture_pinned(io)
+    e2e_io = lambda: step.run_pinned(io)  # noqa: E731
+    time_region(stream, e2e_io, max(args.warmup, 3))
+    barrier(world)
+    e2e_ms = max_over_ranks(time_region(stream, e2e_io, args.steps), world) / args.steps
     h2d = (xh.numel() + rh.numel() + gh.numel() + uh.numel()) * 2
     d2h = (ox.numel() + orr.numel()) * 2
 
@@ -315,7 +327,8 @@ def bench_decode(args, device, rank, world):
             "ms_per_step": round(e2e_ms, 6),
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "api": "memory_bound_decode_fd_gb300.step.DecodeStep.__call__ (pinned host in/out)",
+            "api": "memory_bound_decode_fd_gb300.step.DecodeStep.run_pinned (StepIO captured with the step: fd_copy kernels read and write the pinned host block, one graph launch)",
+            "four_copy_call_ms_per_step": round(e2e_sep_ms, 6),
         },
         "gpu_launches": 2 * spec["layers"] * args.steps,
         "clocks": clocks,

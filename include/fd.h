@@ -47,6 +47,8 @@
 #ifndef FD_H_
 #define FD_H_
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -214,6 +216,18 @@ int fd_w4_dequant_debug(const void *qweight, const void *scales, float *out, int
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *fd_status_string(int status);
+
+/*
+ * fd_copy - copy `bytes` from src to dst with one kernel spread over every SM, for the
+ * per-token inputs and outputs of a decode step. Either side may be device memory or
+ * pinned host memory (cudaHostAlloc / torch pin_memory), which a GB300 reads and writes
+ * over NVLink-C2C. When a side is not accessible to a kernel (pageable host memory) the
+ * call falls back to one cudaMemcpyAsync.
+ * Requires  dst, src 16-byte aligned; bytes > 0 and a multiple of 16; no overlap.
+ * Stream-ordered like every call here; with programmatic dependent launch the kernel
+ * waits for the previous kernel before it reads src.
+ */
+int fd_copy(void *dst, const void *src, size_t bytes, fd_stream_t stream);
 
 /* The cudaError_t value behind the calling thread's most recent FD_ERR_CUDA (0 if none).
  * Thread-local; not reset by successful calls. */

@@ -33,6 +33,7 @@ from ._lib import load as load_library  # noqa: F401
 from .kernels import (  # noqa: F401
     GEMV_PATHS,
     add_rmsnorm,
+    copy,
     decode_mlp_step,
     gemv_uses_tensor_cores,
     set_gemv_path,

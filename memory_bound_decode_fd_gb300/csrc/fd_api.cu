@@ -178,6 +178,14 @@ int fd_w4a16_gate_up_gemv(const void *x, const void *qweight, const void *scales
     return from_cuda(launch_gemv_cc(x, nullptr, qweight, scales, nullptr, o, M, K, N, group, st_));
 }
 
+int fd_copy(void *dst, const void *src, size_t bytes, fd_stream_t stream) {
+    if (!dst || !src) return FD_ERR_NULL;
+    if (bytes == 0 || bytes % 16 != 0) return FD_ERR_SHAPE;
+    if (!aligned16(dst) || !aligned16(src)) return FD_ERR_ALIGN;
+    if (overlaps(dst, bytes, src, bytes)) return FD_ERR_OVERLAP;
+    return from_cuda(launch_copy(dst, src, bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fd_gemv_uses_tensor_cores(int M, int K, int N, int group) {
     if (M <= 0 || K <= 0 || N <= 0 || group <= 0) return 0;
     const int path = g_gemv_path.load(std::memory_order_relaxed);

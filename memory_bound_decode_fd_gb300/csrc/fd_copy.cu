@@ -1,0 +1,65 @@
+// fd_copy.cu - one-kernel copy between device-accessible buffers, for the per-token I/O of
+// a decode step. On GB300 (Grace + Blackwell) pinned host memory is read and written by
+// the GPU over NVLink-C2C; a copy kernel spread over every SM moves a step's inputs
+// (1.85 MB for 32 layers of gate/up at MLP width 14336) several times faster than one
+// copy-engine transfer, which ran at ~68 GB/s here.
+#include "fd_internal.h"
+
+namespace fd {
+namespace {
+
+// 16-byte vectors, grid-stride; waits for the previous kernel in the stream first (the
+// source may be its output) when launched with programmatic dependent launch.
+__global__ void __launch_bounds__(256) copy_kernel(const uint4 *__restrict__ src,
+                                                   uint4 *__restrict__ dst, size_t n16) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+        dst[i] = a;
+        dst[i + stride] = b;
+        dst[i + 2 * stride] = c;
+        dst[i + 3 * stride] = d;
+    }
+    for (; i < n16; i += stride) dst[i] = src[i];
+}
+
+// The device address of `p` if the GPU can access it (device, managed, or mapped pinned
+// host memory), else nullptr.
+const void *device_address(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
+    if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+    return nullptr;
+}
+
+}  // namespace
+
+cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream) {
+    const void *s = device_address(src);
+    void *d = const_cast<void *>(device_address(dst));
+    if (!s || !d) {
+        // not accessible to a kernel (e.g. pageable host memory): the copy engine
+        return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, stream);
+    }
+    DeviceInfo di;
+    cudaError_t err = device_info(&di);
+    if (err != cudaSuccess) return err;
+    const size_t n16 = bytes / 16;
+    long long blocks = (long long)((n16 + 255) / 256);
+    const long long cap = (long long)di.sm_count * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    err = launch_kernel(copy_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, 1,
+                        static_cast<const uint4 *>(s), static_cast<uint4 *>(d), n16);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+}  // namespace fd

@@ -195,6 +195,23 @@ def w4a16_gate_up_gemv(
     return gate_out, up_out
 
 
+def copy(dst: torch.Tensor, src: torch.Tensor, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """dst <- src (same number of bytes, contiguous, 16-byte aligned) with one kernel:
+    either side may be a CUDA tensor or a pinned host tensor (read or written by the GPU
+    over NVLink-C2C). Falls back to one cudaMemcpyAsync for memory a kernel cannot reach."""
+    if not (dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("copy: dst and src must be contiguous")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("copy: dst and src differ in size")
+    for name, t in (("dst", dst), ("src", src)):
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"copy: {name} must be a CUDA tensor or pinned host memory")
+    lib = _lib.load()
+    _lib.check(lib.fd_copy(_ptr(dst), _ptr(src), nbytes, _stream_handle(stream)))
+    return dst
+
+
 def add_rmsnorm(
     x: torch.Tensor,
     residual: torch.Tensor,

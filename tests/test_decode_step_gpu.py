@@ -138,3 +138,45 @@ def test_pdl_flag_roundtrip(cuda_device):
     assert fd.load_library().fd_get_launch_flags() == 0
     fd.set_pdl(prev)
     assert fd.load_library().fd_set_launch_flags(4) == fd.FD_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("captured", [False, True])
+def test_decode_step_pinned_io_matches_call(cuda_device, step_data, captured):
+    # One host->device and one device->host copy per step (StepIO) give the same outputs
+    # as the four-input __call__ path, for two consecutive tokens (the new residual is the
+    # next token's input residual).
+    from memory_bound_decode_fd_gb300.step import DecodeStep
+
+    d = step_data
+    layers = device_layers(d)
+    inter = d["layers"][0]["gate"].shape[1]
+
+    def make():
+        st = DecodeStep([{k: L[k] for k in ("rms_weight", "qweight", "scales")} for L in layers],
+                        d["hidden"], inter, d["group"], EPS, pdl=True)
+        return st.capture()
+
+    a, b = make(), make()
+    gate = torch.from_numpy(np.stack([L["gate"] for L in d["layers"]]).view(np.int16)).view(torch.bfloat16)
+    up = torch.from_numpy(np.stack([L["up"] for L in d["layers"]]).view(np.int16)).view(torch.bfloat16)
+    x = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).reshape(1, -1)
+    res = torch.from_numpy(d["residual"].view(np.int16)).view(torch.bfloat16).reshape(1, -1)
+    pin = lambda t: t.contiguous().pin_memory()  # noqa: E731
+    xh, rh, gh, uh = pin(x), pin(res), pin(gate), pin(up)
+    ox, orr = torch.empty_like(xh).pin_memory(), torch.empty_like(rh).pin_memory()
+    io = b.pinned_io()
+    if captured:
+        b.capture_pinned(io)
+    io.x.copy_(x)
+    io.residual.copy_(res)
+    io.gate.copy_(gate)
+    io.up.copy_(up)
+    for _ in range(2):
+        a(xh, rh, gh, uh, ox, orr)
+        a.stream.synchronize()
+        b.run_pinned(io)
+        b.stream.synchronize()
+        assert torch.equal(io.out_x.view(torch.int16), ox.view(torch.int16))
+        assert torch.equal(io.residual.view(torch.int16), orr.view(torch.int16))
+        rh.copy_(orr)  # the next token starts from the new residual on both paths
+    assert io.h2d_bytes == (2 * d["hidden"] + 2 * len(layers) * inter) * 2

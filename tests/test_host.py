@@ -144,6 +144,19 @@ def test_gate_up_rejects_bad_arguments_without_launching(fdlib, kw, status):
     assert gate_up(fdlib, **kw) == status
 
 
+@pytest.mark.parametrize("args,status", [
+    ((None, B, 1024), _lib.FD_ERR_NULL),
+    ((A, None, 1024), _lib.FD_ERR_NULL),
+    ((A, B, 0), _lib.FD_ERR_SHAPE),
+    ((A, B, 1000), _lib.FD_ERR_SHAPE),
+    ((A + 8, B, 1024), _lib.FD_ERR_ALIGN),
+    ((A, B + 4, 1024), _lib.FD_ERR_ALIGN),
+    ((A, A + 512, 1024), _lib.FD_ERR_OVERLAP),
+])
+def test_copy_rejects_bad_arguments_without_launching(fdlib, args, status):
+    assert fdlib.fd_copy(*args, None) == status
+
+
 def rms(lib, x=A, r=B, w=C, eps=1e-6, out=D, rout=E, rows=4, hidden=4096):
     return lib.fd_add_rmsnorm(x, r, w, ctypes.c_float(eps), out, rout, rows, hidden, None)
 
