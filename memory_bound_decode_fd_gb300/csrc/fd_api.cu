@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "fd_copy.h"
 #include "fd_internal.h"
 
 namespace fd {

@@ -3,6 +3,7 @@
 // the GPU over NVLink-C2C; a copy kernel spread over every SM moves a step's inputs
 // (1.85 MB for 32 layers of gate/up at MLP width 14336) several times faster than one
 // copy-engine transfer, which ran at ~68 GB/s here.
+#include "fd_copy.h"
 #include "fd_internal.h"
 
 namespace fd {

@@ -87,9 +87,6 @@ cudaError_t launch_gemv_cc(const void *gate, const void *up, const void *qweight
 cudaError_t launch_add_rmsnorm(const void *x, const void *residual, const void *weight,
                                float eps, void *out, void *residual_out, int rows,
                                int hidden, cudaStream_t stream);
-// One-kernel copy of `bytes` (multiple of 16) between device-accessible buffers; falls
-// back to cudaMemcpyAsync when either side is not accessible to a kernel.
-cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
 cudaError_t launch_w4_dequant_debug(const void *qweight, const void *scales, float *out,
                                     int K, int N, int group, cudaStream_t stream);
 
