@@ -1,6 +1,9 @@
 // fd_gemv_cc.cu - SwiGLU-prologue W4A16 GEMV on the CUDA cores (any M, tuned for M = 1).
 //
-// y[m, n] = bf16( sum_k silu(g[m, k]) * u[m, k] * q[n, k] * s[n, k / group] )
+// y[m, n] = bf16( [residual[m, n] +] sum_k silu(g[m, k]) * u[m, k] * q[n, k] * s[n, k / group] )
+//
+// With up == nullptr the activation is gate itself (a plain W4A16 GEMV, the horizontal
+// gate/up projection), and the output rows may be split between two tensors (out_at).
 //
 // Sources: "09 - Operator fusion", section 5 (taxonomy item 4, GEMM prologue fusion: the
 // dequantisation happens as the weights are loaded, so only int4 crosses HBM; "The fusion
@@ -24,7 +27,8 @@
 //     per 32-k slice; the activation and group scales multiply the slice's sum.
 //   * Reduction: each lane holds R x MB partials per chunk; a butterfly reduce-scatter
 //     over the warp (V - 1 + log2(32 / V) shuffles for V values) leaves one warp sum per
-//     (row, m) in shared memory; the CTA sums over warps and stores bf16 once per output.
+//     (row, m) in shared memory; the CTA sums over warps, adds the residual if one is
+//     given, and stores bf16 once per output.
 //   * M > MB: the CTA repeats its rows for each chunk of MB activation rows (weights are
 //     then read with an evict-last L2 policy so the repeats hit L2).
 #include <atomic>

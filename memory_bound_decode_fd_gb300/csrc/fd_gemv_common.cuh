@@ -1,6 +1,6 @@
-// fd_gemv_common.cuh - device pieces shared by the two SwiGLU-W4A16 GEMV kernels: the
-// SwiGLU prologue into registers, the 32-k integer dot product, and the warp
-// reduce-scatter.
+// fd_gemv_common.cuh - device pieces shared by the two CUDA-core W4A16 GEMV kernels: the
+// SwiGLU prologue into registers (or the plain-activation one), the 32-k integer dot
+// product, the warp reduce-scatter, the cross-warp sum and the output addressing.
 //
 // Numerics of one 32-k slice (one 16-byte weight vector position, inside one scale
 // group):
@@ -13,7 +13,8 @@
 //   instruction (16-bit x 8-bit products), from the byte split of fd_w4_unpack.cuh;
 //   the slice's contribution to y[n] is float(that sum) * (scale * s[n, group]).
 // Beyond fp32 rounding, the errors are tanh's and the 16-bit encoding of a (at most
-// amax / 65534 per element).
+// amax / 65534 per element). A plain activation x (encode_plain) is encoded the same way,
+// without the tanh step.
 #pragma once
 
 #include "fd_internal.h"

@@ -1,7 +1,9 @@
 // fd_gemv_tc.cu - SwiGLU-prologue W4A16 product for batched decode (M >= 16) on the
 // fifth-generation tensor cores (tcgen05.mma, accumulator in tensor memory).
 //
-// y[m, n] = bf16( sum_k a[m, k] * w[n, k] ),  a = silu(g) * u,  w = q * s[n, k / group]
+// y[m, n] = bf16( [residual[m, n] +] sum_k a[m, k] * w[n, k] ),  a = silu(g) * u,
+//           w = q * s[n, k / group]   (the residual: the down projection's residual-add
+//           epilogue, added to the fp32 sum before the one rounding)
 //
 // Sources: "09 - Operator fusion", section 5 (taxonomy item 4, GEMM prologue fusion:
 // the int4 weights are dequantised on chip as they stream in; "The fusion boundary

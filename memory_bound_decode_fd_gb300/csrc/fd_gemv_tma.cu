@@ -1,6 +1,10 @@
 // fd_gemv_tma.cu - SwiGLU-prologue W4A16 GEMV, bulk-copy (TMA) weight stream.
 //
-// y[m, n] = bf16( sum_k silu(g[m, k]) * u[m, k] * q[n, k] * s[n, k / group] )
+// y[m, n] = bf16( [residual[m, n] +] sum_k silu(g[m, k]) * u[m, k] * q[n, k] * s[n, k / group] )
+//
+// The same kernel in its PLAIN form (template flag) takes a plain activation x instead of
+// silu(g) * u: the horizontal gate/up projection, whose stacked output rows go to two
+// tensors (rows n < split to out, the rest to out2).
 //
 // Sources: "09 - Operator fusion", section 5 (taxonomy item 4: dequantisation as the
 // weights are loaded, only int4 crosses HBM; "The fusion boundary problem": act =
@@ -10,7 +14,9 @@
 //
 // The fast path for K % 1024 == 0, K <= 15360 and (K / group) % 8 == 0 (every
 // decode shape of interest). Design for GB300:
-//   * One persistent CTA per SM owning a contiguous range of output rows n.
+//   * Persistent CTAs, each owning a contiguous range of output rows n: one per SM, or
+//     several per SM when a CTA is small (K=4096: three CTAs of 288 threads), as many as
+//     the registers, threads and shared memory allow.
 //   * Warp specialisation: the last warp is a producer whose lane 0 streams chunks of 8
 //     consecutive weight rows (8 * K/2 bytes, one contiguous bulk copy) and their scales
 //     (8 * K/group * 2 bytes, a second bulk copy) into shared-memory stages, completion
@@ -29,7 +35,8 @@
 //     9 and every lane has half the rows; the encoding of the slice is split between them
 //     (each converts 16 of its 32 k and they swap halves with one shuffle).
 //   * Per chunk a butterfly reduce-scatter (over 16 lanes when LPS = 2) leaves one warp
-//     sum per (row, m) in shared memory; every 64 rows the consumers sum over warps and
+//     sum per (row, m) in shared memory; every 64 rows the consumers sum over warps, add
+//     the residual if one is given (the down projection's residual-add epilogue) and
 //     store bf16 once per output.
 //   * Every mbarrier wait is bounded (fd_tma.cuh). If one gives up, the CTA stops
 //     computing, waits (bounded) for the copies it issued, writes NaN to all of its
