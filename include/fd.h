@@ -203,6 +203,10 @@ int fd_gemv_uses_tensor_cores(int M, int K, int N, int group);
  * fd_set_launch_flags returns FD_ERR_UNSUPPORTED for unknown bits.
  */
 #define FD_LAUNCH_PDL 1u
+/* Test only: every call that would launch work instead returns FD_ERR_CUDA, with
+ * fd_last_cuda_error() = cudaErrorLaunchOutOfResources, without calling CUDA (the error
+ * path of a failed launch, exercised without touching the GPU). */
+#define FD_LAUNCH_TEST_FAIL 256u
 int fd_set_launch_flags(unsigned flags);
 unsigned fd_get_launch_flags(void);
 

@@ -20,6 +20,7 @@ from ._lib import (  # noqa: F401
     FD_ERR_OVERLAP,
     FD_ERR_SHAPE,
     FD_ERR_UNSUPPORTED,
+    FD_LAUNCH_TEST_FAIL,
     FD_MAX_HIDDEN,
     FD_MAX_K,
     FD_MAX_M,

@@ -22,6 +22,7 @@ FD_GEMV_BULK = 2
 FD_GEMV_TENSOR = 3
 
 FD_LAUNCH_PDL = 1
+FD_LAUNCH_TEST_FAIL = 256
 
 FD_MAX_K = 32768
 FD_MAX_M = 256

@@ -29,6 +29,11 @@ bool overlaps(const void *a, size_t a_bytes, const void *b, size_t b_bytes) {
     return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
 }
 
+// FD_LAUNCH_TEST_FAIL: the launch is reported as failed without calling CUDA.
+bool fake_launch_failure() {
+    return (g_launch_flags.load(std::memory_order_relaxed) & FD_LAUNCH_TEST_FAIL) != 0;
+}
+
 int from_cuda(cudaError_t err) {
     if (err == cudaSuccess) return FD_OK;
     g_last_cuda_error = static_cast<int>(err);
@@ -109,6 +114,7 @@ int swiglu_gemv(const void *gate, const void *up, const void *qweight, const voi
          overlaps(residual, out_bytes, qweight, w_bytes) ||
          overlaps(residual, out_bytes, scales, s_bytes)))
         return FD_ERR_OVERLAP;
+    if (fake_launch_failure()) return from_cuda(cudaErrorLaunchOutOfResources);
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
     const int path = g_gemv_path.load(std::memory_order_relaxed);
     if (fd_gemv_uses_tensor_cores(M, K, N, group)) {
@@ -167,6 +173,7 @@ int fd_w4a16_gate_up_gemv(const void *x, const void *qweight, const void *scales
             return FD_ERR_OVERLAP;
     }
     if (overlaps(gate_out, o_bytes, up_out, o_bytes)) return FD_ERR_OVERLAP;
+    if (fake_launch_failure()) return from_cuda(cudaErrorLaunchOutOfResources);
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
     const GemvOut o{gate_out, up_out, I, I};
     const int path = g_gemv_path.load(std::memory_order_relaxed);
@@ -184,6 +191,7 @@ int fd_copy(void *dst, const void *src, size_t bytes, fd_stream_t stream) {
     if (bytes == 0 || bytes % 16 != 0) return FD_ERR_SHAPE;
     if (!aligned16(dst) || !aligned16(src)) return FD_ERR_ALIGN;
     if (overlaps(dst, bytes, src, bytes)) return FD_ERR_OVERLAP;
+    if (fake_launch_failure()) return from_cuda(cudaErrorLaunchOutOfResources);
     return from_cuda(launch_copy(dst, src, bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -203,7 +211,7 @@ int fd_set_gemv_path(int path) {
 int fd_get_gemv_path(void) { return g_gemv_path.load(std::memory_order_relaxed); }
 
 int fd_set_launch_flags(unsigned flags) {
-    if (flags & ~FD_LAUNCH_PDL) return FD_ERR_UNSUPPORTED;
+    if (flags & ~(FD_LAUNCH_PDL | FD_LAUNCH_TEST_FAIL)) return FD_ERR_UNSUPPORTED;
     g_launch_flags.store(flags, std::memory_order_relaxed);
     return FD_OK;
 }
@@ -233,6 +241,7 @@ int fd_add_rmsnorm(const void *x, const void *residual, const void *weight, floa
         return FD_ERR_OVERLAP;
     if (overlaps(weight, w_bytes, out, bytes) || overlaps(weight, w_bytes, residual_out, bytes))
         return FD_ERR_OVERLAP;
+    if (fake_launch_failure()) return from_cuda(cudaErrorLaunchOutOfResources);
     return from_cuda(launch_add_rmsnorm(x, residual, weight, eps, out, residual_out, rows,
                                         hidden, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -247,6 +256,7 @@ int fd_w4_dequant_debug(const void *qweight, const void *scales, float *out, int
     if (overlaps(out, out_bytes, qweight, (size_t)N * K / 2) ||
         overlaps(out, out_bytes, scales, (size_t)N * (K / group) * 2))
         return FD_ERR_OVERLAP;
+    if (fake_launch_failure()) return from_cuda(cudaErrorLaunchOutOfResources);
     return from_cuda(launch_w4_dequant_debug(qweight, scales, out, K, N, group,
                                              reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -1,6 +1,7 @@
 """GPU parity of fd_swiglu_w4a16_gemv and fd_w4_dequant_debug against the CPU oracle,
 called through the C ABI (via the ctypes binding) on seeded synthetic inputs."""
 
+import ctypes
 import gc
 
 import numpy as np
@@ -255,3 +256,39 @@ def test_gemv_back_to_back_calls_identical(cuda_device, K, N):
     bits = host_bits(outs)
     assert all(np.array_equal(bits[i], bits[0]) for i in range(1, 64))
     check_gemv(bits[0], d["gate"], d["up"], d["qweight"], d["scales"], 128)
+
+
+def test_failed_launch_returns_fd_err_cuda_and_records_the_error(cuda_device):
+    # FD_LAUNCH_TEST_FAIL fakes a failed launch on the host (no CUDA call, nothing runs):
+    # every entry point must return FD_ERR_CUDA with the CUDA error recorded, and work
+    # normally once the flag is cleared.
+    lib = fd.load_library()
+    d = inputs.gemv_inputs(1, 1024, 256, 128, seed=0)
+    g, u = dev_bf16(d["gate"]), dev_bf16(d["up"])
+    q, s = dev_i32(d["qweight"]), dev_bf16(d["scales"])
+    out = torch.empty((1, 256), dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((2, 4096), dtype=torch.bfloat16, device="cuda")
+    w = torch.ones((4096,), dtype=torch.bfloat16, device="cuda")
+    y, h = torch.empty_like(x), torch.empty_like(x)
+    q2, s2 = dev_i32(d["qweight"][:128]), dev_bf16(d["scales"][:128])  # 2I = 256 rows
+    go, uo = torch.empty((1, 64), dtype=torch.bfloat16, device="cuda"), torch.empty((1, 64), dtype=torch.bfloat16, device="cuda")
+    calls = [
+        lambda: lib.fd_swiglu_w4a16_gemv(g.data_ptr(), u.data_ptr(), q.data_ptr(), s.data_ptr(), out.data_ptr(), 1, 1024, 256, 128, None),
+        lambda: lib.fd_swiglu_w4a16_gemv_residual(g.data_ptr(), u.data_ptr(), q.data_ptr(), s.data_ptr(), out.data_ptr(), out.data_ptr(), 1, 1024, 256, 128, None),
+        lambda: lib.fd_w4a16_gate_up_gemv(g.data_ptr(), q2.data_ptr(), s2.data_ptr(), go.data_ptr(), uo.data_ptr(), 1, 1024, 64, 128, None),
+        lambda: lib.fd_add_rmsnorm(x.data_ptr(), x.data_ptr(), w.data_ptr(), ctypes.c_float(1e-5), y.data_ptr(), h.data_ptr(), 2, 4096, None),
+        lambda: lib.fd_copy(y.data_ptr(), h.data_ptr(), 2 * 4096 * 2, None),
+    ]
+    prev = lib.fd_get_launch_flags()
+    assert lib.fd_set_launch_flags(fd.FD_LAUNCH_TEST_FAIL) == fd.FD_OK
+    try:
+        for call in calls:
+            assert call() == fd.FD_ERR_CUDA
+            assert lib.fd_last_cuda_error() == 701  # cudaErrorLaunchOutOfResources
+    finally:
+        assert lib.fd_set_launch_flags(prev) == fd.FD_OK
+    for call in calls:
+        assert call() == fd.FD_OK
+    torch.cuda.synchronize()
+    y_ok = run_gemv(d)
+    check_gemv(y_ok, d["gate"], d["up"], d["qweight"], d["scales"], 128)
