@@ -233,6 +233,21 @@ const char *fd_status_string(int status);
  */
 int fd_copy(void *dst, const void *src, size_t bytes, fd_stream_t stream);
 
+/*
+ * fd_debug_plan_gemv - test support: the launch plan the bulk-copy GEMV kernel would use,
+ * computed on the host from given device facts, without any CUDA call.
+ * device  int[6]: SM count, opt-in shared memory per CTA, shared memory per SM, shared
+ *         memory reserved per CTA, the kernel's static shared memory, its registers per
+ *         thread.
+ * plain   0: the SwiGLU activation (gate and up); 1: a plain activation (gate/up GEMV).
+ * plan    int[9] out: grid, rows_base, rows_extra (the first rows_extra CTAs own one more
+ *         row), stages S, weight rows of shared memory, first stage the M = 1 activation
+ *         copy overlays, ring (stages reused), CTAs per SM, dynamic shared memory per CTA.
+ * Returns FD_ERR_UNSUPPORTED when the kernel would not run the call (the CUDA-core kernel
+ * does instead).
+ */
+int fd_debug_plan_gemv(const int *device, int M, int K, int N, int group, int plain, int *plan);
+
 /* The cudaError_t value behind the calling thread's most recent FD_ERR_CUDA (0 if none).
  * Thread-local; not reset by successful calls. */
 int fd_last_cuda_error(void);

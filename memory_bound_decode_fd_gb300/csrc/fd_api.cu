@@ -7,6 +7,7 @@
 #include <cstdint>
 
 #include "fd_copy.h"
+#include "fd_gemv_plan.h"
 #include "fd_internal.h"
 
 namespace fd {
@@ -193,6 +194,23 @@ int fd_copy(void *dst, const void *src, size_t bytes, fd_stream_t stream) {
     if (overlaps(dst, bytes, src, bytes)) return FD_ERR_OVERLAP;
     if (fake_launch_failure()) return from_cuda(cudaErrorLaunchOutOfResources);
     return from_cuda(launch_copy(dst, src, bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fd_debug_plan_gemv(const int *device, int M, int K, int N, int group, int plain, int *plan) {
+    if (!device || !plan) return FD_ERR_NULL;
+    if (M <= 0 || K <= 0 || N <= 0 || group <= 0 || K % 32 != 0 || K % group != 0)
+        return FD_ERR_SHAPE;
+    // the bulk-copy kernel's compile-time shape: one activation row per pass with two lanes
+    // per 32-k slice at M = 1, else two rows per pass with one lane; 8-row chunks, 8 slots
+    const int MB = M == 1 ? 1 : 2;
+    TmaPlanInput in{device[0], device[1], device[2], device[3], device[4], device[5],
+                    M, K, N, group, MB, MB == 1 ? 2 : 1, 8, 8, plain ? 1 : 0};
+    TmaPlan p{};
+    if (!plan_gemv_tma(in, &p)) return FD_ERR_UNSUPPORTED;
+    const int v[9] = {p.grid, p.rows_base, p.rows_extra, p.S, p.w_rows, p.act_first_stage,
+                      p.ring, p.per_sm, (int)p.smem};
+    for (int i = 0; i < 9; ++i) plan[i] = v[i];
+    return FD_OK;
 }
 
 int fd_gemv_uses_tensor_cores(int M, int K, int N, int group) {

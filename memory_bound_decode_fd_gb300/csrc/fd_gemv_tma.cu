@@ -44,6 +44,7 @@
 #include <atomic>
 
 #include "fd_gemv_common.cuh"
+#include "fd_gemv_plan.h"
 #include "fd_tma.cuh"
 
 namespace fd {
@@ -477,87 +478,15 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
         fc = (fa.sharedSizeBytes & 0xFFFFF) | (fa.numRegs << 20);
         func_cache.store(fc, std::memory_order_relaxed);
     }
-    const int static_smem = fc & 0xFFFFF;
-    const int regs = fc >> 20;
     const int nvec = K / 32;
-    const int ngroups = K / group;
-    const int threads = LPS * nvec + 32;
-    const size_t w_row = (size_t)K / 2, s_row = (size_t)ngroups * 2;
-    const size_t red = (size_t)(LPS * nvec / 32) * kWindowRows * MB * 4;
-    const size_t budget = (size_t)di.max_smem_optin - (size_t)static_smem;
-    // gate + up of one row: 4K bytes = 8 weight rows of K/2 (PLAIN: x alone, 4 rows)
-    constexpr int kActRows = PLAIN ? 4 : 8;
-    // Shared memory: w_rows weight rows (stage s = rows [sR, sR + R)), S stages of scales,
-    // then the per-warp partial sums.
-    auto bytes = [&](int wr, int st) { return (size_t)wr * w_row + (size_t)st * R * s_row + red; };
-    struct Plan {
-        int grid, rows_base, rows_extra, S, w_rows, act_first_stage;
-        bool ring;
-    };
-    // The plan for `per_sm` resident CTAs per SM, each within `cap` bytes of dynamic
-    // shared memory; false if the ring would be too small.
-    auto plan_for = [&](int per_sm, size_t cap, Plan &p) -> bool {
-        int grid = di.sm_count * per_sm;
-        if ((long long)grid * R > N) grid = (N + R - 1) / R;
-        if (grid < 1) grid = 1;
-        p.grid = grid;
-        p.rows_base = N / grid;
-        p.rows_extra = N % grid;
-        const int n_max = p.rows_base + (p.rows_extra > 0 ? 1 : 0);
-        const int n_chunks_max = (n_max + R - 1) / R;
-        p.S = 0;
-        p.w_rows = 0;
-        if (M <= MB) {
-            // One pass over the rows: when the CTA's share fits, every chunk gets a stage
-            // of its own and all are issued at once. The activation (M == 1) takes the
-            // stages after the chunks if there is room, else it overlays the last weight
-            // rows and the chunks there are issued once the consumers have read it.
-            const int own = n_chunks_max + (M == 1 ? (kActRows + R - 1) / R : 0);
-            if (own <= kMaxStages && bytes(own * R, own) <= cap) {
-                p.S = own;
-                p.w_rows = own * R;
-            } else if (M == 1 && n_chunks_max <= kMaxStages && n_max >= kActRows &&
-                       bytes(n_max, n_chunks_max) <= cap) {
-                p.S = n_chunks_max;
-                p.w_rows = n_max;
-            }
-        }
-        p.ring = (p.S == 0);
-        if (p.ring) {
-            // a ring of uniform stages, reused across chunks and activation-row passes
-            const size_t stage = (size_t)R * (w_row + s_row);
-            if (red + 2 * stage > cap) return false;
-            p.S = (int)((cap - red) / stage);
-            if (p.S > kMaxStages) p.S = kMaxStages;
-            p.w_rows = p.S * R;
-        }
-        // With M == 1 the gate/up copy borrows the last kActRows weight rows: stages from
-        // act_first_stage on are filled after it is read. A ring keeps two stages for
-        // weights (three when CTAs share an SM).
-        p.act_first_stage = (M == 1) ? (p.w_rows - kActRows) / R : p.S;
-        const int min_free = per_sm > 1 ? 3 : 2;
-        if (p.ring && (M == 1 ? p.act_first_stage : p.S) < min_free) return false;
-        return true;
-    };
-    // Persistent CTAs: one per SM, or several when a CTA is small (few consumer warps at
-    // small K) and the registers (per warp, in units of 256), threads and shared memory
-    // allow. More warps per scheduler hide the row loop's latency: at K=4096 three CTAs of
-    // 288 threads share an SM.
-    const int warps = (threads + 31) / 32;
-    const int regs_per_warp = ((regs * 32 + 255) / 256) * 256;
-    int max_per_sm = regs_per_warp > 0 ? 65536 / (regs_per_warp * warps) : 1;
-    max_per_sm = min(max_per_sm, 2048 / (warps * 32));
-    max_per_sm = min(max_per_sm, 4);
-    Plan plan{};
-    bool planned = false;
-    for (int c = max_per_sm; c > 1 && !planned; --c) {
-        const long long share = (long long)di.smem_per_sm / c - di.smem_reserved - static_smem;
-        if (share > 0) planned = plan_for(c, min((size_t)share, budget), plan);
-    }
-    if (!planned && !plan_for(1, budget, plan)) return cudaSuccess;  // not launched
+    TmaPlanInput in{di.sm_count, di.max_smem_optin, di.smem_per_sm, di.smem_reserved,
+                    fc & 0xFFFFF, fc >> 20, M, K, N, group, MB, LPS, R, kMaxStages, PLAIN ? 1 : 0};
+    TmaPlan plan{};
+    if (!plan_gemv_tma(in, &plan)) return cudaSuccess;  // not launched
     const int S = plan.S, w_rows = plan.w_rows, act_first_stage = plan.act_first_stage;
     const int grid = plan.grid, rows_base = plan.rows_base, rows_extra = plan.rows_extra;
-    const size_t smem = bytes(w_rows, S);
+    const size_t smem = plan.smem;
+    const size_t budget = (size_t)di.max_smem_optin - (size_t)(fc & 0xFFFFF);
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
