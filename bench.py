@@ -10,16 +10,20 @@ is captured once in a CUDA graph and replayed.
 Reported:
   value      achieved GB/s = algorithmic bytes per step / device time per step
              (CUDA events around K replays on the launching stream, max over ranks)
-  e2e        the same metric through the public API with the per-token inputs in
-             pinned host memory: H2D of x, residual and every layer's gate/up, the
-             replay, D2H of x_L and the residual, all inside the timed region
+  e2e        the same metric through the public API (DecodeStep.run_pinned) with the
+             per-token inputs in pinned host memory: the transfer of x, residual and
+             every layer's gate/up in, the 64 kernels, the transfer of x_L and the
+             residual out (fd_copy kernels in the step's graph), all inside the timed
+             region
   roofline   the dominant kernel (the GEMV) - its average launch duration from CUDA
              events around replays of a graph of the step's 32 GEMV launches alone
   cpu_baseline  the CPU oracle, single-threaded, on a bounded sample of the workload
   --impl reference  times the CPU oracle alone (the reference arm of this benchmark)
 
 Other workloads (--workload gemv_94mb | rmsnorm_big | gemv_small | batched_m64 |
-gemv_residual | gate_up) time one call per step and rotate ceil(3 x L2 / bytes) input sets so every step reads HBM.
+gemv_residual | gate_up) time one call per step and rotate ceil(3 x L2 / bytes) input
+sets so every step reads HBM; --workload fused_layer times 32 layers of add-RMSNorm +
+gate/up GEMV + down GEMV with the residual epilogue as one graph.
 """
 
 from __future__ import annotations
