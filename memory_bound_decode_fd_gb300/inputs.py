@@ -14,6 +14,14 @@ Workloads (name: sizes, seed):
   gemv_94mb      GEMV M=1 K=9216 N=2560 group 128 (its fp32 (1,K,N) product is 94 MB), seed 2
   decode_step    32 x [add-RMSNorm 1x4096 eps=1e-5 + GEMV K=14336 N=4096], seed 3
   batched_m64    GEMV M=64 K=14336 N=4096 + add-RMSNorm 64x4096 eps=1e-5, seed 4
+  gemv_residual  the decode-step GEMV with the residual-add epilogue, seed 3
+  gate_up        gate/up GEMV M=1 K=4096 I=14336 (28672 stacked rows), seed 3
+
+NVFP4 operands (``nvfp4_inputs``; M=64 K=4096 N=6144 is a Llama-3.1-8B QKV projection at
+batch 64, seed 5) are drawn as codes: packed FP4 bytes uniform (every nibble one of the
+16 E2M1 codes with equal odds), E4M3 block-scale codes with sign 0, exponent field
+uniform in 3..9 and mantissa uniform in 0..7 (scales from 2^-4 to 7.5), and the fp32
+output multiplier uniform in [0.5, 2).
 """
 
 from __future__ import annotations
@@ -90,6 +98,31 @@ def batched_inputs(M: int = 64, K: int = 14336, N: int = 4096, group: int = 128,
     g = gemv_inputs(M, K, N, group, rng=rng)
     r = rmsnorm_inputs(M, N, rng=rng)
     return {"gemv": g, "rmsnorm": r}
+
+
+def fp4_bytes(rng: np.random.Generator, rows: int, k: int) -> np.ndarray:
+    """Packed FP4 operand [rows, k/2] uint8, every nibble i.i.d. uniform over the 16 codes."""
+    return rng.integers(0, 256, size=(rows, k // 2), dtype=np.uint8)
+
+
+def e4m3_scale_codes(rng: np.random.Generator, rows: int, k: int) -> np.ndarray:
+    """Block-scale codes [rows, k/16] uint8: sign 0, exponent field 3..9, mantissa 0..7."""
+    e = rng.integers(3, 10, size=(rows, k // 16), dtype=np.uint8)
+    m = rng.integers(0, 8, size=(rows, k // 16), dtype=np.uint8)
+    return (e << np.uint8(3)) | m
+
+
+def nvfp4_inputs(M: int = 64, K: int = 4096, N: int = 6144, seed: int = 5, rng=None) -> dict:
+    """Draw order: x, x_sf, w, w_sf, alpha."""
+    rng = rng if rng is not None else np.random.default_rng(seed)
+    return {
+        "x": fp4_bytes(rng, M, K),
+        "x_sf": e4m3_scale_codes(rng, M, K),
+        "w": fp4_bytes(rng, N, K),
+        "w_sf": e4m3_scale_codes(rng, N, K),
+        "alpha": np.float32(rng.uniform(0.5, 2.0)),
+        "M": M, "K": K, "N": N,
+    }
 
 
 WORKLOADS = {

@@ -19,10 +19,16 @@ function cites the passage it follows, by page title and section:
 * [KFM]   "Kernel Fusion, torch.compile and CUDA Graphs, Measured" - "Step 1: why
           elementwise kernels are memory-bound", "Step 2: fusing them by hand in
           Triton", "Step 3: what torch.compile generates".
+* [NVFP4] "PyTorch folds NVFP4 output scaling into NVGEMM candidates for decode
+          workloads" - body (eligibility: packed FP4 operands, E4M3 1x16 block scales, a
+          zero-dimensional fp32 output multiplier; the ATen candidate that runs the scaled
+          matmul and the multiplication separately).
 
 Where the pages are silent the plainest reading is taken (symmetric two's-complement
 int4, eight nibbles per 32-bit word along K, nibble j of word p holding k = 8p + j,
-bf16 scales [N, K/group] with w = q * s). Every function here is pinned by
+bf16 scales [N, K/group] with w = q * s; for NVFP4, E2M1 elements packed two per byte
+with the even k in the low nibble, E4M3 scales [rows, K/16] row-major, and a bf16
+output). Every function here is pinned by
 ``tests/test_oracle_pins.py`` to something other than itself; none is "parity
 unpinned".
 """
@@ -44,6 +50,11 @@ __all__ = [
     "gate_up_gemv",
     "add_rmsnorm",
     "decode_mlp_step",
+    "unpack_fp4",
+    "e2m1_to_f64",
+    "e4m3_to_f64",
+    "nvfp4_dequant",
+    "nvfp4_scaled_mm",
     "unfused_product_bytes",
     "eager_add_rmsnorm_kernels",
     "eager_add_rmsnorm_bytes_per_elem",
@@ -283,6 +294,100 @@ def decode_mlp_step(x_bits, residual_bits, layers, eps: float, group: int):
         res = h_bits
         x = f32_to_bf16_rne(y.astype(np.float32)).reshape(x.shape)
     return record, x, res
+
+
+# --------------------------------------------------------------------------------------
+# NVFP4 scaled matmul with the output scale folded in
+# --------------------------------------------------------------------------------------
+
+def unpack_fp4(packed) -> np.ndarray:
+    """Split packed FP4 bytes [R, K/2] into 4-bit codes [R, K] (uint8, 0..15).
+
+    [NVFP4]: the operands are "packed FP4", two 4-bit elements per byte. The page gives
+    no order; the reading here is element 2p in the low nibble (bits 0..3) of byte p
+    and element 2p + 1 in the high nibble.
+    """
+    b = np.ascontiguousarray(packed).astype(np.uint8)
+    if b.ndim != 2:
+        raise ValueError("packed FP4 operands are [rows, K/2] bytes")
+    codes = np.empty((b.shape[0], b.shape[1] * 2), dtype=np.uint8)
+    codes[:, 0::2] = b & np.uint8(0x0F)
+    codes[:, 1::2] = b >> np.uint8(4)
+    return codes
+
+
+def e2m1_to_f64(codes) -> np.ndarray:
+    """Value of 4-bit E2M1 codes: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0.
+
+    An exponent field of 0 is subnormal, m * 2^-1; otherwise (1 + m/2) * 2^(e - 1). The
+    format has no infinity or NaN, so every code is finite (largest magnitude 6). This
+    is the element type of NVFP4 ([NVFP4] "packed FP4"); the page does not spell the
+    encoding out, and the reading is the standard FP4 E2M1 definition.
+    """
+    c = np.asarray(codes).astype(np.int64)
+    sign = np.where((c >> 3) & 1, -1.0, 1.0)
+    e = (c >> 1) & 3
+    m = (c & 1).astype(np.float64)
+    mag = np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * np.exp2(e - 1.0))
+    return sign * mag
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Value of 8-bit E4M3 codes: sign bit 7, exponent bits 6..3 (bias 7), mantissa bits
+    2..0. An exponent field of 0 is subnormal, (m/8) * 2^-6. S.1111.111 is NaN and there
+    is no infinity, so S.1111.110 = 448 is the largest magnitude.
+
+    [NVFP4]: the block scales are "E4M3 1x16" scales.
+    """
+    c = np.asarray(codes).astype(np.int64)
+    sign = np.where((c >> 7) & 1, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def nvfp4_dequant(packed, sf_codes) -> np.ndarray:
+    """Dequantised NVFP4 operand X[r, k] = e2m1(x[r, k]) * e4m3(sf[r, k // 16]), float64
+    [R, K].
+
+    [NVFP4]: one E4M3 scale per 1x16 block, i.e. per 16 consecutive elements of a row
+    along K. A 2-bit significand times a 4-bit one is exact in float64.
+    """
+    x = e2m1_to_f64(unpack_fp4(packed))
+    sf = e4m3_to_f64(np.asarray(sf_codes))
+    rows, k = x.shape
+    if k % 16 != 0 or sf.shape != (rows, k // 16):
+        raise ValueError("block scales must be [rows, K/16]")
+    return x * np.repeat(sf, 16, axis=1)
+
+
+def nvfp4_scaled_mm(x_packed, x_sf, w_packed, w_sf, alpha):
+    """out[m, n] = alpha * sum_k X[m, k] * W[n, k] with X, W the dequantised NVFP4
+    activations [M, K] and weights [N, K] (an nn.Linear's x @ W^T).
+
+    [NVFP4] body: the scaled matmul of two packed-FP4 operands with E4M3 1x16 block
+    scales, and the zero-dimensional fp32 output multiplier alpha that the fold applies
+    inside the GEMM instead of in a separate multiplication. Unfused here: both operands
+    are dequantised in full, then a float64 library matmul, then the multiplication.
+
+    Returns ``(ref, eager_bits)``:
+      * ``ref``        float64 [M, N], alpha * the sum, nothing rounded;
+      * ``eager_bits`` uint16, the unfolded sequence the page's ATen candidate keeps: the
+                       scaled matmul stores bf16(sum), then a separate multiplication by
+                       alpha computes in float32 and stores bf16 again.
+    """
+    x = nvfp4_dequant(x_packed, x_sf)
+    w = nvfp4_dequant(w_packed, w_sf)
+    if x.shape[1] != w.shape[1]:
+        raise ValueError("activation K does not match the weights")
+    a32 = np.float32(alpha)
+    acc = x @ w.T
+    ref = float(a32) * acc
+    mm_bits = f32_to_bf16_rne(acc.astype(np.float32))
+    eager_bits = f32_to_bf16_rne(bf16_to_f32(mm_bits) * a32)  # float32 multiply, IEEE RNE
+    return ref, eager_bits
 
 
 # --------------------------------------------------------------------------------------

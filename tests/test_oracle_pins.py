@@ -437,6 +437,143 @@ def test_decode_step_zero_weights_pass_residual_through():
     assert np.array_equal(res, h1)
 
 
+# ------------------------------------------------------------------------------ NVFP4
+
+# The FP4 E2M1 code points (sign, 2 exponent bits, 1 mantissa bit), written out as values:
+# the eight magnitudes 0, 1/2, 1, 3/2, 2, 3, 4, 6, then the same with the sign set.
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+               -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def torch_e4m3(codes):
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8))
+    return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e2m1_codes_are_the_fp4_values():
+    v = oracle.e2m1_to_f64(np.arange(16))
+    assert v.tolist() == E2M1_VALUES
+    assert np.signbit(v[8]) and not np.signbit(v[0])
+
+
+def test_e4m3_matches_torch_float8_e4m3fn_on_every_code():
+    codes = np.arange(256)
+    v, t = oracle.e4m3_to_f64(codes), torch_e4m3(codes)
+    nan = np.isnan(t)
+    assert np.array_equal(np.isnan(v), nan) and np.nonzero(nan)[0].tolist() == [0x7F, 0xFF]
+    assert np.array_equal(v[~nan], t[~nan])
+    assert np.array_equal(np.signbit(v[~nan]), np.signbit(t[~nan]))  # -0.0 at 0x80
+    assert v[0x7E] == 448.0 and v[0x01] == 2.0 ** -9 and v[0x38] == 1.0
+
+
+def test_unpack_fp4_even_k_in_low_nibble():
+    codes = oracle.unpack_fp4(np.array([[0x21, 0xF0]], dtype=np.uint8))
+    assert codes.tolist() == [[1, 2, 0, 15]]
+
+
+def nvfp4_brute(x, x_sf, w, w_sf, alpha):
+    """Element by element: nibbles by integer division, values from the code table,
+    scales from torch's float8_e4m3fn."""
+    sx, sw = torch_e4m3(x_sf), torch_e4m3(w_sf)
+    M, N, K = x.shape[0], w.shape[0], 2 * x.shape[1]
+
+    def elem(b, r, k):
+        byte = int(b[r, k // 2])
+        return E2M1_VALUES[byte % 16 if k % 2 == 0 else byte // 16]
+
+    out = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += elem(x, m, k) * sx[m, k // 16] * elem(w, n, k) * sw[n, k // 16]
+            out[m, n] = float(alpha) * acc
+    return out
+
+
+def test_nvfp4_brute_force_tiny():
+    # With these scale codes every product is a multiple of 2^-16 below 2^11, so the
+    # sums are exact in float64 in any order and the two sides agree bit for bit.
+    d = inputs.nvfp4_inputs(M=3, K=48, N=5, rng=np.random.default_rng(40))
+    ref, _ = oracle.nvfp4_scaled_mm(d["x"], d["x_sf"], d["w"], d["w_sf"], d["alpha"])
+    assert np.array_equal(ref, nvfp4_brute(d["x"], d["x_sf"], d["w"], d["w_sf"], d["alpha"]))
+
+
+def test_nvfp4_one_hot_pins_block_index_and_packing():
+    # one nonzero element at k = 17 (high nibble of byte 8, block 1) in x row 0 and in
+    # w row 3; distinct scales per block, so k // 8 or k // 32 picks another scale
+    M, N, K = 2, 4, 64
+    x = np.zeros((M, K // 2), np.uint8)
+    w = np.zeros((N, K // 2), np.uint8)
+    x[0, 8] = 0x20          # code 2 = 1.0 at k = 17
+    w[3, 8] = 0x50          # code 5 = 3.0 at k = 17
+    x_sf = np.tile(np.array([0x38, 0x40, 0x48, 0x50], np.uint8), (M, 1))   # 1, 2, 4, 8
+    w_sf = np.tile(np.array([0x30, 0x28, 0x20, 0x18], np.uint8), (N, 1))   # 1/2, 1/4, 1/8, 1/16
+    ref, eager = oracle.nvfp4_scaled_mm(x, x_sf, w, w_sf, np.float32(1.5))
+    want = np.zeros((M, N))
+    want[0, 3] = 1.5 * (1.0 * 2.0) * (3.0 * 0.25)
+    assert np.array_equal(ref, want)
+    assert np.array_equal(eager, oracle.f32_to_bf16_rne(want.astype(np.float32)))
+
+
+def test_nvfp4_output_scale_fold_against_the_unfolded_pair():
+    d = inputs.nvfp4_inputs(M=16, K=256, N=64, rng=np.random.default_rng(41))
+    args = (d["x"], d["x_sf"], d["w"], d["w_sf"])
+    ref1, eager1 = oracle.nvfp4_scaled_mm(*args, np.float32(1.0))
+    # alpha = 1: the separate multiplication changes nothing
+    assert np.array_equal(eager1, oracle.f32_to_bf16_rne(ref1.astype(np.float32)))
+    # a power of two commutes with rounding: folded and unfolded agree exactly
+    ref4, eager4 = oracle.nvfp4_scaled_mm(*args, np.float32(0.25))
+    assert np.array_equal(ref4, 0.25 * ref1)
+    assert np.array_equal(eager4, oracle.f32_to_bf16_rne(ref4.astype(np.float32)))
+    # any other alpha scales the exact sum; the unfolded pair rounds twice, stays within
+    # one bf16 step of the once-rounded folded result and differs from it somewhere
+    ref, eager = oracle.nvfp4_scaled_mm(*args, np.float32(0.7))
+    assert np.array_equal(ref, float(np.float32(0.7)) * ref1)
+    fused = oracle.bf16_to_f32(oracle.f32_to_bf16_rne(ref.astype(np.float32))).astype(np.float64)
+    e = oracle.bf16_to_f32(eager).astype(np.float64)
+    assert np.all(np.abs(e - fused) <= np.abs(fused) * 2.0 ** -7)
+    assert np.any(e != fused)
+
+
+def test_nvfp4_zero_scale_and_negative_zero_contribute_nothing():
+    d = inputs.nvfp4_inputs(M=2, K=64, N=3, rng=np.random.default_rng(42))
+    ref, _ = oracle.nvfp4_scaled_mm(d["x"], d["x_sf"], d["w"], d["w_sf"], d["alpha"])
+    x_sf = d["x_sf"].copy()
+    x_sf[0, :] = 0x00                                         # row 0: every block scale 0
+    x = d["x"].copy()
+    x[1, :] = 0x88                                            # row 1: every element -0.0
+    ref0, _ = oracle.nvfp4_scaled_mm(x, x_sf, d["w"], d["w_sf"], d["alpha"])
+    assert np.all(ref0 == 0.0)
+    assert np.any(ref != 0.0)
+
+
+def test_nvfp4_fold_removes_one_launch_per_layer():
+    # the page's figures agree with one folded output multiplication (one launch) per
+    # decoder layer, the QKV projection's, over Llama-3's 32 layers; the default NVFP4
+    # workload is that projection at the page's batch
+    f = GOLDEN["nvfp4_output_scale_fold"]
+    assert f["graph_nodes_before"] - f["graph_nodes_after"] == f["fewer_launches_per_step"]
+    layers = GOLDEN["silu_traffic_llama3_8b"]["layers"]
+    assert f["fewer_launches_per_step"] == f["scaling_launches_removed_per_layer"] * layers
+    d = inputs.nvfp4_inputs(K=64, N=8)
+    assert d["M"] == f["batch"]
+
+
+def test_nvfp4_generator_draws_valid_codes():
+    d = inputs.nvfp4_inputs(M=64, K=512, N=128, seed=5)
+    for key in ("x_sf", "w_sf"):
+        sf = d[key]
+        assert sf.dtype == np.uint8 and np.all(sf >> 7 == 0)
+        e = sf >> 3
+        assert e.min() == 3 and e.max() == 9
+        assert set(np.unique(sf & 7).tolist()) == set(range(8))
+    codes = oracle.unpack_fp4(d["w"])
+    assert set(np.unique(codes).tolist()) == set(range(16))
+    assert d["x"].shape == (64, 256) and d["w"].shape == (128, 256)
+    assert d["x_sf"].shape == (64, 32) and 0.5 <= d["alpha"] < 2.0
+
+
 # ------------------------------------------------------------------------------ page figures
 
 def test_byte_model_unfused_product_is_94mb():
