@@ -7,6 +7,7 @@ memory and the stream; nothing here computes.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 
 import torch
@@ -43,9 +44,31 @@ def set_pdl(enabled: bool) -> bool:
     return prev
 
 
-def _stream_handle(stream: torch.cuda.Stream | None) -> ctypes.c_void_p:
-    s = stream if stream is not None else torch.cuda.current_stream()
+def _device_of(*tensors) -> torch.device | None:
+    """The one CUDA device of a call's CUDA tensors (None if it has none, e.g. a copy
+    between two pinned host buffers). Tensors on two devices are an error: the kernels
+    dereference every pointer on the device they run on."""
+    devs = {t.device for t in tensors if t.is_cuda}
+    if len(devs) > 1:
+        raise ValueError(f"all CUDA tensors of a call must be on one device, got {sorted(map(str, devs))}")
+    return devs.pop() if devs else None
+
+
+def _stream_handle(stream, device: torch.device | None) -> ctypes.c_void_p:
+    """The handle of `stream`, else of the current stream of `device`; a stream of
+    another device is an error."""
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    if device is not None and s.device != device:
+        raise ValueError(f"stream is on {s.device} but the tensors are on {device}")
     return ctypes.c_void_p(int(s.cuda_stream))
+
+
+def _on_device(device: torch.device | None):
+    """Make `device` current for the library call (it launches on, and reads the facts
+    of, the calling thread's current device); a no-op when it already is."""
+    if device is None or device.index is None or device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
 
 
 def _check_tensor(name: str, t: torch.Tensor, dtype: torch.dtype, shape: tuple | None = None):
@@ -95,11 +118,13 @@ def swiglu_w4a16_gemv(
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=gate.device)
     _check_tensor("out", out, torch.bfloat16, (M, N))
+    dev = _device_of(gate, up, qweight, scales, out)
     lib = _lib.load()
-    st = lib.fd_swiglu_w4a16_gemv(
-        _ptr(gate), _ptr(up), _ptr(qweight), _ptr(scales), _ptr(out),
-        int(M), int(K), int(N), int(group), _stream_handle(stream),
-    )
+    with _on_device(dev):
+        st = lib.fd_swiglu_w4a16_gemv(
+            _ptr(gate), _ptr(up), _ptr(qweight), _ptr(scales), _ptr(out),
+            int(M), int(K), int(N), int(group), _stream_handle(stream, dev),
+        )
     _lib.check(st)
     return out
 
@@ -141,11 +166,13 @@ def swiglu_w4a16_gemv_residual(
     elif out.dim() == 1:
         out = out.unsqueeze(0)
     _check_tensor("out", out, torch.bfloat16, (M, N))
+    dev = _device_of(gate, up, qweight, scales, residual, out)
     lib = _lib.load()
-    st = lib.fd_swiglu_w4a16_gemv_residual(
-        _ptr(gate), _ptr(up), _ptr(qweight), _ptr(scales), _ptr(residual), _ptr(out),
-        int(M), int(K), int(N), int(group), _stream_handle(stream),
-    )
+    with _on_device(dev):
+        st = lib.fd_swiglu_w4a16_gemv_residual(
+            _ptr(gate), _ptr(up), _ptr(qweight), _ptr(scales), _ptr(residual), _ptr(out),
+            int(M), int(K), int(N), int(group), _stream_handle(stream, dev),
+        )
     _lib.check(st)
     return out
 
@@ -186,11 +213,13 @@ def w4a16_gate_up_gemv(
         up_out = torch.empty((M, inter), dtype=torch.bfloat16, device=x.device)
     _check_tensor("gate_out", gate_out, torch.bfloat16, (M, inter))
     _check_tensor("up_out", up_out, torch.bfloat16, (M, inter))
+    dev = _device_of(x, qweight, scales, gate_out, up_out)
     lib = _lib.load()
-    st = lib.fd_w4a16_gate_up_gemv(
-        _ptr(x), _ptr(qweight), _ptr(scales), _ptr(gate_out), _ptr(up_out),
-        int(M), int(K), int(inter), int(group), _stream_handle(stream),
-    )
+    with _on_device(dev):
+        st = lib.fd_w4a16_gate_up_gemv(
+            _ptr(x), _ptr(qweight), _ptr(scales), _ptr(gate_out), _ptr(up_out),
+            int(M), int(K), int(inter), int(group), _stream_handle(stream, dev),
+        )
     _lib.check(st)
     return gate_out, up_out
 
@@ -207,8 +236,10 @@ def copy(dst: torch.Tensor, src: torch.Tensor, stream: torch.cuda.Stream | None 
     for name, t in (("dst", dst), ("src", src)):
         if not (t.is_cuda or t.is_pinned()):
             raise ValueError(f"copy: {name} must be a CUDA tensor or pinned host memory")
+    dev = _device_of(dst, src)
     lib = _lib.load()
-    _lib.check(lib.fd_copy(_ptr(dst), _ptr(src), nbytes, _stream_handle(stream)))
+    with _on_device(dev):
+        _lib.check(lib.fd_copy(_ptr(dst), _ptr(src), nbytes, _stream_handle(stream, dev)))
     return dst
 
 
@@ -247,11 +278,13 @@ def add_rmsnorm(
         residual_out = residual_out.unsqueeze(0)
     _check_tensor("out", out, torch.bfloat16, (rows, hidden))
     _check_tensor("residual_out", residual_out, torch.bfloat16, (rows, hidden))
+    dev = _device_of(x, residual, weight, out, residual_out)
     lib = _lib.load()
-    st = lib.fd_add_rmsnorm(
-        _ptr(x), _ptr(residual), _ptr(weight), ctypes.c_float(float(eps)), _ptr(out),
-        _ptr(residual_out), int(rows), int(hidden), _stream_handle(stream),
-    )
+    with _on_device(dev):
+        st = lib.fd_add_rmsnorm(
+            _ptr(x), _ptr(residual), _ptr(weight), ctypes.c_float(float(eps)), _ptr(out),
+            _ptr(residual_out), int(rows), int(hidden), _stream_handle(stream, dev),
+        )
     _lib.check(st)
     if squeeze:
         return out.squeeze(0), residual_out.squeeze(0)
@@ -266,20 +299,24 @@ def w4_dequant_debug(
     stream: torch.cuda.Stream | None = None,
 ) -> torch.Tensor:
     """fp32 [N, K] dequantised weights from the GEMV prologue's unpack (test support)."""
+    _check_tensor("qweight", qweight, torch.int32)
+    if qweight.dim() != 2:
+        raise ValueError("qweight must be [N, K/8]")
     N, K8 = qweight.shape
     K = K8 * 8
-    _check_tensor("qweight", qweight, torch.int32)
     if group <= 0 or K % group != 0:
         raise ValueError(f"K={K} must be a multiple of group={group}")
     _check_tensor("scales", scales, torch.bfloat16, (N, K // group))
     if out is None:
         out = torch.empty((N, K), dtype=torch.float32, device=qweight.device)
     _check_tensor("out", out, torch.float32, (N, K))
+    dev = _device_of(qweight, scales, out)
     lib = _lib.load()
-    st = lib.fd_w4_dequant_debug(
-        _ptr(qweight), _ptr(scales), _ptr(out), int(K), int(N), int(group),
-        _stream_handle(stream),
-    )
+    with _on_device(dev):
+        st = lib.fd_w4_dequant_debug(
+            _ptr(qweight), _ptr(scales), _ptr(out), int(K), int(N), int(group),
+            _stream_handle(stream, dev),
+        )
     _lib.check(st)
     return out
 

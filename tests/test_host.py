@@ -208,6 +208,28 @@ def test_binding_rejects_cpu_tensors():
         fd.add_rmsnorm(g, g, g[0], 1e-6)
 
 
+class _FakeCuda:
+    """Stands in for a CUDA tensor or stream in the binding's device checks."""
+
+    def __init__(self, index, is_cuda=True):
+        self.is_cuda = is_cuda
+        self.device = torch.device("cuda", index) if is_cuda else torch.device("cpu")
+        self.cuda_stream = 1234
+
+
+def test_binding_requires_one_device_per_call():
+    from memory_bound_decode_fd_gb300 import kernels
+    a, b, host = _FakeCuda(0), _FakeCuda(1), _FakeCuda(None, is_cuda=False)
+    assert kernels._device_of(a, a, host) == torch.device("cuda", 0)
+    assert kernels._device_of(host, host) is None
+    with pytest.raises(ValueError, match="one device"):
+        kernels._device_of(a, b)
+    # a stream must belong to the tensors' device
+    assert kernels._stream_handle(_FakeCuda(1), torch.device("cuda", 1)).value == 1234
+    with pytest.raises(ValueError, match="stream is on"):
+        kernels._stream_handle(_FakeCuda(0), torch.device("cuda", 1))
+
+
 def test_pack_int4_layout_and_checks():
     q = np.arange(-8, 8, dtype=np.int8).reshape(2, 8)
     w = fd.pack_int4(q).view(np.uint32)
