@@ -3,7 +3,6 @@ for one vector, a ragged count and a decode step's input block, without touching
 bytes around the destination; and under programmatic dependent launch after a kernel
 that writes the source."""
 
-import numpy as np
 import pytest
 import torch
 

@@ -9,7 +9,6 @@ import math
 from pathlib import Path
 
 import numpy as np
-import pytest
 import torch
 
 import oracle

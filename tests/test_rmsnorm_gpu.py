@@ -2,7 +2,6 @@
 
 import gc
 
-import numpy as np
 import pytest
 import torch
 
