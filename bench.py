@@ -65,6 +65,14 @@ KERNEL_SOURCES = {
 
 # ----------------------------------------------------------------------------- helpers
 
+# The arithmetic each GEMV kernel computes in: the M = 1 and CUDA-core kernels encode the
+# activation per 32-k slice as block-scaled int16 and take exact int32 dp2a dot products
+# with the int4 weights; the tensor-core kernel multiplies bf16 operands into fp32.
+DTYPE_DP2A = "int4 weights x block-scaled int16 activations: exact int32 dp2a dots, fp32 sums; bf16 in/out"
+DTYPE_TC = "int4 weights dequantised to bf16 x bf16 activations on tcgen05, fp32 accumulation; bf16 in/out"
+DTYPE_RMSNORM = "bf16 in/out, fp32 arithmetic"
+
+
 def read_peaks():
     p = REPO / "MEASURED_PEAKS.json"
     if p.exists():
@@ -301,7 +309,7 @@ def bench_decode(args, device, rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16 (int4 weights, fp32 accumulation)",
+        "dtype": DTYPE_DP2A + "; add-RMSNorm " + DTYPE_RMSNORM,
         "data": "synthetic (seeded: int4 weights uniform on [-8,7], bf16 scales U[0.005,0.02], activations and residual N(0,1), norm weights N(1,0.1))",
         "config": {
             "workload": "decode_step: 32 x [add-RMSNorm 1x4096 eps 1e-5 + SwiGLU-W4A16 GEMV M=1 K=14336 N=4096 group 128], seed 3",
@@ -537,11 +545,17 @@ def bench_single(args, device, rank, world):
     us_call = ms * 1e3 / n_calls
     k_us = us_call  # the graph holds only this kernel's launches
     gbs = world * nbytes / (us_call * 1e-6) / 1e9
+    if "gemv" not in kname:
+        dtype = DTYPE_RMSNORM
+    elif kind in ("gemv", "batched", "gemv_residual") and fd.gemv_uses_tensor_cores(M, K, N, g):
+        dtype = DTYPE_TC
+    else:
+        dtype = DTYPE_DP2A
     return {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
         "steps": n_calls, "warmup": args.warmup, "ms_per_step": round(us_call / 1e3, 6),
         "us_per_call": round(us_call, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16 (int4 weights, fp32 accumulation)" if "gemv" in kname else "bf16 (fp32 reduction)",
+        "vs_baseline": None, "dtype": dtype,
         "data": "synthetic (seeded)",
         "config": {"workload": f"{args.workload}: {desc}", "bytes_per_call": nbytes,
                    "l2": f"{len(calls)} rotating input sets ({len(calls)} x {nbytes} B vs L2 {l2} B)",
@@ -625,7 +639,7 @@ def bench_fused_layer(args, device, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
         "us_per_step": round(ms_step * 1e3, 3), "us_per_layer": round(ms_step * 1e3 / L, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 (int4 weights, fp32 accumulation)", "data": "synthetic (seeded, drawn on the device)",
+        "dtype": DTYPE_DP2A + "; add-RMSNorm " + DTYPE_RMSNORM, "data": "synthetic (seeded, drawn on the device)",
         "config": {"workload": f"fused_layer: {L} x [add-RMSNorm 1x{hidden} + gate/up GEMV K={hidden} I={inter} "
                                f"+ down GEMV K={inter} N={hidden} with SwiGLU prologue and residual epilogue], seed {seed}",
                    "bytes_per_step": nbytes, "l2": f"{nbytes} B of weights per step vs L2 (defeats it)",
