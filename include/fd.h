@@ -59,7 +59,8 @@ typedef struct CUstream_st *fd_stream_t;
 typedef enum fd_status {
     FD_OK = 0,
     FD_ERR_NULL = 1,        /* a required pointer is NULL */
-    FD_ERR_SHAPE = 2,       /* a size is <= 0 or breaks a divisibility rule */
+    FD_ERR_SHAPE = 2,       /* a size is negative, zero where it may not be, or breaks a
+                               divisibility rule */
     FD_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
     FD_ERR_UNSUPPORTED = 4, /* a size is above the supported maximum */
     FD_ERR_CUDA = 5,        /* the CUDA runtime reported an error */
@@ -84,8 +85,10 @@ typedef enum fd_status {
  *           complement integer in [-8, 7] (symmetric, no zero point).
  * scales    bf16 [N, K/group] row-major; group consecutive k share one scale.
  * out       bf16 [M, N] row-major. Must not overlap any input.
- * Requires  1 <= M <= FD_MAX_M, 32 <= K <= FD_MAX_K, N >= 1, K % 32 == 0,
+ * Requires  0 <= M <= FD_MAX_M, 32 <= K <= FD_MAX_K, N >= 0, K % 32 == 0,
  *           group % 32 == 0, K % group == 0.
+ * Empty     M == 0 or N == 0 (with valid K and group) returns FD_OK at once: no
+ *           pointer is read (any may be NULL) and nothing is launched.
  * The silu/mul intermediate and the dequantised weights are kept on chip; the kernel
  * reads each packed weight word from HBM once per call.
  */
@@ -128,8 +131,9 @@ int fd_swiglu_w4a16_gemv_residual(const void *gate, const void *up, const void *
  *            projection's I rows, each in the nibble layout of fd_swiglu_w4a16_gemv.
  * scales     bf16 [2I, K/group].
  * gate_out, up_out  bf16 [M, I] row-major; they may not overlap each other or an input.
- * Requires   1 <= M <= FD_MAX_M, 32 <= K <= FD_MAX_K, I >= 1, K % 32 == 0,
- *            group % 32 == 0, K % group == 0.
+ * Requires   0 <= M <= FD_MAX_M, 32 <= K <= FD_MAX_K, I >= 0, K % 32 == 0,
+ *            group % 32 == 0, K % group == 0. M == 0 or I == 0 is an empty call:
+ *            FD_OK at once, no pointer read, nothing launched.
  * gate_out and up_out are the gate and up inputs of fd_swiglu_w4a16_gemv(_residual): the
  * two calls are the whole MLP, and silu(g) * u exists only in the second kernel's
  * registers. x is encoded per 32-k slice like the SwiGLU activation (block-scaled int16).
@@ -153,8 +157,9 @@ int fd_w4a16_gate_up_gemv(const void *x, const void *qweight, const void *scales
  * out, residual_out   bf16 [rows, hidden] row-major.
  * Aliasing            residual_out == residual and/or out == x (exactly the same pointer)
  *                     are allowed; any other overlap returns FD_ERR_OVERLAP.
- * Requires            rows >= 1, 8 <= hidden <= FD_MAX_HIDDEN, hidden % 8 == 0,
- *                     eps >= 0 and finite.
+ * Requires            rows >= 0, 8 <= hidden <= FD_MAX_HIDDEN, hidden % 8 == 0,
+ *                     eps >= 0 and finite. rows == 0 is an empty call: FD_OK at once,
+ *                     no pointer read, nothing launched.
  * Reads 4 bytes and writes 4 bytes per element (plus the weight row once per CTA).
  */
 int fd_add_rmsnorm(const void *x, const void *residual, const void *weight, float eps,
@@ -213,7 +218,8 @@ unsigned fd_get_launch_flags(void);
 /*
  * fd_w4_dequant_debug - write the dequantised weights W[n, k] = q[n, k] * s[n, k/group]
  * as fp32 [N, K] (test support: the unpack and scale of the GEMV prologue, checked bit
- * for bit). Same layouts and size rules as fd_swiglu_w4a16_gemv; `out` is fp32 [N, K].
+ * for bit). Same layouts and size rules as fd_swiglu_w4a16_gemv (N == 0 is empty);
+ * `out` is fp32 [N, K].
  */
 int fd_w4_dequant_debug(const void *qweight, const void *scales, float *out, int K, int N,
                         int group, fd_stream_t stream);
@@ -227,7 +233,8 @@ const char *fd_status_string(int status);
  * pinned host memory (cudaHostAlloc / torch pin_memory), which a GB300 reads and writes
  * over NVLink-C2C. When a side is not accessible to a kernel (pageable host memory) the
  * call falls back to one cudaMemcpyAsync.
- * Requires  dst, src 16-byte aligned; bytes > 0 and a multiple of 16; no overlap.
+ * Requires  dst, src 16-byte aligned; bytes a multiple of 16; no overlap. bytes == 0
+ *           returns FD_OK at once (no pointer read, nothing launched).
  * Stream-ordered like every call here; with programmatic dependent launch the kernel
  * waits for the previous kernel before it reads src.
  */

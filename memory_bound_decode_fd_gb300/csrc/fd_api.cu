@@ -41,6 +41,16 @@ int from_cuda(cudaError_t err) {
     return FD_ERR_CUDA;
 }
 
+// Sizes of a W4 GEMV call apart from its pointers: FD_OK, an error, or kEmpty when there is
+// nothing to compute (M == 0 or N == 0), in which case no pointer is read.
+constexpr int kEmpty = -1;
+int check_w4_sizes(int M, int K, int N, int group) {
+    if (M < 0 || N < 0 || K <= 0 || group <= 0) return FD_ERR_SHAPE;
+    if (K % 32 != 0 || group % 32 != 0 || K % group != 0) return FD_ERR_SHAPE;
+    if (K > FD_MAX_K || M > FD_MAX_M) return FD_ERR_UNSUPPORTED;
+    return (M == 0 || N == 0) ? kEmpty : FD_OK;
+}
+
 int check_w4_layout(const void *qweight, const void *scales, int K, int N, int group) {
     if (!qweight || !scales) return FD_ERR_NULL;
     if (K <= 0 || N <= 0 || group <= 0) return FD_ERR_SHAPE;
@@ -93,11 +103,12 @@ namespace {
 int swiglu_gemv(const void *gate, const void *up, const void *qweight, const void *scales,
                 const void *residual, void *out, int M, int K, int N, int group,
                 fd_stream_t stream) {
+    const int sz = check_w4_sizes(M, K, N, group);
+    if (sz == kEmpty) return FD_OK;
     if (!gate || !up || !out) return FD_ERR_NULL;
+    if (sz != FD_OK) return sz;
     int st = check_w4_layout(qweight, scales, K, N, group);
     if (st != FD_OK) return st;
-    if (M <= 0) return FD_ERR_SHAPE;
-    if (M > FD_MAX_M) return FD_ERR_UNSUPPORTED;
     if (!aligned16(gate) || !aligned16(up) || !aligned16(out)) return FD_ERR_ALIGN;
     if (residual && !aligned16(residual)) return FD_ERR_ALIGN;
     const size_t act_bytes = (size_t)M * K * 2;
@@ -148,6 +159,7 @@ int fd_swiglu_w4a16_gemv(const void *gate, const void *up, const void *qweight,
 int fd_swiglu_w4a16_gemv_residual(const void *gate, const void *up, const void *qweight,
                                   const void *scales, const void *residual, void *out, int M,
                                   int K, int N, int group, fd_stream_t stream) {
+    if (check_w4_sizes(M, K, N, group) == kEmpty) return FD_OK;
     if (!residual) return FD_ERR_NULL;
     return swiglu_gemv(gate, up, qweight, scales, residual, out, M, K, N, group, stream);
 }
@@ -155,14 +167,15 @@ int fd_swiglu_w4a16_gemv_residual(const void *gate, const void *up, const void *
 int fd_w4a16_gate_up_gemv(const void *x, const void *qweight, const void *scales,
                           void *gate_out, void *up_out, int M, int K, int I, int group,
                           fd_stream_t stream) {
-    if (!x || !gate_out || !up_out) return FD_ERR_NULL;
-    if (I <= 0) return FD_ERR_SHAPE;
+    if (I < 0) return FD_ERR_SHAPE;
     if (I > (INT32_MAX - 1) / 2) return FD_ERR_UNSUPPORTED;
     const int N = 2 * I;  // gate rows, then up rows
+    const int sz = check_w4_sizes(M, K, N, group);
+    if (sz == kEmpty) return FD_OK;
+    if (!x || !gate_out || !up_out) return FD_ERR_NULL;
+    if (sz != FD_OK) return sz;
     int st = check_w4_layout(qweight, scales, K, N, group);
     if (st != FD_OK) return st;
-    if (M <= 0) return FD_ERR_SHAPE;
-    if (M > FD_MAX_M) return FD_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(gate_out) || !aligned16(up_out)) return FD_ERR_ALIGN;
     const size_t x_bytes = (size_t)M * K * 2;
     const size_t o_bytes = (size_t)M * I * 2;
@@ -188,8 +201,9 @@ int fd_w4a16_gate_up_gemv(const void *x, const void *qweight, const void *scales
 }
 
 int fd_copy(void *dst, const void *src, size_t bytes, fd_stream_t stream) {
+    if (bytes == 0) return FD_OK;  // empty: nothing read or written
     if (!dst || !src) return FD_ERR_NULL;
-    if (bytes == 0 || bytes % 16 != 0) return FD_ERR_SHAPE;
+    if (bytes % 16 != 0) return FD_ERR_SHAPE;
     if (!aligned16(dst) || !aligned16(src)) return FD_ERR_ALIGN;
     if (overlaps(dst, bytes, src, bytes)) return FD_ERR_OVERLAP;
     if (fake_launch_failure()) return from_cuda(cudaErrorLaunchOutOfResources);
@@ -238,10 +252,11 @@ unsigned fd_get_launch_flags(void) { return g_launch_flags.load(std::memory_orde
 
 int fd_add_rmsnorm(const void *x, const void *residual, const void *weight, float eps,
                    void *out, void *residual_out, int rows, int hidden, fd_stream_t stream) {
-    if (!x || !residual || !weight || !out || !residual_out) return FD_ERR_NULL;
-    if (rows <= 0 || hidden <= 0 || hidden % 8 != 0 || hidden < 8) return FD_ERR_SHAPE;
+    if (rows < 0 || hidden <= 0 || hidden % 8 != 0) return FD_ERR_SHAPE;
     if (!(eps >= 0.0f) || !std::isfinite(eps)) return FD_ERR_SHAPE;
     if (hidden > FD_MAX_HIDDEN) return FD_ERR_UNSUPPORTED;
+    if (rows == 0) return FD_OK;  // empty: nothing read or written
+    if (!x || !residual || !weight || !out || !residual_out) return FD_ERR_NULL;
     if (!aligned16(x) || !aligned16(residual) || !aligned16(weight) || !aligned16(out) ||
         !aligned16(residual_out))
         return FD_ERR_ALIGN;
@@ -266,7 +281,10 @@ int fd_add_rmsnorm(const void *x, const void *residual, const void *weight, floa
 
 int fd_w4_dequant_debug(const void *qweight, const void *scales, float *out, int K, int N,
                         int group, fd_stream_t stream) {
+    const int sz = check_w4_sizes(1, K, N, group);
+    if (sz == kEmpty) return FD_OK;
     if (!out) return FD_ERR_NULL;
+    if (sz != FD_OK) return sz;
     int st = check_w4_layout(qweight, scales, K, N, group);
     if (st != FD_OK) return st;
     if (!aligned16(out)) return FD_ERR_ALIGN;

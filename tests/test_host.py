@@ -73,14 +73,14 @@ def gemv(lib, gate=A, up=B, qw=C, sc=D, out=E, M=1, K=1024, N=256, group=128):
     (dict(qw=None), _lib.FD_ERR_NULL),
     (dict(sc=None), _lib.FD_ERR_NULL),
     (dict(out=None), _lib.FD_ERR_NULL),
-    (dict(M=0), _lib.FD_ERR_SHAPE),
     (dict(M=-1), _lib.FD_ERR_SHAPE),
+    (dict(N=-1), _lib.FD_ERR_SHAPE),
+    (dict(M=0, K=1000), _lib.FD_ERR_SHAPE),    # an empty call still has valid sizes
     (dict(K=0), _lib.FD_ERR_SHAPE),
     (dict(K=1000), _lib.FD_ERR_SHAPE),
     (dict(K=1024, group=48), _lib.FD_ERR_SHAPE),
     (dict(K=1056, group=128), _lib.FD_ERR_SHAPE),
     (dict(group=0), _lib.FD_ERR_SHAPE),
-    (dict(N=0), _lib.FD_ERR_SHAPE),
     (dict(M=257), _lib.FD_ERR_UNSUPPORTED),
     (dict(K=32768 + 128), _lib.FD_ERR_UNSUPPORTED),
     (dict(gate=A + 2), _lib.FD_ERR_ALIGN),
@@ -103,7 +103,7 @@ def gemv_res(lib, gate=A, up=B, qw=C, sc=D, res=F, out=E, M=1, K=1024, N=256, gr
 @pytest.mark.parametrize("kw,status", [
     (dict(res=None), _lib.FD_ERR_NULL),
     (dict(gate=None), _lib.FD_ERR_NULL),
-    (dict(M=0), _lib.FD_ERR_SHAPE),
+    (dict(M=-1), _lib.FD_ERR_SHAPE),
     (dict(K=1000), _lib.FD_ERR_SHAPE),
     (dict(M=257), _lib.FD_ERR_UNSUPPORTED),
     (dict(res=F + 2), _lib.FD_ERR_ALIGN),
@@ -127,8 +127,8 @@ def gate_up(lib, x=A, qw=C, sc=D, g=E, u=F, M=1, K=1024, I=128, group=128):
     (dict(g=None), _lib.FD_ERR_NULL),
     (dict(u=None), _lib.FD_ERR_NULL),
     (dict(qw=None), _lib.FD_ERR_NULL),
-    (dict(I=0), _lib.FD_ERR_SHAPE),
-    (dict(M=0), _lib.FD_ERR_SHAPE),
+    (dict(I=-1), _lib.FD_ERR_SHAPE),
+    (dict(M=-1), _lib.FD_ERR_SHAPE),
     (dict(K=1000), _lib.FD_ERR_SHAPE),
     (dict(group=48), _lib.FD_ERR_SHAPE),
     (dict(M=257), _lib.FD_ERR_UNSUPPORTED),
@@ -147,7 +147,6 @@ def test_gate_up_rejects_bad_arguments_without_launching(fdlib, kw, status):
 @pytest.mark.parametrize("args,status", [
     ((None, B, 1024), _lib.FD_ERR_NULL),
     ((A, None, 1024), _lib.FD_ERR_NULL),
-    ((A, B, 0), _lib.FD_ERR_SHAPE),
     ((A, B, 1000), _lib.FD_ERR_SHAPE),
     ((A + 8, B, 1024), _lib.FD_ERR_ALIGN),
     ((A, B + 4, 1024), _lib.FD_ERR_ALIGN),
@@ -165,7 +164,8 @@ def rms(lib, x=A, r=B, w=C, eps=1e-6, out=D, rout=E, rows=4, hidden=4096):
     (dict(x=None), _lib.FD_ERR_NULL),
     (dict(w=None), _lib.FD_ERR_NULL),
     (dict(rout=None), _lib.FD_ERR_NULL),
-    (dict(rows=0), _lib.FD_ERR_SHAPE),
+    (dict(rows=-1), _lib.FD_ERR_SHAPE),
+    (dict(rows=0, hidden=12), _lib.FD_ERR_SHAPE),
     (dict(hidden=12), _lib.FD_ERR_SHAPE),
     (dict(hidden=0), _lib.FD_ERR_SHAPE),
     (dict(eps=-1e-6), _lib.FD_ERR_SHAPE),
@@ -183,6 +183,19 @@ def rms(lib, x=A, r=B, w=C, eps=1e-6, out=D, rout=E, rows=4, hidden=4096):
 ])
 def test_rmsnorm_rejects_bad_arguments_without_launching(fdlib, kw, status):
     assert rms(fdlib, **kw) == status
+
+
+def test_empty_calls_return_ok_without_reading_pointers(fdlib):
+    # nothing to compute: FD_OK at once, NULL pointers never read, nothing launched
+    N0 = None
+    assert gemv(fdlib, gate=N0, up=N0, qw=N0, sc=N0, out=N0, M=0) == _lib.FD_OK
+    assert gemv(fdlib, gate=N0, up=N0, qw=N0, sc=N0, out=N0, N=0) == _lib.FD_OK
+    assert gemv_res(fdlib, gate=N0, up=N0, qw=N0, sc=N0, res=N0, out=N0, M=0) == _lib.FD_OK
+    assert gate_up(fdlib, x=N0, qw=N0, sc=N0, g=N0, u=N0, M=0) == _lib.FD_OK
+    assert gate_up(fdlib, x=N0, qw=N0, sc=N0, g=N0, u=N0, I=0) == _lib.FD_OK
+    assert fdlib.fd_copy(N0, N0, 0, None) == _lib.FD_OK
+    assert rms(fdlib, x=N0, r=N0, w=N0, out=N0, rout=N0, rows=0) == _lib.FD_OK
+    assert fdlib.fd_w4_dequant_debug(N0, N0, N0, 1024, 0, 128, None) == _lib.FD_OK
 
 
 def test_dequant_debug_rejects_bad_arguments(fdlib):
