@@ -95,3 +95,43 @@ def test_plan_invariants(fdlib, M, K, N, plain, regs):
         assert p["act_first_stage"] * R * w_row <= p["w_rows"] * w_row - act
         if p["ring"]:
             assert p["act_first_stage"] >= (3 if c > 1 else 2)
+
+
+def producer_schedule(p, M, N, MB, R):
+    """The bulk-copy kernel's producer, replayed on the host: for every CTA, the chunks it
+    issues in order, as (chunk index, stage, first row, rows)."""
+    for b in range(p["grid"]):
+        n_begin = b * p["rows_base"] + min(b, p["rows_extra"])
+        n_cnt = p["rows_base"] + (1 if b < p["rows_extra"] else 0)
+        n_chunks = -(-n_cnt // R)
+        total = n_chunks * -(-M // MB)
+        ps = pnc = 0
+        for c in range(total):
+            yield b, c, ps, n_begin + pnc * R, min(R, n_cnt - pnc * R), total
+            ps = (ps + 1) % p["S"]
+            pnc = (pnc + 1) % n_chunks
+
+
+@pytest.mark.parametrize("M,K,N,plain,regs", SWEEP)
+def test_producer_copies_stay_in_bounds(fdlib, M, K, N, plain, regs):
+    group, R = 128, 8
+    sms, optin, per_sm_smem, reserved, static, _ = GB300
+    st, p = plan(fdlib, M, K, N, group, plain, (sms, optin, per_sm_smem, reserved, static, regs))
+    if st != 0:
+        return
+    MB = 1 if M == 1 else 2
+    w_row = K // 2
+    act = K * (2 if plain else 4)
+    owned = [0] * N
+    for b, c, stage, n0, rows, total in producer_schedule(p, M, N, MB, R):
+        assert rows >= 1 and 0 <= n0 and n0 + rows <= N            # global rows in range
+        assert stage * R + rows <= p["w_rows"]                      # inside the weight rows
+        if M == 1 and c < p["act_first_stage"]:
+            # filled before the consumers have read the activation: clear of its bytes
+            assert (stage * R + rows) * w_row <= p["w_rows"] * w_row - act
+        if not p["ring"]:
+            assert total <= p["S"]                                  # no stage is reused
+        if c < -(-(p["rows_base"] + (b < p["rows_extra"])) // R):   # first activation pass
+            for n in range(n0, n0 + rows):
+                owned[n] += 1
+    assert owned == [1] * N                                         # every row streamed once per pass
