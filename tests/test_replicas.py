@@ -34,7 +34,7 @@ def _rank_main(rank, world, port, out):
 def test_two_rank_max_and_job_throughput():
     world = 2
     port = _free_port()
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()  # no fork of this multi-threaded process
     out = manager.dict()
     mp.start_processes(_rank_main, args=(world, port, out), nprocs=world, join=True,
                        start_method="spawn")
