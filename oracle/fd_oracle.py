@@ -44,6 +44,7 @@ __all__ = [
     "swiglu_activation",
     "unpack_int4",
     "dequant_w4",
+    "contract",
     "swiglu_w4a16_gemv",
     "swiglu_w4a16_gemv_residual",
     "w4a16_gemv",
@@ -156,14 +157,32 @@ def dequant_w4(qweight, scale_bits, group: int) -> np.ndarray:
     return w.astype(np.float32)
 
 
+def contract(a, w) -> np.ndarray:
+    """y[m, n] = sum_k a[m, k] * w[n, k] in float64, one output at a time.
+
+    The matrix product of an nn.Linear layer (out = x @ W^T, [FIX] "Reproduction and
+    analysis") written as the plain loop over outputs (m, n); only the innermost sum over
+    k is one vectorised float64 dot product. No blocking or reordering beyond that.
+    """
+    a = np.asarray(a, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    if a.ndim != 2 or w.ndim != 2 or a.shape[1] != w.shape[1]:
+        raise ValueError("contract: a is [M, K] and w is [N, K]")
+    y = np.empty((a.shape[0], w.shape[0]), dtype=np.float64)
+    for m in range(a.shape[0]):
+        for n in range(w.shape[0]):
+            y[m, n] = np.dot(a[m], w[n])
+    return y
+
+
 def swiglu_w4a16_gemv(gate_bits, up_bits, qweight, scale_bits, group: int) -> np.ndarray:
     """y[m, n] = sum_k a[m, k] * W[n, k] with a = silu(g) * u, as float64 [M, N].
 
     Unfused on purpose: the activation, the dequantised weight matrix and the product
     are each formed in full before the next step. [FIX] "Reproduction and analysis"
     (single-row matmul y = x @ W with a SwiGLU pre-operation and int4 weights);
-    [FUSE] "The fusion boundary problem" (out = act @ W_down). The contraction uses a
-    float64 library matmul.
+    [FUSE] "The fusion boundary problem" (out = act @ W_down). The contraction is the
+    plain per-output sum of ``contract``.
     """
     a = swiglu_activation(gate_bits, up_bits)
     if a.ndim == 1:
@@ -171,7 +190,7 @@ def swiglu_w4a16_gemv(gate_bits, up_bits, qweight, scale_bits, group: int) -> np
     w = dequant_w4(qweight, scale_bits, group).astype(np.float64)
     if a.shape[1] != w.shape[1]:
         raise ValueError("gate/up K does not match the weights")
-    return a @ w.T
+    return contract(a, w)
 
 
 def swiglu_w4a16_gemv_residual(gate_bits, up_bits, qweight, scale_bits, residual_bits,
@@ -204,8 +223,8 @@ def w4a16_gemv(x_bits, qweight, scale_bits, group: int) -> np.ndarray:
     """y[m, n] = sum_k x[m, k] * W[n, k] as float64 [M, N], x a plain bf16 activation.
 
     [FUSE] "The taxonomy of fusions", item 4 (dequantise the int4 weights, then the
-    matmul) with no pre-operation on the activation. Unfused: W is formed in full, then a
-    float64 library matmul.
+    matmul) with no pre-operation on the activation. Unfused: W is formed in full, then
+    the plain per-output sum of ``contract``.
     """
     x = bf16_to_f32(np.asarray(x_bits, dtype=np.uint16)).astype(np.float64)
     if x.ndim == 1:
@@ -213,7 +232,7 @@ def w4a16_gemv(x_bits, qweight, scale_bits, group: int) -> np.ndarray:
     w = dequant_w4(qweight, scale_bits, group).astype(np.float64)
     if x.shape[1] != w.shape[1]:
         raise ValueError("x K does not match the weights")
-    return x @ w.T
+    return contract(x, w)
 
 
 def gate_up_gemv(x_bits, qweight, scale_bits, group: int):
@@ -370,7 +389,8 @@ def nvfp4_scaled_mm(x_packed, x_sf, w_packed, w_sf, alpha):
     [NVFP4] body: the scaled matmul of two packed-FP4 operands with E4M3 1x16 block
     scales, and the zero-dimensional fp32 output multiplier alpha that the fold applies
     inside the GEMM instead of in a separate multiplication. Unfused here: both operands
-    are dequantised in full, then a float64 library matmul, then the multiplication.
+    are dequantised in full, then the plain per-output sum of ``contract``, then the
+    multiplication.
 
     Returns ``(ref, eager_bits)``:
       * ``ref``        float64 [M, N], alpha * the sum, nothing rounded;
@@ -383,7 +403,7 @@ def nvfp4_scaled_mm(x_packed, x_sf, w_packed, w_sf, alpha):
     if x.shape[1] != w.shape[1]:
         raise ValueError("activation K does not match the weights")
     a32 = np.float32(alpha)
-    acc = x @ w.T
+    acc = contract(x, w)
     ref = float(a32) * acc
     mm_bits = f32_to_bf16_rne(acc.astype(np.float32))
     eager_bits = f32_to_bf16_rne(bf16_to_f32(mm_bits) * a32)  # float32 multiply, IEEE RNE

@@ -9,6 +9,7 @@ import math
 from pathlib import Path
 
 import numpy as np
+import pytest
 import torch
 
 import oracle
@@ -434,6 +435,161 @@ def test_decode_step_zero_weights_pass_residual_through():
     assert np.array_equal(rec[1][0], h1)  # x_1 = 0, so h_2 = h_1
     assert np.all(rec[0][3] == 0) and np.all(oracle.bf16_to_f32(x_last) == 0)
     assert np.array_equal(res, h1)
+
+
+def _torch_bf16(v: float) -> float:
+    """A float rounded to bf16 by torch (independent of the oracle's rounding)."""
+    return float(torch.tensor(v, dtype=torch.float32).to(torch.bfloat16).float())
+
+
+def _torch_bf16_bits(v) -> np.ndarray:
+    t = torch.as_tensor(np.asarray(v, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+# The two-layer chain of the pin below (hidden 64, MLP width 128, group 32, eps 1e-5):
+#   x0 = r0 = 0.5 everywhere, so h1 = 1.0 everywhere;
+#   layer 1: rms_weight 1.0; gate 1, up 2, one int4 weight q = -8 at (n1, k1) with scale
+#            3/32: y1[n1] = silu(1) * 2 * (-8) * 3/32, every other output 0;
+#   x1 = bf16(y1): bf16(y1[n1]) = -1.09375, so h2 = bf16(-1.09375 + 1.0) = -0.09375 at
+#            n1 (with x1 left unrounded the same add gives -0.0966796875) and 1.0 elsewhere;
+#   layer 2: rms_weight 0.5; gate -1, up 1, one weight q = 5 at (n2, k2) with scale 1/4:
+#            y2[n2] = silu(-1) * 5 / 4.
+PIN_HIDDEN, PIN_INTER, PIN_GROUP, PIN_EPS = 64, 128, 32, 1e-5
+PIN_N1, PIN_K1, PIN_N2, PIN_K2 = 17, 37, 40, 100
+SIGMOID_1 = 0.7310585786300049  # 1 / (1 + e^-1), published value (also in the GEMV pins)
+
+
+def _pin_layers():
+    def one_hot(n, k, q, s):
+        qq = np.zeros((PIN_HIDDEN, PIN_INTER), np.int8)
+        qq[n, k] = q
+        ss = np.full((PIN_HIDDEN, PIN_INTER // PIN_GROUP), 0.5)
+        ss[n, k // PIN_GROUP] = s
+        return pack_int4(qq), inputs.to_bf16_bits(ss)
+
+    q1, s1 = one_hot(PIN_N1, PIN_K1, -8, 3 / 32)
+    q2, s2 = one_hot(PIN_N2, PIN_K2, 5, 0.25)
+    full = lambda v, shape: inputs.to_bf16_bits(np.full(shape, v))  # noqa: E731
+    return [
+        {"rms_weight": full(1.0, (PIN_HIDDEN,)), "gate": full(1.0, (1, PIN_INTER)),
+         "up": full(2.0, (1, PIN_INTER)), "qweight": q1, "scales": s1},
+        {"rms_weight": full(0.5, (PIN_HIDDEN,)), "gate": full(-1.0, (1, PIN_INTER)),
+         "up": full(1.0, (1, PIN_INTER)), "qweight": q2, "scales": s2},
+    ]
+
+
+def _check_two_layer_pin(step_fn):
+    """Run `step_fn` (decode_mlp_step or a planted mutant) on the two-layer chain and
+    assert every field of every layer against the values worked out by hand above."""
+    H = PIN_HIDDEN
+    x0 = inputs.to_bf16_bits(np.full((1, H), 0.5))
+    r0 = inputs.to_bf16_bits(np.full((1, H), 0.5))
+    rec, x_last, res = step_fn(x0, r0, _pin_layers(), PIN_EPS, PIN_GROUP)
+    assert len(rec) == 2
+
+    # layer 1: h = 1 everywhere; unit mean square; weight 1
+    y1 = SIGMOID_1 * 2.0 * -8 * (3 / 32)
+    rstd1 = 1.0 / math.sqrt(1.0 + PIN_EPS)
+    h1 = np.full((1, H), 1.0)
+    assert np.array_equal(rec[0][0], _torch_bf16_bits(h1))
+    np.testing.assert_allclose(rec[0][1], np.full((1, H), rstd1), rtol=1e-14)
+    assert np.array_equal(rec[0][2], _torch_bf16_bits(np.full((1, H), _torch_bf16(_torch_bf16(rstd1) * 1.0))))
+    y1_ref = np.zeros((1, H))
+    y1_ref[0, PIN_N1] = y1
+    np.testing.assert_allclose(rec[0][3], y1_ref, rtol=1e-15, atol=0)
+
+    # layer 2: x1 = bf16(y1) joins the residual h1
+    x1_hot = _torch_bf16(y1)
+    assert x1_hot == -1.09375
+    h2_hot = _torch_bf16(x1_hot + 1.0)
+    assert h2_hot == -0.09375
+    h2 = np.full((1, H), 1.0)
+    h2[0, PIN_N1] = h2_hot
+    ms2 = ((H - 1) * 1.0 + h2_hot * h2_hot) / H
+    rstd2 = 1.0 / math.sqrt(ms2 + PIN_EPS)
+    assert np.array_equal(rec[1][0], _torch_bf16_bits(h2))
+    np.testing.assert_allclose(rec[1][1], h2 * rstd2 * 0.5, rtol=1e-14)
+    eager2 = np.array([[_torch_bf16(_torch_bf16(v * rstd2) * 0.5) for v in h2[0]]])
+    assert np.array_equal(rec[1][2], _torch_bf16_bits(eager2))
+    y2 = -(1.0 - SIGMOID_1) * 5 * 0.25  # silu(-1) = -sigmoid(-1) = -(1 - sigmoid(1))
+    y2_ref = np.zeros((1, H))
+    y2_ref[0, PIN_N2] = y2
+    np.testing.assert_allclose(rec[1][3], y2_ref, rtol=1e-14, atol=0)
+
+    # after the chain: x_2 = bf16(y2), the residual stream is h2
+    x2 = np.zeros((1, H))
+    x2[0, PIN_N2] = _torch_bf16(y2)
+    assert np.array_equal(np.asarray(x_last).reshape(1, H), _torch_bf16_bits(x2))
+    assert np.array_equal(np.asarray(res).reshape(1, H), _torch_bf16_bits(h2))
+
+
+def test_decode_step_two_layer_closed_form():
+    # Every field of every layer's record, the handed-on x and the final residual.
+    # [FUSE] "The fusion boundary problem" (add_rmsnorm writes the residual and the
+    # normalised row; the down projection's output joins the stream at the next add);
+    # [KFM] Step 2 (h rounded to bf16, then normalised; two roundings of the output).
+    _check_two_layer_pin(oracle.decode_mlp_step)
+
+
+def _mutant_step(slip):
+    """decode_mlp_step with one planted mistake, built from the oracle's own pieces."""
+    def step(x_bits, residual_bits, layers, eps, group):
+        x = np.asarray(x_bits, dtype=np.uint16)
+        xf = None  # the unrounded x of the "unrounded x_next" slip
+        res = np.asarray(residual_bits, dtype=np.uint16)
+        record = []
+        for i, layer in enumerate(layers):
+            w = layers[(i + 1) % len(layers)]["rms_weight"] if slip == "wrong_weight" else layer["rms_weight"]
+            if xf is not None:
+                h_bits = oracle.f32_to_bf16_rne(xf + oracle.bf16_to_f32(res))
+                _, y_norm, y_eager = oracle.add_rmsnorm(np.zeros_like(res), h_bits, w, eps)
+            else:
+                h_bits, y_norm, y_eager = oracle.add_rmsnorm(x, res, w, eps)
+            if slip == "no_rstd":
+                y_norm = oracle.bf16_to_f32(h_bits).astype(np.float64) * oracle.bf16_to_f32(w)
+            y = oracle.swiglu_w4a16_gemv(layer["gate"], layer["up"], layer["qweight"], layer["scales"], group)
+            record.append((h_bits, y_norm, y_eager, y))
+            y_bits = oracle.f32_to_bf16_rne(y.astype(np.float32)).reshape(x.shape)
+            if slip == "swap_roles":
+                res, x = y_bits, h_bits
+            else:
+                res, x = h_bits, y_bits
+            if slip == "unrounded_x":
+                xf = y.astype(np.float32).reshape(x.shape)
+        return record, x, res
+    return step
+
+
+@pytest.mark.parametrize("slip", ["wrong_weight", "unrounded_x", "swap_roles", "no_rstd"])
+def test_decode_step_pin_catches_planted_slips(slip):
+    # Each plausible mistake in the chain (the next layer's norm weight, x handed on
+    # without its bf16 rounding, residual and x exchanged, the rstd factor dropped) fails
+    # the closed-form pin.
+    with pytest.raises(AssertionError):
+        _check_two_layer_pin(_mutant_step(slip))
+
+
+def test_decode_step_pin_mutant_harness_is_faithful():
+    # With no slip planted the mutant harness passes the pin, so the failures above come
+    # from the planted mistakes alone.
+    _check_two_layer_pin(_mutant_step(None))
+
+
+def test_contract_is_the_plain_triple_loop():
+    rng = np.random.default_rng(77)
+    a = rng.normal(size=(3, 20))
+    w = rng.normal(size=(5, 20))
+    ref = np.zeros((3, 5))
+    for m in range(3):
+        for n in range(5):
+            acc = 0.0
+            for k in range(20):
+                acc += float(a[m, k]) * float(w[n, k])
+            ref[m, n] = acc
+    np.testing.assert_allclose(oracle.contract(a, w), ref, rtol=1e-13, atol=1e-13)
+    t = torch.nn.functional.linear(torch.from_numpy(a), torch.from_numpy(w)).numpy()
+    np.testing.assert_allclose(oracle.contract(a, w), t, rtol=1e-13, atol=1e-13)
 
 
 # ------------------------------------------------------------------------------ NVFP4
