@@ -77,18 +77,48 @@ def test_decode_step_32_layers_matches_oracle_chain(cuda_device, step_data, orac
     stated_bar(bf16_f64(res_final), bf16_f64(res_ref))
 
 
-def test_decode_step_first_layer_is_exact_where_inputs_are_shared(cuda_device, step_data):
-    # Layer 0 sees exactly the oracle's inputs: residual_out bit-exact, normed within one
-    # bf16 step, GEMV within the derived bound.
+@pytest.fixture(scope="module")
+def eager_layers(cuda_device, step_data):
+    """The chain run layer by layer through the C ABI, with every layer's own inputs
+    kept: (x_l, residual before, normed_l, residual after, y_l) as host bits."""
     d = step_data
-    normed, ys, _ = run_step(d, graph=False)
-    L0 = d["layers"][0]
-    x, r, w = dev_bf16(d["x"]), dev_bf16(d["residual"]), dev_bf16(L0["rms_weight"])
-    y, h = fd.add_rmsnorm(x, r, w, EPS)
-    torch.cuda.synchronize()
-    check_add_rmsnorm(host_bits(y), host_bits(h), d["x"], d["residual"], L0["rms_weight"], EPS)
-    assert np.array_equal(host_bits(y), normed[0])
-    check_gemv(ys[0], L0["gate"], L0["up"], L0["qweight"], L0["scales"], d["group"])
+    layers = device_layers(d)
+    x = dev_bf16(d["x"])
+    res = dev_bf16(d["residual"])
+    rec = []
+    for L in layers:
+        x_in, res_in = host_bits(x), host_bits(res)
+        normed, _ = fd.add_rmsnorm(x, res, L["rms_weight"], EPS, residual_out=res)
+        y = fd.swiglu_w4a16_gemv(L["gate"], L["up"], L["qweight"], L["scales"], group=d["group"])
+        torch.cuda.synchronize()
+        rec.append((x_in, res_in, host_bits(normed), host_bits(res), host_bits(y)))
+        x = y
+    return rec
+
+
+def test_decode_step_every_layer_exact_on_its_own_inputs(cuda_device, step_data, eager_layers):
+    # Each layer checked against the oracle on the bf16 x and residual the GPU handed it:
+    # residual_out bit-exact, the normalised row within the add-RMSNorm element bound, and
+    # every GEMV output within the GEMV's derived element-wise bound.
+    d = step_data
+    for l, (x_in, res_in, normed, res_out, y) in enumerate(eager_layers):
+        L = d["layers"][l]
+        check_add_rmsnorm(normed, res_out, x_in, res_in, L["rms_weight"], EPS)
+        res = check_gemv(y, L["gate"], L["up"], L["qweight"], L["scales"], d["group"])
+        assert res["n_checked"] == d["hidden"]
+    # the chain's links: layer l + 1 starts from layer l's y and residual
+    for a, b in zip(eager_layers, eager_layers[1:]):
+        assert np.array_equal(b[0], a[4]) and np.array_equal(b[1], a[3])
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_decode_step_equals_the_per_layer_checked_chain(cuda_device, step_data, eager_layers, graph):
+    # decode_mlp_step (eager, and captured in a CUDA graph) reproduces, bit for bit, the
+    # layer-by-layer chain whose every layer is checked above.
+    normed, ys, res_final = run_step(step_data, graph)
+    for l, rec in enumerate(eager_layers):
+        assert np.array_equal(normed[l], rec[2]) and np.array_equal(ys[l], rec[4])
+    assert np.array_equal(res_final, eager_layers[-1][3])
 
 
 def test_decode_step_graph_and_eager_agree_bitwise(cuda_device, step_data):
@@ -141,10 +171,11 @@ def test_pdl_flag_roundtrip(cuda_device):
 
 
 @pytest.mark.parametrize("captured", [False, True])
-def test_decode_step_pinned_io_matches_call(cuda_device, step_data, captured):
-    # One host->device and one device->host copy per step (StepIO) give the same outputs
-    # as the four-input __call__ path, for two consecutive tokens (the new residual is the
-    # next token's input residual).
+def test_decode_step_pinned_io_matches_call(cuda_device, step_data, oracle_chain, eager_layers, captured):
+    # One host->device and one device->host copy per step (StepIO, the end-to-end path the
+    # benchmark times) give the same outputs as the four-input __call__ path, for two
+    # consecutive tokens (the new residual is the next token's input residual); the first
+    # token's host outputs are checked against the oracle.
     from memory_bound_decode_fd_gb300.step import DecodeStep
 
     d = step_data
@@ -171,12 +202,22 @@ def test_decode_step_pinned_io_matches_call(cuda_device, step_data, captured):
     io.residual.copy_(res)
     io.gate.copy_(gate)
     io.up.copy_(up)
-    for _ in range(2):
+    for token in range(2):
         a(xh, rh, gh, uh, ox, orr)
         a.stream.synchronize()
         b.run_pinned(io)
         b.stream.synchronize()
         assert torch.equal(io.out_x.view(torch.int16), ox.view(torch.int16))
         assert torch.equal(io.residual.view(torch.int16), orr.view(torch.int16))
+        if token == 0:
+            # the first token's host outputs against the oracle's chain
+            out_x = io.out_x.view(torch.int16).numpy().view(np.uint16).copy()
+            out_res = io.residual.view(torch.int16).numpy().view(np.uint16).copy()
+            record, x_last, res_ref = oracle_chain
+            stated_bar(bf16_f64(out_x), record[-1][3])
+            stated_bar(bf16_f64(out_res), bf16_f64(res_ref))
+            # and bit for bit the layer-by-layer chain checked per layer above
+            assert np.array_equal(out_x.reshape(-1), eager_layers[-1][4].reshape(-1))
+            assert np.array_equal(out_res.reshape(-1), eager_layers[-1][3].reshape(-1))
         rh.copy_(orr)  # the next token starts from the new residual on both paths
     assert io.h2d_bytes == (2 * d["hidden"] + 2 * len(layers) * inter) * 2

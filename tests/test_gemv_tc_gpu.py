@@ -140,8 +140,7 @@ def test_tc_back_to_back_calls_identical(tensor_path):
     torch.cuda.synchronize()
     bits = host_bits(outs)
     assert all(np.array_equal(bits[i], bits[0]) for i in range(1, 16))
-    rows = np.sort(np.random.default_rng(3).choice(4096, 384, replace=False))
-    check_gemv(bits[0], d["gate"], d["up"], d["qweight"], d["scales"], 128, rows=rows)
+    check_gemv(bits[0], d["gate"], d["up"], d["qweight"], d["scales"], 128)
 
 
 def test_tc_graph_replay_matches_eager(tensor_path):
