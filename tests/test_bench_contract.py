@@ -32,4 +32,21 @@ def test_reference_arm_prints_one_contract_line():
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
-    assert "workload" in line["config"] and "sample" in line["config"]
+    assert "workload" in line["config"] and line["sample"]
+    # the same config dict as the GPU arm's decode-step line, and a measured step time
+    sys.path.insert(0, str(REPO))
+    import bench
+
+    assert line["config"] == bench.decode_config(1)
+    assert line["ms_per_step"] > 0 and line["ms_per_full_step_extrapolated"] > line["ms_per_step"]
+
+
+def test_reference_arm_other_workloads():
+    for wl in ("gemv_94mb", "rmsnorm_big"):
+        r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", wl,
+                            "--steps", "1", "--warmup", "0"], cwd=REPO, capture_output=True,
+                           text=True, timeout=300)
+        assert r.returncode == 0, r.stderr
+        line = json.loads(r.stdout.strip().splitlines()[-1])
+        assert line["impl"] == "reference" and line["value"] > 0
+        assert line["config"]["workload"] == wl
