@@ -27,7 +27,7 @@ Reported:
              a bounded sample of the chosen workload; ms_per_step is one sample's time
 
 Other workloads (--workload gemv_94mb | rmsnorm_big | gemv_small | batched_m64 |
-gemv_residual | gate_up) time one call per step and rotate ceil(3 x L2 / bytes) input
+gemv_residual | gate_up | nvfp4_qkv) time one call per step and rotate ceil(3 x L2 / bytes) input
 sets so every step reads HBM; --workload fused_layer times 32 layers of add-RMSNorm +
 gate/up GEMV + down GEMV with the residual epilogue as one graph.
 """
@@ -77,6 +77,7 @@ KERNEL_SOURCES = {
 DTYPE_DP2A = "int4 weights x block-scaled int16 activations: exact int32 dp2a dots, fp32 sums; bf16 in/out"
 DTYPE_TC = "int4 weights dequantised to bf16 x bf16 activations on tcgen05, fp32 accumulation; bf16 in/out"
 DTYPE_RMSNORM = "bf16 in/out, fp32 arithmetic"
+DTYPE_NVFP4 = "packed FP4 (E2M1) x E4M3 1x16 block scales on the tcgen05 block-scaled MMA, fp32 accumulation, alpha folded; bf16 out"
 
 
 def read_peaks():
@@ -444,6 +445,16 @@ def oracle_sampler(workload: str):
 
         nbytes = lambda rows: rows * K // 2 + rows * (K // g) * 2 + M * K * 2 + M * rows * 2  # noqa: E731
         return run, nbytes, 2 * inter, f"gate/up GEMV M={M} K={K} over {{rows}} of {2 * inter} stacked rows"
+    if kind == "nvfp4":
+        M, K, N = spec["M"], spec["K"], spec["N"]
+        d = inputs.nvfp4_inputs(M, K, N, seed=spec["seed"])
+
+        def run(i, rows):
+            lo = (i * 97) % (N - rows + 1)
+            oracle.nvfp4_scaled_mm(d["x"], d["x_sf"], d["w"][lo:lo + rows], d["w_sf"][lo:lo + rows], d["alpha"])
+
+        nbytes = lambda rows: traffic.nvfp4_bytes(M, K, rows)  # noqa: E731
+        return run, nbytes, N, f"NVFP4 scaled matmul M={M} K={K} over {{rows}} of {N} weight rows"
     rows_all, hidden = spec["rows"], spec["hidden"]
     d = inputs.rmsnorm_inputs(rows_all, hidden, seed=spec["seed"])
 
@@ -469,10 +480,15 @@ def reference_arm(args):
         run(i, rows)
         return time.perf_counter() - t0
 
-    # calibrate the slice so one sample takes about target_s
-    probe = min(64, total_rows)
-    t_probe = min(sample(0, probe) for _ in range(2))
-    rows = int(max(min(8, total_rows), min(total_rows, probe * target_s / max(t_probe, 1e-6))))
+    # calibrate the slice so one sample takes about target_s (re-measured, since a sample
+    # has fixed costs besides its per-row work)
+    rows = min(64, total_rows)
+    for _ in range(4):
+        t = sample(0, rows)
+        new_rows = int(max(min(8, total_rows), min(total_rows, rows * target_s / max(t, 1e-6))))
+        if abs(new_rows - rows) <= 0.25 * rows:
+            break
+        rows = new_rows
     sample_bytes = nbytes(rows)
     times = []
     for i in range(total):
@@ -521,8 +537,9 @@ def reference_arm(args):
 # The workload configurations measured in the default run's "configs" object, besides the
 # decode step itself: the small GEMV, the 8192 x 4096 add-RMSNorm and the K=9216 N=2560
 # GEMV (the two shapes held to the 70 % target), the batched M=64 product (tensor-core
-# vs CUDA-core kernel), and the fused layer's other two kernels.
-CONFIG_WORKLOADS = ["gemv_small", "rmsnorm_big", "gemv_94mb", "batched_m64", "gemv_residual", "gate_up"]
+# vs CUDA-core kernel), the fused layer's other two kernels and the NVFP4 QKV projection.
+CONFIG_WORKLOADS = ["gemv_small", "rmsnorm_big", "gemv_94mb", "batched_m64", "gemv_residual", "gate_up",
+                    "nvfp4_qkv"]
 TARGET_PCT = {"rmsnorm_big": 70.0, "gemv_94mb": 70.0}
 
 
@@ -576,6 +593,24 @@ def build_single_calls(name, device, l2):
         kname = "w4a16_gate_up_gemv"
         extra["traffic_tag"] = f"K{K}_I{inter}_M{M}"
         desc = f"gate/up GEMV (horizontal fusion) M={M} K={K} I={inter} (2I={2 * inter} rows) group {g}, seed {spec['seed']}"
+    elif kind == "nvfp4":
+        M, K, N = spec["M"], spec["K"], spec["N"]
+        extra.update(M=M, K=K, N=N)
+        nbytes = fd.nvfp4_bytes(M, K, N)
+        nsets = max(1, min(4096, math.ceil(3 * l2 / nbytes)))
+        d = inputs.nvfp4_inputs(M, K, N, seed=spec["seed"])
+        x, xs = to_dev(d["x"], device), to_dev(d["x_sf"], device)
+        alpha = torch.tensor([float(d["alpha"])], dtype=torch.float32, device=device)
+        rng = np.random.default_rng(spec["seed"] + 1)
+        ws = [(to_dev(d["w"], device), to_dev(d["w_sf"], device))] + [
+            (to_dev(inputs.fp4_bytes(rng, N, K), device), to_dev(inputs.e4m3_scale_codes(rng, N, K), device))
+            for _ in range(nsets - 1)]
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        for w, wsf in ws:
+            calls.append(lambda w=w, wsf=wsf: fd.nvfp4_scaled_mm(x, xs, w, wsf, alpha, out=out))
+        kname = "nvfp4_scaled_mm"
+        desc = (f"NVFP4 scaled matmul, output multiplier folded in, M={M} K={K} N={N} "
+                f"(E2M1, E4M3 1x16 block scales), seed {spec['seed']}")
     else:
         rows, hidden = spec["rows"], spec["hidden"]
         nbytes = fd.add_rmsnorm_bytes(rows, hidden)
@@ -667,7 +702,9 @@ def measure_workload(name, device, world, steps=None, warmup=3, target_ms=300.0,
     n_calls = reps * len(calls)
     us_call = ms * 1e3 / n_calls
     gbs = nbytes / (us_call * 1e-6) / 1e9
-    if "gemv" not in kname:
+    if kind == "nvfp4":
+        dtype = DTYPE_NVFP4
+    elif "gemv" not in kname:
         dtype = DTYPE_RMSNORM
     elif kind in ("gemv", "batched", "gemv_residual") and fd.gemv_uses_tensor_cores(
             extra["M"], extra["K"], extra["N"], extra["group"]):
@@ -691,6 +728,8 @@ def measure_workload(name, device, world, steps=None, warmup=3, target_ms=300.0,
     if name in TARGET_PCT:
         rec["target_pct_of_peak"] = TARGET_PCT[name]
         rec["meets_target"] = bool(rec["pct_of_measured_hbm"] >= TARGET_PCT[name])
+    if kind == "nvfp4":
+        rec["tflops"] = round(fd.nvfp4_flops(extra["M"], extra["K"], extra["N"]) / (us_call * 1e-6) / 1e12, 1)
     if compare:
         rec["paths"] = compare
     if extra.get("traffic_tag"):
@@ -834,7 +873,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--workload", default="decode_step",
                     choices=["decode_step", "gemv_94mb", "rmsnorm_big", "gemv_small", "batched_m64",
-                             "gemv_residual", "gate_up", "fused_layer"])
+                             "gemv_residual", "gate_up", "nvfp4_qkv", "fused_layer"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="decode step only: skip timing the other workload configurations")

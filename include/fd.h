@@ -15,6 +15,9 @@
  *   fd_w4a16_gate_up_gemv  the horizontally fused gate and up projections of the MLP, one
  *                          W4A16 GEMV over both weight matrices ("horizontal fusion"):
  *                          one read of x, g and u written for the down projection.
+ *   fd_nvfp4_scaled_mm     the NVFP4 (packed FP4, E4M3 1x16 block scales) matmul of batched
+ *                          decode with its fp32 output multiplier folded in, on the
+ *                          tensor cores' block-scaled MMA.
  *
  * Sources (web pages, cited by title and section):
  *   [FIX]  "PyTorch Community Proposes Fusion Fix as Large Intermediate Buffers May Slow
@@ -29,6 +32,9 @@
  *          epilogue that writes new_residual = x + out).
  *   [KFM]  "Kernel Fusion, torch.compile and CUDA Graphs, Measured" - "Step 1" (silu(g) *
  *          u), "Step 2: fusing them by hand in Triton" (add + RMSNorm order and roundings).
+ *   [NVFP4] "PyTorch folds NVFP4 output scaling into NVGEMM candidates for decode
+ *          workloads" - body and metrics table (the scaled FP4 matmul and the fold of its
+ *          output multiplier).
  *
  * Conventions shared by every entry point
  *   - Every tensor pointer is a DEVICE pointer (cudaMalloc / PyTorch CUDA memory) on the
@@ -223,6 +229,51 @@ unsigned fd_get_launch_flags(void);
  */
 int fd_w4_dequant_debug(const void *qweight, const void *scales, float *out, int K, int N,
                         int group, fd_stream_t stream);
+
+/*
+ * fd_nvfp4_scaled_mm - NVFP4 scaled matmul with the fp32 output multiplier folded into the
+ * GEMM ([NVFP4] "PyTorch folds NVFP4 output scaling into NVGEMM candidates for decode
+ * workloads", body and metrics table: packed FP4 operands with E4M3 1x16 block scales and
+ * a zero-dimensional fp32 multiplier applied inside the GEMM instead of by a separate
+ * multiplication kernel):
+ *
+ *   X[m, k]   = e2m1(x[m, k]) * e4m3(x_sf[m, k / 16])
+ *   W[n, k]   = e2m1(w[n, k]) * e4m3(w_sf[n, k / 16])
+ *   out[m, n] = bf16( alpha * sum_k X[m, k] * W[n, k] )   (fp32 accumulation, one rounding)
+ *
+ * x       packed FP4 [M, K/2] bytes: element 2p in the low nibble (bits 0..3) of byte p,
+ *         element 2p + 1 in the high nibble. E2M1 codes: sign bit 3, exponent bits 2..1
+ *         (bias 1; field 0 is subnormal, m/2), mantissa bit 0: +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+ * x_sf    E4M3 scale codes [M, K/16] bytes, row-major: one per 16 consecutive k of a row
+ *         (bias 7, no infinity, S.1111.111 is NaN).
+ * w, w_sf the weights [N, K/2] (nn.Linear [out, in] orientation) and their scales [N, K/16].
+ * alpha   pointer to ONE fp32 in device memory (the 0-dim multiplier), read by the kernel
+ *         after its dependency wait, so a previous kernel in the stream may write it.
+ * out     bf16 [M, N] row-major; must not overlap any input (FD_ERR_OVERLAP).
+ * Requires 0 <= M <= FD_MAX_M, N >= 0, K a multiple of 256 (FD_ERR_SHAPE otherwise) and
+ *         one of: K <= 1024, K <= 2048 with K % 512 == 0, K <= 4096 with K % 1024 == 0,
+ *         K <= FD_NVFP4_MAX_K with K % 2048 == 0 (FD_ERR_UNSUPPORTED otherwise). M == 0 or
+ *         N == 0 is an empty call: FD_OK at once, no pointer read, nothing launched.
+ *         x, x_sf, w, w_sf and out 16-byte aligned, alpha 4-byte aligned (FD_ERR_ALIGN).
+ * Runs on the tensor cores' block-scaled MMA (tcgen05, kind::mxf4nvf4): each E2M1 x E2M1
+ * product with both scales is exact; sums accumulate in fp32 in tensor memory, alpha
+ * multiplies the fp32 sum and the result is rounded once. K is split over a thread-block
+ * cluster whose partial sums meet in distributed shared memory: no global scratch.
+ */
+#define FD_NVFP4_MAX_K 8192
+int fd_nvfp4_scaled_mm(const void *x, const void *x_sf, const void *w, const void *w_sf,
+                       const float *alpha, void *out, int M, int K, int N, fd_stream_t stream);
+
+/*
+ * fd_debug_plan_nvfp4 - test support: the launch plan of fd_nvfp4_scaled_mm for one launch
+ * of M (1..128) activation rows, computed on the host without any CUDA call.
+ * plan int[11] out: split (CTAs per cluster along K), k per CTA, 256-k stages, padded batch,
+ *         128-row weight tiles, shared-memory offsets of the activations, weight scales and
+ *         activation scales (weights at 0), the reduction buffer's bytes (from offset 0),
+ *         dynamic shared memory per CTA, and 1 if it fits `smem_budget` bytes.
+ * Returns FD_ERR_UNSUPPORTED when the kernel has no plan for the shape.
+ */
+int fd_debug_plan_nvfp4(int M, int K, int N, int smem_budget, int *plan);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *fd_status_string(int status);

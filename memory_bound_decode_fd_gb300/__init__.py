@@ -6,6 +6,8 @@
 * ``w4a16_gate_up_gemv``: the gate and up projections as one W4A16 GEMV (horizontal
   fusion), writing the g and u that ``swiglu_w4a16_gemv`` consumes.
 * ``add_rmsnorm``: residual add + RMSNorm, one pass, two outputs.
+* ``nvfp4_scaled_mm``: the NVFP4 (packed FP4, E4M3 1x16 block scales) matmul with its fp32
+  output multiplier folded in, on the tensor cores' block-scaled MMA.
 * ``decode_mlp_step``: L layers of the two, in stream order.
 
 The compute runs in ``libfd.so`` (C ABI in ``include/fd.h``); this package marshals
@@ -24,6 +26,7 @@ from ._lib import (  # noqa: F401
     FD_MAX_HIDDEN,
     FD_MAX_K,
     FD_MAX_M,
+    FD_NVFP4_MAX_K,
     FD_OK,
     LIB_PATH,
     FdError,
@@ -37,6 +40,7 @@ from .kernels import (  # noqa: F401
     copy,
     decode_mlp_step,
     gemv_uses_tensor_cores,
+    nvfp4_scaled_mm,
     set_gemv_path,
     set_pdl,
     swiglu_w4a16_gemv,
@@ -45,6 +49,14 @@ from .kernels import (  # noqa: F401
     w4a16_gate_up_gemv,
 )
 from .packing import pack_int4  # noqa: F401
-from .traffic import add_rmsnorm_bytes, decode_step_bytes, gate_up_bytes, gemv_bytes, gemv_flops  # noqa: F401
+from .traffic import (  # noqa: F401
+    add_rmsnorm_bytes,
+    decode_step_bytes,
+    gate_up_bytes,
+    gemv_bytes,
+    gemv_flops,
+    nvfp4_bytes,
+    nvfp4_flops,
+)
 
 __version__ = "1.0.0"

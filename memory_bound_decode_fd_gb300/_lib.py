@@ -27,6 +27,7 @@ FD_LAUNCH_TEST_FAIL = 256
 FD_MAX_K = 32768
 FD_MAX_M = 256
 FD_MAX_HIDDEN = 32768
+FD_NVFP4_MAX_K = 8192
 
 # Every symbol include/fd.h declares, with its ctypes signature.
 _VP = ctypes.c_void_p
@@ -37,6 +38,8 @@ SIGNATURES = {
     "fd_w4a16_gate_up_gemv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "fd_copy": (_I, [_VP, _VP, ctypes.c_size_t, _VP]),
     "fd_debug_plan_gemv": (_I, [_VP, _I, _I, _I, _I, _I, _VP]),
+    "fd_nvfp4_scaled_mm": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _VP]),
+    "fd_debug_plan_nvfp4": (_I, [_I, _I, _I, _I, _VP]),
     "fd_add_rmsnorm": (_I, [_VP, _VP, _VP, ctypes.c_float, _VP, _VP, _I, _I, _VP]),
     "fd_w4_dequant_debug": (_I, [_VP, _VP, _VP, _I, _I, _I, _VP]),
     "fd_status_string": (ctypes.c_char_p, [_I]),

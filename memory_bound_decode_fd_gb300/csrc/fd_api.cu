@@ -9,6 +9,7 @@
 #include "fd_copy.h"
 #include "fd_gemv_plan.h"
 #include "fd_internal.h"
+#include "fd_nvfp4_plan.h"
 
 namespace fd {
 
@@ -198,6 +199,39 @@ int fd_w4a16_gate_up_gemv(const void *x, const void *qweight, const void *scales
         if (err != cudaSuccess || launched) return from_cuda(err);
     }
     return from_cuda(launch_gemv_cc(x, nullptr, qweight, scales, nullptr, o, M, K, N, group, st_));
+}
+
+int fd_nvfp4_scaled_mm(const void *x, const void *x_sf, const void *w, const void *w_sf,
+                       const float *alpha, void *out, int M, int K, int N, fd_stream_t stream) {
+    if (M < 0 || N < 0 || K <= 0 || K % kNfStageK != 0) return FD_ERR_SHAPE;
+    if (M > FD_MAX_M || K > FD_NVFP4_MAX_K || nvfp4_split(K) == 0) return FD_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return FD_OK;  // empty: nothing read or written
+    if (!x || !x_sf || !w || !w_sf || !alpha || !out) return FD_ERR_NULL;
+    if (!aligned16(x) || !aligned16(x_sf) || !aligned16(w) || !aligned16(w_sf) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(alpha) & 3u) != 0)
+        return FD_ERR_ALIGN;
+    const size_t out_bytes = (size_t)M * N * 2;
+    if (overlaps(out, out_bytes, x, (size_t)M * K / 2) ||
+        overlaps(out, out_bytes, x_sf, (size_t)M * K / 16) ||
+        overlaps(out, out_bytes, w, (size_t)N * K / 2) ||
+        overlaps(out, out_bytes, w_sf, (size_t)N * K / 16) || overlaps(out, out_bytes, alpha, 4))
+        return FD_ERR_OVERLAP;
+    if (fake_launch_failure()) return from_cuda(cudaErrorLaunchOutOfResources);
+    return from_cuda(launch_nvfp4_mm(x, x_sf, w, w_sf, alpha, out, M, K, N,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fd_debug_plan_nvfp4(int M, int K, int N, int smem_budget, int *plan) {
+    if (!plan) return FD_ERR_NULL;
+    Nvfp4Plan p{};
+    const int budget = smem_budget > 0 ? smem_budget : 1 << 30;
+    if (M < 1 || M > kNfMaxBatch || N < 1 || nvfp4_split(K) == 0 || !plan_nvfp4(M, K, N, budget, &p))
+        return FD_ERR_UNSUPPORTED;
+    const int v[11] = {p.split, p.k_cta, p.stages, p.npad, p.n_tiles, (int)p.off_x,
+                       (int)p.off_wsf, (int)p.off_xsf, (int)p.recv_bytes, (int)p.smem,
+                       (smem_budget > 0 && p.smem <= (uint32_t)smem_budget) ? 1 : 0};
+    for (int i = 0; i < 11; ++i) plan[i] = v[i];
+    return FD_OK;
 }
 
 int fd_copy(void *dst, const void *src, size_t bytes, fd_stream_t stream) {

@@ -87,6 +87,11 @@ cudaError_t launch_gemv_cc(const void *gate, const void *up, const void *qweight
 cudaError_t launch_add_rmsnorm(const void *x, const void *residual, const void *weight,
                                float eps, void *out, void *residual_out, int rows,
                                int hidden, cudaStream_t stream);
+// NVFP4 scaled matmul with the output multiplier folded in (fd_nvfp4.cu); the shape has
+// passed plan_nvfp4's rules for every 128-row batch chunk.
+cudaError_t launch_nvfp4_mm(const void *x, const void *x_sf, const void *w, const void *w_sf,
+                            const float *alpha, void *out, int M, int K, int N,
+                            cudaStream_t stream);
 cudaError_t launch_w4_dequant_debug(const void *qweight, const void *scales, float *out,
                                     int K, int N, int group, cudaStream_t stream);
 

@@ -69,6 +69,22 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint
         : "memory");
 }
 
+// D[tmem] (+)= (A * SFA) * (B * SFB)^T for one K = 64 step of packed FP4 (E2M1) operands
+// with one E4M3 scale per 16 elements of each row (block-scaled MMA, scale vectors of 4 per
+// K = 64), issued by one thread. `sfa_tmem` / `sfb_tmem` are the TMEM addresses of the
+// scale factors of this step (4 columns each, see tmem_st_x4).
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem,
+                                            uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // One arrival on `bar` once every tcgen05.mma this thread issued before has completed.
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile(
@@ -91,6 +107,18 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Each lane of the warp writes 4 consecutive 32-bit columns of its own TMEM lane (the warp
+// may only address lanes 32 * (warp % 4) .. + 31); tmem_st_wait makes them complete.
+__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2,
+                                           uint32_t v3) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+                 "r"(v0), "r"(v1), "r"(v2), "r"(v3)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor, no swizzle ("interleaved" 8 x 16-byte core
 // matrices, each 128 contiguous bytes). For a K-major operand: `lbo` = byte distance
 // between the two core matrices adjacent along K, `sbo` = byte distance between
@@ -99,6 +127,27 @@ __device__ __forceinline__ uint64_t smem_desc_interleaved(uint32_t saddr, uint32
                                                           uint32_t sbo) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzle layout
+// that a tensor-map copy with CU_TENSOR_MAP_SWIZZLE_128B writes: rows of 128 bytes, 16-byte
+// chunk c of row r stored at chunk c ^ (r & 7), 8-row atoms of 1024 bytes (the stride
+// between 8-row groups, SBO). The leading-dimension offset is unused for this layout (1).
+// The atom must be 1024-byte aligned; a K step inside the 128-byte row advances the start
+// address by its byte offset (the swizzle is applied to the absolute address).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024u >> 4) << 32) |
+           (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::mxf4nvf4: E2M1 A and B (packed FP4), UE4M3 scale
+// factors (one per 16 elements), fp32 D, both K-major, M x N tile, scale-factor ids 0.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int m, int n) {
+    return (1u << 7)                        // A format: E2M1
+           | (1u << 10)                     // B format: E2M1
+           | ((uint32_t)(n >> 3) << 17)     // N / 8
+           | (0u << 23)                     // scale format: UE4M3
+           | ((uint32_t)(m >> 4) << 24);    // M / 16
 }
 
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major, M x N tile.

@@ -16,6 +16,7 @@ Workloads (name: sizes, seed):
   batched_m64    GEMV M=64 K=14336 N=4096 + add-RMSNorm 64x4096 eps=1e-5, seed 4
   gemv_residual  the decode-step GEMV with the residual-add epilogue, seed 3
   gate_up        gate/up GEMV M=1 K=4096 I=14336 (28672 stacked rows), seed 3
+  nvfp4_qkv      NVFP4 scaled matmul M=64 K=4096 N=6144 (``nvfp4_inputs``), seed 5
 
 NVFP4 operands (``nvfp4_inputs``; M=64 K=4096 N=6144 is a Llama-3.1-8B QKV projection at
 batch 64, seed 5) are drawn as codes: packed FP4 bytes uniform (every nibble one of the
@@ -136,4 +137,6 @@ WORKLOADS = {
     "gemv_residual": dict(kind="gemv_residual", M=1, K=14336, N=4096, group=128, seed=3),
     # the gate and up projections of the same MLP as one horizontally fused W4A16 GEMV
     "gate_up": dict(kind="gate_up", M=1, K=4096, I=14336, group=128, seed=3),
+    # the NVFP4 QKV projection at batch 64 (Llama-3.1-8B: 32 query + 8 key/value heads of 128)
+    "nvfp4_qkv": dict(kind="nvfp4", M=64, K=4096, N=6144, seed=5),
 }

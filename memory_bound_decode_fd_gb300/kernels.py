@@ -224,6 +224,49 @@ def w4a16_gate_up_gemv(
     return gate_out, up_out
 
 
+def nvfp4_scaled_mm(
+    x: torch.Tensor,
+    x_sf: torch.Tensor,
+    w: torch.Tensor,
+    w_sf: torch.Tensor,
+    alpha: torch.Tensor,
+    out: torch.Tensor | None = None,
+    stream: torch.cuda.Stream | None = None,
+) -> torch.Tensor:
+    """out[m, n] = bf16(alpha * sum_k X[m, k] * W[n, k]) for NVFP4 operands, the output
+    multiplier folded into the GEMM.
+
+    x: uint8 [M, K/2] packed FP4 (element 2p in the low nibble of byte p); x_sf: uint8
+    [M, K/16] E4M3 scale codes (one per 16 k); w: uint8 [N, K/2]; w_sf: uint8 [N, K/16];
+    alpha: a one-element float32 CUDA tensor (the 0-dim multiplier, read by the kernel);
+    out: bf16 [M, N] (allocated if None). See fd_nvfp4_scaled_mm in include/fd.h.
+    """
+    if x.dim() != 2 or w.dim() != 2 or x_sf.dim() != 2 or w_sf.dim() != 2:
+        raise ValueError("x [M, K/2], x_sf [M, K/16], w [N, K/2], w_sf [N, K/16]")
+    M, K2 = x.shape
+    N = w.shape[0]
+    K = 2 * K2
+    _check_tensor("x", x, torch.uint8)
+    _check_tensor("x_sf", x_sf, torch.uint8, (M, K // 16))
+    _check_tensor("w", w, torch.uint8, (N, K2))
+    _check_tensor("w_sf", w_sf, torch.uint8, (N, K // 16))
+    if not isinstance(alpha, torch.Tensor) or not alpha.is_cuda or alpha.dtype != torch.float32 \
+            or alpha.numel() != 1:
+        raise ValueError("alpha must be a one-element float32 CUDA tensor")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check_tensor("out", out, torch.bfloat16, (M, N))
+    dev = _device_of(x, x_sf, w, w_sf, alpha, out)
+    lib = _lib.load()
+    with _on_device(dev):
+        st = lib.fd_nvfp4_scaled_mm(
+            _ptr(x), _ptr(x_sf), _ptr(w), _ptr(w_sf), _ptr(alpha), _ptr(out),
+            int(M), int(K), int(N), _stream_handle(stream, dev),
+        )
+    _lib.check(st)
+    return out
+
+
 def copy(dst: torch.Tensor, src: torch.Tensor, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
     """dst <- src (same number of bytes, contiguous, 16-byte aligned) with one kernel:
     either side may be a CUDA tensor or a pinned host tensor (read or written by the GPU

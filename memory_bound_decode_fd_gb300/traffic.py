@@ -31,3 +31,13 @@ def add_rmsnorm_bytes(rows: int, hidden: int) -> int:
 
 def decode_step_bytes(layers: int, hidden: int, inter: int, group: int) -> int:
     return layers * (add_rmsnorm_bytes(1, hidden) + gemv_bytes(1, inter, hidden, group))
+
+
+def nvfp4_bytes(M: int, K: int, N: int) -> int:
+    """Packed FP4 weights and activations (K/2 bytes per row), their E4M3 scales (K/16
+    bytes per row) and the bf16 output; alpha's 4 bytes are not counted."""
+    return (N + M) * (K // 2 + K // 16) + M * N * 2
+
+
+def nvfp4_flops(M: int, K: int, N: int) -> int:
+    return 2 * M * K * N
