@@ -59,7 +59,10 @@ METRIC = "µs/call and achieved HBM GB/s (% of GB300 peak) for SwiGLU-W4A16 GEMV
 FALLBACK_HBM_GBS = 6800.0
 SPEC_HBM_GBS = 8000.0
 KERNEL_SOURCES = {
-    # the M = 1 kernel the decode step runs (bulk-copy kernel) and the headers it uses
+    # the M = 1 kernel the decode step runs (bulk-copy kernel, with the folded add-RMSNorm)
+    # and the headers it uses
+    "swiglu_w4a16_gemv_add_rmsnorm": ["csrc/fd_gemv_tma.cu", "csrc/fd_gemv_common.cuh", "csrc/fd_tma.cuh",
+                                      "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
     "swiglu_w4a16_gemv": ["csrc/fd_gemv_tma.cu", "csrc/fd_gemv_common.cuh", "csrc/fd_tma.cuh",
                           "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
     "add_rmsnorm": ["csrc/fd_add_rmsnorm.cu", "csrc/fd_internal.h"],
@@ -250,19 +253,28 @@ def bench_decode(args, device, rank, world):
     ms_per_step = ms / args.steps
     value_gbs = job_throughput_gbs(world, bytes_per_step, ms_per_step)
 
-    # Per-kernel durations: each kernel's 32 launches of the step, captured alone in a
-    # CUDA graph (same buffers and weights, programmatic dependent launch as in the
-    # step) and replayed on the same stream; average launch duration = event time /
-    # launches. Includes the small inter-kernel gap, so it is conservative.
+    # Per-kernel durations: each kernel's launches of the step, captured alone in a CUDA
+    # graph (same buffers and weights, programmatic dependent launch as in the step) and
+    # replayed on the same stream; average launch duration = event time / launches.
+    # Includes the small inter-kernel gap, so it is conservative. The step runs the 32
+    # add-RMSNorm and 32 GEMV launches; the GEMV with the next layer's add-RMSNorm folded
+    # in (fd_swiglu_w4a16_gemv_add_rmsnorm, not used by the step) is timed as well.
     hidden = spec["hidden"]
+    L = spec["layers"]
+    fold_scratch = fd.fold_scratch(device)
     kern_launch = {
-        "add_rmsnorm": [lambda L=L, i=i: fd.add_rmsnorm(
-            step.y[i - 1] if i else step.x, step.residual, L["rms_weight"], spec["eps"],
+        "swiglu_w4a16_gemv_add_rmsnorm": [lambda L_=ly, i=i: fd.swiglu_w4a16_gemv_add_rmsnorm(
+            L_["gate"], L_["up"], L_["qweight"], L_["scales"], step.residual,
+            step.layers[i + 1]["rms_weight"], spec["eps"], fold_scratch, y=step.y[i],
+            normed=step.normed[i + 1], residual_out=step.residual, group=spec["group"], stream=stream)
+            for i, ly in enumerate(step.layers[:-1])],
+        "swiglu_w4a16_gemv": [lambda L_=ly, i=i: fd.swiglu_w4a16_gemv(
+            L_["gate"], L_["up"], L_["qweight"], L_["scales"], out=step.y[i], group=spec["group"],
+            stream=stream) for i, ly in enumerate(step.layers)],
+        "add_rmsnorm": [lambda L_=ly, i=i: fd.add_rmsnorm(
+            step.y[i - 1] if i else step.x, step.residual, L_["rms_weight"], spec["eps"],
             out=step.normed[i], residual_out=step.residual, stream=stream)
-            for i, L in enumerate(step.layers)],
-        "swiglu_w4a16_gemv": [lambda L=L, i=i: fd.swiglu_w4a16_gemv(
-            L["gate"], L["up"], L["qweight"], L["scales"], out=step.y[i], group=spec["group"],
-            stream=stream) for i, L in enumerate(step.layers)],
+            for i, ly in enumerate(step.layers)],
     }
     kernels = {}
     prev_pdl = fd.set_pdl(step.pdl)
@@ -285,6 +297,10 @@ def bench_decode(args, device, rank, world):
         fd.set_pdl(prev_pdl)
     gemv_bytes = fd.gemv_bytes(1, spec["inter"], hidden, spec["group"])
     rms_bytes = fd.add_rmsnorm_bytes(1, hidden)
+    # the folded call moves the GEMV's bytes plus the add-RMSNorm's minus its read of y,
+    # which stays on chip: residual in, new residual and normalised row out, weight row
+    fold_bytes = gemv_bytes + 8 * hidden
+    kernels["swiglu_w4a16_gemv_add_rmsnorm"]["bytes"] = fold_bytes
     kernels["swiglu_w4a16_gemv"]["bytes"] = gemv_bytes
     kernels["add_rmsnorm"]["bytes"] = rms_bytes
     for k in kernels.values():
@@ -292,6 +308,21 @@ def bench_decode(args, device, rank, world):
     gemv_us = kernels["swiglu_w4a16_gemv"]["us"]
     achieved = gemv_bytes / (gemv_us * 1e-6) / 1e9
     traffic = recorded_traffic("swiglu_w4a16_gemv", "K14336_N4096_M1")
+
+    # The step launched eagerly (no CUDA graph: every launch pays the host's launch cost),
+    # with separate kernels (64 launches) and with each later add-RMSNorm folded into the
+    # GEMV before it (33 launches).
+    eager = {}
+    res_save = step.residual.clone()
+    for name, sc in (("separate_64_launches", None), ("folded_33_launches", fold_scratch)):
+        run = lambda sc=sc: fd.decode_mlp_step(step.x, step.residual, step.layers, spec["eps"],  # noqa: E731
+                                               spec["group"], normed=step.normed, y=step.y,
+                                               stream=stream, scratch=sc)
+        with torch.cuda.stream(stream):
+            time_region(stream, run, 3)
+            n_eager = max(5, min(50, args.steps // 10))
+            eager[name] = round(time_region(stream, run, n_eager) / n_eager, 4)
+    step.residual.copy_(res_save)
 
     # End to end: pinned host inputs -> device, replay, device -> pinned host.
     pin = dict(dtype=torch.bfloat16, pin_memory=True)
@@ -350,6 +381,7 @@ def bench_decode(args, device, rank, world):
             "frac": round(achieved / hbm_peak, 4),
             "traffic": traffic,
             "algorithmic_bytes_per_launch": gemv_bytes,
+            "launches_per_step": L,
         },
         "e2e": {
             "value": round(job_throughput_gbs(world, bytes_per_step, e2e_ms), 2),
@@ -360,6 +392,7 @@ def bench_decode(args, device, rank, world):
             "api": "memory_bound_decode_fd_gb300.step.DecodeStep.run_pinned (StepIO captured with the step: fd_copy kernels read and write the pinned host block, one graph launch)",
             "four_copy_call_ms_per_step": round(e2e_sep_ms, 6),
         },
+        "eager_ms_per_step": eager,
         "gpu_launches": 2 * spec["layers"] * args.steps,
         "clocks": clocks,
     }

@@ -15,6 +15,9 @@
  *   fd_w4a16_gate_up_gemv  the horizontally fused gate and up projections of the MLP, one
  *                          W4A16 GEMV over both weight matrices ("horizontal fusion"):
  *                          one read of x, g and u written for the down projection.
+ *   fd_swiglu_w4a16_gemv_add_rmsnorm
+ *                          the down projection with the next layer's add + RMSNorm folded
+ *                          into its tail (one launch per decode layer instead of two).
  *   fd_nvfp4_scaled_mm     the NVFP4 (packed FP4, E4M3 1x16 block scales) matmul of batched
  *                          decode with its fp32 output multiplier folded in, on the
  *                          tensor cores' block-scaled MMA.
@@ -150,6 +153,41 @@ int fd_w4a16_gate_up_gemv(const void *x, const void *qweight, const void *scales
                           fd_stream_t stream);
 
 /*
+ * fd_swiglu_w4a16_gemv_add_rmsnorm - one decode layer's SwiGLU-W4A16 down projection with
+ * the NEXT layer's residual add + RMSNorm folded into its tail ("09 - Operator fusion",
+ * "The fusion boundary problem": the down projection's output joins the residual stream at
+ * the next add_rmsnorm, whose two outputs are the new residual and the normalised row):
+ *
+ *   y[n]            = bf16( sum_k silu(g[k]) * u[k] * W[n, k] )       (fd_swiglu_w4a16_gemv)
+ *   residual_out[n] = h[n] = bf16( f32(y[n]) + f32(residual[n]) )
+ *   normed[n]       = bf16( f32(bf16( h[n] * rstd )) * f32(rms_weight[n]) ),
+ *                     rstd = 1 / sqrt( (1/N) sum_n h[n]^2 + eps )        (fd_add_rmsnorm)
+ *
+ * One activation row (M = 1). gate, up bf16 [1, K]; qweight, scales as fd_swiglu_w4a16_gemv;
+ * y, residual, residual_out, normed bf16 [1, N]; rms_weight bf16 [N]. residual_out ==
+ * residual (in place) is allowed; any other overlap of an output with an input or another
+ * output returns FD_ERR_OVERLAP.
+ * scratch  device memory of FD_FOLD_SCRATCH_BYTES bytes, 16-byte aligned, ZERO before its
+ *          first use; every completed call leaves it zero again. Each CTA of the GEMV writes
+ *          its partial sum of h^2 there and takes a ticket from a counter in it; the CTA that
+ *          draws the last ticket normalises the row and resets the counter, so no CTA waits
+ *          for another. Calls that share a scratch buffer must not run concurrently (use one
+ *          stream, or one buffer per stream).
+ * Requires K, N, group as fd_swiglu_w4a16_gemv, N % 8 == 0, eps >= 0 and finite. N == 0 is an
+ *          empty call: FD_OK at once, no pointer read, nothing launched.
+ * Runs the bulk-copy GEMV kernel with the fold where it applies (kernel selection AUTO or
+ * BULK, K % 1024 == 0, K <= 15360, (K / group) % 8 == 0); otherwise the selected GEMV kernel
+ * followed by fd_add_rmsnorm's kernel (same results up to the order of the sum of squares;
+ * the scratch is not touched).
+ */
+#define FD_FOLD_SCRATCH_BYTES 4096
+int fd_swiglu_w4a16_gemv_add_rmsnorm(const void *gate, const void *up, const void *qweight,
+                                     const void *scales, void *y, const void *residual,
+                                     const void *rms_weight, float eps, void *normed,
+                                     void *residual_out, void *scratch, int K, int N, int group,
+                                     fd_stream_t stream);
+
+/*
  * fd_add_rmsnorm - fused residual add + RMSNorm, one pass over HBM.     [KFM Step 2]
  *
  *   h[i, j]   = bf16( f32(x[i, j]) + f32(residual[i, j]) )            -> residual_out
@@ -218,8 +256,30 @@ int fd_gemv_uses_tensor_cores(int M, int K, int N, int group);
  * fd_last_cuda_error() = cudaErrorLaunchOutOfResources, without calling CUDA (the error
  * path of a failed launch, exercised without touching the GPU). */
 #define FD_LAUNCH_TEST_FAIL 256u
+/* Test only: the bulk-copy GEMV kernel (the M = 1 kernel of FD_GEMV_AUTO and FD_GEMV_BULK)
+ * gives its waits a limit of about 2^20 SM clocks instead of about 2^31 and its copy thread
+ * leaves the first weight chunk of every CTA uncopied, so the waits for that chunk run out:
+ * the call's outputs are NaN and fd_device_status reports FD_DEVICE_STATUS_WAIT_TIMEOUT. No
+ * fault and no hang: every wait is bounded and no copy is left in flight. */
+#define FD_LAUNCH_TEST_WAIT_TIMEOUT 512u
 int fd_set_launch_flags(unsigned flags);
 unsigned fd_get_launch_flags(void);
+
+/*
+ * fd_device_status - failures that kernels of this library recorded on the current device
+ * since the last clear. Every wait inside a kernel is bounded (about a second); a CTA whose
+ * wait gives up stops, waits (bounded) for the copies it issued, makes the call's outputs
+ * NaN and sets FD_DEVICE_STATUS_WAIT_TIMEOUT in a device status word, so the context stays
+ * usable and the failure is visible to the host.
+ * stream  the status is read after the work already in `stream` (a cudaStream_t; NULL = the
+ *         legacy default stream); this call synchronises that stream.
+ * status  out: the OR of the recorded FD_DEVICE_STATUS_* bits (0: none).
+ * clear   nonzero: reset the word after reading it.
+ * Returns FD_ERR_NULL for a NULL `status`, FD_ERR_CUDA if a copy or the synchronisation
+ * fails. Not capturable in a CUDA graph (it synchronises).
+ */
+#define FD_DEVICE_STATUS_WAIT_TIMEOUT 1u
+int fd_device_status(fd_stream_t stream, unsigned *status, int clear);
 
 /*
  * fd_w4_dequant_debug - write the dequantised weights W[n, k] = q[n, k] * s[n, k/group]
@@ -251,26 +311,28 @@ int fd_w4_dequant_debug(const void *qweight, const void *scales, float *out, int
  *         after its dependency wait, so a previous kernel in the stream may write it.
  * out     bf16 [M, N] row-major; must not overlap any input (FD_ERR_OVERLAP).
  * Requires 0 <= M <= FD_MAX_M, N >= 0, K a multiple of 256 (FD_ERR_SHAPE otherwise) and
- *         one of: K <= 1024, K <= 2048 with K % 512 == 0, K <= 4096 with K % 1024 == 0,
- *         K <= FD_NVFP4_MAX_K with K % 2048 == 0 (FD_ERR_UNSUPPORTED otherwise). M == 0 or
- *         N == 0 is an empty call: FD_OK at once, no pointer read, nothing launched.
+ *         K <= FD_NVFP4_MAX_K (FD_ERR_UNSUPPORTED otherwise). M == 0 or N == 0 is an empty
+ *         call: FD_OK at once, no pointer read, nothing launched.
  *         x, x_sf, w, w_sf and out 16-byte aligned, alpha 4-byte aligned (FD_ERR_ALIGN).
  * Runs on the tensor cores' block-scaled MMA (tcgen05, kind::mxf4nvf4): each E2M1 x E2M1
  * product with both scales is exact; sums accumulate in fp32 in tensor memory, alpha
  * multiplies the fp32 sum and the result is rounded once. K is split over a thread-block
- * cluster whose partial sums meet in distributed shared memory: no global scratch.
+ * cluster of up to 8 CTAs whose partial sums meet in distributed shared memory: no global
+ * scratch.
  */
-#define FD_NVFP4_MAX_K 8192
+#define FD_NVFP4_MAX_K 16384
 int fd_nvfp4_scaled_mm(const void *x, const void *x_sf, const void *w, const void *w_sf,
                        const float *alpha, void *out, int M, int K, int N, fd_stream_t stream);
 
 /*
  * fd_debug_plan_nvfp4 - test support: the launch plan of fd_nvfp4_scaled_mm for one launch
  * of M (1..128) activation rows, computed on the host without any CUDA call.
- * plan int[11] out: split (CTAs per cluster along K), k per CTA, 256-k stages, padded batch,
- *         128-row weight tiles, shared-memory offsets of the activations, weight scales and
- *         activation scales (weights at 0), the reduction buffer's bytes (from offset 0),
- *         dynamic shared memory per CTA, and 1 if it fits `smem_budget` bytes.
+ * smem_budget  dynamic shared memory a CTA may use (bytes).
+ * plan    int[13] out: split (CTAs per cluster along K), 256-k stages of K, stages of the
+ *         largest slice, padded batch, 128-row weight tiles, TMEM columns, output rows per
+ *         rank, scale bytes copied per row, shared-memory offsets of the activations, the
+ *         weight scales and the activation scales (weights at 0), the reduction buffer's
+ *         bytes (from offset 0), dynamic shared memory per CTA.
  * Returns FD_ERR_UNSUPPORTED when the kernel has no plan for the shape.
  */
 int fd_debug_plan_nvfp4(int M, int K, int N, int smem_budget, int *plan);

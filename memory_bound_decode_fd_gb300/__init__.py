@@ -6,6 +6,8 @@
 * ``w4a16_gate_up_gemv``: the gate and up projections as one W4A16 GEMV (horizontal
   fusion), writing the g and u that ``swiglu_w4a16_gemv`` consumes.
 * ``add_rmsnorm``: residual add + RMSNorm, one pass, two outputs.
+* ``swiglu_w4a16_gemv_add_rmsnorm``: the GEMV with the next layer's add-RMSNorm folded into
+  its tail (one launch per decode layer).
 * ``nvfp4_scaled_mm``: the NVFP4 (packed FP4, E4M3 1x16 block scales) matmul with its fp32
   output multiplier folded in, on the tensor cores' block-scaled MMA.
 * ``decode_mlp_step``: L layers of the two, in stream order.
@@ -39,11 +41,14 @@ from .kernels import (  # noqa: F401
     add_rmsnorm,
     copy,
     decode_mlp_step,
+    device_status,
+    fold_scratch,
     gemv_uses_tensor_cores,
     nvfp4_scaled_mm,
     set_gemv_path,
     set_pdl,
     swiglu_w4a16_gemv,
+    swiglu_w4a16_gemv_add_rmsnorm,
     swiglu_w4a16_gemv_residual,
     w4_dequant_debug,
     w4a16_gate_up_gemv,

@@ -23,11 +23,14 @@ FD_GEMV_TENSOR = 3
 
 FD_LAUNCH_PDL = 1
 FD_LAUNCH_TEST_FAIL = 256
+FD_LAUNCH_TEST_WAIT_TIMEOUT = 512
+FD_DEVICE_STATUS_WAIT_TIMEOUT = 1
 
 FD_MAX_K = 32768
 FD_MAX_M = 256
 FD_MAX_HIDDEN = 32768
-FD_NVFP4_MAX_K = 8192
+FD_NVFP4_MAX_K = 16384
+FD_FOLD_SCRATCH_BYTES = 4096
 
 # Every symbol include/fd.h declares, with its ctypes signature.
 _VP = ctypes.c_void_p
@@ -35,9 +38,12 @@ _I = ctypes.c_int
 SIGNATURES = {
     "fd_swiglu_w4a16_gemv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "fd_swiglu_w4a16_gemv_residual": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
+    "fd_swiglu_w4a16_gemv_add_rmsnorm": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float,
+                                             _VP, _VP, _VP, _I, _I, _I, _VP]),
     "fd_w4a16_gate_up_gemv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "fd_copy": (_I, [_VP, _VP, ctypes.c_size_t, _VP]),
     "fd_debug_plan_gemv": (_I, [_VP, _I, _I, _I, _I, _I, _VP]),
+    "fd_device_status": (_I, [_VP, _VP, _I]),
     "fd_nvfp4_scaled_mm": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _VP]),
     "fd_debug_plan_nvfp4": (_I, [_I, _I, _I, _I, _VP]),
     "fd_add_rmsnorm": (_I, [_VP, _VP, _VP, ctypes.c_float, _VP, _VP, _I, _I, _VP]),

@@ -165,6 +165,63 @@ int fd_swiglu_w4a16_gemv_residual(const void *gate, const void *up, const void *
     return swiglu_gemv(gate, up, qweight, scales, residual, out, M, K, N, group, stream);
 }
 
+int fd_swiglu_w4a16_gemv_add_rmsnorm(const void *gate, const void *up, const void *qweight,
+                                     const void *scales, void *y, const void *residual,
+                                     const void *rms_weight, float eps, void *normed,
+                                     void *residual_out, void *scratch, int K, int N, int group,
+                                     fd_stream_t stream) {
+    const int sz = check_w4_sizes(1, K, N, group);
+    if (sz == kEmpty) return FD_OK;
+    if (!(eps >= 0.0f) || !std::isfinite(eps) || N % 8 != 0) return FD_ERR_SHAPE;
+    if (!gate || !up || !y || !residual || !rms_weight || !normed || !residual_out || !scratch)
+        return FD_ERR_NULL;
+    if (sz != FD_OK) return sz;
+    int st = check_w4_layout(qweight, scales, K, N, group);
+    if (st != FD_OK) return st;
+    if (!aligned16(gate) || !aligned16(up) || !aligned16(y) || !aligned16(residual) ||
+        !aligned16(rms_weight) || !aligned16(normed) || !aligned16(residual_out) ||
+        !aligned16(scratch))
+        return FD_ERR_ALIGN;
+    const size_t act = (size_t)K * 2, row = (size_t)N * 2;
+    const size_t w_bytes = (size_t)N * K / 2, s_bytes = (size_t)N * (K / group) * 2;
+    const void *ins[] = {gate, up, qweight, scales, rms_weight};
+    const size_t in_bytes[] = {act, act, w_bytes, s_bytes, row};
+    // outputs: y, normed, residual_out (== residual allowed), scratch
+    const void *outs[] = {y, normed, residual_out, scratch};
+    const size_t out_bytes[] = {row, row, row, (size_t)FD_FOLD_SCRATCH_BYTES};
+    for (int i = 0; i < 4; ++i) {
+        for (int j = 0; j < 5; ++j)
+            if (overlaps(outs[i], out_bytes[i], ins[j], in_bytes[j])) return FD_ERR_OVERLAP;
+        for (int j = i + 1; j < 4; ++j)
+            if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return FD_ERR_OVERLAP;
+        if (outs[i] != residual_out && overlaps(outs[i], out_bytes[i], residual, row))
+            return FD_ERR_OVERLAP;
+    }
+    if (residual_out != residual && overlaps(residual_out, row, residual, row)) return FD_ERR_OVERLAP;
+    if (fake_launch_failure()) return from_cuda(cudaErrorLaunchOutOfResources);
+    cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+    const int path = g_gemv_path.load(std::memory_order_relaxed);
+    if (path == FD_GEMV_AUTO || path == FD_GEMV_BULK) {
+        unsigned char *sc = static_cast<unsigned char *>(scratch);
+        const FoldArgs fold{static_cast<const uint16_t *>(residual),
+                            static_cast<uint16_t *>(residual_out),
+                            static_cast<const uint16_t *>(rms_weight),
+                            static_cast<uint16_t *>(normed),
+                            reinterpret_cast<float *>(sc + kFoldPartialsOffset),
+                            reinterpret_cast<unsigned *>(sc), eps, 1.0f / (float)N};
+        bool launched = false;
+        cudaError_t err = launch_gemv_tma(gate, up, qweight, scales, nullptr,
+                                          GemvOut{y, nullptr, N, N}, 1, K, N, group, st_,
+                                          &launched, &fold);
+        if (err != cudaSuccess || launched) return from_cuda(err);
+    }
+    // the GEMV on the selected kernel, then the separate add-RMSNorm kernel
+    st = swiglu_gemv(gate, up, qweight, scales, nullptr, y, 1, K, N, group, stream);
+    if (st != FD_OK) return st;
+    return from_cuda(launch_add_rmsnorm(y, residual, rms_weight, eps, normed, residual_out, 1, N,
+                                        st_));
+}
+
 int fd_w4a16_gate_up_gemv(const void *x, const void *qweight, const void *scales,
                           void *gate_out, void *up_out, int M, int K, int I, int group,
                           fd_stream_t stream) {
@@ -204,7 +261,7 @@ int fd_w4a16_gate_up_gemv(const void *x, const void *qweight, const void *scales
 int fd_nvfp4_scaled_mm(const void *x, const void *x_sf, const void *w, const void *w_sf,
                        const float *alpha, void *out, int M, int K, int N, fd_stream_t stream) {
     if (M < 0 || N < 0 || K <= 0 || K % kNfStageK != 0) return FD_ERR_SHAPE;
-    if (M > FD_MAX_M || K > FD_NVFP4_MAX_K || nvfp4_split(K) == 0) return FD_ERR_UNSUPPORTED;
+    if (M > FD_MAX_M || K > FD_NVFP4_MAX_K) return FD_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return FD_OK;  // empty: nothing read or written
     if (!x || !x_sf || !w || !w_sf || !alpha || !out) return FD_ERR_NULL;
     if (!aligned16(x) || !aligned16(x_sf) || !aligned16(w) || !aligned16(w_sf) || !aligned16(out) ||
@@ -224,13 +281,11 @@ int fd_nvfp4_scaled_mm(const void *x, const void *x_sf, const void *w, const voi
 int fd_debug_plan_nvfp4(int M, int K, int N, int smem_budget, int *plan) {
     if (!plan) return FD_ERR_NULL;
     Nvfp4Plan p{};
-    const int budget = smem_budget > 0 ? smem_budget : 1 << 30;
-    if (M < 1 || M > kNfMaxBatch || N < 1 || nvfp4_split(K) == 0 || !plan_nvfp4(M, K, N, budget, &p))
-        return FD_ERR_UNSUPPORTED;
-    const int v[11] = {p.split, p.k_cta, p.stages, p.npad, p.n_tiles, (int)p.off_x,
-                       (int)p.off_wsf, (int)p.off_xsf, (int)p.recv_bytes, (int)p.smem,
-                       (smem_budget > 0 && p.smem <= (uint32_t)smem_budget) ? 1 : 0};
-    for (int i = 0; i < 11; ++i) plan[i] = v[i];
+    if (!plan_nvfp4(M, K, N, smem_budget, &p)) return FD_ERR_UNSUPPORTED;
+    const int v[13] = {p.split, p.s_total, p.max_stages, p.npad, p.n_tiles, p.tmem_cols,
+                       p.rows_own, (int)p.sf_row, (int)p.off_x, (int)p.off_wsf, (int)p.off_xsf,
+                       (int)p.recv_bytes, (int)p.smem};
+    for (int i = 0; i < 13; ++i) plan[i] = v[i];
     return FD_OK;
 }
 
@@ -277,7 +332,8 @@ int fd_set_gemv_path(int path) {
 int fd_get_gemv_path(void) { return g_gemv_path.load(std::memory_order_relaxed); }
 
 int fd_set_launch_flags(unsigned flags) {
-    if (flags & ~(FD_LAUNCH_PDL | FD_LAUNCH_TEST_FAIL)) return FD_ERR_UNSUPPORTED;
+    if (flags & ~(FD_LAUNCH_PDL | FD_LAUNCH_TEST_FAIL | FD_LAUNCH_TEST_WAIT_TIMEOUT))
+        return FD_ERR_UNSUPPORTED;
     g_launch_flags.store(flags, std::memory_order_relaxed);
     return FD_OK;
 }
@@ -342,6 +398,28 @@ const char *fd_status_string(int status) {
         case FD_ERR_OVERLAP: return "FD_ERR_OVERLAP: an output overlaps an input in a way the kernel does not allow";
         default: return "fd: unknown status";
     }
+}
+
+int fd_device_status(fd_stream_t stream, unsigned *status, int clear) {
+    if (!status) return FD_ERR_NULL;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // one word per file with bounded waits; pinned so the copies are truly asynchronous
+    static thread_local unsigned *words = nullptr;
+    if (!words) {
+        cudaError_t err = cudaMallocHost(&words, 3 * sizeof(unsigned));
+        if (err != cudaSuccess) return from_cuda(err);
+    }
+    cudaError_t (*const readers[3])(cudaStream_t, unsigned *, bool) = {
+        status_gemv_tma, status_gemv_tc, status_nvfp4};
+    for (int i = 0; i < 3; ++i) {
+        words[i] = 0;
+        cudaError_t err = readers[i](st, &words[i], clear != 0);
+        if (err != cudaSuccess) return from_cuda(err);
+    }
+    cudaError_t err = cudaStreamSynchronize(st);
+    if (err != cudaSuccess) return from_cuda(err);
+    *status = words[0] | words[1] | words[2];
+    return FD_OK;
 }
 
 int fd_last_cuda_error(void) { return g_last_cuda_error; }

@@ -94,6 +94,14 @@ __device__ __forceinline__ float tanh_approx(float x) {
     return y;
 }
 
+// Power-of-two factor applied to a slice before its int16 encoding: 2^64 when the slice's
+// largest magnitude is below 2^-64, else 1. The code of a_k is rint(a_k * 32767 / amax),
+// and 32767 / amax overflows fp32 for amax below about 2^-113; scaling both by 2^64 is
+// exact and keeps the quotient finite, so tiny (even subnormal) slices encode like others.
+__device__ __forceinline__ float slice_prescale(float amax) {
+    return amax < 0x1p-64f ? 0x1p64f : 1.0f;
+}
+
 __device__ __forceinline__ void encode_floats(const float2 (&a)[16], Act16 &act);
 
 // Encodes one slice of a = silu(g) * u (see Act16).
@@ -133,16 +141,18 @@ __device__ __forceinline__ void encode_floats(const float2 (&a)[16], Act16 &act)
     float amax = 0.f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fmaxf(fabsf(a[k].x), fabsf(a[k].y)));
-    const float s_inv = amax > 0.f ? __fdividef(32767.0f, amax) : 0.f;
+    const float pre = slice_prescale(amax);
+    const float s_inv = amax > 0.f ? __fdividef(32767.0f, amax * pre) : 0.f;
     act.scale = amax * (1.0f / 32767.0f);
     // round(a * s_inv) by one fma with 1.5 * 2^23: the low 16 bits of the result are the
     // int16 code (two's complement), and the integer sum is the bit sum minus the bias
     const float2 sv = make_float2(s_inv, s_inv);
     const float2 mg = make_float2(12582912.0f, 12582912.0f);
+    const float2 pv = make_float2(pre, pre);
     uint32_t b[32];
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        const float2 r = __ffma2_rn(a[k], sv, mg);
+        const float2 r = __ffma2_rn(__fmul2_rn(a[k], pv), sv, mg);
         b[2 * k] = __float_as_uint(r.x);
         b[2 * k + 1] = __float_as_uint(r.y);
     }
@@ -209,14 +219,16 @@ __device__ __forceinline__ void encode_floats_pair(const float2 (&a)[8], int h, 
 #pragma unroll
     for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fmaxf(fabsf(a[k].x), fabsf(a[k].y)));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 16));
-    const float s_inv = amax > 0.f ? __fdividef(32767.0f, amax) : 0.f;
+    const float pre = slice_prescale(amax);
+    const float s_inv = amax > 0.f ? __fdividef(32767.0f, amax * pre) : 0.f;
     act.scale = amax * (1.0f / 32767.0f);
     const float2 sv = make_float2(s_inv, s_inv);
     const float2 mg = make_float2(12582912.0f, 12582912.0f);
+    const float2 pv = make_float2(pre, pre);
     uint32_t b[16];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const float2 r = __ffma2_rn(a[k], sv, mg);
+        const float2 r = __ffma2_rn(__fmul2_rn(a[k], pv), sv, mg);
         b[2 * k] = __float_as_uint(r.x);
         b[2 * k + 1] = __float_as_uint(r.y);
     }
@@ -291,13 +303,16 @@ __device__ __forceinline__ int dot32_q16(const Act16 &act, uint4 wv, const W4Key
     return lo + (hi >> 4);
 }
 
-// For MB activation rows: d[mb] = fp32 contribution of this vector position.
+// For MB activation rows: d[mb] = fp32 contribution of this vector position. The integer
+// sum is scaled by the activation scale first, then by the group scale: for a slice of
+// tiny activations (scale below about 2^-100) the product of the two scales alone would
+// fall into the subnormal range and lose precision, the sum times the scale does not.
 template <int MB>
 __device__ __forceinline__ void dot32(const Act16 *act, uint4 wv, const W4Keys &keys,
                                       float group_scale, float d[MB]) {
 #pragma unroll
     for (int mb = 0; mb < MB; ++mb)
-        d[mb] = (float)dot32_q16(act[mb], wv, keys) * (act[mb].scale * group_scale);
+        d[mb] = ((float)dot32_q16(act[mb], wv, keys) * act[mb].scale) * group_scale;
 }
 
 __host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v >> 1); }

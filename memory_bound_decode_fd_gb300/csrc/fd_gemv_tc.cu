@@ -608,4 +608,6 @@ cudaError_t launch_gemv_tc(const void *gate, const void *up, const void *qweight
     return cudaSuccess;
 }
 
+FD_DEFINE_STATUS_ACCESSOR(status_gemv_tc)
+
 }  // namespace fd

@@ -38,9 +38,9 @@
 //     sum per (row, m) in shared memory; every 64 rows the consumers sum over warps, add
 //     the residual if one is given (the down projection's residual-add epilogue) and
 //     store bf16 once per output.
-//   * Every mbarrier wait is bounded (fd_tma.cuh). If one gives up, the CTA stops
-//     computing, waits (bounded) for the copies it issued, writes NaN to all of its
-//     outputs (so the failure is visible to the caller) and exits.
+//   * Every mbarrier wait is bounded (fd_tma.cuh). If one gives up, the CTA records the
+//     timeout in the device status word (fd_device_status), stops computing, waits
+//     (bounded) for the copies it issued, writes NaN to all of its outputs and exits.
 #include <atomic>
 
 #include "fd_gemv_common.cuh"
@@ -53,6 +53,60 @@ namespace {
 constexpr int kMaxStages = 8;
 constexpr int kChunkRows = 8;  // rows per bulk-copy chunk
 
+// The fold's tail, run by every thread of every CTA after its rows are stored. Each CTA
+// publishes the sum of h^2 over its rows (warp sums, then warps in order) and takes a
+// ticket; the CTA that draws the last one sums the partials in CTA order (so the result
+// does not depend on arrival order), forms rstd = 1/sqrt(mean h^2 + eps) and writes the
+// whole normalised row, bf16(bf16(h * rstd) * w) (the two roundings of the separate
+// add-RMSNorm kernel), then resets the counter for the next call. No CTA waits for another.
+__device__ __forceinline__ void fold_tail(const FoldArgs &fold, float ss, int N, float *red,
+                                          int *last, bool failed) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (tid == 0) {
+        float t = 0.f;
+        for (int w = 0; w < nwarps; ++w) t += red[w];
+        // a CTA that gave up poisons the sum, so the normalised row is NaN like its outputs
+        fold.partials[blockIdx.x] = failed ? __int_as_float(0x7FC00000) : t;
+        __threadfence();  // the h rows and the partial before the ticket
+        const unsigned ticket = atomicAdd(fold.counter, 1u);
+        *last = (ticket == gridDim.x - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!*last) return;
+    __threadfence();  // every other CTA's h rows and partial are visible after its ticket
+    if (warp == 0) {
+        float t = 0.f;
+        for (int b = lane; b < (int)gridDim.x; b += 32) t += __ldcg(&fold.partials[b]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+        if (lane == 0) red[0] = t;
+    }
+    __syncthreads();
+    const float rstd = rsqrtf(fmaf(red[0], fold.inv_n, fold.eps));
+    const uint4 *h4 = reinterpret_cast<const uint4 *>(fold.res_out);
+    const uint4 *w4 = reinterpret_cast<const uint4 *>(fold.weight);
+    uint4 *o4 = reinterpret_cast<uint4 *>(fold.normed);
+    for (int v = tid; v < N / 8; v += blockDim.x) {
+        const uint4 hv = __ldcg(h4 + v);
+        const uint4 wv = w4[v];
+        const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+        uint32_t yw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t t = pack_bf16x2(bf16lo(hw[j]) * rstd, bf16hi(hw[j]) * rstd);
+            yw[j] = pack_bf16x2(bf16lo(t) * bf16lo(ww[j]), bf16hi(t) * bf16hi(ww[j]));
+        }
+        o4[v] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+    }
+    if (tid == 0) *fold.counter = 0u;  // ready for the next call in the stream
+}
+
 // NVEC_C / NG_C: compile-time K/32 and K/group for the common shapes (0 = runtime), so
 // the per-row shared-memory offsets fold into instruction immediates.
 //
@@ -63,16 +117,20 @@ constexpr int kChunkRows = 8;  // rows per bulk-copy chunk
 // behind it (loaded from global memory instead, they arrived behind the weights and the
 // call took 10-25 % longer on GB300); stages from act_first_stage on are filled only
 // after every consumer warp has read its slice.
-template <int MB, int R, int NVEC_C, int NG_C, int LPS, bool PLAIN>
+// FOLD: the next layer's add-RMSNorm in the tail (M = 1, SwiGLU form only); a separate
+// instantiation, so the other kernels' code is unchanged by it.
+template <int MB, int R, int NVEC_C, int NG_C, int LPS, bool PLAIN, bool FOLD>
 __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
     gemv_tma_kernel(const uint16_t *__restrict__ gate, const uint16_t *__restrict__ up,
                     const unsigned char *__restrict__ qweight,
                     const uint16_t *__restrict__ scales, const uint16_t *residual,
                     uint16_t *out, uint16_t *out2, int split, int ldo, int M, int K, int N,
                     int group, int rows_base, int rows_extra, int S,
-                    int w_rows, int act_first_stage, int weights_evict_first) {
+                    int w_rows, int act_first_stage, int weights_evict_first,
+                    int test_timeout, const FoldArgs fold) {
     static_assert(R * MB <= 32 && (R * MB & (R * MB - 1)) == 0, "R*MB: power of 2, <= 32");
     static_assert(LPS == 1 || (LPS == 2 && MB == 1 && R % 2 == 0), "paired lanes: M = 1 only");
+    static_assert(!FOLD || (MB == 1 && LPS == 2 && !PLAIN), "the fold: M = 1, SwiGLU form");
     static_assert(kWindowRows % R == 0, "window must hold whole chunks");
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -80,6 +138,8 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
     __shared__ __align__(8) uint64_t act_full_bar;
     __shared__ __align__(8) uint64_t act_free_bar;
     __shared__ int abort_flag;
+    __shared__ float fold_red[FOLD ? 32 : 1];
+    __shared__ int fold_last;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -112,25 +172,32 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
     // Lane 0 of the last warp is the producer. It initialises the barriers itself and
     // issues the activation copy and the chunks that fit in free stages before the
     // CTA-wide barrier, so they are in flight while the other warps start up.
+    // test_timeout (FD_LAUNCH_TEST_WAIT_TIMEOUT): short waits, and chunk 0 is never copied,
+    // so the consumers' wait for it runs out
+    const long long limit = test_timeout ? kTestWaitLimitCycles : kWaitLimitCycles;
+    const int skip_chunk = test_timeout ? 0 : -1;
     const bool producer = (warp == ncw && lane == 0);
+    float fold_ss = 0.f;  // the fold: this thread's sum of h^2 over the rows it stores
     uint64_t pol_w = 0, pol_s = 0;
     int issued = 0, ps = 0, pround = 0, pnc = 0, pc = 0;
     bool pok = true;
     auto issue_chunk = [&](int c) {
         if (act_in_smem && c == act_first_stage)
-            pok = mbar_wait_bounded(&act_free_bar, 0, &abort_flag);
+            pok = mbar_wait_bounded(&act_free_bar, 0, &abort_flag, limit);
         if (pok && pround > 0)
-            pok = mbar_wait_bounded(&empty_bar[ps], (pround - 1) & 1, &abort_flag);
+            pok = mbar_wait_bounded(&empty_bar[ps], (pround - 1) & 1, &abort_flag, limit);
         if (!pok) return;
-        const int rows = min(R, n_cnt - pnc * R);
-        const size_t n0 = (size_t)n_begin + (size_t)pnc * R;
-        const uint32_t wb = (uint32_t)rows * w_row_bytes;
-        const uint32_t sb = (uint32_t)rows * s_row_bytes;
-        mbar_arrive_expect_tx(&full_bar[ps], wb + sb);
-        bulk_g2s(smem + (size_t)ps * w_stage_bytes, qweight + n0 * w_row_bytes, wb,
-                 &full_bar[ps], pol_w);
-        bulk_g2s(s_region + (size_t)ps * s_stage_bytes, scales + n0 * ngroups, sb,
-                 &full_bar[ps], pol_s);
+        if (c != skip_chunk) {
+            const int rows = min(R, n_cnt - pnc * R);
+            const size_t n0 = (size_t)n_begin + (size_t)pnc * R;
+            const uint32_t wb = (uint32_t)rows * w_row_bytes;
+            const uint32_t sb = (uint32_t)rows * s_row_bytes;
+            mbar_arrive_expect_tx(&full_bar[ps], wb + sb);
+            bulk_g2s(smem + (size_t)ps * w_stage_bytes, qweight + n0 * w_row_bytes, wb,
+                     &full_bar[ps], pol_w);
+            bulk_g2s(s_region + (size_t)ps * s_stage_bytes, scales + n0 * ngroups, sb,
+                     &full_bar[ps], pol_s);
+        }
         issued = c + 1;
         if (++ps == S) { ps = 0; ++pround; }
         if (++pnc == n_chunks) pnc = 0;
@@ -175,17 +242,26 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
             // Every issued copy must land before the CTA exits: wait (bounded) on the
             // last phase of each stage that was used, and on the activation copy.
             for (int c = max(0, issued - S); c < issued; ++c) {
+                if (c == skip_chunk) continue;
                 const int st_idx = c % S;
                 const long long t0 = clock64();
-                while (!mbar_test_parity(&full_bar[st_idx], (c / S) & 1) &&
-                       clock64() - t0 < kWaitLimitCycles) {
+                while (!mbar_test_parity(&full_bar[st_idx], (c / S) & 1)) {
+                    if (clock64() - t0 > limit) {
+                        record_wait_timeout();
+                        break;
+                    }
                     __nanosleep(64);
                 }
             }
             if (act_in_smem) {
                 const long long t0 = clock64();
-                while (!mbar_test_parity(&act_full_bar, 0) && clock64() - t0 < kWaitLimitCycles)
+                while (!mbar_test_parity(&act_full_bar, 0)) {
+                    if (clock64() - t0 > limit) {
+                        record_wait_timeout();
+                        break;
+                    }
                     __nanosleep(64);
+                }
             }
         }
     } else if constexpr (LPS == 2) {
@@ -199,6 +275,11 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
         // now so that the final store does not wait on its load.
         float res0 = 0.f;
         if (residual && tid < min(n_cnt, kWindowRows)) res0 = bf16lo(residual[n_begin + tid]);
+        // the fold's residual stream of the same rows, likewise requested early
+        float fres0 = 0.f;
+        if constexpr (FOLD) {
+            if (tid < min(n_cnt, kWindowRows)) fres0 = bf16lo(fold.res_in[n_begin + tid]);
+        }
         const int hh = lane >> 4;
         const int slice = 16 * warp + (lane & 15);
         const int col = (slice * 32) / group;  // this lane's scale column
@@ -208,7 +289,7 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
             GateUpHalf gu;
             bool act_ok = true;
             if (act_in_smem) {
-                act_ok = mbar_wait_bounded(&act_full_bar, 0, &abort_flag);
+                act_ok = mbar_wait_bounded(&act_full_bar, 0, &abort_flag, limit);
                 if (act_ok) {
                     const uint4 *g4 = reinterpret_cast<const uint4 *>(act_smem + slice * 32 + 16 * hh);
                     gu.g[0] = g4[0];
@@ -250,7 +331,7 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
         int s = 0, phase = 0, nc = 0;
         for (int c = 0; c < total; ++c) {
             float part[kRowsPerLane];
-            const bool ok = mbar_wait_bounded(&full_bar[s], phase, &abort_flag);
+            const bool ok = mbar_wait_bounded(&full_bar[s], phase, &abort_flag, limit);
             const int rows_valid = min(R, n_cnt - nc * R);
             const uint4 *wst =
                 reinterpret_cast<const uint4 *>(smem + (size_t)s * w_stage_bytes) + slice + hh * nvec;
@@ -304,10 +385,22 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                     // The split output (gate/up halves) only where it is used: in the SwiGLU
                     // kernel the extra select changed the register allocation of the row
                     // loop and cost 2.8 % per call at K=14336 on GB300.
-                    if constexpr (PLAIN)
+                    if constexpr (PLAIN) {
                         *out_at(out, out2, split, ldo, 0, n) = *reinterpret_cast<uint16_t *>(&y);
-                    else
-                        out[n] = *reinterpret_cast<uint16_t *>(&y);
+                    } else {
+                        const uint16_t yb = *reinterpret_cast<uint16_t *>(&y);
+                        out[n] = yb;
+                        if constexpr (FOLD) {
+                            // the next layer's add: h = bf16(f32(y) + f32(residual)), the
+                            // rounded y as the separate kernel would read it
+                            const float r = window_base == 0 ? fres0 : bf16lo(fold.res_in[n]);
+                            const __nv_bfloat16 h = __float2bfloat16_rn(bf16lo(yb) + r);
+                            const uint16_t hb = *reinterpret_cast<const uint16_t *>(&h);
+                            fold.res_out[n] = hb;
+                            const float hf = bf16lo(hb);
+                            fold_ss = fmaf(hf, hf, fold_ss);
+                        }
+                    }
                 }
                 named_bar_sync(1, ncons);
                 window_base = last_chunk ? 0 : rows_done;
@@ -334,7 +427,7 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                     if (m0 + mb < M) {
                         GateUp gu;
                         if (act_in_smem) {
-                            if (mbar_wait_bounded(&act_full_bar, 0, &abort_flag)) {
+                            if (mbar_wait_bounded(&act_full_bar, 0, &abort_flag, limit)) {
                                 // Each lane's slice is 64 contiguous bytes, read in order.
                                 // (The reads are 4-way bank conflicted; rotating their order
                                 // by lane avoids that but needs per-lane register selects,
@@ -379,7 +472,7 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                 }
             }
             float part[R * MB];
-            const bool ok = mbar_wait_bounded(&full_bar[s], phase, &abort_flag);
+            const bool ok = mbar_wait_bounded(&full_bar[s], phase, &abort_flag, limit);
             const int rows_valid = min(R, n_cnt - nc * R);
             const uint4 *wst = reinterpret_cast<const uint4 *>(smem + (size_t)s * w_stage_bytes) + tid;
             const uint16_t *sst =
@@ -460,16 +553,17 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                 out[(size_t)m * N + n_begin + r] = 0x7FC0;
         }
     }
+    if constexpr (FOLD) fold_tail(fold, fold_ss, N, fold_red, &fold_last, abort_flag != 0);
 }
 
-template <int MB, int R, int NVEC_C, int NG_C, int LPS, bool PLAIN>
+template <int MB, int R, int NVEC_C, int NG_C, int LPS, bool PLAIN, bool FOLD>
 cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
                        const void *qweight, const void *scales, const void *residual,
                        GemvOut o, int M, int K, int N, int group, cudaStream_t stream,
-                       bool *launched) {
+                       bool *launched, const FoldArgs *fold) {
     static std::atomic<uint64_t> attr_done{0};
     static std::atomic<int> func_cache{-1};  // static shared memory | registers << 20
-    auto kern = gemv_tma_kernel<MB, R, NVEC_C, NG_C, LPS, PLAIN>;
+    auto kern = gemv_tma_kernel<MB, R, NVEC_C, NG_C, LPS, PLAIN, FOLD>;
     int fc = func_cache.load(std::memory_order_relaxed);
     if (fc < 0) {
         cudaFuncAttributes fa;
@@ -483,6 +577,8 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
                     fc & 0xFFFFF, fc >> 20, M, K, N, group, MB, LPS, R, kMaxStages, PLAIN ? 1 : 0};
     TmaPlan plan{};
     if (!plan_gemv_tma(in, &plan)) return cudaSuccess;  // not launched
+    if (fold && plan.grid > kFoldMaxCtas) return cudaSuccess;  // not launched: no room for partials
+    const FoldArgs fa = fold ? *fold : FoldArgs{};
     const int S = plan.S, w_rows = plan.w_rows, act_first_stage = plan.act_first_stage;
     const int grid = plan.grid, rows_base = plan.rows_base, rows_extra = plan.rows_extra;
     const size_t smem = plan.smem;
@@ -507,7 +603,7 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
                         static_cast<const uint16_t *>(residual), static_cast<uint16_t *>(o.out),
                         static_cast<uint16_t *>(o.out2), o.split, o.ldo, M, K, N, group,
                         rows_base, rows_extra, S, w_rows, act_first_stage,
-                        M <= MB ? 1 : 0);
+                        M <= MB ? 1 : 0, (launch_flags() & FD_LAUNCH_TEST_WAIT_TIMEOUT) ? 1 : 0, fa);
     *launched = true;
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
@@ -516,17 +612,18 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *gate, const void *up,
 // LPS = 2 (two lanes per 32-k slice) for one activation row, else one lane per slice.
 // The SwiGLU form is specialised for the down-projection widths, the plain form for the
 // model width (the gate/up projection's K).
-template <int MB, bool PLAIN>
+template <int MB, bool PLAIN, bool FOLD>
 cudaError_t launch_mb(const DeviceInfo &di, const void *gate, const void *up,
                       const void *qweight, const void *scales, const void *residual, GemvOut o,
-                      int M, int K, int N, int group, cudaStream_t stream, bool *launched) {
+                      int M, int K, int N, int group, cudaStream_t stream, bool *launched,
+                      const FoldArgs *fold) {
     constexpr int R = kChunkRows;
     constexpr int LPS = MB == 1 ? 2 : 1;
 #define FD_SHAPE(KK, GG)                                                                          \
     if (K == KK && group == GG)                                                                   \
-        return launch_cfg<MB, R, KK / 32, KK / GG, LPS, PLAIN>(di, gate, up, qweight, scales,      \
+        return launch_cfg<MB, R, KK / 32, KK / GG, LPS, PLAIN, FOLD>(di, gate, up, qweight, scales,\
                                                               residual, o, M, K, N, group, stream, \
-                                                              launched);
+                                                              launched, fold);
     if constexpr (PLAIN) {
         FD_SHAPE(4096, 128)
     } else {
@@ -536,8 +633,8 @@ cudaError_t launch_mb(const DeviceInfo &di, const void *gate, const void *up,
         FD_SHAPE(1024, 128)
     }
 #undef FD_SHAPE
-    return launch_cfg<MB, R, 0, 0, LPS, PLAIN>(di, gate, up, qweight, scales, residual, o, M, K,
-                                               N, group, stream, launched);
+    return launch_cfg<MB, R, 0, 0, LPS, PLAIN, FOLD>(di, gate, up, qweight, scales, residual, o,
+                                                     M, K, N, group, stream, launched, fold);
 }
 
 }  // namespace
@@ -550,24 +647,32 @@ bool gemv_tma_supported(int M, int K, int group) {
 
 cudaError_t launch_gemv_tma(const void *gate, const void *up, const void *qweight,
                             const void *scales, const void *residual, GemvOut o, int M, int K,
-                            int N, int group, cudaStream_t stream, bool *launched) {
+                            int N, int group, cudaStream_t stream, bool *launched,
+                            const FoldArgs *fold) {
     *launched = false;
     if (!gemv_tma_supported(M, K, group)) return cudaSuccess;
     DeviceInfo di;
     cudaError_t err = device_info(&di);
     if (err != cudaSuccess) return err;
+    if (fold) {
+        if (M != 1 || up == nullptr || residual != nullptr) return cudaSuccess;
+        return launch_mb<1, false, true>(di, gate, up, qweight, scales, residual, o, M, K, N,
+                                         group, stream, launched, fold);
+    }
     if (up == nullptr) {
         if (M == 1)
-            return launch_mb<1, true>(di, gate, up, qweight, scales, residual, o, M, K, N, group,
-                                      stream, launched);
-        return launch_mb<2, true>(di, gate, up, qweight, scales, residual, o, M, K, N, group,
-                                  stream, launched);
+            return launch_mb<1, true, false>(di, gate, up, qweight, scales, residual, o, M, K, N,
+                                             group, stream, launched, nullptr);
+        return launch_mb<2, true, false>(di, gate, up, qweight, scales, residual, o, M, K, N,
+                                         group, stream, launched, nullptr);
     }
     if (M == 1)
-        return launch_mb<1, false>(di, gate, up, qweight, scales, residual, o, M, K, N, group,
-                                   stream, launched);
-    return launch_mb<2, false>(di, gate, up, qweight, scales, residual, o, M, K, N, group,
-                               stream, launched);
+        return launch_mb<1, false, false>(di, gate, up, qweight, scales, residual, o, M, K, N,
+                                          group, stream, launched, nullptr);
+    return launch_mb<2, false, false>(di, gate, up, qweight, scales, residual, o, M, K, N, group,
+                                      stream, launched, nullptr);
 }
+
+FD_DEFINE_STATUS_ACCESSOR(status_gemv_tma)
 
 }  // namespace fd

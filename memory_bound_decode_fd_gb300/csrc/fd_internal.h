@@ -69,12 +69,34 @@ struct GemvOut {
     int ldo;
 };
 
+// The next layer's residual add + RMSNorm folded into the tail of an M = 1 GEMV
+// (fd_swiglu_w4a16_gemv_add_rmsnorm): each CTA writes h = bf16(y + res_in) of its rows to
+// res_out and its partial sum of h^2 to partials[blockIdx.x]; the last CTA to arrive
+// (atomic ticket on *counter) normalises the whole row into `normed` and resets *counter.
+// A null `normed` means no fold.
+struct FoldArgs {
+    const uint16_t *res_in;
+    uint16_t *res_out;
+    const uint16_t *weight;
+    uint16_t *normed;
+    float *partials;
+    unsigned *counter;
+    float eps;
+    float inv_n;
+};
+// Scratch of the fold: the counter, then one fp32 partial per CTA.
+constexpr int kFoldPartialsOffset = 256;
+constexpr int kFoldMaxCtas = (FD_FOLD_SCRATCH_BYTES - kFoldPartialsOffset) / 4;
+
 // `up` null: the activation is gate itself (a plain W4A16 GEMV), else silu(gate) * up.
 // `residual` (bf16 [M, N], may equal `out`, or null) is added to the sum before the single
-// rounding to bf16 (the residual-add epilogue of the down projection).
+// rounding to bf16 (the residual-add epilogue of the down projection). `fold` (M = 1, SwiGLU
+// form, no residual) adds the next layer's add + RMSNorm; a fold the kernel cannot run
+// (grid above kFoldMaxCtas) leaves *launched false.
 cudaError_t launch_gemv_tma(const void *gate, const void *up, const void *qweight,
                             const void *scales, const void *residual, GemvOut o, int M, int K,
-                            int N, int group, cudaStream_t stream, bool *launched);
+                            int N, int group, cudaStream_t stream, bool *launched,
+                            const FoldArgs *fold = nullptr);
 // Tensor-core path (tcgen05) for batched decode; sets *launched = false when the shape
 // is outside its rules (K % 1024, N % 128, group % 64, (K / group) % 8).
 bool gemv_tc_supported(int M, int K, int N, int group);
@@ -94,6 +116,13 @@ cudaError_t launch_nvfp4_mm(const void *x, const void *x_sf, const void *w, cons
                             cudaStream_t stream);
 cudaError_t launch_w4_dequant_debug(const void *qweight, const void *scales, float *out,
                                     int K, int N, int group, cudaStream_t stream);
+
+// Host accessors of the device status words of the files whose kernels have bounded waits
+// (FD_DEFINE_STATUS_ACCESSOR in fd_tma.cuh): copy the word to *out on `stream`, then zero it
+// if `clear`.
+cudaError_t status_gemv_tma(cudaStream_t stream, unsigned *out, bool clear);
+cudaError_t status_gemv_tc(cudaStream_t stream, unsigned *out, bool clear);
+cudaError_t status_nvfp4(cudaStream_t stream, unsigned *out, bool clear);
 
 // ------------------------------------------------------------------------------------
 // Device helpers.

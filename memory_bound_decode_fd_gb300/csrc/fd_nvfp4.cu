@@ -18,11 +18,12 @@
 //     warp 0 issues every tensor-map copy at once: per 256-k stage one 128-byte-swizzled
 //     box of 128 weight rows and one of NPAD activation rows, already in the tensor core's
 //     K-major operand layout (no transform on the CUDA cores).
-//   * Four warps copy the E4M3 scale factors into tensor memory (tcgen05.st): for each
-//     K = 64 step, 4 columns for the weights and 4 for the activations; lane l of every
-//     32-lane quarter holds, in column c, the four 16-element scales of row l + 32c.
+//   * Four warps copy the E4M3 scale factors into tensor memory (tcgen05.st), one 256-k
+//     stage at a time: for each K = 64 step, 4 columns for the weights and 4 for the
+//     activations; lane l of every 32-lane quarter holds, in column c, the four
+//     16-element scales of row l + 32c.
 //   * Warp 1 lane 0 issues one block-scaled MMA per K = 64 step (M = 128, N = NPAD) into a
-//     TMEM accumulator as each stage lands, then commits.
+//     TMEM accumulator as each stage's operands and scales are ready, then commits.
 //   * The same four warps read the accumulator (lane = weight row), exchange partial sums
 //     through the cluster, and the owner of each row range applies alpha (read from device
 //     memory, the page's 0-dim multiplier) to the fp32 sum and rounds once to bf16.
@@ -40,7 +41,6 @@ namespace {
 
 constexpr int kNfThreads = 6 * 32;   // producer, MMA, four scale / epilogue warps
 constexpr int kNfFirstEpi = 2;
-constexpr uint32_t kNfSfCol0 = 128;  // TMEM column of the first scale factors
 
 // Bounded wait that ignores the abort flag: used where the CTA must not go on before the
 // hardware is done (copies landing, MMAs completing), even after a failure.
@@ -55,13 +55,13 @@ __global__ void __launch_bounds__(kNfThreads, 1)
                     const __grid_constant__ CUtensorMap map_x,
                     const __grid_constant__ CUtensorMap map_wsf,
                     const __grid_constant__ CUtensorMap map_xsf, const float *alpha,
-                    uint16_t *out, int M, int N, int k_cta, uint32_t off_x, uint32_t off_wsf,
-                    uint32_t off_xsf) {
+                    uint16_t *out, int M, int N, int s_total, uint32_t sf_row, int rows_own,
+                    uint32_t tmem_cols, uint32_t off_x, uint32_t off_wsf, uint32_t off_xsf) {
     static_assert(NPAD == 16 || NPAD == 32 || NPAD == 64 || NPAD == 128, "MMA N");
     constexpr uint32_t kXStage = NPAD * kNfStageK / 2;    // activation bytes per stage
-    constexpr uint32_t kStageTx = kNfWStage + kXStage;
-    __shared__ __align__(8) uint64_t full_bar[kNfMaxStages];
-    __shared__ __align__(8) uint64_t sf_full, sf_ready, acc_full;
+    __shared__ __align__(8) uint64_t full_bar[kNfMaxStages];  // a stage's operands
+    __shared__ __align__(8) uint64_t sf_ready[kNfMaxStages];  // a stage's scales are in TMEM
+    __shared__ __align__(8) uint64_t sf_full, acc_full;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ uint32_t peer_abort[kNfMaxSplit];
@@ -75,23 +75,24 @@ __global__ void __launch_bounds__(kNfThreads, 1)
     const uint32_t rank = cluster_ctarank();
     const int split = (int)gridDim.x;
     const int n0 = blockIdx.y * kNfRows;
-    const int k0 = (int)rank * k_cta;
-    const int S = k_cta / kNfStageK;
-    const int KB = k_cta / kNfMmaK;            // K = 64 steps
-    const uint32_t sf_row = (uint32_t)k_cta / 16;  // scale bytes per row in this slice
-    const int rows_own = kNfRows / split;      // output rows each cluster rank finishes
+    // this rank's K slice: stages [s_begin, s_end) of the s_total 256-k stages
+    const int s_begin = nvfp4_first_stage((int)rank, s_total, split);
+    const int S = nvfp4_first_stage((int)rank + 1, s_total, split) - s_begin;
+    const int k0 = s_begin * kNfStageK;
 
     if (tid == 0) {
-        for (int s = 0; s < kNfMaxStages; ++s) mbar_init(&full_bar[s], 1);
+        for (int s = 0; s < kNfMaxStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&sf_ready[s], 4);
+        }
         mbar_init(&sf_full, 1);
-        mbar_init(&sf_ready, 4);
         mbar_init(&acc_full, 1);
         abort_flag = 0;
         for (int p = 0; p < kNfMaxSplit; ++p) peer_abort[p] = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(&tmem_slot, kNfTmemCols);
+        tmem_alloc(&tmem_slot, tmem_cols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -112,12 +113,14 @@ __global__ void __launch_bounds__(kNfThreads, 1)
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();  // each weight byte is read once
             const uint64_t pol_x = policy_evict_last();   // every weight tile reads them
+            // the scale boxes are max_stages wide: a shorter slice copies a few unused (or
+            // out-of-range, zero-filled) columns past its end
             mbar_arrive_expect_tx(&sf_full, (uint32_t)(kNfRows + NPAD) * sf_row);
             tma_load_2d(smem + off_wsf, &map_wsf, k0 / 16, n0, &sf_full, pol_w);
             tma_load_2d(smem + off_xsf, &map_xsf, k0 / 16, 0, &sf_full, pol_x);
             for (int s = 0; s < S; ++s) {
                 const int xb = (k0 + s * kNfStageK) / 2;  // byte column, a multiple of 128
-                mbar_arrive_expect_tx(&full_bar[s], kStageTx);
+                mbar_arrive_expect_tx(&full_bar[s], kNfWStage + kXStage);
                 tma_load_2d(smem + (size_t)s * kNfWStage, &map_w, xb, n0, &full_bar[s], pol_w);
                 tma_load_2d(smem + off_x + (size_t)s * kXStage, &map_x, xb, 0, &full_bar[s], pol_x);
             }
@@ -132,11 +135,10 @@ __global__ void __launch_bounds__(kNfThreads, 1)
         grid_dep_launch();
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_nvf4(kNfRows, NPAD);
-            bool ok = mbar_wait_bounded(&sf_ready, 0, &abort_flag);
-            tc_fence_after();
             const uint32_t w_base = smem_u32(smem);
             const uint32_t x_base = smem_u32(smem + off_x);
-            for (int s = 0; s < S && ok; ++s) {
+            for (int s = 0; s < S; ++s) {
+                if (!mbar_wait_bounded(&sf_ready[s], 0, &abort_flag)) break;
                 if (!mbar_wait_bounded(&full_bar[s], 0, &abort_flag)) break;
                 tc_fence_after();
 #pragma unroll
@@ -158,27 +160,38 @@ __global__ void __launch_bounds__(kNfThreads, 1)
         grid_dep_launch();
         const uint32_t q = (uint32_t)(warp & 3);  // this warp's TMEM lane quarter
         const bool ok = mbar_wait_bounded(&sf_full, 0, &abort_flag);
-        if (ok) {
-            const unsigned char *wsf = smem + off_wsf;
-            const unsigned char *xsf = smem + off_xsf;
-            const uint32_t lane_addr = tmem + ((32u * q) << 16);
-            for (int kb = 0; kb < KB; ++kb) {
-                uint32_t a[4], b[4];
+        const unsigned char *wsf = smem + off_wsf;
+        const unsigned char *xsf = smem + off_xsf;
+        const uint32_t lane_addr = tmem + ((32u * q) << 16);
+        // One stage (4 K = 64 steps) at a time: a 16-byte load gives a row's scales of all
+        // 4 steps, so each lane loads its 4 weight rows and 4 activation rows once per
+        // stage (rows 64 bytes apart: at most 4-way bank conflicts), and the MMA thread may
+        // start on a stage as soon as its scales are in TMEM.
+        for (int s = 0; s < S; ++s) {
+            if (ok) {
+                uint4 a[4], b[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int r = lane + 32 * c;
-                    a[c] = *reinterpret_cast<const uint32_t *>(wsf + (size_t)r * sf_row + 4 * kb);
-                    b[c] = r < NPAD ? *reinterpret_cast<const uint32_t *>(xsf + (size_t)r * sf_row + 4 * kb)
-                                    : 0u;
+                    a[c] = *reinterpret_cast<const uint4 *>(wsf + (size_t)r * sf_row + 16 * s);
+                    b[c] = r < NPAD ? *reinterpret_cast<const uint4 *>(xsf + (size_t)r * sf_row + 16 * s)
+                                    : make_uint4(0, 0, 0, 0);
                 }
-                tmem_st_x4(lane_addr + kNfSfCol0 + 8u * kb, a[0], a[1], a[2], a[3]);
-                tmem_st_x4(lane_addr + kNfSfCol0 + 8u * kb + 4u, b[0], b[1], b[2], b[3]);
+                const uint32_t col = kNfSfCol0 + kNfSfColsPerStage * s;  // 8 per K = 64 step
+                tmem_st_x4(lane_addr + col + 0u, a[0].x, a[1].x, a[2].x, a[3].x);
+                tmem_st_x4(lane_addr + col + 4u, b[0].x, b[1].x, b[2].x, b[3].x);
+                tmem_st_x4(lane_addr + col + 8u, a[0].y, a[1].y, a[2].y, a[3].y);
+                tmem_st_x4(lane_addr + col + 12u, b[0].y, b[1].y, b[2].y, b[3].y);
+                tmem_st_x4(lane_addr + col + 16u, a[0].z, a[1].z, a[2].z, a[3].z);
+                tmem_st_x4(lane_addr + col + 20u, b[0].z, b[1].z, b[2].z, b[3].z);
+                tmem_st_x4(lane_addr + col + 24u, a[0].w, a[1].w, a[2].w, a[3].w);
+                tmem_st_x4(lane_addr + col + 28u, b[0].w, b[1].w, b[2].w, b[3].w);
+                tmem_st_wait();
             }
-            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sf_ready[s]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sf_ready);
         // the accumulator is complete once the MMA thread's commit fires
         if (lane == 0) nf_wait_hw(&acc_full, 0);
         __syncwarp();
@@ -226,8 +239,9 @@ __global__ void __launch_bounds__(kNfThreads, 1)
             const int j = i / rows_own, rr = i % rows_own;
             float acc = 0.f;
             for (int src = 0; src < split; ++src) acc += rv[(src * NPAD + j) * rows_own + rr];
-            const int n = n0 + (int)rank * rows_own + rr;
-            if (j < M && n < N) {
+            const int row = (int)rank * rows_own + rr;
+            const int n = n0 + row;
+            if (j < M && n < N && row < kNfRows) {
                 const __nv_bfloat16 y = __float2bfloat16_rn(a * acc);
                 out[(size_t)j * N + n] = failed ? (uint16_t)0x7FC0 : *reinterpret_cast<const uint16_t *>(&y);
             }
@@ -237,7 +251,7 @@ __global__ void __launch_bounds__(kNfThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kNfTmemCols);
+        tmem_dealloc(tmem, tmem_cols);
     }
 }
 
@@ -290,32 +304,35 @@ cudaError_t launch_npad(const DeviceInfo &di, const unsigned char *x, const unsi
         static_smem = (int)fa.sharedSizeBytes;
         static_smem_cache.store(static_smem, std::memory_order_relaxed);
     }
-    Nvfp4Plan p{};
-    if (!plan_nvfp4(mc, K, N, di.max_smem_optin - static_smem, &p) || p.npad != NPAD)
-        return cudaErrorInvalidValue;
-    CUtensorMap mw, mx, mwsf, mxsf;
-    if (!encode_bytes_2d(&mw, w, (uint64_t)K / 2, (uint64_t)N, kNfStageK / 2, kNfRows,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_bytes_2d(&mx, x, (uint64_t)K / 2, (uint64_t)mc, kNfStageK / 2, NPAD,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_bytes_2d(&mwsf, w_sf, (uint64_t)K / 16, (uint64_t)N, (uint32_t)p.k_cta / 16,
-                         kNfRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_bytes_2d(&mxsf, x_sf, (uint64_t)K / 16, (uint64_t)mc, (uint32_t)p.k_cta / 16,
-                         NPAD, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
+    const int budget = di.max_smem_optin - static_smem;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   di.max_smem_optin - static_smem);
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
+        if (err != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   cudaSharedmemCarveoutMaxShared);
         if (err != cudaSuccess) return err;
         attr_done.fetch_or(bit, std::memory_order_acq_rel);
     }
+    Nvfp4Plan p{};
+    if (!plan_nvfp4(mc, K, N, budget, &p) || p.npad != NPAD) return cudaErrorInvalidValue;
+    CUtensorMap mw, mx, mwsf, mxsf;
+    if (!encode_bytes_2d(&mw, w, (uint64_t)K / 2, (uint64_t)N, kNfStageK / 2, kNfRows,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_bytes_2d(&mx, x, (uint64_t)K / 2, (uint64_t)mc, kNfStageK / 2, NPAD,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_bytes_2d(&mwsf, w_sf, (uint64_t)K / 16, (uint64_t)N, p.sf_row, kNfRows,
+                         CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_bytes_2d(&mxsf, x_sf, (uint64_t)K / 16, (uint64_t)mc, p.sf_row, NPAD,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
     err = launch_kernel(kern, dim3((unsigned)p.split, (unsigned)p.n_tiles), dim3(kNfThreads),
                         (size_t)p.smem, stream, p.split, mw, mx, mwsf, mxsf, alpha, out, mc, N,
-                        p.k_cta, p.off_x, p.off_wsf, p.off_xsf);
+                        p.s_total, p.sf_row, p.rows_own, (uint32_t)p.tmem_cols, p.off_x,
+                        p.off_wsf, p.off_xsf);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
@@ -328,9 +345,15 @@ cudaError_t launch_nvfp4_mm(const void *x, const void *x_sf, const void *w, cons
     DeviceInfo di;
     cudaError_t err = device_info(&di);
     if (err != cudaSuccess) return err;
-    // batches above 128 rows run in launches of 128 activation rows
-    for (int m0 = 0; m0 < M; m0 += kNfMaxBatch) {
-        const int mc = M - m0 < kNfMaxBatch ? M - m0 : kNfMaxBatch;
+    // batches above 128 rows run in launches of 128 activation rows; where 128 padded rows
+    // do not fit shared memory (K above 12288) in launches of 64
+    Nvfp4Plan probe{};
+    const int widest = K / kNfStageK < kNfMaxSplit ? K / kNfStageK : kNfMaxSplit;
+    const int chunk = plan_nvfp4_split(kNfMaxBatch, K, N, widest, di.max_smem_optin - 1024, &probe)
+                          ? kNfMaxBatch
+                          : kNfMaxBatch / 2;
+    for (int m0 = 0; m0 < M; m0 += chunk) {
+        const int mc = M - m0 < chunk ? M - m0 : chunk;
         const unsigned char *xm = static_cast<const unsigned char *>(x) + (size_t)m0 * (K / 2);
         const unsigned char *xsfm = static_cast<const unsigned char *>(x_sf) + (size_t)m0 * (K / 16);
         uint16_t *om = static_cast<uint16_t *>(out) + (size_t)m0 * N;
@@ -347,5 +370,7 @@ cudaError_t launch_nvfp4_mm(const void *x, const void *x_sf, const void *w, cons
     }
     return cudaSuccess;
 }
+
+FD_DEFINE_STATUS_ACCESSOR(status_nvfp4)
 
 }  // namespace fd

@@ -1,8 +1,9 @@
 // fd_nvfp4_plan.h - launch planning of the NVFP4 block-scaled MMA kernel (fd_nvfp4.cu):
-// the K split over a cluster, the padded batch and the shared-memory layout, as a pure
-// host function (no CUDA calls, so it is testable without a GPU).
+// the K split over a cluster, the padded batch, the shared-memory layout and the tensor
+// memory, as a pure host function (no CUDA calls, so it is testable without a GPU).
 #pragma once
 
+#include <cuda_runtime.h>  // __host__ __device__
 #include <stdint.h>
 
 namespace fd {
@@ -11,24 +12,22 @@ constexpr int kNfRows = 128;          // weight rows per CTA (the MMA's M)
 constexpr int kNfStageK = 256;        // k per copy stage: one 128-byte row of packed FP4
 constexpr int kNfMmaK = 64;           // k per block-scaled MMA
 constexpr uint32_t kNfWStage = kNfRows * kNfStageK / 2;  // weight bytes per stage: 16384
-constexpr int kNfMaxKCta = 1024;      // k per CTA
-constexpr int kNfMaxStages = kNfMaxKCta / kNfStageK;
-constexpr int kNfMaxSplit = 8;        // CTAs per cluster along K
-constexpr int kNfMaxK = kNfMaxKCta * kNfMaxSplit;
+constexpr int kNfMaxStages = 12;      // stages per CTA (all resident; mbarrier slots)
+constexpr int kNfMaxSplit = 8;        // CTAs per cluster along K (portable cluster size)
+constexpr int kNfMaxK = 16384;        // checked by the C ABI (FD_NVFP4_MAX_K)
 constexpr int kNfMaxBatch = 128;      // activation rows per launch (the MMA's N, padded)
-constexpr uint32_t kNfTmemCols = 256; // accumulator (<= 128 columns) + scale factors (<= 128)
-// Shared memory each CTA requests at least: with 80 KB a third CTA never fits on an SM
-// (3 x (80 + 1) KB > 228 KB), so at most two share one and their 2 x 256 TMEM columns are
-// always free. A third CTA would wait in tcgen05.alloc while the others of its cluster
-// wait for it at a cluster barrier, which could hold every CTA involved.
-constexpr uint32_t kNfMinSmem = 80 * 1024;
+constexpr uint32_t kNfSfCol0 = 128;   // TMEM column of the first scale factors (D below it)
+constexpr uint32_t kNfSfColsPerStage = 32;  // 4 K = 64 steps x (4 weight + 4 activation)
 
 struct Nvfp4Plan {
     int split;      // CTAs per cluster along K
-    int k_cta;      // k per CTA
-    int stages;     // 256-k copy stages per CTA (all resident)
+    int s_total;    // 256-k stages in K
+    int max_stages; // stages of the largest K slice (rank r: stages [r S / split, (r+1) S / split))
     int npad;       // the batch padded to the MMA's N (16, 32, 64 or 128)
     int n_tiles;    // 128-row weight tiles (clusters)
+    int tmem_cols;  // 256 or 512
+    int rows_own;   // output rows each cluster rank finishes (ceil(128 / split))
+    uint32_t sf_row;                   // scale bytes per row copied (max_stages x 16)
     uint32_t off_x, off_wsf, off_xsf;  // shared-memory offsets (weights at 0)
     uint32_t recv_bytes;               // the cluster reduction's buffer (from offset 0)
     uint32_t smem;                     // dynamic shared memory per CTA, with alignment slack
@@ -37,38 +36,63 @@ struct Nvfp4Plan {
 // The padded batch of `m` activation rows (1 <= m <= 128).
 inline int nvfp4_npad(int m) { return m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 128; }
 
-// The smallest split in {1, 2, 4, 8} whose K slice is a whole number of 256-k stages and
-// at most 1024 k; 0 if there is none (K not a multiple of 256, or above 8192).
-inline int nvfp4_split(int K) {
-    if (K <= 0 || K % kNfStageK != 0) return 0;
-    for (int s = 1; s <= kNfMaxSplit; s *= 2)
-        if (K % (kNfStageK * s) == 0 && K / s <= kNfMaxKCta) return s;
-    return 0;
+// First stage of rank r's K slice (the slice is [first(r), first(r + 1))).
+__host__ __device__ inline int nvfp4_first_stage(int r, int s_total, int split) {
+    return (int)((long long)r * s_total / split);
 }
 
-// Fills `p` for one launch of `m` (1..128) activation rows; false when the shape is
-// outside the kernel's rules or its shared memory exceeds `smem_budget`.
-inline bool plan_nvfp4(int m, int K, int N, int smem_budget, Nvfp4Plan *p) {
-    if (m < 1 || m > kNfMaxBatch || N < 1) return false;
-    const int split = nvfp4_split(K);
-    if (split == 0) return false;
+// Fills `p` for one launch of `m` (1..128) activation rows with K split over `split` CTAs;
+// false when the shape is outside the kernel's rules for that split or its shared memory
+// exceeds `smem_budget`.
+inline bool plan_nvfp4_split(int m, int K, int N, int split, int smem_budget, Nvfp4Plan *p) {
+    if (m < 1 || m > kNfMaxBatch || N < 1 || K <= 0 || K % kNfStageK != 0 || K > kNfMaxK)
+        return false;
+    if (split < 1 || split > kNfMaxSplit || split > K / kNfStageK) return false;
     p->split = split;
-    p->k_cta = K / split;
-    p->stages = p->k_cta / kNfStageK;
+    p->s_total = K / kNfStageK;
+    p->max_stages = (p->s_total + split - 1) / split;
+    // tensor memory: the accumulator below column 128, scale columns above it
+    if (p->max_stages > kNfMaxStages ||
+        kNfSfCol0 + kNfSfColsPerStage * (uint32_t)p->max_stages > 512u)
+        return false;
     p->npad = nvfp4_npad(m);
     p->n_tiles = (N + kNfRows - 1) / kNfRows;
+    p->tmem_cols = kNfSfCol0 + kNfSfColsPerStage * p->max_stages <= 256 ? 256 : 512;
+    p->rows_own = (kNfRows + split - 1) / split;
     const uint32_t x_stage = (uint32_t)p->npad * kNfStageK / 2;
-    const uint32_t sf_row = (uint32_t)p->k_cta / 16;
-    p->off_x = (uint32_t)p->stages * kNfWStage;
-    p->off_wsf = p->off_x + (uint32_t)p->stages * x_stage;
-    p->off_xsf = p->off_wsf + (uint32_t)kNfRows * sf_row;
-    const uint32_t end = p->off_xsf + (uint32_t)p->npad * sf_row;
-    // [src rank][npad][128 / split] fp32: npad * 128 * 4 bytes for any split
-    p->recv_bytes = (uint32_t)p->npad * kNfRows * 4;
+    p->sf_row = (uint32_t)p->max_stages * 16;
+    p->off_x = (uint32_t)p->max_stages * kNfWStage;
+    p->off_wsf = p->off_x + (uint32_t)p->max_stages * x_stage;
+    p->off_xsf = p->off_wsf + (uint32_t)kNfRows * p->sf_row;
+    const uint32_t end = p->off_xsf + (uint32_t)p->npad * p->sf_row;
+    // [src rank][npad][rows_own] fp32
+    p->recv_bytes = (uint32_t)split * p->npad * p->rows_own * 4;
     const uint32_t used = end > p->recv_bytes ? end : p->recv_bytes;
     p->smem = used + 1024;  // the kernel aligns its base to 1024 bytes
-    if (p->smem < kNfMinSmem) p->smem = kNfMinSmem;
+    // Shared memory bounds the CTAs per SM so that their TMEM allocations always fit the
+    // SM's 512 columns: with 256 columns at most two CTAs (each >= 80 KB: three never fit
+    // in 228 KB), with 512 at most one (each >= 116 KB). A CTA over the limit would wait
+    // in tcgen05.alloc while the others of its cluster wait for it at a cluster barrier.
+    const uint32_t min_smem = p->tmem_cols == 256 ? 80u * 1024 : 116u * 1024;
+    if (p->smem < min_smem) p->smem = min_smem;
     return smem_budget > 0 && p->smem <= (uint32_t)smem_budget;
+}
+
+// The split for one launch: the smallest split whose K slices have at most 4 stages (256
+// TMEM columns and ~110 KB of shared memory per CTA, so two CTAs share an SM), else the
+// smallest split whose plan fits. Measured on GB300 for M=64 K=4096 N=6144: split 4 (192
+// CTAs, 4 stages) 10.9 us, split 2 (96 CTAs, 8 stages) 16.2 us: more CTAs streaming at once
+// is what counts. Returns false if no split fits.
+inline bool plan_nvfp4(int m, int K, int N, int smem_budget, Nvfp4Plan *p) {
+    for (int pass = 0; pass < 2; ++pass)
+        for (int s = 1; s <= kNfMaxSplit; ++s) {
+            Nvfp4Plan c{};
+            if (!plan_nvfp4_split(m, K, N, s, smem_budget, &c)) continue;
+            if (pass == 0 && c.max_stages > 4) continue;
+            *p = c;
+            return true;
+        }
+    return false;
 }
 
 }  // namespace fd

@@ -131,13 +131,14 @@ __device__ __forceinline__ uint64_t smem_desc_interleaved(uint32_t saddr, uint32
 
 // Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzle layout
 // that a tensor-map copy with CU_TENSOR_MAP_SWIZZLE_128B writes: rows of 128 bytes, 16-byte
-// chunk c of row r stored at chunk c ^ (r & 7), 8-row atoms of 1024 bytes (the stride
-// between 8-row groups, SBO). The leading-dimension offset is unused for this layout (1).
+// chunk c of row r stored at chunk c ^ (r & 7), 8-row atoms of 1024 bytes; `sbo` is the
+// stride between 8-row groups (1024 when the atoms are contiguous, a multiple of 1024
+// otherwise). The leading-dimension offset is unused for this layout (1).
 // The atom must be 1024-byte aligned; a K step inside the 128-byte row advances the start
 // address by its byte offset (the swizzle is applied to the absolute address).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024u >> 4) << 32) |
-           (1ull << 46) | (2ull << 61);
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo = 1024u) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
 // Instruction descriptor of kind::mxf4nvf4: E2M1 A and B (packed FP4), UE4M3 scale

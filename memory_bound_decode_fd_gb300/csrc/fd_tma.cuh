@@ -9,6 +9,31 @@
 namespace fd {
 
 constexpr long long kWaitLimitCycles = 1ll << 31;
+// The limit under FD_LAUNCH_TEST_WAIT_TIMEOUT (about 0.5 ms at 2 GHz).
+constexpr long long kTestWaitLimitCycles = 1ll << 20;
+
+// Set by a kernel of this translation unit whose bounded wait gave up
+// (FD_DEVICE_STATUS_WAIT_TIMEOUT); read and cleared on the host through the accessor that
+// FD_DEFINE_STATUS_ACCESSOR defines in the same file (see fd_device_status in fd.h).
+static __device__ unsigned int g_wait_status;
+
+__device__ __forceinline__ void record_wait_timeout() {
+    atomicOr(&g_wait_status, (unsigned)FD_DEVICE_STATUS_WAIT_TIMEOUT);
+}
+
+// Host accessor of this translation unit's status word: copies it to *out (pinned or
+// pageable host memory) on `stream` and, with `clear`, zeroes it after the copy. The caller
+// synchronises the stream.
+#define FD_DEFINE_STATUS_ACCESSOR(name)                                                      \
+    cudaError_t name(cudaStream_t stream, unsigned *out, bool clear) {                       \
+        cudaError_t err = cudaMemcpyFromSymbolAsync(out, g_wait_status, sizeof(unsigned), 0, \
+                                                    cudaMemcpyDeviceToHost, stream);         \
+        if (err != cudaSuccess || !clear) return err;                                        \
+        void *p = nullptr;                                                                   \
+        err = cudaGetSymbolAddress(&p, g_wait_status);                                       \
+        if (err != cudaSuccess) return err;                                                  \
+        return cudaMemsetAsync(p, 0, sizeof(unsigned), stream);                              \
+    }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -80,33 +105,35 @@ __device__ __forceinline__ void mbar_arrive_at(uint32_t bar) {
 // Slow path of mbar_wait_bounded (kept out of line so the fast path stays small):
 // several suspending polls between checks of the abort flag and the cycle budget.
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity,
-                                            volatile int *abort_flag) {
+                                                   volatile int *abort_flag, long long limit) {
     const long long t0 = clock64();
     while (true) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             if (mbar_try_parity(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             *abort_flag = 1;
+            record_wait_timeout();
             return false;
         }
     }
 }
 
-// Waits for the phase with parity `parity`. Returns false if the wait ran past the
-// cycle limit or `*abort_flag` became nonzero (another thread gave up); in the first
-// case it also sets `*abort_flag`.
+// Waits for the phase with parity `parity`. Returns false if the wait ran past `limit`
+// SM clocks or `*abort_flag` became nonzero (another thread gave up); in the first case it
+// also sets `*abort_flag` and the translation unit's status word.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
-                                                  volatile int *abort_flag) {
+                                                  volatile int *abort_flag,
+                                                  long long limit = kWaitLimitCycles) {
     if (mbar_try_parity(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, abort_flag);
+    return mbar_wait_slow(bar, parity, abort_flag, limit);
 }
 __device__ __forceinline__ bool mbar_wait_bounded_at(uint32_t bar, uint32_t parity,
                                                      volatile int *abort_flag) {
     if (mbar_try_parity_at(bar, parity)) return true;
     return mbar_wait_slow(reinterpret_cast<uint64_t *>(__cvta_shared_to_generic(bar)), parity,
-                          abort_flag);
+                          abort_flag, kWaitLimitCycles);
 }
 
 // Bulk copy global -> shared (this CTA), completion counted in bytes on `bar`.

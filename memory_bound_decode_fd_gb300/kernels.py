@@ -44,6 +44,16 @@ def set_pdl(enabled: bool) -> bool:
     return prev
 
 
+def device_status(clear: bool = True, stream: torch.cuda.Stream | None = None) -> int:
+    """The FD_DEVICE_STATUS_* bits kernels recorded on the current device since the last
+    clear (a bounded wait that gave up sets FD_DEVICE_STATUS_WAIT_TIMEOUT). Synchronises
+    `stream` (default: the current stream). See fd_device_status in include/fd.h."""
+    lib = _lib.load()
+    out = ctypes.c_uint(0)
+    _lib.check(lib.fd_device_status(_stream_handle(stream, None), ctypes.byref(out), int(bool(clear))))
+    return int(out.value)
+
+
 def _device_of(*tensors) -> torch.device | None:
     """The one CUDA device of a call's CUDA tensors (None if it has none, e.g. a copy
     between two pinned host buffers). Tensors on two devices are an error: the kernels
@@ -175,6 +185,71 @@ def swiglu_w4a16_gemv_residual(
         )
     _lib.check(st)
     return out
+
+
+def fold_scratch(device=None) -> torch.Tensor:
+    """A zeroed scratch buffer for swiglu_w4a16_gemv_add_rmsnorm (FD_FOLD_SCRATCH_BYTES
+    bytes); every completed call leaves it zero again. One per stream."""
+    return torch.zeros(_lib.FD_FOLD_SCRATCH_BYTES, dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def swiglu_w4a16_gemv_add_rmsnorm(
+    gate: torch.Tensor,
+    up: torch.Tensor,
+    qweight: torch.Tensor,
+    scales: torch.Tensor,
+    residual: torch.Tensor,
+    rms_weight: torch.Tensor,
+    eps: float,
+    scratch: torch.Tensor,
+    y: torch.Tensor | None = None,
+    normed: torch.Tensor | None = None,
+    residual_out: torch.Tensor | None = None,
+    group: int = 128,
+    stream: torch.cuda.Stream | None = None,
+) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(y, normed, residual_out): the SwiGLU-W4A16 GEMV of one row with the next layer's
+    residual add + RMSNorm folded into its tail: y = gemv(...), residual_out = bf16(y +
+    residual), normed = RMSNorm(residual_out) * rms_weight. residual_out may be residual (in
+    place). scratch: fold_scratch(). See fd_swiglu_w4a16_gemv_add_rmsnorm in include/fd.h."""
+    if gate.dim() == 1:
+        gate = gate.unsqueeze(0)
+        up = up.unsqueeze(0)
+    if residual.dim() == 1:
+        residual = residual.unsqueeze(0)
+    if gate.dim() != 2 or gate.shape[0] != 1 or qweight.dim() != 2 or scales.dim() != 2:
+        raise ValueError("gate/up must be [1, K]; qweight [N, K/8]; scales [N, K/group]")
+    K = gate.shape[1]
+    N = qweight.shape[0]
+    _check_tensor("gate", gate, torch.bfloat16)
+    _check_tensor("up", up, torch.bfloat16, (1, K))
+    _check_tensor("qweight", qweight, torch.int32, (N, K // 8))
+    if group <= 0 or K % group != 0:
+        raise ValueError(f"K={K} must be a multiple of group={group}")
+    _check_tensor("scales", scales, torch.bfloat16, (N, K // group))
+    _check_tensor("residual", residual, torch.bfloat16, (1, N))
+    _check_tensor("rms_weight", rms_weight, torch.bfloat16, (N,))
+    _check_tensor("scratch", scratch, torch.uint8, (_lib.FD_FOLD_SCRATCH_BYTES,))
+    outs = []
+    for name, t in (("y", y), ("normed", normed), ("residual_out", residual_out)):
+        if t is None:
+            t = torch.empty((1, N), dtype=torch.bfloat16, device=gate.device)
+        elif t.dim() == 1:
+            t = t.unsqueeze(0)
+        _check_tensor(name, t, torch.bfloat16, (1, N))
+        outs.append(t)
+    y, normed, residual_out = outs
+    dev = _device_of(gate, up, qweight, scales, residual, rms_weight, scratch, y, normed, residual_out)
+    lib = _lib.load()
+    with _on_device(dev):
+        st = lib.fd_swiglu_w4a16_gemv_add_rmsnorm(
+            _ptr(gate), _ptr(up), _ptr(qweight), _ptr(scales), _ptr(y), _ptr(residual),
+            _ptr(rms_weight), ctypes.c_float(float(eps)), _ptr(normed), _ptr(residual_out),
+            _ptr(scratch), int(K), int(N), int(group), _stream_handle(stream, dev),
+        )
+    _lib.check(st)
+    return y, normed, residual_out
 
 
 def w4a16_gate_up_gemv(
@@ -373,6 +448,7 @@ def decode_mlp_step(
     normed: list[torch.Tensor] | None = None,
     y: list[torch.Tensor] | None = None,
     stream: torch.cuda.Stream | None = None,
+    scratch: torch.Tensor | None = None,
 ) -> tuple[torch.Tensor, torch.Tensor]:
     """One decode step over L layers of ("09 - Operator fusion", "The fusion boundary
     problem"): (normed_l, residual) = add_rmsnorm(x_l, residual); y_l = down(g_l, u_l);
@@ -380,8 +456,27 @@ def decode_mlp_step(
     updated in place. ``layers`` holds per-layer device tensors ``rms_weight``, ``gate``,
     ``up``, ``qweight``, ``scales``. ``normed``/``y`` are optional preallocated outputs
     (one [1, hidden] tensor per layer) so the step allocates nothing and can be captured
-    in a CUDA graph. Returns (x_L, residual).
+    in a CUDA graph. With ``scratch`` (fold_scratch()) each layer's add-RMSNorm after the
+    first is folded into the previous layer's GEMV (swiglu_w4a16_gemv_add_rmsnorm): L + 1
+    launches instead of 2L, the same dataflow. Returns (x_L, residual).
     """
+    if scratch is not None:
+        n_out = normed[0] if normed is not None else None
+        n_out, _ = add_rmsnorm(x, residual, layers[0]["rms_weight"], eps, out=n_out,
+                               residual_out=residual, stream=stream)
+        cur = x
+        for i, layer in enumerate(layers):
+            y_out = y[i] if y is not None else None
+            if i + 1 < len(layers):
+                nxt = normed[i + 1] if normed is not None else None
+                cur, _, _ = swiglu_w4a16_gemv_add_rmsnorm(
+                    layer["gate"], layer["up"], layer["qweight"], layer["scales"], residual,
+                    layers[i + 1]["rms_weight"], eps, scratch, y=y_out, normed=nxt,
+                    residual_out=residual, group=group, stream=stream)
+            else:
+                cur = swiglu_w4a16_gemv(layer["gate"], layer["up"], layer["qweight"],
+                                        layer["scales"], out=y_out, group=group, stream=stream)
+        return cur, residual
     cur = x
     for i, layer in enumerate(layers):
         n_out = normed[i] if normed is not None else None

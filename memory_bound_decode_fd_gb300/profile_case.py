@@ -4,6 +4,7 @@
     python -m memory_bound_decode_fd_gb300.profile_case gemv --M 64 --path tensor
     python -m memory_bound_decode_fd_gb300.profile_case rmsnorm --rows 8192 --hidden 4096
     python -m memory_bound_decode_fd_gb300.profile_case gate_up --K 4096 --N 14336
+    python -m memory_bound_decode_fd_gb300.profile_case nvfp4 --M 64 --K 4096 --N 6144
 
 Each iteration uses the next of --sets input sets, so that consecutive launches do not
 find their weights in L2. Exits 0 after a final synchronize.
@@ -29,7 +30,7 @@ def main(argv=None) -> int:
     from memory_bound_decode_fd_gb300 import build, inputs
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["gemv", "rmsnorm", "gate_up"])
+    ap.add_argument("case", choices=["gemv", "rmsnorm", "gate_up", "nvfp4"])
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--K", type=int, default=14336)
     ap.add_argument("--N", type=int, default=4096, help="rows (gate_up: I, the stacked weight has 2I)")
@@ -67,6 +68,17 @@ def main(argv=None) -> int:
         for i in range(args.iters):
             q, s = sets[i % len(sets)]
             fd.w4a16_gate_up_gemv(x, q, s, gate_out=g, up_out=u, group=args.group)
+    elif args.case == "nvfp4":
+        sets = []
+        for i in range(args.sets):
+            d = inputs.nvfp4_inputs(args.M, args.K, args.N, seed=5 + i)
+            sets.append(tuple(torch.from_numpy(np.ascontiguousarray(d[k])).to(dev)
+                              for k in ("x", "x_sf", "w", "w_sf")))
+        alpha = torch.tensor([1.25], dtype=torch.float32, device=dev)
+        out = torch.empty((args.M, args.N), dtype=torch.bfloat16, device=dev)
+        for i in range(args.iters):
+            x, xs, w, ws = sets[i % len(sets)]
+            fd.nvfp4_scaled_mm(x, xs, w, ws, alpha, out=out)
     else:
         sets = []
         for i in range(args.sets):

@@ -96,6 +96,50 @@ def eager_layers(cuda_device, step_data):
     return rec
 
 
+@pytest.fixture(scope="module")
+def folded_layers(cuda_device, step_data):
+    """The chain with each later layer's add-RMSNorm folded into the previous layer's GEMV
+    (swiglu_w4a16_gemv_add_rmsnorm), run call by call with every layer's own inputs kept:
+    (x_l, residual before, normed_l, residual after, y_l) as host bits."""
+    d = step_data
+    layers = device_layers(d)
+    x = dev_bf16(d["x"])
+    res = dev_bf16(d["residual"])
+    scratch = fd.fold_scratch()
+    x_in, res_in = host_bits(x), host_bits(res)
+    normed, _ = fd.add_rmsnorm(x, res, layers[0]["rms_weight"], EPS, residual_out=res)
+    torch.cuda.synchronize()
+    rec = []
+    normed_bits, res_after = host_bits(normed), host_bits(res)
+    for i, L in enumerate(layers):
+        if i + 1 < len(layers):
+            y, nxt, _ = fd.swiglu_w4a16_gemv_add_rmsnorm(
+                L["gate"], L["up"], L["qweight"], L["scales"], res, layers[i + 1]["rms_weight"],
+                EPS, scratch, residual_out=res, group=d["group"])
+        else:
+            y = fd.swiglu_w4a16_gemv(L["gate"], L["up"], L["qweight"], L["scales"], group=d["group"])
+            nxt = None
+        torch.cuda.synchronize()
+        y_bits = host_bits(y)
+        rec.append((x_in, res_in, normed_bits, res_after, y_bits))
+        if nxt is not None:
+            x_in, res_in = y_bits, res_after
+            normed_bits, res_after = host_bits(nxt), host_bits(res)
+    return rec
+
+
+def test_folded_decode_step_every_layer_exact_on_its_own_inputs(cuda_device, step_data, folded_layers):
+    # The folded chain: every layer's add-RMSNorm (computed in the previous GEMV's tail)
+    # checked on its own inputs, every GEMV output within its bound, the links intact.
+    d = step_data
+    for l, (x_in, res_in, normed, res_out, y) in enumerate(folded_layers):
+        L = d["layers"][l]
+        check_add_rmsnorm(normed, res_out, x_in, res_in, L["rms_weight"], EPS)
+        check_gemv(y, L["gate"], L["up"], L["qweight"], L["scales"], d["group"])
+    for a, b in zip(folded_layers, folded_layers[1:]):
+        assert np.array_equal(b[0], a[4]) and np.array_equal(b[1], a[3])
+
+
 def test_decode_step_every_layer_exact_on_its_own_inputs(cuda_device, step_data, eager_layers):
     # Each layer checked against the oracle on the bf16 x and residual the GPU handed it:
     # residual_out bit-exact, the normalised row within the add-RMSNorm element bound, and
@@ -128,12 +172,13 @@ def test_decode_step_graph_and_eager_agree_bitwise(cuda_device, step_data):
         assert np.array_equal(ta, tb)
 
 
-def _step_outputs(d, pdl: bool):
+def _step_outputs(d, pdl: bool, fold: bool = False):
     from memory_bound_decode_fd_gb300.step import DecodeStep
 
     layers = device_layers(d)
     step = DecodeStep([{k: L[k] for k in ("rms_weight", "qweight", "scales")} for L in layers],
-                      d["hidden"], d["layers"][0]["gate"].shape[1], d["group"], EPS, pdl=pdl)
+                      d["hidden"], d["layers"][0]["gate"].shape[1], d["group"], EPS, pdl=pdl,
+                      fold=fold)
     step.x.copy_(dev_bf16(d["x"]))
     step.residual.copy_(dev_bf16(d["residual"]))
     for i, L in enumerate(layers):
@@ -143,6 +188,21 @@ def _step_outputs(d, pdl: bool):
     step.replay()
     torch.cuda.synchronize()
     return [host_bits(t) for t in step.normed] + [host_bits(t) for t in step.y] + [host_bits(step.residual)]
+
+
+@pytest.mark.parametrize("fold", [True, False])
+def test_decode_step_graph_equals_the_checked_chain(cuda_device, step_data, eager_layers,
+                                                    folded_layers, fold):
+    # The captured DecodeStep (programmatic dependent launch) reproduces, bit for bit, the
+    # call-by-call chain whose every layer is checked: the folded chain (L + 1 launches) or
+    # the plain one (2L launches).
+    ref = folded_layers if fold else eager_layers
+    out = _step_outputs(step_data, pdl=True, fold=fold)
+    L = len(ref)
+    for l, rec in enumerate(ref):
+        assert np.array_equal(out[l].reshape(-1), rec[2].reshape(-1))
+        assert np.array_equal(out[L + l].reshape(-1), rec[4].reshape(-1))
+    assert np.array_equal(out[-1].reshape(-1), ref[-1][3].reshape(-1))
 
 
 def test_decode_step_with_pdl_matches_plain_launches(cuda_device, step_data, oracle_chain):
@@ -216,7 +276,7 @@ def test_decode_step_pinned_io_matches_call(cuda_device, step_data, oracle_chain
             record, x_last, res_ref = oracle_chain
             stated_bar(bf16_f64(out_x), record[-1][3])
             stated_bar(bf16_f64(out_res), bf16_f64(res_ref))
-            # and bit for bit the layer-by-layer chain checked per layer above
+            # and bit for bit the chain checked layer by layer above
             assert np.array_equal(out_x.reshape(-1), eager_layers[-1][4].reshape(-1))
             assert np.array_equal(out_res.reshape(-1), eager_layers[-1][3].reshape(-1))
         rh.copy_(orr)  # the next token starts from the new residual on both paths

@@ -11,7 +11,7 @@ import torch
 import memory_bound_decode_fd_gb300 as fd
 import oracle
 from memory_bound_decode_fd_gb300 import inputs
-from fd_check import GuardedBuffer, check_gemv, dev_bf16, dev_i32, host_bits
+from fd_check import GuardedBuffer, check_gemv, dev_bf16, dev_i32, host_bits, stated_bar
 
 pytestmark = pytest.mark.gpu
 
@@ -292,3 +292,36 @@ def test_failed_launch_returns_fd_err_cuda_and_records_the_error(cuda_device):
     torch.cuda.synchronize()
     y_ok = run_gemv(d)
     check_gemv(y_ok, d["gate"], d["up"], d["qweight"], d["scales"], 128)
+
+
+def _tiny(bits, factor):
+    """bf16 bit patterns times a power of two (exact in bf16 down to 2^-133)."""
+    return inputs.to_bf16_bits(oracle.bf16_to_f32(bits).astype(np.float64) * factor)
+
+
+def test_gemv_tiny_activation_slices(gemv_path):
+    # Every other 32-k slice of gate and up scaled by 2^-60 (a = silu(g) u near 2^-121,
+    # far below the int16 encoding's 32767 / amax range without its power-of-two
+    # prescale): every output within the derived bound.
+    M, K, N, group = 1, 4096, 512, 128
+    d = inputs.gemv_inputs(M, K, N, group, seed=31)
+    for key in ("gate", "up"):
+        v = d[key].reshape(M, K // 64, 64).copy()
+        v[:, :, :32] = _tiny(v[:, :, :32], 2.0**-60)
+        d[key] = v.reshape(M, K)
+    y = run_gemv(d)
+    check_gemv(y, d["gate"], d["up"], d["qweight"], d["scales"], group)
+
+
+def test_gemv_all_tiny_activation_row(gemv_path):
+    # The whole activation near 2^-120: finite, nonzero outputs within the stated bar of
+    # the oracle (the activation scale amax / 32767 is then an fp32 subnormal, which
+    # limits its precision to about 2^-15; the stated bar holds).
+    M, K, N, group = 1, 4096, 512, 128
+    d = inputs.gemv_inputs(M, K, N, group, seed=32)
+    d["gate"] = _tiny(d["gate"], 2.0**-60)
+    d["up"] = _tiny(d["up"], 2.0**-60)
+    y = oracle.bf16_to_f32(run_gemv(d)).astype(np.float64)
+    ref = oracle.swiglu_w4a16_gemv(d["gate"], d["up"], d["qweight"], d["scales"], group)
+    assert np.all(np.isfinite(y)) and np.count_nonzero(y) > N // 2
+    stated_bar(y.reshape(ref.shape), ref)

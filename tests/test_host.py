@@ -37,7 +37,8 @@ def test_library_exports_every_declared_symbol(fdlib):
 
 def test_header_constants_match_binding():
     text = HEADER.read_text()
-    for name in ("FD_MAX_K", "FD_MAX_M", "FD_MAX_HIDDEN", "FD_LAUNCH_PDL", "FD_LAUNCH_TEST_FAIL"):
+    for name in ("FD_MAX_K", "FD_MAX_M", "FD_MAX_HIDDEN", "FD_LAUNCH_PDL", "FD_LAUNCH_TEST_FAIL",
+                 "FD_LAUNCH_TEST_WAIT_TIMEOUT", "FD_DEVICE_STATUS_WAIT_TIMEOUT", "FD_NVFP4_MAX_K"):
         m = re.search(rf"#define {name} (\d+)", text)
         assert int(m.group(1)) == getattr(_lib, name)
     for name in ("FD_OK", "FD_ERR_NULL", "FD_ERR_SHAPE", "FD_ERR_ALIGN", "FD_ERR_UNSUPPORTED",

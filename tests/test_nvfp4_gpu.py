@@ -196,3 +196,4 @@ def test_zero_scales_give_zero(cuda_device):
     d["w_sf"] = np.zeros_like(d["w_sf"])
     y = bf16_f64(run(d))
     assert np.all(y == 0)
+
