@@ -188,6 +188,38 @@ int fd_swiglu_w4a16_gemv_add_rmsnorm(const void *gate, const void *up, const voi
                                      fd_stream_t stream);
 
 /*
+ * fd_swiglu_w4a16_gemv_add_rmsnorm_noalloc - fd_swiglu_w4a16_gemv_add_rmsnorm without the
+ * scratch argument: the call allocates nothing and needs no buffer from the caller. It is
+ * for callers that cannot allocate device memory when they make the call: code that runs
+ * while its stream is being captured into a CUDA graph (cudaMalloc is not a stream
+ * operation and is not allowed during capture), a plugin run inside another runtime that
+ * gives its plugins no allocator (an engine that plans all of its device memory ahead), or a
+ * process whose device memory belongs to an arena it does not control. The source pages
+ * have no counterpart of it; it serves these callers only.
+ *
+ * Results, arguments, requirements and the kernel choice are those of
+ * fd_swiglu_w4a16_gemv_add_rmsnorm (gate, up, qweight, scales, y, residual, rms_weight, eps,
+ * normed, residual_out, K, N, group, stream: the same meaning, layouts and rules).
+ * Scratch    the library's own device array of FD_FOLD_SCRATCH_BYTES bytes (a counter and
+ *            one fp32 partial sum per CTA, so at most 960 CTAs), in the memory of every GPU
+ *            that loads this library until the process exits. The first call on a device
+ *            looks up its device address (cudaGetSymbolAddress) and zeroes it on `stream`;
+ *            make that first call before any stream capture. Every call shares the array
+ *            and leaves its counter at zero: calls that overlap on the GPU (other streams,
+ *            or other host threads on one device) race on it and must not be made.
+ * Returns    FD_ERR_UNSUPPORTED, launching nothing, when the fold's grid would need more
+ *            partial sums than the array holds (a device with more than 240 SMs). Where the
+ *            fold's kernel does not run the shape, the GEMV kernel and fd_add_rmsnorm's
+ *            kernel run instead; they use no scratch. No cudaMalloc, cudaFree or other
+ *            allocating call is made.
+ */
+int fd_swiglu_w4a16_gemv_add_rmsnorm_noalloc(const void *gate, const void *up,
+                                             const void *qweight, const void *scales, void *y,
+                                             const void *residual, const void *rms_weight,
+                                             float eps, void *normed, void *residual_out, int K,
+                                             int N, int group, fd_stream_t stream);
+
+/*
  * fd_add_rmsnorm - fused residual add + RMSNorm, one pass over HBM.     [KFM Step 2]
  *
  *   h[i, j]   = bf16( f32(x[i, j]) + f32(residual[i, j]) )            -> residual_out

@@ -49,6 +49,7 @@ from .kernels import (  # noqa: F401
     set_pdl,
     swiglu_w4a16_gemv,
     swiglu_w4a16_gemv_add_rmsnorm,
+    swiglu_w4a16_gemv_add_rmsnorm_noalloc,
     swiglu_w4a16_gemv_residual,
     w4_dequant_debug,
     w4a16_gate_up_gemv,

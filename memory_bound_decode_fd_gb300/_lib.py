@@ -40,6 +40,8 @@ SIGNATURES = {
     "fd_swiglu_w4a16_gemv_residual": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "fd_swiglu_w4a16_gemv_add_rmsnorm": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float,
                                              _VP, _VP, _VP, _I, _I, _I, _VP]),
+    "fd_swiglu_w4a16_gemv_add_rmsnorm_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                                     ctypes.c_float, _VP, _VP, _I, _I, _I, _VP]),
     "fd_w4a16_gate_up_gemv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "fd_copy": (_I, [_VP, _VP, ctypes.c_size_t, _VP]),
     "fd_debug_plan_gemv": (_I, [_VP, _I, _I, _I, _I, _I, _VP]),

@@ -222,6 +222,53 @@ int fd_swiglu_w4a16_gemv_add_rmsnorm(const void *gate, const void *up, const voi
                                         st_));
 }
 
+int fd_swiglu_w4a16_gemv_add_rmsnorm_noalloc(const void *gate, const void *up,
+                                             const void *qweight, const void *scales, void *y,
+                                             const void *residual, const void *rms_weight,
+                                             float eps, void *normed, void *residual_out, int K,
+                                             int N, int group, fd_stream_t stream) {
+    const int sz = check_w4_sizes(1, K, N, group);
+    if (sz == kEmpty) return FD_OK;
+    if (!(eps >= 0.0f) || !std::isfinite(eps) || N % 8 != 0) return FD_ERR_SHAPE;
+    if (!gate || !up || !y || !residual || !rms_weight || !normed || !residual_out)
+        return FD_ERR_NULL;
+    if (sz != FD_OK) return sz;
+    int st = check_w4_layout(qweight, scales, K, N, group);
+    if (st != FD_OK) return st;
+    if (!aligned16(gate) || !aligned16(up) || !aligned16(y) || !aligned16(residual) ||
+        !aligned16(rms_weight) || !aligned16(normed) || !aligned16(residual_out))
+        return FD_ERR_ALIGN;
+    const size_t act = (size_t)K * 2, row = (size_t)N * 2;
+    const size_t w_bytes = (size_t)N * K / 2, s_bytes = (size_t)N * (K / group) * 2;
+    const void *ins[] = {gate, up, qweight, scales, rms_weight};
+    const size_t in_bytes[] = {act, act, w_bytes, s_bytes, row};
+    const void *outs[] = {y, normed, residual_out};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 5; ++j)
+            if (overlaps(outs[i], row, ins[j], in_bytes[j])) return FD_ERR_OVERLAP;
+        for (int j = i + 1; j < 3; ++j)
+            if (overlaps(outs[i], row, outs[j], row)) return FD_ERR_OVERLAP;
+        if (outs[i] != residual_out && overlaps(outs[i], row, residual, row)) return FD_ERR_OVERLAP;
+    }
+    if (residual_out != residual && overlaps(residual_out, row, residual, row)) return FD_ERR_OVERLAP;
+    if (fake_launch_failure()) return from_cuda(cudaErrorLaunchOutOfResources);
+    cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+    const int path = g_gemv_path.load(std::memory_order_relaxed);
+    if (path == FD_GEMV_AUTO || path == FD_GEMV_BULK) {
+        bool launched = false, too_big = false;
+        cudaError_t err = launch_gemv_fold_noalloc(gate, up, qweight, scales, y, residual,
+                                                   rms_weight, eps, normed, residual_out, K, N,
+                                                   group, st_, &launched, &too_big);
+        if (err != cudaSuccess || launched) return from_cuda(err);
+        if (too_big) return FD_ERR_UNSUPPORTED;
+    }
+    // the selected GEMV kernel, then the separate add-RMSNorm kernel: no scratch at all
+    st = swiglu_gemv(gate, up, qweight, scales, nullptr, y, 1, K, N, group, stream);
+    if (st != FD_OK) return st;
+    return from_cuda(launch_add_rmsnorm(y, residual, rms_weight, eps, normed, residual_out, 1, N,
+                                        st_));
+}
+
 int fd_w4a16_gate_up_gemv(const void *x, const void *qweight, const void *scales,
                           void *gate_out, void *up_out, int M, int K, int I, int group,
                           fd_stream_t stream) {

@@ -42,6 +42,7 @@
 //     timeout in the device status word (fd_device_status), stops computing, waits
 //     (bounded) for the copies it issued, writes NaN to all of its outputs and exits.
 #include <atomic>
+#include <mutex>
 
 #include "fd_gemv_common.cuh"
 #include "fd_gemv_plan.h"
@@ -637,7 +638,98 @@ cudaError_t launch_mb(const DeviceInfo &di, const void *gate, const void *up,
                                                      M, K, N, group, stream, launched, fold);
 }
 
+// The grid the FOLD kernel would launch for an M = 1 call (0: the kernel does not run the
+// shape), from the same plan as launch_cfg.
+template <int NVEC_C, int NG_C>
+cudaError_t fold_grid_cfg(const DeviceInfo &di, int K, int N, int group, int *grid) {
+    static std::atomic<int> func_cache{-1};
+    auto kern = gemv_tma_kernel<1, kChunkRows, NVEC_C, NG_C, 2, false, true>;
+    int fc = func_cache.load(std::memory_order_relaxed);
+    if (fc < 0) {
+        cudaFuncAttributes fa;
+        cudaError_t err = cudaFuncGetAttributes(&fa, kern);
+        if (err != cudaSuccess) return err;
+        fc = (fa.sharedSizeBytes & 0xFFFFF) | (fa.numRegs << 20);
+        func_cache.store(fc, std::memory_order_relaxed);
+    }
+    TmaPlanInput in{di.sm_count, di.max_smem_optin, di.smem_per_sm, di.smem_reserved,
+                    fc & 0xFFFFF, fc >> 20, 1, K, N, group, 1, 2, kChunkRows, kMaxStages, 0};
+    TmaPlan plan{};
+    *grid = plan_gemv_tma(in, &plan) ? plan.grid : 0;
+    return cudaSuccess;
+}
+
+// The library's own scratch for fd_swiglu_w4a16_gemv_add_rmsnorm_noalloc: the fold's
+// counter and per-CTA partial sums (FD_FOLD_SCRATCH_BYTES). Every GPU that loads this
+// library holds it until the process exits; every call of the entry point shares it.
+static __device__ __align__(256) unsigned char g_fold_scratch[FD_FOLD_SCRATCH_BYTES];
+
+// Set-up, once per device, with that device current: the array's device address (in host
+// code its name is only a stand-in, not a device address) and one zeroing of it on
+// `stream`, ordered before the call's kernel. Every completed call leaves the counter at
+// zero again.
+cudaError_t fold_scratch_address(cudaStream_t stream, void **ptr) {
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev & 63]) {
+        void *p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_fold_scratch);
+        if (err != cudaSuccess) return err;
+        err = cudaMemsetAsync(p, 0, FD_FOLD_SCRATCH_BYTES, stream);
+        if (err != cudaSuccess) return err;
+        addr[dev & 63] = p;
+    }
+    *ptr = addr[dev & 63];
+    return cudaSuccess;
+}
+
 }  // namespace
+
+bool gemv_tma_supported(int M, int K, int group);
+
+cudaError_t launch_gemv_fold_noalloc(const void *gate, const void *up, const void *qweight,
+                                     const void *scales, void *y, const void *residual,
+                                     const void *rms_weight, float eps, void *normed,
+                                     void *residual_out, int K, int N, int group,
+                                     cudaStream_t stream, bool *launched, bool *too_big) {
+    *launched = false;
+    *too_big = false;
+    if (!gemv_tma_supported(1, K, group)) return cudaSuccess;
+    DeviceInfo di;
+    cudaError_t err = device_info(&di);
+    if (err != cudaSuccess) return err;
+    int grid = 0;
+    if (K == 14336 && group == 128)
+        err = fold_grid_cfg<14336 / 32, 14336 / 128>(di, K, N, group, &grid);
+    else if (K == 9216 && group == 128)
+        err = fold_grid_cfg<9216 / 32, 9216 / 128>(di, K, N, group, &grid);
+    else if (K == 4096 && group == 128)
+        err = fold_grid_cfg<4096 / 32, 4096 / 128>(di, K, N, group, &grid);
+    else if (K == 1024 && group == 128)
+        err = fold_grid_cfg<1024 / 32, 1024 / 128>(di, K, N, group, &grid);
+    else
+        err = fold_grid_cfg<0, 0>(di, K, N, group, &grid);
+    if (err != cudaSuccess || grid == 0) return err;
+    if (grid > kFoldMaxCtas) {  // more per-CTA sums than the array holds
+        *too_big = true;
+        return cudaSuccess;
+    }
+    void *scratch = nullptr;
+    err = fold_scratch_address(stream, &scratch);
+    if (err != cudaSuccess) return err;
+    unsigned char *sc = static_cast<unsigned char *>(scratch);
+    const FoldArgs fold{static_cast<const uint16_t *>(residual),
+                        static_cast<uint16_t *>(residual_out),
+                        static_cast<const uint16_t *>(rms_weight), static_cast<uint16_t *>(normed),
+                        reinterpret_cast<float *>(sc + kFoldPartialsOffset),
+                        reinterpret_cast<unsigned *>(sc), eps, 1.0f / (float)N};
+    return launch_gemv_tma(gate, up, qweight, scales, nullptr, GemvOut{y, nullptr, N, N}, 1, K,
+                           N, group, stream, launched, &fold);
+}
 
 bool gemv_tma_supported(int M, int K, int group) {
     (void)M;

@@ -97,6 +97,14 @@ cudaError_t launch_gemv_tma(const void *gate, const void *up, const void *qweigh
                             const void *scales, const void *residual, GemvOut o, int M, int K,
                             int N, int group, cudaStream_t stream, bool *launched,
                             const FoldArgs *fold = nullptr);
+// fd_swiglu_w4a16_gemv_add_rmsnorm_noalloc's fold on the library's own static scratch
+// (fd_gemv_tma.cu): *launched = false when the bulk-copy kernel does not run the shape;
+// *too_big when its grid needs more per-CTA sums than the array holds.
+cudaError_t launch_gemv_fold_noalloc(const void *gate, const void *up, const void *qweight,
+                                     const void *scales, void *y, const void *residual,
+                                     const void *rms_weight, float eps, void *normed,
+                                     void *residual_out, int K, int N, int group,
+                                     cudaStream_t stream, bool *launched, bool *too_big);
 // Tensor-core path (tcgen05) for batched decode; sets *launched = false when the shape
 // is outside its rules (K % 1024, N % 128, group % 64, (K / group) % 8).
 bool gemv_tc_supported(int M, int K, int N, int group);

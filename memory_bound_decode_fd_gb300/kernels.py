@@ -252,6 +252,53 @@ def swiglu_w4a16_gemv_add_rmsnorm(
     return y, normed, residual_out
 
 
+def swiglu_w4a16_gemv_add_rmsnorm_noalloc(
+    gate: torch.Tensor,
+    up: torch.Tensor,
+    qweight: torch.Tensor,
+    scales: torch.Tensor,
+    residual: torch.Tensor,
+    rms_weight: torch.Tensor,
+    eps: float,
+    y: torch.Tensor,
+    normed: torch.Tensor,
+    residual_out: torch.Tensor,
+    group: int = 128,
+    stream: torch.cuda.Stream | None = None,
+) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """swiglu_w4a16_gemv_add_rmsnorm without a scratch buffer, for callers that cannot
+    allocate device memory when they call (see fd_swiglu_w4a16_gemv_add_rmsnorm_noalloc in
+    include/fd.h): the library uses its own static array, shared by every call, so calls
+    must not overlap on the GPU. Every output is passed in (nothing is allocated here
+    either); residual_out may be residual (in place)."""
+    if gate.dim() == 1:
+        gate = gate.unsqueeze(0)
+        up = up.unsqueeze(0)
+    K = gate.shape[-1]
+    N = qweight.shape[0]
+    _check_tensor("gate", gate, torch.bfloat16, (1, K))
+    _check_tensor("up", up, torch.bfloat16, (1, K))
+    _check_tensor("qweight", qweight, torch.int32, (N, K // 8))
+    if group <= 0 or K % group != 0:
+        raise ValueError(f"K={K} must be a multiple of group={group}")
+    _check_tensor("scales", scales, torch.bfloat16, (N, K // group))
+    _check_tensor("rms_weight", rms_weight, torch.bfloat16, (N,))
+    for name, t in (("residual", residual), ("y", y), ("normed", normed), ("residual_out", residual_out)):
+        _check_tensor(name, t, torch.bfloat16)
+        if t.numel() != N:
+            raise ValueError(f"{name} must hold N={N} elements")
+    dev = _device_of(gate, up, qweight, scales, residual, rms_weight, y, normed, residual_out)
+    lib = _lib.load()
+    with _on_device(dev):
+        st = lib.fd_swiglu_w4a16_gemv_add_rmsnorm_noalloc(
+            _ptr(gate), _ptr(up), _ptr(qweight), _ptr(scales), _ptr(y), _ptr(residual),
+            _ptr(rms_weight), ctypes.c_float(float(eps)), _ptr(normed), _ptr(residual_out),
+            int(K), int(N), int(group), _stream_handle(stream, dev),
+        )
+    _lib.check(st)
+    return y, normed, residual_out
+
+
 def w4a16_gate_up_gemv(
     x: torch.Tensor,
     qweight: torch.Tensor,
