@@ -361,8 +361,8 @@ int fd_nvfp4_scaled_mm(const void *x, const void *x_sf, const void *w, const voi
  * of M (1..128) activation rows, computed on the host without any CUDA call.
  * smem_budget  dynamic shared memory a CTA may use (bytes).
  * plan    int[13] out: split (CTAs per cluster along K), 256-k stages of K, stages of the
- *         largest slice, padded batch, 128-row weight tiles, TMEM columns, output rows per
- *         rank, scale bytes copied per row, shared-memory offsets of the activations, the
+ *         largest slice, padded batch, 128-row weight tiles, TMEM columns, output columns
+ *         (activation rows) per rank, scale bytes copied per row, shared-memory offsets of the activations, the
  *         weight scales and the activation scales (weights at 0), the reduction buffer's
  *         bytes (from offset 0), dynamic shared memory per CTA.
  * Returns FD_ERR_UNSUPPORTED when the kernel has no plan for the shape.

@@ -330,7 +330,7 @@ int fd_debug_plan_nvfp4(int M, int K, int N, int smem_budget, int *plan) {
     Nvfp4Plan p{};
     if (!plan_nvfp4(M, K, N, smem_budget, &p)) return FD_ERR_UNSUPPORTED;
     const int v[13] = {p.split, p.s_total, p.max_stages, p.npad, p.n_tiles, p.tmem_cols,
-                       p.rows_own, (int)p.sf_row, (int)p.off_x, (int)p.off_wsf, (int)p.off_xsf,
+                       p.cols_own, (int)p.sf_row, (int)p.off_x, (int)p.off_wsf, (int)p.off_xsf,
                        (int)p.recv_bytes, (int)p.smem};
     for (int i = 0; i < 13; ++i) plan[i] = v[i];
     return FD_OK;

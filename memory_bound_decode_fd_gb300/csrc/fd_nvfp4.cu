@@ -24,9 +24,15 @@
 //     16-element scales of row l + 32c.
 //   * Warp 1 lane 0 issues one block-scaled MMA per K = 64 step (M = 128, N = NPAD) into a
 //     TMEM accumulator as each stage's operands and scales are ready, then commits.
-//   * The same four warps read the accumulator (lane = weight row), exchange partial sums
-//     through the cluster, and the owner of each row range applies alpha (read from device
-//     memory, the page's 0-dim multiplier) to the fp32 sum and rounds once to bf16.
+//   * The same four warps copy the accumulator (lane = weight row, 32 columns per wait) to
+//     shared memory as [column][row]; each cluster rank owns a range of output columns
+//     (activation rows), and one bulk copy per rank moves that range's partial sums into the
+//     owner's shared memory (distributed shared memory, completion on the owner's
+//     mbarrier). The owner adds the ranks' partials in rank order, applies alpha (read from
+//     device memory, the page's 0-dim multiplier, early in the kernel) and rounds once to
+//     bf16.
+//   * Thread 0 initialises the barriers and issues every copy before the block-wide
+//     barrier, so the copies are in flight while warp 1 allocates the tensor memory.
 //   * Every wait is bounded (fd_tma.cuh); a CTA that gives up still takes part in both
 //     cluster barriers and frees its TMEM, and its cluster writes NaN to the outputs.
 #include <atomic>
@@ -43,25 +49,40 @@ constexpr int kNfThreads = 6 * 32;   // producer, MMA, four scale / epilogue war
 constexpr int kNfFirstEpi = 2;
 
 // Bounded wait that ignores the abort flag: used where the CTA must not go on before the
-// hardware is done (copies landing, MMAs completing), even after a failure.
+// hardware is done (copies landing, MMAs completing), even after a failure. try_wait
+// suspends the thread until the phase completes or a hardware time limit passes.
 __device__ __forceinline__ void nf_wait_hw(uint64_t *bar, uint32_t parity) {
     const long long t0 = clock64();
-    while (!mbar_test_parity(bar, parity) && clock64() - t0 < kWaitLimitCycles) __nanosleep(64);
+    while (!mbar_try_parity(bar, parity) && clock64() - t0 < kWaitLimitCycles) {
+    }
+}
+// The same, returning whether the phase completed (a timeout is recorded in the status word).
+__device__ __forceinline__ bool nf_wait_hw_ok(uint64_t *bar, uint32_t parity) {
+    nf_wait_hw(bar, parity);
+    if (mbar_test_parity(bar, parity)) return true;
+    record_wait_timeout();
+    return false;
 }
 
-template <int NPAD>
+// TCOLS, the TMEM columns a CTA allocates (256 or 512, as the launch plan asks), is a
+// compile-time constant. (The occupancy API reports one CTA per SM for any kernel that
+// allocates tensor memory, whatever the count; on GB300 two CTAs of 256 columns were seen
+// resident on one SM at run time, which is what the plan's shared-memory floor allows.)
+template <int NPAD, uint32_t TCOLS>
 __global__ void __launch_bounds__(kNfThreads, 1)
     nvfp4_mm_kernel(const __grid_constant__ CUtensorMap map_w,
                     const __grid_constant__ CUtensorMap map_x,
                     const __grid_constant__ CUtensorMap map_wsf,
                     const __grid_constant__ CUtensorMap map_xsf, const float *alpha,
-                    uint16_t *out, int M, int N, int s_total, uint32_t sf_row, int rows_own,
-                    uint32_t tmem_cols, uint32_t off_x, uint32_t off_wsf, uint32_t off_xsf) {
+                    uint16_t *out, int M, int N, int s_total, uint32_t sf_row, int cols_own,
+                    uint32_t off_x, uint32_t off_wsf, uint32_t off_xsf) {
     static_assert(NPAD == 16 || NPAD == 32 || NPAD == 64 || NPAD == 128, "MMA N");
+    static_assert(TCOLS == 256 || TCOLS == 512, "TMEM columns");
     constexpr uint32_t kXStage = NPAD * kNfStageK / 2;    // activation bytes per stage
     __shared__ __align__(8) uint64_t full_bar[kNfMaxStages];  // a stage's operands
     __shared__ __align__(8) uint64_t sf_ready[kNfMaxStages];  // a stage's scales are in TMEM
     __shared__ __align__(8) uint64_t sf_full, acc_full;
+    __shared__ __align__(8) uint64_t red_bar;  // the other ranks' partial sums have landed
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ uint32_t peer_abort[kNfMaxSplit];
@@ -79,52 +100,63 @@ __global__ void __launch_bounds__(kNfThreads, 1)
     const int s_begin = nvfp4_first_stage((int)rank, s_total, split);
     const int S = nvfp4_first_stage((int)rank + 1, s_total, split) - s_begin;
     const int k0 = s_begin * kNfStageK;
+    // The cluster reduction: rank p finishes the output columns (activation rows)
+    // [p c, (p + 1) c), c = cols_own. Once the operands are dead, shared memory from offset
+    // 0 holds `split` receive slots [src rank][c][128 rows] fp32 and then this CTA's
+    // accumulator as [column][128 rows] fp32, in which rank p's columns are one contiguous
+    // chunk: one bulk copy per rank sends it, completing on that rank's red_bar.
+    const uint32_t chunk = (uint32_t)cols_own * kNfRows * 4;
+    const uint32_t recv_base = smem_u32(smem);
+    const uint32_t acc_base = recv_base + (uint32_t)split * chunk;
 
     if (tid == 0) {
-        for (int s = 0; s < kNfMaxStages; ++s) {
+        prefetch_tensormap(&map_w);
+        prefetch_tensormap(&map_x);
+        prefetch_tensormap(&map_wsf);
+        prefetch_tensormap(&map_xsf);
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&sf_ready[s], 4);
         }
         mbar_init(&sf_full, 1);
         mbar_init(&acc_full, 1);
+        mbar_init(&red_bar, 1);
+        mbar_arrive_expect_tx(&red_bar, (uint32_t)(split - 1) * chunk);
         abort_flag = 0;
         for (int p = 0; p < kNfMaxSplit; ++p) peer_abort[p] = 0;
         fence_mbar_init();
+        // -------------------------------------------------- every copy, issued at once,
+        // while warp 1 allocates the tensor memory
+        grid_dep_wait();  // the activations may come from the previous kernel
+        grid_dep_launch();
+        const uint64_t pol_w = policy_evict_first();  // each weight byte is read once
+        const uint64_t pol_x = policy_evict_last();   // every weight tile reads them
+        // the scale boxes are max_stages wide: a shorter slice copies a few unused (or
+        // out-of-range, zero-filled) columns past its end
+        mbar_arrive_expect_tx(&sf_full, (uint32_t)(kNfRows + NPAD) * sf_row);
+        tma_load_2d(smem + off_wsf, &map_wsf, k0 / 16, n0, &sf_full, pol_w);
+        tma_load_2d(smem + off_xsf, &map_xsf, k0 / 16, 0, &sf_full, pol_x);
+        for (int s = 0; s < S; ++s) {
+            const int xb = (k0 + s * kNfStageK) / 2;  // byte column, a multiple of 128
+            mbar_arrive_expect_tx(&full_bar[s], kNfWStage + kXStage);
+            tma_load_2d(smem + (size_t)s * kNfWStage, &map_w, xb, n0, &full_bar[s], pol_w);
+            tma_load_2d(smem + off_x + (size_t)s * kXStage, &map_x, xb, 0, &full_bar[s], pol_x);
+        }
     }
     if (warp == 1) {
-        tmem_alloc(&tmem_slot, tmem_cols);
+        tmem_alloc(&tmem_slot, TCOLS);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    float out_scale = 0.f;  // alpha, read by the epilogue warps once they may
 
     if (warp == 0) {
-        // -------------------------------------------------- every copy, issued at once
-        if (lane == 0) {
-            prefetch_tensormap(&map_w);
-            prefetch_tensormap(&map_x);
-            prefetch_tensormap(&map_wsf);
-            prefetch_tensormap(&map_xsf);
-        }
-        grid_dep_wait();  // the activations may come from the previous kernel
+        grid_dep_wait();
         grid_dep_launch();
-        if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();  // each weight byte is read once
-            const uint64_t pol_x = policy_evict_last();   // every weight tile reads them
-            // the scale boxes are max_stages wide: a shorter slice copies a few unused (or
-            // out-of-range, zero-filled) columns past its end
-            mbar_arrive_expect_tx(&sf_full, (uint32_t)(kNfRows + NPAD) * sf_row);
-            tma_load_2d(smem + off_wsf, &map_wsf, k0 / 16, n0, &sf_full, pol_w);
-            tma_load_2d(smem + off_xsf, &map_xsf, k0 / 16, 0, &sf_full, pol_x);
-            for (int s = 0; s < S; ++s) {
-                const int xb = (k0 + s * kNfStageK) / 2;  // byte column, a multiple of 128
-                mbar_arrive_expect_tx(&full_bar[s], kNfWStage + kXStage);
-                tma_load_2d(smem + (size_t)s * kNfWStage, &map_w, xb, n0, &full_bar[s], pol_w);
-                tma_load_2d(smem + off_x + (size_t)s * kXStage, &map_x, xb, 0, &full_bar[s], pol_x);
-            }
-            // every copy must land before the CTA reuses the memory or exits
+        if (lane == 0) {  // every copy must land before the CTA reuses the memory or exits
             nf_wait_hw(&sf_full, 0);
             for (int s = 0; s < S; ++s) nf_wait_hw(&full_bar[s], 0);
         }
@@ -156,8 +188,9 @@ __global__ void __launch_bounds__(kNfThreads, 1)
         __syncwarp();
     } else {
         // -------------------------------------------------- scale factors into TMEM
-        grid_dep_wait();
+        grid_dep_wait();  // alpha may be written, and `out` read, by the previous kernel
         grid_dep_launch();
+        out_scale = *alpha;
         const uint32_t q = (uint32_t)(warp & 3);  // this warp's TMEM lane quarter
         const bool ok = mbar_wait_bounded(&sf_full, 0, &abort_flag);
         const unsigned char *wsf = smem + off_wsf;
@@ -199,59 +232,87 @@ __global__ void __launch_bounds__(kNfThreads, 1)
     }
 
     // ------------------------------------------------------ cluster reduction + store
-    // #1: every CTA of the cluster is done with its operand memory (copies landed, MMAs
-    // complete), so it can take the partial sums: [src rank][NPAD][rows_own] fp32.
-    cluster_sync_all();
-    const uint32_t recv = smem_u32(smem);
-    if (warp >= kNfFirstEpi) {
-        const int q = warp & 3;
-        const int r = 32 * q + lane;  // this thread's weight row in the tile
-        const int owner = r / rows_own, rr = r % rows_own;
-        const uint32_t dst = map_to_rank(recv, (uint32_t)owner);
-#pragma unroll 1
-        for (int c8 = 0; c8 < NPAD / 8; ++c8) {
-            uint32_t v[8];
-            tmem_ld_x8(tmem + ((uint32_t)(32 * q) << 16) + 8u * c8, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = 8 * c8 + i;
-                st_cluster_f32(dst + (uint32_t)(((int)rank * NPAD + j) * rows_own + rr) * 4u,
-                               __uint_as_float(v[i]));
-            }
-        }
-    }
-    if (tid == 0) {
+    if (tid == 0) {  // this CTA's failure flag, to every rank
         for (int p = 0; p < split; ++p)
             st_cluster_u32(map_to_rank(smem_u32(&peer_abort[rank]), (uint32_t)p), (uint32_t)abort_flag);
     }
     __syncwarp();
-    // #2: all partial sums and failure flags have arrived.
+    // #1: every CTA of the cluster is done with its operand memory (copies landed, MMAs
+    // complete) and has published its failure flag.
     cluster_sync_all();
+    const int mcols = M < NPAD ? M : NPAD;  // columns past the batch are never stored
     if (warp >= kNfFirstEpi) {
-        grid_dep_wait();  // alpha may be written, and `out` read, by the previous kernel
-        const float a = *alpha;
-        bool failed = false;
+        const int q = warp & 3;
+        const int r = 32 * q + lane;  // this thread's weight row in the tile (its TMEM lane)
+        float *acc_col = reinterpret_cast<float *>(smem + (size_t)split * chunk) + r;
+        constexpr int kChunk = NPAD < 32 ? NPAD : 32;
+#pragma unroll 1
+        for (int c0 = 0; c0 < mcols; c0 += kChunk) {
+            uint32_t v[kChunk];
+            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
+            tmem_ld_x16(ta, v);
+            if constexpr (kChunk == 32) tmem_ld_x16(ta + 16u, v + 16);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i)  // a warp stores 128 contiguous bytes
+                if (c0 + i < mcols) acc_col[(c0 + i) * kNfRows] = __uint_as_float(v[i]);
+        }
+        fence_proxy_async_smem();  // the stores above, before the bulk copies read them
+        named_bar_sync(1, 4 * 32);
+        if (tid == kNfFirstEpi * 32) {
+            for (int p = 0; p < split; ++p)
+                if (p != (int)rank)
+                    bulk_s2cluster(map_to_rank(recv_base + rank * chunk, (uint32_t)p),
+                                   acc_base + (uint32_t)p * chunk, chunk,
+                                   map_to_rank(smem_u32(&red_bar), (uint32_t)p));
+        }
+        // every other rank's partial sums of this rank's columns
+        bool failed = split > 1 && !nf_wait_hw_ok(&red_bar, 0);
         for (int p = 0; p < split; ++p) failed |= peer_abort[p] != 0;
-        const float *rv = reinterpret_cast<const float *>(smem);
-        const int et = tid - kNfFirstEpi * 32;
-        for (int i = et; i < NPAD * rows_own; i += 4 * 32) {
-            const int j = i / rows_own, rr = i % rows_own;
-            float acc = 0.f;
-            for (int src = 0; src < split; ++src) acc += rv[(src * NPAD + j) * rows_own + rr];
-            const int row = (int)rank * rows_own + rr;
-            const int n = n0 + row;
-            if (j < M && n < N && row < kNfRows) {
-                const __nv_bfloat16 y = __float2bfloat16_rn(a * acc);
-                out[(size_t)j * N + n] = failed ? (uint16_t)0x7FC0 : *reinterpret_cast<const uint16_t *>(&y);
+        // lane l finishes rows 4l .. 4l + 3 of the columns j0 + q, j0 + q + 4, ...
+        const int j0 = (int)rank * cols_own;
+        const int own = mcols - j0 < cols_own ? mcols - j0 : cols_own;
+        const int n = n0 + 4 * lane;
+        const bool vec = (N & 3) == 0 && n + 3 < N;
+        for (int jj = q; jj < own; jj += 4) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};  // partial sums in rank order
+#pragma unroll
+            for (int src = 0; src < kNfMaxSplit; ++src) {
+                if (src < split) {
+                    const uint32_t a = src == (int)rank
+                        ? acc_base + (uint32_t)(((j0 + jj) * kNfRows + 4 * lane) * 4)
+                        : recv_base + (uint32_t)src * chunk + (uint32_t)((jj * kNfRows + 4 * lane) * 4);
+                    const uint4 v = lds_v4(a);
+                    acc[0] += __uint_as_float(v.x);
+                    acc[1] += __uint_as_float(v.y);
+                    acc[2] += __uint_as_float(v.z);
+                    acc[3] += __uint_as_float(v.w);
+                }
+            }
+            uint16_t y[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                y[e] = failed ? (uint16_t)0x7FC0 : __bfloat16_as_ushort(__float2bfloat16_rn(out_scale * acc[e]));
+            uint16_t *o = out + (size_t)(j0 + jj) * N + n;
+            if (vec) {
+                *reinterpret_cast<uint2 *>(o) = make_uint2((uint32_t)y[0] | ((uint32_t)y[1] << 16),
+                                                           (uint32_t)y[2] | ((uint32_t)y[3] << 16));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (n + e < N) o[e] = y[e];
             }
         }
     }
+    // #2: no CTA leaves while a bulk copy may still read from or write to its memory
+    // (each rank passes this barrier only after its own copies in have landed).
+    __syncwarp();
+    cluster_sync_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, tmem_cols);
+        tmem_dealloc(tmem, TCOLS);
     }
 }
 
@@ -289,22 +350,13 @@ bool encode_bytes_2d(CUtensorMap *map, const void *base, uint64_t row_bytes, uin
            CUDA_SUCCESS;
 }
 
-template <int NPAD>
-cudaError_t launch_npad(const DeviceInfo &di, const unsigned char *x, const unsigned char *x_sf,
-                        const void *w, const void *w_sf, const float *alpha, uint16_t *out,
-                        int mc, int K, int N, cudaStream_t stream) {
+template <int NPAD, uint32_t TCOLS>
+cudaError_t launch_plan(const Nvfp4Plan &p, int budget, const unsigned char *x,
+                        const unsigned char *x_sf, const void *w, const void *w_sf,
+                        const float *alpha, uint16_t *out, int mc, int K, int N,
+                        cudaStream_t stream) {
     static std::atomic<uint64_t> attr_done{0};
-    static std::atomic<int> static_smem_cache{-1};
-    auto kern = nvfp4_mm_kernel<NPAD>;
-    int static_smem = static_smem_cache.load(std::memory_order_relaxed);
-    if (static_smem < 0) {
-        cudaFuncAttributes fa;
-        cudaError_t err = cudaFuncGetAttributes(&fa, kern);
-        if (err != cudaSuccess) return err;
-        static_smem = (int)fa.sharedSizeBytes;
-        static_smem_cache.store(static_smem, std::memory_order_relaxed);
-    }
-    const int budget = di.max_smem_optin - static_smem;
+    auto kern = nvfp4_mm_kernel<NPAD, TCOLS>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -317,8 +369,6 @@ cudaError_t launch_npad(const DeviceInfo &di, const unsigned char *x, const unsi
         if (err != cudaSuccess) return err;
         attr_done.fetch_or(bit, std::memory_order_acq_rel);
     }
-    Nvfp4Plan p{};
-    if (!plan_nvfp4(mc, K, N, budget, &p) || p.npad != NPAD) return cudaErrorInvalidValue;
     CUtensorMap mw, mx, mwsf, mxsf;
     if (!encode_bytes_2d(&mw, w, (uint64_t)K / 2, (uint64_t)N, kNfStageK / 2, kNfRows,
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -331,10 +381,31 @@ cudaError_t launch_npad(const DeviceInfo &di, const unsigned char *x, const unsi
         return cudaErrorInvalidValue;
     err = launch_kernel(kern, dim3((unsigned)p.split, (unsigned)p.n_tiles), dim3(kNfThreads),
                         (size_t)p.smem, stream, p.split, mw, mx, mwsf, mxsf, alpha, out, mc, N,
-                        p.s_total, p.sf_row, p.rows_own, (uint32_t)p.tmem_cols, p.off_x,
-                        p.off_wsf, p.off_xsf);
+                        p.s_total, p.sf_row, p.cols_own, p.off_x, p.off_wsf, p.off_xsf);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
+}
+
+template <int NPAD>
+cudaError_t launch_npad(const DeviceInfo &di, const unsigned char *x, const unsigned char *x_sf,
+                        const void *w, const void *w_sf, const float *alpha, uint16_t *out,
+                        int mc, int K, int N, cudaStream_t stream) {
+    // both column variants declare the same static shared memory
+    static std::atomic<int> static_smem_cache{-1};
+    int static_smem = static_smem_cache.load(std::memory_order_relaxed);
+    if (static_smem < 0) {
+        cudaFuncAttributes fa;
+        cudaError_t err = cudaFuncGetAttributes(&fa, nvfp4_mm_kernel<NPAD, 512>);
+        if (err != cudaSuccess) return err;
+        static_smem = (int)fa.sharedSizeBytes;
+        static_smem_cache.store(static_smem, std::memory_order_relaxed);
+    }
+    const int budget = di.max_smem_optin - static_smem;
+    Nvfp4Plan p{};
+    if (!plan_nvfp4(mc, K, N, budget, &p) || p.npad != NPAD) return cudaErrorInvalidValue;
+    if (p.tmem_cols == 256)
+        return launch_plan<NPAD, 256>(p, budget, x, x_sf, w, w_sf, alpha, out, mc, K, N, stream);
+    return launch_plan<NPAD, 512>(p, budget, x, x_sf, w, w_sf, alpha, out, mc, K, N, stream);
 }
 
 }  // namespace

@@ -26,10 +26,10 @@ struct Nvfp4Plan {
     int npad;       // the batch padded to the MMA's N (16, 32, 64 or 128)
     int n_tiles;    // 128-row weight tiles (clusters)
     int tmem_cols;  // 256 or 512
-    int rows_own;   // output rows each cluster rank finishes (ceil(128 / split))
+    int cols_own;   // output columns (activation rows) each cluster rank finishes: ceil(npad / split)
     uint32_t sf_row;                   // scale bytes per row copied (max_stages x 16)
     uint32_t off_x, off_wsf, off_xsf;  // shared-memory offsets (weights at 0)
-    uint32_t recv_bytes;               // the cluster reduction's buffer (from offset 0)
+    uint32_t recv_bytes;               // the cluster reduction's buffers (from offset 0)
     uint32_t smem;                     // dynamic shared memory per CTA, with alignment slack
 };
 
@@ -58,15 +58,16 @@ inline bool plan_nvfp4_split(int m, int K, int N, int split, int smem_budget, Nv
     p->npad = nvfp4_npad(m);
     p->n_tiles = (N + kNfRows - 1) / kNfRows;
     p->tmem_cols = kNfSfCol0 + kNfSfColsPerStage * p->max_stages <= 256 ? 256 : 512;
-    p->rows_own = (kNfRows + split - 1) / split;
+    p->cols_own = (p->npad + split - 1) / split;
     const uint32_t x_stage = (uint32_t)p->npad * kNfStageK / 2;
     p->sf_row = (uint32_t)p->max_stages * 16;
     p->off_x = (uint32_t)p->max_stages * kNfWStage;
     p->off_wsf = p->off_x + (uint32_t)p->max_stages * x_stage;
     p->off_xsf = p->off_wsf + (uint32_t)kNfRows * p->sf_row;
     const uint32_t end = p->off_xsf + (uint32_t)p->npad * p->sf_row;
-    // [src rank][npad][rows_own] fp32
-    p->recv_bytes = (uint32_t)split * p->npad * p->rows_own * 4;
+    // receive slots [src rank][cols_own][128 rows] fp32, then the CTA's own accumulator as
+    // `split` chunks [cols_own][128 rows] fp32
+    p->recv_bytes = 2u * (uint32_t)split * (uint32_t)p->cols_own * kNfRows * 4;
     const uint32_t used = end > p->recv_bytes ? end : p->recv_bytes;
     p->smem = used + 1024;  // the kernel aligns its base to 1024 bytes
     // Shared memory bounds the CTAs per SM so that their TMEM allocations always fit the
@@ -80,9 +81,10 @@ inline bool plan_nvfp4_split(int m, int K, int N, int split, int smem_budget, Nv
 
 // The split for one launch: the smallest split whose K slices have at most 4 stages (256
 // TMEM columns and ~110 KB of shared memory per CTA, so two CTAs share an SM), else the
-// smallest split whose plan fits. Measured on GB300 for M=64 K=4096 N=6144: split 4 (192
-// CTAs, 4 stages) 10.9 us, split 2 (96 CTAs, 8 stages) 16.2 us: more CTAs streaming at once
-// is what counts. Returns false if no split fits.
+// smallest split whose plan fits. Measured on GB300 for M=64 K=4096 N=6144 (per-CTA
+// timelines): split 4 (192 CTAs of 4 stages) finishes first; split 2 streams through only
+// 96 SMs, and splits 3, 6 and 8 leave clusters for a second wave. Returns false if no
+// split fits.
 inline bool plan_nvfp4(int m, int K, int N, int smem_budget, Nvfp4Plan *p) {
     for (int pass = 0; pass < 2; ++pass)
         for (int s = 1; s <= kNfMaxSplit; ++s) {

@@ -17,7 +17,7 @@ KS = [256, 512, 768, 1024, 1280, 1536, 2048, 3072, 4096, 6144, 8192, 12288, 1638
 def plan(lib, M, K, N, budget=SMEM_OPTIN):
     p = (ctypes.c_int * 13)()
     st = lib.fd_debug_plan_nvfp4(M, K, N, budget, p)
-    keys = ("split", "s_total", "max_stages", "npad", "n_tiles", "tmem_cols", "rows_own",
+    keys = ("split", "s_total", "max_stages", "npad", "n_tiles", "tmem_cols", "cols_own",
             "sf_row", "off_x", "off_wsf", "off_xsf", "recv", "smem")
     return st, dict(zip(keys, list(p)))
 
@@ -28,7 +28,7 @@ def test_qkv_workload_plan(fdlib):
     st, p = plan(fdlib, 64, 4096, 6144)
     assert st == _lib.FD_OK
     assert (p["split"], p["max_stages"], p["npad"], p["n_tiles"]) == (4, 4, 64, 48)
-    assert p["tmem_cols"] == 256 and 2 * (p["smem"] + 1024) <= 233472
+    assert p["tmem_cols"] == 256 and 2 * (p["smem"] + 256 + 1024) <= 233472
 
 
 def first_stage(r, s_total, split):
@@ -60,7 +60,7 @@ def test_plan_invariants_and_replay(fdlib, M, K, N):
     assert npad <= SF_COL0 and SF_COL0 + 32 * ms <= p["tmem_cols"] in (256, 512)
     # at most two CTAs per SM with 256 columns, one with 512 (SM: 233472 bytes, 1 KB
     # reserved per CTA), so the allocations always fit the SM's 512 columns
-    per_sm = 233472 // (p["smem"] + 1024)
+    per_sm = 233472 // (p["smem"] + 256 + 1024)
     assert per_sm * p["tmem_cols"] <= 512 and p["smem"] <= SMEM_OPTIN
     # shared memory: stage bases 1024-byte aligned, regions in order
     w_stage, x_stage, sf_row = 16384, npad * 128, p["sf_row"]
@@ -69,8 +69,13 @@ def test_plan_invariants_and_replay(fdlib, M, K, N):
     assert p["off_wsf"] == p["off_x"] + ms * x_stage and p["off_xsf"] == p["off_wsf"] + 128 * sf_row
     end = p["off_xsf"] + npad * sf_row
     assert p["smem"] >= max(end, p["recv"]) + 1024
-    # the reduction buffer [split][npad][rows_own] and the rows each rank finishes
-    assert p["rows_own"] * split >= 128 and p["recv"] == split * npad * p["rows_own"] * 4
+    # the reduction buffers, receive slots [split][cols_own][128 rows] then the CTA's own
+    # accumulator [split * cols_own][128 rows], and the output columns (activation rows)
+    # each rank finishes
+    cols = p["cols_own"]
+    chunk = cols * 128 * 4
+    assert cols == -(-npad // split) and chunk % 16 == 0
+    assert p["recv"] == 2 * split * chunk
     # replay of one CTA per rank: copies and operand reads inside their regions, global
     # coordinates inside the tensors (the scale box may run past K: zero-filled)
     for r in range(split):
@@ -84,12 +89,17 @@ def test_plan_invariants_and_replay(fdlib, M, K, N):
                 assert SF_COL0 + 32 * s + 8 * j + 8 <= p["tmem_cols"]
             assert p["off_wsf"] + 127 * sf_row + 16 * s + 16 <= p["off_xsf"]
             assert p["off_xsf"] + (npad - 1) * sf_row + 16 * s + 16 <= p["smem"] - 1024
-        for row in (0, 127):
-            owner, rr = divmod(row, p["rows_own"])
+        # rank r's partial sum of column j, row `row`, lands in the owner of j at
+        # [r][j - owner cols_own][row]; every column of the batch has an owner
+        for j in (0, min(M, npad) - 1):
+            owner, jj = divmod(j, cols)
             assert owner < split
-            addr = ((r * npad + npad - 1) * p["rows_own"] + rr) * 4
-            assert addr + 4 <= p["recv"]
-
+            for row in (0, 127):
+                slot = r * chunk + (jj * 128 + row) * 4  # in the owner's receive slots
+                own = split * chunk + (j * 128 + row) * 4  # in rank r's accumulator
+                assert slot + 4 <= split * chunk and split * chunk <= own and own + 4 <= p["recv"]
+            # the chunk rank r sends to `owner` lies inside its accumulator
+            assert split * chunk + (owner + 1) * chunk <= p["recv"]
 
 @pytest.mark.parametrize("K", [0, 128, 300, 4097])
 def test_bad_k_is_a_shape_error(fdlib, K):
