@@ -69,6 +69,8 @@ KERNEL_SOURCES = {
     # the horizontal gate/up GEMV runs the same kernel's plain-activation form
     "w4a16_gate_up_gemv": ["csrc/fd_gemv_tma.cu", "csrc/fd_gemv_common.cuh", "csrc/fd_tma.cuh",
                            "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
+    "nvfp4_scaled_mm": ["csrc/fd_nvfp4.cu", "csrc/fd_nvfp4_plan.h", "csrc/fd_tc.cuh", "csrc/fd_tma.cuh",
+                        "csrc/fd_internal.h"],
 }
 
 
@@ -642,6 +644,7 @@ def build_single_calls(name, device, l2):
         for w, wsf in ws:
             calls.append(lambda w=w, wsf=wsf: fd.nvfp4_scaled_mm(x, xs, w, wsf, alpha, out=out))
         kname = "nvfp4_scaled_mm"
+        extra["traffic_tag"] = f"M{M}_K{K}_N{N}"
         desc = (f"NVFP4 scaled matmul, output multiplier folded in, M={M} K={K} N={N} "
                 f"(E2M1, E4M3 1x16 block scales), seed {spec['seed']}")
     else:
