@@ -353,6 +353,26 @@ def bench_decode(args, device, rank, world):
     h2d = (xh.numel() + rh.numel() + gh.numel() + uh.numel()) * 2
     d2h = (ox.numel() + orr.numel()) * 2
 
+    # The same step as one persistent cooperative launch (fd_decode_mlp_step: a memset and
+    # one kernel per step, bit-identical outputs), captured in a graph and timed the same way.
+    from memory_bound_decode_fd_gb300.step import DecodeStep
+    pers = DecodeStep(step.layers, step.hidden, step.inter, step.group, step.eps, device,
+                      persistent=True)
+    pers.x.copy_(step.x)
+    pers.residual.copy_(step.residual)
+    pers.gate.copy_(step.gate)
+    pers.up.copy_(step.up)
+    pers.capture()
+    with torch.cuda.stream(pers.stream):
+        time_region(pers.stream, pers.replay, max(args.warmup, 3))
+        barrier(world)
+        pers_ms = max_over_ranks(time_region(pers.stream, pers.replay, args.steps), world) / args.steps
+    persistent = {"ms_per_step": round(pers_ms, 6),
+                  "value": round(job_throughput_gbs(world, bytes_per_step, pers_ms), 2),
+                  "unit": "GB/s",
+                  "launch": "fd_decode_mlp_step: one cooperative kernel (one CTA per SM, all 32 layers) and one memset per step"}
+    del pers
+
     line = {
         "metric": METRIC,
         "value": round(value_gbs, 2),
@@ -395,6 +415,7 @@ def bench_decode(args, device, rank, world):
             "four_copy_call_ms_per_step": round(e2e_sep_ms, 6),
         },
         "eager_ms_per_step": eager,
+        "persistent_step": persistent,
         "gpu_launches": 2 * spec["layers"] * args.steps,
         "clocks": clocks,
     }

@@ -21,6 +21,8 @@
  *   fd_nvfp4_scaled_mm     the NVFP4 (packed FP4, E4M3 1x16 block scales) matmul of batched
  *                          decode with its fp32 output multiplier folded in, on the
  *                          tensor cores' block-scaled MMA.
+ *   fd_decode_mlp_step     a whole decode step (add-RMSNorm + down projection per layer)
+ *                          as one persistent launch, bit-identical to the chain of calls.
  *
  * Sources (web pages, cited by title and section):
  *   [FIX]  "PyTorch Community Proposes Fusion Fix as Large Intermediate Buffers May Slow
@@ -218,6 +220,66 @@ int fd_swiglu_w4a16_gemv_add_rmsnorm_noalloc(const void *gate, const void *up,
                                              const void *residual, const void *rms_weight,
                                              float eps, void *normed, void *residual_out, int K,
                                              int N, int group, fd_stream_t stream);
+
+/*
+ * fd_decode_mlp_step - a whole decode step of n_layers layers in one launch:
+ *     for l in 0 .. n_layers - 1:
+ *         h = bf16(x_l + residual); residual = h; normed_l = add-RMSNorm(h) * rms_weight_l
+ *         y_l = swiglu_w4a16_gemv(gate_l, up_l, qweight_l, scales_l);  x_{l+1} = y_l
+ * with x_0 = x0: the chain of fd_add_rmsnorm (rows = 1) and fd_swiglu_w4a16_gemv (M = 1)
+ * calls of "Kernel Fusion, torch.compile and CUDA Graphs, Measured", Step 4 (the step run
+ * as one unit instead of per-kernel launches), and every output is bit-identical to that
+ * chain of separate calls: the same row partition, reduction orders and roundings.
+ * A persistent cooperative kernel: one CTA per SM for all layers, each streaming the next
+ * layer's weight rows while the current layer finishes. Each CTA publishes h of its rows
+ * as words tagged with the layer and counts in; every CTA, once all have counted in and it
+ * has read the whole tagged row, computes the next add-RMSNorm over the whole row (the row
+ * kernel's reduction order); a
+ * CTA reads layer l+1's activations only when it holds the complete normed_{l+1} row, as
+ * the chain's GEMV starts only after its add-RMSNorm has finished.
+ * layers      DEVICE array of n_layers fd_step_layer (below); the library does not read it on
+ *             the host. Every pointer in it must be a device pointer, 16-byte aligned; the
+ *             tensors have the layouts of fd_swiglu_w4a16_gemv (K = inter, N = hidden,
+ *             M = 1) and fd_add_rmsnorm (rows = 1); y_l, normed_l and residual must not
+ *             overlap one another or any input.
+ * n_layers    1 .. FD_STEP_MAX_LAYERS.
+ * x0          bf16 [hidden], the first layer's input (not written).
+ * residual    bf16 [hidden], in and out: the residual stream, left as h of the last layer.
+ * eps         the RMSNorm epsilon (finite, >= 0).
+ * hidden      the model width (the GEMV's N and the RMSNorm row), a multiple of 8.
+ * inter       the GEMV's K: 14336 with group 128 (the decode shape).
+ * scratch     device buffer of at least FD_STEP_SCRATCH_BYTES(n_layers, hidden) bytes,
+ *             16-byte aligned, owned by the caller: one counter per layer, then two rows of
+ *             tagged h words (32 bits per element). The call zeroes it on `stream` first;
+ *             concurrent calls need separate buffers.
+ * Returns FD_OK; FD_ERR_NULL, FD_ERR_SHAPE, FD_ERR_ALIGN, FD_ERR_OVERLAP (x0, residual,
+ * scratch) for bad arguments, launching nothing; FD_ERR_UNSUPPORTED, launching nothing, for
+ * another inter/group, a hidden above 64 rows per SM (9728) or above 8192 (the add-RMSNorm
+ * row's 256 threads x 4 vectors), or rows that do not fit one CTA's shared memory;
+ * FD_ERR_CUDA if the launch fails (for example when the device cannot hold one CTA per SM at
+ * once).
+ * A wait that gives up (about a second) writes NaN outputs and sets
+ * FD_DEVICE_STATUS_WAIT_TIMEOUT (fd_device_status). Capturable in a CUDA graph (a memset and
+ * one kernel node).
+ */
+typedef struct fd_step_layer {
+    const void *gate;       /* bf16 [inter] */
+    const void *up;         /* bf16 [inter] */
+    const void *qweight;    /* int32 [hidden, inter / 8] */
+    const void *scales;     /* bf16 [hidden, inter / group] */
+    const void *rms_weight; /* bf16 [hidden] */
+    void *normed;           /* bf16 [hidden], out: the layer's normalised row */
+    void *y;                /* bf16 [hidden], out: the layer's GEMV output */
+} fd_step_layer;
+#define FD_STEP_MAX_LAYERS 1024
+/* the scratch: n_layers 32-bit counters padded to 16 bytes, then two rows of 32-bit tagged
+ * words */
+#define FD_STEP_SCRATCH_HROWS_OFFSET(n_layers) ((((size_t)(n_layers) * 4 + 15) / 16) * 16)
+#define FD_STEP_SCRATCH_BYTES(n_layers, hidden) \
+    (FD_STEP_SCRATCH_HROWS_OFFSET(n_layers) + (size_t)(hidden) * 8)
+int fd_decode_mlp_step(const fd_step_layer *layers, int n_layers, const void *x0,
+                       void *residual, float eps, int hidden, int inter, int group,
+                       void *scratch, fd_stream_t stream);
 
 /*
  * fd_add_rmsnorm - fused residual add + RMSNorm, one pass over HBM.     [KFM Step 2]

@@ -11,6 +11,7 @@
 * ``nvfp4_scaled_mm``: the NVFP4 (packed FP4, E4M3 1x16 block scales) matmul with its fp32
   output multiplier folded in, on the tensor cores' block-scaled MMA.
 * ``decode_mlp_step``: L layers of the two, in stream order.
+* ``decode_mlp_step_persistent``: the same L layers as one persistent launch, bit-identical.
 
 The compute runs in ``libfd.so`` (C ABI in ``include/fd.h``); this package marshals
 PyTorch CUDA tensors into it. Build the library with ``build.build()``. There is no CPU
@@ -41,12 +42,15 @@ from .kernels import (  # noqa: F401
     add_rmsnorm,
     copy,
     decode_mlp_step,
+    decode_mlp_step_persistent,
     device_status,
     fold_scratch,
     gemv_uses_tensor_cores,
     nvfp4_scaled_mm,
     set_gemv_path,
     set_pdl,
+    step_layer_table,
+    step_scratch,
     swiglu_w4a16_gemv,
     swiglu_w4a16_gemv_add_rmsnorm,
     swiglu_w4a16_gemv_add_rmsnorm_noalloc,

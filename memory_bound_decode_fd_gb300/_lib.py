@@ -31,6 +31,15 @@ FD_MAX_M = 256
 FD_MAX_HIDDEN = 32768
 FD_NVFP4_MAX_K = 16384
 FD_FOLD_SCRATCH_BYTES = 4096
+FD_STEP_MAX_LAYERS = 1024
+
+
+
+
+def step_scratch_bytes(n_layers: int, hidden: int) -> int:
+    """FD_STEP_SCRATCH_BYTES(n_layers, hidden) of include/fd.h: the layer counters padded
+    to 16 bytes, then two rows of 32-bit tagged h words."""
+    return (n_layers * 4 + 15) // 16 * 16 + hidden * 8
 
 # Every symbol include/fd.h declares, with its ctypes signature.
 _VP = ctypes.c_void_p
@@ -46,6 +55,7 @@ SIGNATURES = {
     "fd_copy": (_I, [_VP, _VP, ctypes.c_size_t, _VP]),
     "fd_debug_plan_gemv": (_I, [_VP, _I, _I, _I, _I, _I, _VP]),
     "fd_device_status": (_I, [_VP, _VP, _I]),
+    "fd_decode_mlp_step": (_I, [_VP, _I, _VP, _VP, ctypes.c_float, _I, _I, _I, _VP, _VP]),
     "fd_nvfp4_scaled_mm": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _VP]),
     "fd_debug_plan_nvfp4": (_I, [_I, _I, _I, _I, _VP]),
     "fd_add_rmsnorm": (_I, [_VP, _VP, _VP, ctypes.c_float, _VP, _VP, _I, _I, _VP]),

@@ -447,25 +447,49 @@ const char *fd_status_string(int status) {
     }
 }
 
+int fd_decode_mlp_step(const fd_step_layer *layers, int n_layers, const void *x0,
+                       void *residual, float eps, int hidden, int inter, int group,
+                       void *scratch, fd_stream_t stream) {
+    if (!layers || !x0 || !residual || !scratch) return FD_ERR_NULL;
+    if (n_layers < 1 || n_layers > FD_STEP_MAX_LAYERS || hidden <= 0 || hidden % 8 != 0 ||
+        inter <= 0 || group <= 0 || !(eps >= 0.0f) || !std::isfinite(eps))
+        return FD_ERR_SHAPE;
+    if (!aligned16(x0) || !aligned16(residual) || !aligned16(scratch) ||
+        !aligned16(layers))
+        return FD_ERR_ALIGN;
+    const size_t row = (size_t)hidden * 2;
+    const size_t sync_bytes = FD_STEP_SCRATCH_BYTES(n_layers, hidden);
+    if (overlaps(x0, row, residual, row) || overlaps(scratch, sync_bytes, residual, row) ||
+        overlaps(scratch, sync_bytes, x0, row))
+        return FD_ERR_OVERLAP;
+    if (!step_shape_supported(hidden, inter, group)) return FD_ERR_UNSUPPORTED;
+    if (fake_launch_failure()) return from_cuda(cudaErrorLaunchOutOfResources);
+    bool launched = false;
+    cudaError_t err = launch_decode_step(layers, n_layers, x0, residual, eps, hidden, inter, group,
+                                         scratch, reinterpret_cast<cudaStream_t>(stream), &launched);
+    if (err != cudaSuccess) return from_cuda(err);
+    return launched ? FD_OK : FD_ERR_UNSUPPORTED;
+}
+
 int fd_device_status(fd_stream_t stream, unsigned *status, int clear) {
     if (!status) return FD_ERR_NULL;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // one word per file with bounded waits; pinned so the copies are truly asynchronous
     static thread_local unsigned *words = nullptr;
     if (!words) {
-        cudaError_t err = cudaMallocHost(&words, 3 * sizeof(unsigned));
+        cudaError_t err = cudaMallocHost(&words, 4 * sizeof(unsigned));
         if (err != cudaSuccess) return from_cuda(err);
     }
-    cudaError_t (*const readers[3])(cudaStream_t, unsigned *, bool) = {
-        status_gemv_tma, status_gemv_tc, status_nvfp4};
-    for (int i = 0; i < 3; ++i) {
+    cudaError_t (*const readers[4])(cudaStream_t, unsigned *, bool) = {
+        status_gemv_tma, status_gemv_tc, status_nvfp4, status_decode_step};
+    for (int i = 0; i < 4; ++i) {
         words[i] = 0;
         cudaError_t err = readers[i](st, &words[i], clear != 0);
         if (err != cudaSuccess) return from_cuda(err);
     }
     cudaError_t err = cudaStreamSynchronize(st);
     if (err != cudaSuccess) return from_cuda(err);
-    *status = words[0] | words[1] | words[2];
+    *status = words[0] | words[1] | words[2] | words[3];
     return FD_OK;
 }
 

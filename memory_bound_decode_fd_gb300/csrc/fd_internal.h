@@ -108,6 +108,12 @@ cudaError_t launch_gemv_fold_noalloc(const void *gate, const void *up, const voi
 // Tensor-core path (tcgen05) for batched decode; sets *launched = false when the shape
 // is outside its rules (K % 1024, N % 128, group % 64, (K / group) % 8).
 bool gemv_tc_supported(int M, int K, int N, int group);
+// The decode step as one persistent kernel (fd_decode_step.cu); *launched = false when the
+// shape has no kernel or no plan.
+bool step_shape_supported(int hidden, int inter, int group);
+cudaError_t launch_decode_step(const fd_step_layer *layers, int n_layers, const void *x0,
+                               void *residual, float eps, int hidden, int inter, int group,
+                               void *scratch, cudaStream_t stream, bool *launched);
 cudaError_t launch_gemv_tc(const void *gate, const void *up, const void *qweight,
                            const void *scales, const void *residual, void *out, int M, int K,
                            int N, int group, cudaStream_t stream, bool *launched);
@@ -131,6 +137,7 @@ cudaError_t launch_w4_dequant_debug(const void *qweight, const void *scales, flo
 cudaError_t status_gemv_tma(cudaStream_t stream, unsigned *out, bool clear);
 cudaError_t status_gemv_tc(cudaStream_t stream, unsigned *out, bool clear);
 cudaError_t status_nvfp4(cudaStream_t stream, unsigned *out, bool clear);
+cudaError_t status_decode_step(cudaStream_t stream, unsigned *out, bool clear);
 
 // ------------------------------------------------------------------------------------
 // Device helpers.

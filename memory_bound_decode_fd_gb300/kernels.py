@@ -252,6 +252,65 @@ def swiglu_w4a16_gemv_add_rmsnorm(
     return y, normed, residual_out
 
 
+def step_layer_table(layers, normed, y, device=None) -> torch.Tensor:
+    """The device array of fd_step_layer that decode_mlp_step_persistent reads: per layer
+    the pointers (gate, up, qweight, scales, rms_weight, normed, y), as int64. ``layers``:
+    dicts of gate and up [1, inter] (or [inter]), qweight [hidden, inter/8] int32, scales
+    [hidden, inter/group] and rms_weight [hidden] bf16; ``normed`` and ``y``: per-layer
+    [1, hidden] bf16 outputs. The tensors must stay alive while the table is used."""
+    rows = []
+    for i, (l, n, yy) in enumerate(zip(layers, normed, y)):
+        hidden, k8 = l["qweight"].shape
+        _check_tensor(f"layers[{i}].qweight", l["qweight"], torch.int32, (hidden, k8))
+        for name in ("gate", "up"):
+            _check_tensor(f"layers[{i}].{name}", l[name], torch.bfloat16)
+            if l[name].numel() != 8 * k8:
+                raise ValueError(f"layers[{i}].{name} must hold inter={8 * k8} elements")
+        _check_tensor(f"layers[{i}].scales", l["scales"], torch.bfloat16)
+        _check_tensor(f"layers[{i}].rms_weight", l["rms_weight"], torch.bfloat16, (hidden,))
+        for name, t in (("normed", n), ("y", yy)):
+            _check_tensor(f"{name}[{i}]", t, torch.bfloat16)
+            if t.numel() != hidden:
+                raise ValueError(f"{name}[{i}] must hold hidden={hidden} elements")
+        rows.append([l["gate"].data_ptr(), l["up"].data_ptr(), l["qweight"].data_ptr(),
+                     l["scales"].data_ptr(), l["rms_weight"].data_ptr(), n.data_ptr(),
+                     yy.data_ptr()])
+    dev = device if device is not None else layers[0]["qweight"].device
+    return torch.tensor(rows, dtype=torch.int64, device=dev)
+
+
+def step_scratch(n_layers: int, hidden: int, device=None) -> torch.Tensor:
+    """The scratch of decode_mlp_step_persistent (a counter per layer and two rows of
+    tagged h words; every call zeroes it)."""
+    return torch.zeros(_lib.step_scratch_bytes(n_layers, hidden), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def decode_mlp_step_persistent(x, residual, table, eps, inter, group, scratch, stream=None):
+    """A whole decode step in one launch (fd_decode_mlp_step): for every layer of
+    ``table`` (step_layer_table), add-RMSNorm of (x_l, residual) into the layer's normed,
+    then its GEMV into its y, with x_0 = x and x_{l+1} = y_l; ``residual`` is left as the
+    last layer's h. Every output is bit-identical to decode_mlp_step's chain of separate
+    calls. ``inter`` is the GEMV's K. Nothing is allocated here."""
+    n_layers = int(table.shape[0])
+    hidden = x.numel()
+    _check_tensor("x", x, torch.bfloat16)
+    _check_tensor("residual", residual, torch.bfloat16)
+    if residual.numel() != hidden:
+        raise ValueError("residual must hold hidden elements")
+    _check_tensor("table", table, torch.int64, (n_layers, 7))
+    _check_tensor("scratch", scratch, torch.uint8)
+    if scratch.numel() < _lib.step_scratch_bytes(n_layers, hidden):
+        raise ValueError("scratch is too small (step_scratch)")
+    dev = _device_of(x, residual, table, scratch)
+    lib = _lib.load()
+    with _on_device(dev):
+        st = lib.fd_decode_mlp_step(_ptr(table), n_layers, _ptr(x), _ptr(residual),
+                                    ctypes.c_float(float(eps)), int(hidden), int(inter),
+                                    int(group), _ptr(scratch), _stream_handle(stream, dev))
+    _lib.check(st)
+
+
 def swiglu_w4a16_gemv_add_rmsnorm_noalloc(
     gate: torch.Tensor,
     up: torch.Tensor,

@@ -12,7 +12,8 @@ from __future__ import annotations
 
 import torch
 
-from .kernels import copy, decode_mlp_step, fold_scratch, set_pdl
+from .kernels import (copy, decode_mlp_step, decode_mlp_step_persistent, fold_scratch,
+                      set_pdl, step_layer_table, step_scratch)
 
 
 class DecodeStep:
@@ -26,7 +27,7 @@ class DecodeStep:
 
     def __init__(self, layers, hidden: int, inter: int, group: int, eps: float,
                  device="cuda", stream: torch.cuda.Stream | None = None, pdl: bool = True,
-                 fold: bool = False):
+                 fold: bool = False, persistent: bool = False):
         self.device = torch.device(device)
         self.eps = eps
         self.group = group
@@ -68,8 +69,18 @@ class DecodeStep:
         # on GB300 (the fold's last CTA adds about 3 us of dependent L2 round trips per
         # layer, the separate add-RMSNorm about 1.35 us), so it is off by default.
         self.scratch = fold_scratch(self.device) if fold else None
+        # persistent=True: the whole step as one cooperative launch (fd_decode_mlp_step), with
+        # the same outputs bit for bit; the layer table points at this object's buffers.
+        self.persistent = persistent
+        if persistent:
+            self.table = step_layer_table(self.layers, self.normed, self.y, self.device)
+            self.step_sync = step_scratch(L, self.hidden, self.device)
 
     def _launch(self):
+        if self.persistent:
+            decode_mlp_step_persistent(self.x, self.residual, self.table, self.eps, self.inter,
+                                       self.group, self.step_sync, stream=self.stream)
+            return self.y[-1], self.residual
         return decode_mlp_step(self.x, self.residual, self.layers, self.eps, self.group,
                                normed=self.normed, y=self.y, stream=self.stream,
                                scratch=self.scratch)

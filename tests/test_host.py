@@ -38,6 +38,7 @@ def test_library_exports_every_declared_symbol(fdlib):
 def test_header_constants_match_binding():
     text = HEADER.read_text()
     for name in ("FD_MAX_K", "FD_MAX_M", "FD_MAX_HIDDEN", "FD_LAUNCH_PDL", "FD_LAUNCH_TEST_FAIL",
+                 "FD_STEP_MAX_LAYERS",
                  "FD_LAUNCH_TEST_WAIT_TIMEOUT", "FD_DEVICE_STATUS_WAIT_TIMEOUT", "FD_NVFP4_MAX_K"):
         m = re.search(rf"#define {name} (\d+)", text)
         assert int(m.group(1)) == getattr(_lib, name)
