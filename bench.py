@@ -29,7 +29,9 @@ Reported:
 Other workloads (--workload gemv_94mb | rmsnorm_big | gemv_small | batched_m64 |
 gemv_residual | gate_up | nvfp4_qkv) time one call per step and rotate ceil(3 x L2 / bytes) input
 sets so every step reads HBM; --workload fused_layer times 32 layers of add-RMSNorm +
-gate/up GEMV + down GEMV with the residual epilogue as one graph.
+gate/up GEMV + down GEMV with the residual epilogue as one graph; --workload
+persistent_step [--layers L] times the decode step as one persistent cooperative launch
+(fd_decode_mlp_step; the decode_step line reports it too, as persistent_step).
 """
 
 from __future__ import annotations
@@ -898,6 +900,70 @@ def bench_fused_layer(args, device, rank, world):
 
 # ----------------------------------------------------------------------------- distributed plumbing
 
+def bench_persistent(args, device, rank, world):
+    """The decode step (add-RMSNorm + SwiGLU-W4A16 GEMV per layer, Llama-3-8B shapes) as one
+    persistent cooperative launch, fd_decode_mlp_step: one CTA per SM for all layers, the
+    outputs bit-identical to the chain of separate kernels. Timed as a CUDA graph of the
+    memset and the kernel; end to end through DecodeStep.run_pinned."""
+    import memory_bound_decode_fd_gb300 as fd
+    from memory_bound_decode_fd_gb300.step import DecodeStep
+
+    L = args.layers
+    d, base, bytes_per_step = build_decode(device, layers=L)
+    step = DecodeStep(base.layers, base.hidden, base.inter, base.group, base.eps, device,
+                      persistent=True)
+    step.x.copy_(base.x)
+    step.residual.copy_(base.residual)
+    step.gate.copy_(base.gate)
+    step.up.copy_(base.up)
+    step.capture()
+    del base
+    stream = step.stream
+    hbm_peak, peak_kind, _ = read_peaks()
+    sampler = ClockSampler(smi_index())
+    sampler.start()
+    with torch.cuda.stream(stream):
+        time_region(stream, step.replay, max(args.warmup, 3))
+        barrier(world)
+        ms = max_over_ranks(time_region(stream, step.replay, args.steps), world) / args.steps
+    clocks = sampler.stop()
+    io = step.pinned_io()
+    io.x.copy_(step.x.cpu())
+    io.residual.copy_(step.residual.cpu())
+    io.gate.copy_(step.gate.cpu())
+    io.up.copy_(step.up.cpu())
+    step.capture_pinned(io)
+    with torch.cuda.stream(stream):
+        time_region(stream, lambda: step.run_pinned(io), max(args.warmup, 3))
+        barrier(world)
+        e2e_ms = max_over_ranks(time_region(stream, lambda: step.run_pinned(io), args.steps), world) / args.steps
+    h2d, d2h = io.h2d_bytes, io.d2h_bytes
+    gbs = job_throughput_gbs(world, bytes_per_step, ms)
+    return {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "us_per_step": round(ms * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": DTYPE_DP2A + "; add-RMSNorm " + DTYPE_RMSNORM,
+        "data": "synthetic (seeded, as the decode_step workload)",
+        "config": {"workload": f"persistent_step: {L} x [add-RMSNorm 1x4096 eps 1e-5 + SwiGLU-W4A16 "
+                               "GEMV M=1 K=14336 N=4096 group 128], seed 3, one cooperative launch",
+                   "bytes_per_step": bytes_per_step,
+                   "l2": f"inputs larger than L2 ({bytes_per_step / 1e6:.0f} MB per step vs 129 MB L2); no flush",
+                   "parallelism": f"replicas x{world}"},
+        "launch": "CUDA graph of one memset and one cooperative kernel per step",
+        "pct_of_measured_hbm": round(100 * gbs / world / hbm_peak, 1),
+        "roofline": {"kernel": "decode_step_kernel (the whole step)", "bound": "hbm",
+                     "achieved": round(gbs / world, 1), "peak": hbm_peak,
+                     "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(gbs / world / hbm_peak, 4), "traffic": None},
+        "e2e": {"value": round(job_throughput_gbs(world, bytes_per_step, e2e_ms), 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "memory_bound_decode_fd_gb300.step.DecodeStep(persistent=True).run_pinned"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -930,7 +996,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--workload", default="decode_step",
                     choices=["decode_step", "gemv_94mb", "rmsnorm_big", "gemv_small", "batched_m64",
-                             "gemv_residual", "gate_up", "nvfp4_qkv", "fused_layer"])
+                             "gemv_residual", "gate_up", "nvfp4_qkv", "fused_layer",
+                             "persistent_step"])
+    ap.add_argument("--layers", type=int, default=32, help="persistent_step: layers per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="decode step only: skip timing the other workload configurations")
@@ -945,6 +1013,9 @@ def main(argv=None):
             if args.workload == "fused_layer":
                 line = {"impl": "reference", "unavailable": "the oracle has no gate/up-fed fused-layer chain; "
                         "its parts are timed by --workload gate_up and gemv_residual"}
+            elif args.workload == "persistent_step":
+                line = {"impl": "reference", "unavailable": "the same computation as decode_step "
+                        "(bit-identical outputs): --workload decode_step times the oracle on it"}
             else:
                 line = reference_arm(args)
             print(json.dumps(line), flush=True)
@@ -968,6 +1039,8 @@ def main(argv=None):
             line["cpu_baseline"] = cpu_baseline_decode(d)
     elif args.workload == "fused_layer":
         line = bench_fused_layer(args, device, rank, world)
+    elif args.workload == "persistent_step":
+        line = bench_persistent(args, device, rank, world)
     else:
         line = bench_single(args, device, rank, world)
     if rank == 0:

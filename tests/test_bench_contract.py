@@ -50,3 +50,13 @@ def test_reference_arm_other_workloads():
         line = json.loads(r.stdout.strip().splitlines()[-1])
         assert line["impl"] == "reference" and line["value"] > 0
         assert line["config"]["workload"] == wl
+
+
+def test_reference_arm_persistent_step_is_unavailable():
+    # the one-launch step computes exactly the decode step, whose oracle arm is decode_step
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                        "persistent_step", "--steps", "1", "--warmup", "0"], cwd=REPO,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and "decode_step" in line["unavailable"]
