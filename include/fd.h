@@ -354,7 +354,11 @@ int fd_gemv_uses_tensor_cores(int M, int K, int N, int group);
  * gives its waits a limit of about 2^20 SM clocks instead of about 2^31 and its copy thread
  * leaves the first weight chunk of every CTA uncopied, so the waits for that chunk run out:
  * the call's outputs are NaN and fd_device_status reports FD_DEVICE_STATUS_WAIT_TIMEOUT. No
- * fault and no hang: every wait is bounded and no copy is left in flight. */
+ * fault and no hang: every wait is bounded and no copy is left in flight.
+ * fd_decode_mlp_step under this flag: the same short limit, and one CTA never adds itself to
+ * the first layer's count, so every CTA's wait for that count runs out; layer 0's y and
+ * normalised row are correct, every later output and the residual are NaN, and the status
+ * reports FD_DEVICE_STATUS_WAIT_TIMEOUT. */
 #define FD_LAUNCH_TEST_WAIT_TIMEOUT 512u
 int fd_set_launch_flags(unsigned flags);
 unsigned fd_get_launch_flags(void);

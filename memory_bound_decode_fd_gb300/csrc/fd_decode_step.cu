@@ -42,7 +42,8 @@
 //     GEMV kernel.
 //   * Every wait is bounded (fd_tma.cuh). A wait that gives up records the status word; the
 //     CTA keeps taking part in every count (so no other CTA waits on it) and writes NaN
-//     where its results would have gone.
+//     where its results would have gone. FD_LAUNCH_TEST_WAIT_TIMEOUT makes the first
+//     count's waits run out on purpose, on a short limit.
 #include <atomic>
 
 #include "fd_gemv_common.cuh"
@@ -56,13 +57,13 @@ constexpr int kStepMaxStages = 8;     // chunks of one layer's rows per CTA
 constexpr int kStepRmsMaxVpt = 4;
 
 // Bounded spin until *p >= target, with acquire ordering at GPU scope.
-__device__ __forceinline__ bool wait_counter(const unsigned *p, unsigned target) {
+__device__ __forceinline__ bool wait_counter(const unsigned *p, unsigned target, long long limit) {
     const long long t0 = clock64();
     while (true) {
         unsigned v;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
         if (v >= target) return true;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             record_wait_timeout();
             return false;
         }
@@ -102,7 +103,7 @@ __device__ __forceinline__ void st_relaxed_u32(void *p, uint32_t v) {
 // Bounded re-read of the 8 tagged words of h vector v until all carry `tag`; returns the
 // 8 bf16 as one 16-byte vector (false if the wait gave up).
 __device__ __forceinline__ bool read_tagged_vec(const uint32_t *row, int v, uint32_t tag,
-                                                uint4 *out) {
+                                                uint4 *out, long long limit) {
     const uint4 *p = reinterpret_cast<const uint4 *>(row + 8 * v);
     const long long t0 = clock64();
     while (true) {
@@ -116,7 +117,7 @@ __device__ __forceinline__ bool read_tagged_vec(const uint32_t *row, int v, uint
                               __byte_perm(w[4], w[5], 0x5410), __byte_perm(w[6], w[7], 0x5410));
             return true;
         }
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             *out = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
             return false;
         }
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(1024, 1)
     decode_step_kernel(const fd_step_layer *__restrict__ layers, int n_layers,
                        const uint16_t *x0, uint16_t *residual, float eps, int N,
                        int rows_base, int rows_extra, int S, int w_rows, int rms_vpt,
-                       int rms_threads, unsigned *count, uint32_t *hrows) {
+                       int rms_threads, unsigned *count, uint32_t *hrows, int test_timeout) {
     constexpr int nvec = NVEC_C;      // 32-k slices
     constexpr int ngroups = NG_C;
     constexpr int ncons = 2 * nvec;   // two lanes per slice
@@ -228,6 +229,11 @@ __global__ void __launch_bounds__(1024, 1)
     // hrows[(l & 1) * N ..]: h_{l+1} as tagged words (tag l + 1), written at the end of
     // layer l; count[l]: the CTAs that have written theirs (count[0] is also the exit
     // count of a single-layer call).
+    // test_timeout (FD_LAUNCH_TEST_WAIT_TIMEOUT): short waits, and CTA 0 never adds itself
+    // to count[0], so every CTA's wait for it runs out; the CTAs carry on (every count
+    // after it is complete) and write NaN from the first normalised row that needed it.
+    const long long limit = test_timeout ? kTestWaitLimitCycles : kWaitLimitCycles;
+    const bool withhold = test_timeout && b == 0;
 
     if (tid == 0) {
         for (int s = 0; s < n_chunks; ++s) {
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(1024, 1)
                 const uint16_t *sc = static_cast<const uint16_t *>(layers[l].scales);
                 for (int c = 0; c < n_chunks; ++c) {
                     // the consumers have read chunk c of the previous layer
-                    if (ok && l > 0) ok = mbar_wait_bounded(&empty_bar[c], (l - 1) & 1, &abort_flag);
+                    if (ok && l > 0) ok = mbar_wait_bounded(&empty_bar[c], (l - 1) & 1, &abort_flag, limit);
                     if (!ok) break;
                     const int rows = min(kStepR, n_cnt - c * kStepR);
                     const size_t n0 = (size_t)n_begin + (size_t)c * kStepR;
@@ -266,7 +272,7 @@ __global__ void __launch_bounds__(1024, 1)
             // or after a failure whatever was issued)
             for (int c = 0; c < n_chunks; ++c) {
                 const long long t0 = clock64();
-                while (!mbar_try_parity(&full_bar[c], (n_layers - 1) & 1) && clock64() - t0 < kWaitLimitCycles) {
+                while (!mbar_try_parity(&full_bar[c], (n_layers - 1) & 1) && clock64() - t0 < limit) {
                 }
             }
         }
@@ -334,7 +340,7 @@ __global__ void __launch_bounds__(1024, 1)
         // ------------------------------------------------- the CTA's rows of y_l
         for (int c = 0; c < n_chunks; ++c) {
             float part[kRowsPerLane];
-            const bool ok = mbar_wait_bounded(&full_bar[c], l & 1, &abort_flag);
+            const bool ok = mbar_wait_bounded(&full_bar[c], l & 1, &abort_flag, limit);
             const int rows_valid = min(kStepR, n_cnt - c * kStepR);
             const uint4 *wst = reinterpret_cast<const uint4 *>(smem + (size_t)c * kStepR * w_row_bytes) +
                                slice + hh * nvec;
@@ -398,8 +404,8 @@ __global__ void __launch_bounds__(1024, 1)
         load_norm_weight(layers[l + 1].rms_weight, nvec_h, rms_vpt, rms_threads, wv);
         named_bar_sync(1, ncons);
         if (tid == 0) {
-            atomicAdd(&count[l], 1u);
-            if (!wait_counter(&count[l], (unsigned)grid)) abort_flag = 1;
+            if (!(withhold && l == 0)) atomicAdd(&count[l], 1u);
+            if (!wait_counter(&count[l], (unsigned)grid, limit)) abort_flag = 1;
         }
         named_bar_sync(1, ncons);
         bool got = true;
@@ -407,7 +413,7 @@ __global__ void __launch_bounds__(1024, 1)
         for (int i = 0; i < kStepRmsMaxVpt; ++i) {
             const int v = tid + i * rms_threads;
             hv[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (tid < rms_threads && i < rms_vpt && v < nvec_h) got &= read_tagged_vec(hbuf, v, tag, &hv[i]);
+            if (tid < rms_threads && i < rms_vpt && v < nvec_h) got &= read_tagged_vec(hbuf, v, tag, &hv[i], limit);
         }
         if (!got) {
             record_wait_timeout();
@@ -428,8 +434,8 @@ __global__ void __launch_bounds__(1024, 1)
     if (n_layers == 1) {
         named_bar_sync(1, ncons);
         if (tid == 0) {
-            atomicAdd(&count[0], 1u);
-            if (!wait_counter(&count[0], (unsigned)grid)) abort_flag = 1;
+            if (!withhold) atomicAdd(&count[0], 1u);
+            if (!wait_counter(&count[0], (unsigned)grid, limit)) abort_flag = 1;
         }
         named_bar_sync(1, ncons);
     }
@@ -514,7 +520,8 @@ cudaError_t launch_shape(const DeviceInfo &di, const fd_step_layer *layers, int 
                              plan.rows_extra, plan.S, plan.w_rows, rms_vpt, rms_threads,
                              static_cast<unsigned *>(scratch),
                              reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(scratch) +
-                                                          FD_STEP_SCRATCH_HROWS_OFFSET(n_layers)));
+                                                          FD_STEP_SCRATCH_HROWS_OFFSET(n_layers)),
+                             (launch_flags() & FD_LAUNCH_TEST_WAIT_TIMEOUT) ? 1 : 0);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }

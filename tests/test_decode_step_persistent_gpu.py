@@ -155,5 +155,44 @@ def test_persistent_run_pinned_equals_the_kernel_graph(step_data, dev_layers):
             io.x.copy_(io.out_x)
 
 
+@pytest.mark.parametrize("n", [1, 3])
+def test_persistent_wait_timeout_is_reported(step_data, dev_layers, chain, n):
+    # FD_LAUNCH_TEST_WAIT_TIMEOUT: one CTA withholds its first count, every CTA's wait for it
+    # runs out on the short limit; layer 0 stays correct, everything after it is NaN, the
+    # status is reported once, and the next call is bit-identical again
+    import time
+
+    from memory_bound_decode_fd_gb300 import _lib
+
+    lib = _lib.load()
+    persistent(step_data, dev_layers[:n])  # the kernel's launch facts, outside the flag
+    assert fd.device_status(clear=True) == 0
+    flags = lib.fd_get_launch_flags()
+    assert lib.fd_set_launch_flags(flags | _lib.FD_LAUNCH_TEST_WAIT_TIMEOUT) == _lib.FD_OK
+    try:
+        t0 = time.perf_counter()
+        normed, ys, res = persistent(step_data, dev_layers[:n])
+        elapsed = time.perf_counter() - t0
+    finally:
+        lib.fd_set_launch_flags(flags)
+    assert elapsed < 5.0, elapsed
+    n_ref, _, y_ref = chain[0]
+    assert np.array_equal(normed[0].reshape(-1), n_ref.reshape(-1))
+    assert np.array_equal(ys[0].reshape(-1), y_ref.reshape(-1))
+    nan = lambda bits: np.all(np.isnan(bf16_float(bits)))  # noqa: E731
+    for l in range(1, n):
+        assert nan(normed[l]) and nan(ys[l]), l
+    assert nan(res)
+    assert fd.device_status(clear=True) & _lib.FD_DEVICE_STATUS_WAIT_TIMEOUT
+    assert fd.device_status(clear=True) == 0
+    assert_same(persistent(step_data, dev_layers[:n]), chain[:n])
+    assert fd.device_status(clear=True) == 0
+
+
+def bf16_float(bits):
+    b = np.asarray(bits).reshape(-1).astype(np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32)
+
+
 def test_device_status_clean_after_the_persistent_steps(cuda_device):
     assert fd.device_status(clear=True) == 0
