@@ -73,6 +73,15 @@ KERNEL_SOURCES = {
                            "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
     "nvfp4_scaled_mm": ["csrc/fd_nvfp4.cu", "csrc/fd_nvfp4_plan.h", "csrc/fd_tc.cuh", "csrc/fd_tma.cuh",
                         "csrc/fd_internal.h"],
+    # the residual-add epilogue is the same bulk-copy kernel's residual form
+    "swiglu_w4a16_gemv_residual": ["csrc/fd_gemv_tma.cu", "csrc/fd_gemv_common.cuh", "csrc/fd_tma.cuh",
+                                   "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
+    # the tensor-core GEMV of batched decode (M >= 16)
+    "gemv_tc": ["csrc/fd_gemv_tc.cu", "csrc/fd_tc.cuh", "csrc/fd_gemv_common.cuh", "csrc/fd_tma.cuh",
+                "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
+    # the decode step as one persistent kernel
+    "decode_step": ["csrc/fd_decode_step.cu", "csrc/fd_gemv_common.cuh", "csrc/fd_tma.cuh",
+                    "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
 }
 
 
@@ -615,6 +624,10 @@ def build_single_calls(name, device, l2):
     if kind in ("gemv", "batched", "gemv_residual"):
         M, K, N, g = spec["M"], spec["K"], spec["N"], spec["group"]
         extra.update(M=M, K=K, N=N, group=g)
+        if fd.gemv_uses_tensor_cores(M, K, N, g):
+            extra.update(traffic_kernel="gemv_tc", traffic_tag=f"M{M}_K{K}_N{N}")
+        else:
+            extra["traffic_tag"] = f"K{K}_N{N}_M{M}"
         with_res = kind == "gemv_residual"
         nbytes = fd.gemv_bytes(M, K, N, g) + (M * N * 2 if with_res else 0)
         nsets = max(1, min(4096, math.ceil(3 * l2 / nbytes)))
@@ -682,6 +695,7 @@ def build_single_calls(name, device, l2):
         for x, r in sets:
             calls.append(lambda x=x, r=r: fd.add_rmsnorm(x, r, w, spec["eps"], out=y, residual_out=h))
         kname, desc = "add_rmsnorm", f"add-RMSNorm rows={rows} hidden={hidden} eps {spec['eps']}, seed {spec['seed']}"
+        extra["traffic_tag"] = f"R{rows}_H{hidden}"
     return calls, nbytes, kname, desc, extra
 
 
@@ -792,7 +806,7 @@ def measure_workload(name, device, world, steps=None, warmup=3, target_ms=300.0,
     if compare:
         rec["paths"] = compare
     if extra.get("traffic_tag"):
-        rec["traffic"] = recorded_traffic(kname, extra["traffic_tag"])
+        rec["traffic"] = recorded_traffic(extra.get("traffic_kernel", kname), extra["traffic_tag"])
     return rec
 
 
@@ -939,6 +953,10 @@ def bench_persistent(args, device, rank, world):
         e2e_ms = max_over_ranks(time_region(stream, lambda: step.run_pinned(io), args.steps), world) / args.steps
     h2d, d2h = io.h2d_bytes, io.d2h_bytes
     gbs = job_throughput_gbs(world, bytes_per_step, ms)
+    # DRAM bytes per launch: the 8-layer ncu capture, scaled by the layers (every layer
+    # moves the same bytes)
+    t8 = recorded_traffic("decode_step", "L8")
+    traffic = None if t8 is None else int(round(t8 * L / 8))
     return {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
@@ -955,7 +973,8 @@ def bench_persistent(args, device, rank, world):
         "roofline": {"kernel": "decode_step_kernel (the whole step)", "bound": "hbm",
                      "achieved": round(gbs / world, 1), "peak": hbm_peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(gbs / world / hbm_peak, 4), "traffic": None},
+                     "frac": round(gbs / world / hbm_peak, 4), "traffic": traffic,
+                     "traffic_note": "8-layer capture scaled by layers / 8"},
         "e2e": {"value": round(job_throughput_gbs(world, bytes_per_step, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "memory_bound_decode_fd_gb300.step.DecodeStep(persistent=True).run_pinned"},

@@ -2,6 +2,7 @@
 
     python -m memory_bound_decode_fd_gb300.profile_case gemv --M 1 --K 14336 --N 4096
     python -m memory_bound_decode_fd_gb300.profile_case gemv --M 64 --path tensor
+    python -m memory_bound_decode_fd_gb300.profile_case gemv_residual --M 1 --K 14336 --N 4096
     python -m memory_bound_decode_fd_gb300.profile_case rmsnorm --rows 8192 --hidden 4096
     python -m memory_bound_decode_fd_gb300.profile_case gate_up --K 4096 --N 14336
     python -m memory_bound_decode_fd_gb300.profile_case nvfp4 --M 64 --K 4096 --N 6144
@@ -30,7 +31,7 @@ def main(argv=None) -> int:
     from memory_bound_decode_fd_gb300 import build, inputs
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["gemv", "rmsnorm", "gate_up", "nvfp4"])
+    ap.add_argument("case", choices=["gemv", "gemv_residual", "rmsnorm", "gate_up", "nvfp4"])
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--K", type=int, default=14336)
     ap.add_argument("--N", type=int, default=4096, help="rows (gate_up: I, the stacked weight has 2I)")
@@ -46,7 +47,7 @@ def main(argv=None) -> int:
     build.build()
     fd.set_gemv_path(args.path)
     dev = torch.device("cuda:0")
-    if args.case == "gemv":
+    if args.case in ("gemv", "gemv_residual"):
         rng = np.random.default_rng(0)
         d = inputs.gemv_inputs(args.M, args.K, args.N, args.group, rng=rng)
         g, u = _dev(d["gate"], dev), _dev(d["up"], dev)
@@ -54,9 +55,13 @@ def main(argv=None) -> int:
                  _dev(inputs.scales_bf16(rng, args.N, args.K, args.group), dev))
                 for _ in range(args.sets)]
         out = torch.empty((args.M, args.N), dtype=torch.bfloat16, device=dev)
+        res = _dev(inputs.normal_bf16(rng, (args.M, args.N)), dev)
         for i in range(args.iters):
             q, s = sets[i % len(sets)]
-            fd.swiglu_w4a16_gemv(g, u, q, s, out=out, group=args.group)
+            if args.case == "gemv":
+                fd.swiglu_w4a16_gemv(g, u, q, s, out=out, group=args.group)
+            else:
+                fd.swiglu_w4a16_gemv_residual(g, u, q, s, res, out=out, group=args.group)
     elif args.case == "gate_up":
         rng = np.random.default_rng(0)
         x = _dev(inputs.normal_bf16(rng, (args.M, args.K)), dev)
