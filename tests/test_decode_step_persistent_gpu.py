@@ -106,6 +106,36 @@ def test_persistent_other_hidden(cuda_device):
     assert_same(persistent(d, layers), separate_chain(d, layers))
 
 
+@pytest.mark.parametrize("hidden", [8, 64, 1216, 4104, 4408])
+def test_persistent_edge_hidden(cuda_device, hidden):
+    # 1 CTA of 8 rows; 8 CTAs; 8 rows on every SM; 27 rows on every SM (a last chunk of
+    # 3 rows); 29 rows on every SM, the most whose weights fit one CTA's shared memory
+    d = inputs.decode_step_inputs(layers=2, hidden=hidden, seed=13)
+    layers = device_layers(d)
+    assert_same(persistent(d, layers), separate_chain(d, layers))
+
+
+def test_persistent_rows_beyond_shared_memory_are_unsupported(cuda_device):
+    # hidden 8192: 54 rows per CTA do not fit one CTA's shared memory; nothing is launched
+    from memory_bound_decode_fd_gb300 import _lib
+
+    d = inputs.decode_step_inputs(layers=1, hidden=8192, seed=14)
+    layers = device_layers(d)
+    x = dev_bf16(d["x"])
+    res = dev_bf16(d["residual"])
+    res0 = res.clone()
+    normed = [torch.zeros((1, 8192), dtype=torch.bfloat16, device="cuda")]
+    ys = [torch.zeros((1, 8192), dtype=torch.bfloat16, device="cuda")]
+    table = fd.step_layer_table(layers, normed, ys)
+    with pytest.raises(_lib.FdError) as e:
+        fd.decode_mlp_step_persistent(x, res, table, EPS, d["inter"], d["group"],
+                                      fd.step_scratch(1, 8192))
+    assert e.value.status == _lib.FD_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert torch.equal(res.view(torch.int16), res0.view(torch.int16))
+    assert not normed[0].view(torch.int16).any() and not ys[0].view(torch.int16).any()
+
+
 def _decode_step(d, layers, persistent_mode):
     from memory_bound_decode_fd_gb300.step import DecodeStep
 
