@@ -43,7 +43,7 @@ namespace fd {
 namespace {
 
 constexpr int kTcRows = 128;                 // weight rows per CTA (MMA M)
-constexpr int kTcStepK = 64;                 // k per pipeline step
+constexpr int kTcGuBoxK = 64;                // k per gate/up tensor-map box (128 bytes)
 constexpr int kTcSplit = 4;                  // CTAs per cluster (K quarters)
 constexpr int kTcFirstWorker = 3;            // warps 0, 1, 2: weights, gate/up, MMA
 constexpr int kTcDequantWarps = 8;           // then the A-operand (weight) warps
@@ -54,11 +54,12 @@ constexpr int kTcSiluThreads = kTcSiluWarps * 32;
 constexpr int kTcEpilogueThreads = kTcDequantWarps * 32;  // the dequant warps
 constexpr int kTcMaxStages = 16;
 constexpr int kTcWTileK = 256;               // k per weight tile (128 bytes of a row)
-constexpr int kTcStepsPerWTile = kTcWTileK / kTcStepK;
 constexpr uint32_t kWStageBytes = kTcRows * kTcWTileK / 2;  // int4 tile: 16384
-constexpr uint32_t kATileBytes = kTcRows * kTcStepK * 2;   // bf16 A tile: 16384
 constexpr uint32_t kCoreBytes = 128;                       // 8 rows x 16 bytes
-constexpr uint32_t kGroupBytes = 8 * kCoreBytes;           // 8-row group of a 64-k tile
+
+// k per pipeline step: 128 for up to 64 activation rows (half the per-step handshakes per
+// weight byte), 64 for 128 rows (whose larger operand stages would not fit twice).
+__host__ __device__ constexpr int tc_step_k(int npad) { return npad <= 64 ? 128 : 64; }
 
 // Bias of the nibble trick: bf16 0x4300 | u is 128 + u, and u = q + 8.
 constexpr uint32_t kMagic136x2 = 0x43084308u;
@@ -70,7 +71,7 @@ __device__ __forceinline__ void wait_parity_hw(uint64_t *bar, uint32_t parity) {
     while (!mbar_test_parity(bar, parity) && clock64() - t0 < kWaitLimitCycles) __nanosleep(64);
 }
 
-template <int NPAD>
+template <int NPAD, int STEPK>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap map_w,
                    const __grid_constant__ CUtensorMap map_s,
@@ -79,10 +80,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    uint16_t *out, int M, int N, int group, int k_cta, int s_w, int s_gu, int s_op,
                    uint32_t off_gu, uint32_t off_op, uint32_t off_sc, int sg) {
     static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 128, "N of the MMA");
+    static_assert(STEPK == 64 || STEPK == 128, "k per step");
     constexpr int kCols = NPAD < 32 ? 32 : NPAD;  // TMEM columns (power of two)
-    constexpr uint32_t kGuTile = NPAD * 128;      // one gate or up tile (NPAD x 64 bf16)
-    constexpr uint32_t kGuStage = 2 * kGuTile;
-    constexpr uint32_t kOpStage = kATileBytes + NPAD * 128;
+    constexpr int kBoxes = STEPK / kTcGuBoxK;     // gate (or up) boxes per step
+    constexpr uint32_t kGuTile = NPAD * 128;      // one box: NPAD x 64 bf16
+    constexpr uint32_t kGuStage = 2 * kBoxes * kGuTile;  // gate boxes, then up boxes
+    constexpr uint32_t kATileBytes = kTcRows * STEPK * 2;  // bf16 A tile
+    constexpr uint32_t kGroupBytes = (STEPK / 8) * kCoreBytes;  // 8-row group of a tile
+    constexpr uint32_t kOpStage = kATileBytes + NPAD * STEPK * 2;
+    constexpr int kStepsPerWTile = kTcWTileK / STEPK;
+    constexpr int kChunks = STEPK / 64;           // 32-k weight chunks per thread per step
     constexpr int kHalf = NPAD / 2;               // accumulator columns per epilogue warp
 
     __shared__ __align__(8) uint64_t w_full[kTcMaxStages], w_empty[kTcMaxStages];
@@ -102,7 +109,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t rank = cluster_ctarank();
     const int n0 = blockIdx.y * kTcRows;
     const int k0 = (int)rank * k_cta;
-    const int n_steps = k_cta / kTcStepK;
+    const int n_steps = k_cta / STEPK;
     const int g_op = s_op / 2;  // operand stages per commit (the ring has two halves)
     const int x0_scale = (k0 / group) & ~7;
 
@@ -185,8 +192,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) {
                 unsigned char *st = smem + off_gu + (size_t)s * kGuStage;
                 mbar_arrive_expect_tx(&gu_full[s], kGuStage);
-                tma_load_2d(st, &map_g, k0 + t * kTcStepK, 0, &gu_full[s], pol);
-                tma_load_2d(st + kGuTile, &map_u, k0 + t * kTcStepK, 0, &gu_full[s], pol);
+#pragma unroll
+                for (int bx = 0; bx < kBoxes; ++bx) {
+                    const int kx = k0 + t * STEPK + bx * kTcGuBoxK;
+                    tma_load_2d(st + bx * kGuTile, &map_g, kx, 0, &gu_full[s], pol);
+                    tma_load_2d(st + (kBoxes + bx) * kGuTile, &map_u, kx, 0, &gu_full[s], pol);
+                }
             }
             issued = t + 1;
             if (++s == s_gu) { s = 0; ++round; }
@@ -216,7 +227,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!mbar_wait_bounded(&op_full[s], phase, &abort_flag)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int j = 0; j < kTcStepK / 16; ++j)
+                for (int j = 0; j < STEPK / 16; ++j)
                     tc_mma_f16(tmem, ad + j * kStepField, bd + j * kStepField, idesc, (t | j) != 0);
                 if (++gpos == g_op || t == n_steps - 1) {
                     tc_commit(&op_empty[gcount & 1]);
@@ -243,55 +254,67 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int wt = tid - kTcFirstWorker * 32;
         const uint32_t key = opaque_u32(kMagic136x2);
         const uint32_t magic = opaque_u32(kMagic136x2);
-        const int row = wt & (kTcRows - 1);  // weight row and 32-k half of each step
+        const int row = wt & (kTcRows - 1);  // weight row and k half of each step
         const int h = wt >> 7;
-        const int steps_per_group = group / kTcStepK;
-        int gstep = (k0 % group) / kTcStepK;
-        // 128-byte swizzle of the tensor-map copy: 16-byte chunk c of row r sits at c ^ (r & 7)
+        // 128-byte swizzle of the tensor-map copy: 16-byte chunk c of row r sits at c ^ (r & 7);
+        // this thread's chunks of step q of a tile: 2 q kChunks + h kChunks + j
         const uint32_t w_row0 = smem_u32(smem) + row * 128;
-        uint32_t chunk_off[kTcStepsPerWTile];
+        uint32_t chunk_off[kStepsPerWTile][kChunks];
 #pragma unroll
-        for (int q = 0; q < kTcStepsPerWTile; ++q) chunk_off[q] = ((uint32_t)(2 * q + h) ^ (row & 7)) << 4;
+        for (int q = 0; q < kStepsPerWTile; ++q)
+#pragma unroll
+            for (int j = 0; j < kChunks; ++j)
+                chunk_off[q][j] = ((uint32_t)(2 * q * kChunks + h * kChunks + j) ^ (row & 7)) << 4;
         const uint32_t a_row0 = smem_u32(smem + off_op) + (row >> 3) * kGroupBytes + (row & 7) * 16 +
-                                h * 4 * kCoreBytes;
-        uint32_t sc_at = smem_u32(smem + off_sc) + (uint32_t)(row * sg + (k0 / group - x0_scale)) * 2;
+                                h * (STEPK / 16) * kCoreBytes;
+        // the group scale of this thread's k range (STEPK / 2 k, never across a group: group is
+        // a multiple of 64 and the range starts at a multiple of STEPK / 2)
+        int gk = k0 % group + h * (STEPK / 2);
+        uint32_t sc_at = smem_u32(smem + off_sc) +
+                         (uint32_t)(row * sg + (k0 / group - x0_scale) + gk / group) * 2;
+        gk %= group;
         const uint32_t w_full0 = smem_u32(&w_full[0]), w_empty0 = smem_u32(&w_empty[0]);
         const uint32_t op_full0 = smem_u32(&op_full[0]), op_empty0 = smem_u32(&op_empty[0]);
         bool ok = mbar_wait_bounded(&sc_full, 0, &abort_flag);
         int ws = 0, wph = 0, os = 0, gpos = 0, gcount = 0;
         uint32_t w_at = w_row0, a_at = a_row0;
         for (int t = 0; t < n_steps && ok; ++t) {
-            const int wsub = t & (kTcStepsPerWTile - 1);
+            const int wsub = t & (kStepsPerWTile - 1);
             // entering a ring half: wait for the commit of its previous use
             ok = (wsub != 0 || mbar_wait_bounded_at(w_full0 + 8 * ws, wph, &abort_flag)) &&
                  (gpos != 0 || gcount < 2 ||
                   mbar_wait_bounded_at(op_empty0 + 8 * (gcount & 1), ((gcount >> 1) - 1) & 1,
                                        &abort_flag));
             if (!ok) break;
-            const uint4 wv = lds_v4(w_at + chunk_off[wsub]);
+            uint4 wv[kChunks];
+#pragma unroll
+            for (int j = 0; j < kChunks; ++j) wv[j] = lds_v4(w_at + chunk_off[wsub][j]);
             const uint32_t sc = lds_u16(sc_at);
             const uint32_t s2 = sc | (sc << 16);
-            const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                // pairs (k_j, k_j+4) of the word's 8 k: 136 + q as bf16, exact
-                const uint32_t w = wd[i];
-                const uint32_t t0 = mask_xor<0x000F000Fu>(w, key);
-                const uint32_t t1 = mask_xor<0x000F000Fu>(w >> 4, key);
-                const uint32_t t2 = mask_xor<0x000F000Fu>(w >> 8, key);
-                const uint32_t t3 = mask_xor<0x000F000Fu>(w >> 12, key);
-                uint4 o;
-                o.x = bf16x2_mul(bf16x2_sub(t0, magic), s2);
-                o.y = bf16x2_mul(bf16x2_sub(t1, magic), s2);
-                o.z = bf16x2_mul(bf16x2_sub(t2, magic), s2);
-                o.w = bf16x2_mul(bf16x2_sub(t3, magic), s2);
-                sts_v4(a_at + i * kCoreBytes, o);
+            for (int j = 0; j < kChunks; ++j) {
+                const uint32_t wd[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    // pairs (k_j, k_j+4) of the word's 8 k: 136 + q as bf16, exact
+                    const uint32_t w = wd[i];
+                    const uint32_t t0 = mask_xor<0x000F000Fu>(w, key);
+                    const uint32_t t1 = mask_xor<0x000F000Fu>(w >> 4, key);
+                    const uint32_t t2 = mask_xor<0x000F000Fu>(w >> 8, key);
+                    const uint32_t t3 = mask_xor<0x000F000Fu>(w >> 12, key);
+                    uint4 o;
+                    o.x = bf16x2_mul(bf16x2_sub(t0, magic), s2);
+                    o.y = bf16x2_mul(bf16x2_sub(t1, magic), s2);
+                    o.z = bf16x2_mul(bf16x2_sub(t2, magic), s2);
+                    o.w = bf16x2_mul(bf16x2_sub(t3, magic), s2);
+                    sts_v4(a_at + (4 * j + i) * kCoreBytes, o);
+                }
             }
             // generic writes of A before the tensor core reads them; generic reads of the
             // weight stage before the next bulk copy overwrites it
             fence_proxy_async_smem();
             __syncwarp();
-            const bool tile_done = (wsub == kTcStepsPerWTile - 1);
+            const bool tile_done = (wsub == kStepsPerWTile - 1);
             if (lane == 0) {
                 if (tile_done) mbar_arrive_at(w_empty0 + 8 * ws);
                 mbar_arrive_at(op_full0 + 8 * os);
@@ -301,12 +324,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (++os == s_op) { os = 0; a_at = a_row0; } else { a_at += kOpStage; }
             if (++gpos == g_op) { gpos = 0; ++gcount; }
-            if (++gstep == steps_per_group) { gstep = 0; sc_at += 2; }
+            for (gk += STEPK; gk >= group; gk -= group) sc_at += 2;
         }
         __syncwarp();
     } else {
         // -------------------------------------------------- SwiGLU warps: B operand
-        constexpr int kItems = (NPAD * 8 + kTcSiluThreads - 1) / kTcSiluThreads;
+        constexpr int kC = STEPK / 8;                 // 16-byte chunks per row of a step
+        constexpr int kCBits = STEPK == 128 ? 4 : 3;
+        constexpr int kItems = (NPAD * kC + kTcSiluThreads - 1) / kTcSiluThreads;
         const int st = tid - kTcFirstSilu * 32;
         const float2 half2 = make_float2(0.5f, 0.5f);
         // lanes 0..7 take rows 0..7 of one core matrix: conflict-free reads (128-byte
@@ -316,10 +341,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int j = 0; j < kItems; ++j) {
             const int item = st + j * kTcSiluThreads;
-            const int m = (item & 7) | ((item >> 6) << 3);
-            const int c = (item >> 3) & 7;
-            active[j] = item < NPAD * 8;
-            src_off[j] = m * 128 + ((c ^ (m & 7)) << 4);
+            const int m = (item & 7) | ((item >> (3 + kCBits)) << 3);
+            const int c = (item >> 3) & (kC - 1);
+            active[j] = item < NPAD * kC;
+            // box c / 8 of the step, chunk c % 8 of its 128-byte row
+            src_off[j] = (c >> 3) * kGuTile + m * 128 + (((c & 7) ^ (m & 7)) << 4);
             dst_off[j] = (m >> 3) * kGroupBytes + c * kCoreBytes + (m & 7) * 16;
         }
         const uint32_t g_row0 = smem_u32(smem + off_gu);
@@ -339,7 +365,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int j = 0; j < kItems; ++j) {
                 if (active[j]) {
                     const uint4 gv = lds_v4(g_at + src_off[j]);
-                    const uint4 uv = lds_v4(g_at + kGuTile + src_off[j]);
+                    const uint4 uv = lds_v4(g_at + kBoxes * kGuTile + src_off[j]);
                     const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
                     const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
                     float2 a[4];  // a[i] = (element 2i, element 2i + 1)
@@ -480,21 +506,24 @@ struct TcPlan {
     uint32_t off_gu, off_op, off_sc, smem;
 };
 
-// Shared-memory plan: a deep ring of int4 weight tiles (the HBM stream), then as many
-// gate/up and operand stages as fit (2..4 each).
-bool make_plan(int npad, int k_cta, int group, size_t budget, TcPlan *p) {
-    const uint32_t gu_stage = 2u * npad * 128;
-    const uint32_t op_stage = kATileBytes + npad * 128u;
+// Shared-memory plan: a ring of int4 weight tiles (the HBM stream; 4 tiles, fewer where the
+// operand stages need the room), then as many gate/up and operand stages as fit (2..4 each).
+bool make_plan(int npad, int stepk, int k_cta, int group, size_t budget, TcPlan *p) {
+    const uint32_t gu_stage = 2u * (stepk / kTcGuBoxK) * npad * 128;
+    const uint32_t op_stage = (uint32_t)kTcRows * stepk * 2 + (uint32_t)npad * stepk * 2;
     p->sg = ((k_cta + group - 1) / group + 7 + 7) & ~7;
     if (p->sg > 256) return false;
-    p->s_w = 4;
-    const uint32_t w_bytes = p->s_w * kWStageBytes;
     const uint32_t sc_bytes = ((uint32_t)kTcRows * p->sg * 2 + 1023u) & ~1023u;
-    if (budget < 1024 + w_bytes + sc_bytes) return false;
-    const size_t avail = budget - 1024 - w_bytes - sc_bytes;
+    size_t avail = 0;
+    for (p->s_w = 4; p->s_w >= 2; --p->s_w) {
+        const size_t fixed = 1024 + (size_t)p->s_w * kWStageBytes + sc_bytes;
+        avail = budget > fixed ? budget - fixed : 0;
+        if (2 * (size_t)gu_stage + 2 * (size_t)op_stage <= avail) break;
+    }
+    if (p->s_w < 2) return false;
+    const uint32_t w_bytes = p->s_w * kWStageBytes;
     int s_gu = 2, s_op = 2;
     size_t used = 2 * (size_t)gu_stage + 2 * (size_t)op_stage;
-    if (used > avail) return false;
     for (bool grew = true; grew;) {
         grew = false;
         if (s_op < 4 && used + op_stage <= avail) { ++s_op; used += op_stage; grew = true; }
@@ -517,7 +546,8 @@ cudaError_t launch_npad(const DeviceInfo &di, const void *gate, const void *up,
                         bool *launched) {
     static std::atomic<uint64_t> attr_done{0};
     static std::atomic<int> static_smem_cache{-1};
-    auto kern = gemv_tc_kernel<NPAD>;
+    constexpr int kStepK = tc_step_k(NPAD);
+    auto kern = gemv_tc_kernel<NPAD, kStepK>;
     int static_smem = static_smem_cache.load(std::memory_order_relaxed);
     if (static_smem < 0) {
         cudaFuncAttributes fa;
@@ -529,7 +559,7 @@ cudaError_t launch_npad(const DeviceInfo &di, const void *gate, const void *up,
     const int k_cta = K / kTcSplit;
     TcPlan plan;
     const size_t budget = (size_t)di.max_smem_optin - (size_t)static_smem;
-    if (!make_plan(NPAD, k_cta, group, budget, &plan)) return cudaSuccess;  // not launched
+    if (!make_plan(NPAD, kStepK, k_cta, group, budget, &plan)) return cudaSuccess;  // not launched
 
     CUtensorMap mw, ms, mg, mu;
     if (!encode_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, qweight, (uint64_t)K / 2, (uint64_t)N,
@@ -538,9 +568,9 @@ cudaError_t launch_npad(const DeviceInfo &di, const void *gate, const void *up,
                    (uint64_t)N, (uint64_t)(K / group) * 2, (uint32_t)plan.sg, kTcRows,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, gate, (uint64_t)K, (uint64_t)mc,
-                   (uint64_t)K * 2, kTcStepK, NPAD, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                   (uint64_t)K * 2, kTcGuBoxK, NPAD, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, up, (uint64_t)K, (uint64_t)mc,
-                   (uint64_t)K * 2, kTcStepK, NPAD, CU_TENSOR_MAP_SWIZZLE_128B))
+                   (uint64_t)K * 2, kTcGuBoxK, NPAD, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
 
     int dev = 0;
@@ -567,7 +597,7 @@ cudaError_t launch_npad(const DeviceInfo &di, const void *gate, const void *up,
 
 bool gemv_tc_supported(int M, int K, int N, int group) {
     if (M < 1 || K % (kTcSplit * 256) != 0 || N % kTcRows != 0) return false;
-    if (group % kTcStepK != 0 || K % group != 0 || (K / group) % 8 != 0) return false;
+    if (group % kTcGuBoxK != 0 || K % group != 0 || (K / group) % 8 != 0) return false;
     const int k_cta = K / kTcSplit;
     return ((k_cta + group - 1) / group + 14) <= 256;
 }
