@@ -27,13 +27,12 @@
 //     every CTA reads the whole h row, re-reading a 16-byte vector in the rare case that
 //     not all its words carry the layer's tag yet. (Polling the tagged row itself, with no
 //     counter, measured slower: 152 CTAs re-reading the same lines.) It computes the next
-//     layer's
-//     add-RMSNorm for the whole row exactly as the row kernel does (the same thread count,
-//     vector layout and reduction order) into shared memory and stores its own rows of
-//     the normalised row. So each CTA holds the complete normalised row before it reads
-//     the next layer's activations, as the next kernel of a chain starts only after
-//     add-RMSNorm has finished. The first layer's add-RMSNorm needs no wait: every CTA
-//     computes it from x0 and the residual.
+//     layer's add-RMSNorm for the whole row exactly as the row kernel does (the same
+//     thread count, vector layout and reduction order) into shared memory and stores its
+//     own rows of the normalised row. So each CTA holds the complete normalised row before
+//     it reads the next layer's activations, as the next kernel of a chain starts only
+//     after add-RMSNorm has finished. The first layer's add-RMSNorm needs no wait: every
+//     CTA computes it from x0 and the residual.
 //   * A CTA writes h row l + 2 into the buffer that held h row l only after it has read
 //     the whole h row l + 1, which every CTA writes only after it has read h row l. The
 //     call zeroes the rows first, so no tag of an earlier call is taken for this one.
