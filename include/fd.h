@@ -466,6 +466,19 @@ int fd_copy(void *dst, const void *src, size_t bytes, fd_stream_t stream);
  */
 int fd_debug_plan_gemv(const int *device, int M, int K, int N, int group, int plain, int *plan);
 
+/*
+ * fd_debug_plan_step - test support: the launch plan fd_decode_mlp_step would use, computed
+ * on the host from given device facts, without any CUDA call.
+ * device  int[6], as for fd_debug_plan_gemv (the persistent kernel's static shared memory in
+ *         device[4]; the budget is device[1] - device[4]).
+ * plan    int[8] out: grid, rows_base, rows_extra (the first rows_extra CTAs own one more
+ *         row), chunks of the largest CTA's rows, weight rows of shared memory, dynamic shared
+ *         memory per CTA, and the add-RMSNorm row's 16-byte vectors per thread and threads.
+ * Returns FD_ERR_SHAPE for a non-positive size or hidden not a multiple of 8;
+ * FD_ERR_UNSUPPORTED when the step has no kernel or no plan for the shape.
+ */
+int fd_debug_plan_step(const int *device, int hidden, int inter, int group, int *plan);
+
 /* The cudaError_t value behind the calling thread's most recent FD_ERR_CUDA (0 if none).
  * Thread-local; not reset by successful calls. */
 int fd_last_cuda_error(void);

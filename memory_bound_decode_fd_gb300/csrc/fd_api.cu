@@ -10,6 +10,7 @@
 #include "fd_gemv_plan.h"
 #include "fd_internal.h"
 #include "fd_nvfp4_plan.h"
+#include "fd_step_plan.h"
 
 namespace fd {
 
@@ -360,6 +361,22 @@ int fd_debug_plan_gemv(const int *device, int M, int K, int N, int group, int pl
     const int v[9] = {p.grid, p.rows_base, p.rows_extra, p.S, p.w_rows, p.act_first_stage,
                       p.ring, p.per_sm, (int)p.smem};
     for (int i = 0; i < 9; ++i) plan[i] = v[i];
+    return FD_OK;
+}
+
+int fd_debug_plan_step(const int *device, int hidden, int inter, int group, int *plan) {
+    if (!device || !plan) return FD_ERR_NULL;
+    if (hidden <= 0 || hidden % 8 != 0 || inter <= 0 || group <= 0) return FD_ERR_SHAPE;
+    if (!step_shape_supported(hidden, inter, group)) return FD_ERR_UNSUPPORTED;
+    int vpt = 0, threads = 0;
+    if (!step_rms_shape(hidden, &vpt, &threads)) return FD_ERR_UNSUPPORTED;
+    // the launcher's budget: the opt-in shared memory less the kernel's static shared memory
+    const long long budget = (long long)device[1] - (long long)device[4];
+    StepPlan p{};
+    if (budget <= 0 || !plan_step(device[0], (size_t)budget, inter, hidden, group, &p))
+        return FD_ERR_UNSUPPORTED;
+    const int v[8] = {p.grid, p.rows_base, p.rows_extra, p.S, p.w_rows, (int)p.smem, vpt, threads};
+    for (int i = 0; i < 8; ++i) plan[i] = v[i];
     return FD_OK;
 }
 

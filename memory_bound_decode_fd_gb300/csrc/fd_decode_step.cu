@@ -46,14 +46,13 @@
 #include <atomic>
 
 #include "fd_gemv_common.cuh"
+#include "fd_step_plan.h"
 #include "fd_tma.cuh"
 
 namespace fd {
 namespace {
 
-constexpr int kStepR = 8;             // weight rows per chunk (the GEMV kernel's chunk)
-constexpr int kStepMaxStages = 8;     // chunks of one layer's rows per CTA
-constexpr int kStepRmsMaxVpt = 4;
+static_assert(kStepWindowRows == kWindowRows, "the cross-warp sums of the GEMV kernel");
 
 // Bounded spin until *p >= target, with acquire ordering at GPU scope.
 __device__ __forceinline__ bool wait_counter(const unsigned *p, unsigned target, long long limit) {
@@ -444,34 +443,6 @@ __global__ void __launch_bounds__(1024, 1)
     }
 }
 
-// The step's launch facts for one shape: the bulk-copy GEMV's row partition at one CTA per
-// SM, every chunk of a CTA's rows in a stage of its own, no activation area.
-struct StepPlan {
-    int grid, rows_base, rows_extra, S, w_rows;
-    size_t smem;
-};
-
-bool plan_step(int sm_count, size_t budget, int K, int N, int group, StepPlan *p) {
-    const int nvec = K / 32, ngroups = K / group;
-    int grid = sm_count;
-    if ((long long)grid * kStepR > N) grid = (N + kStepR - 1) / kStepR;
-    if (grid < 1) return false;
-    p->grid = grid;
-    p->rows_base = N / grid;
-    p->rows_extra = N % grid;
-    const int n_max = p->rows_base + (p->rows_extra > 0 ? 1 : 0);
-    if (n_max > kWindowRows) return false;  // one flush of the cross-warp sums per layer
-    p->S = (n_max + kStepR - 1) / kStepR;
-    if (p->S > kStepMaxStages) return false;
-    p->w_rows = n_max;
-    const size_t w_bytes = (size_t)p->w_rows * nvec * 16;
-    const size_t s_bytes = (size_t)p->S * kStepR * ngroups * 2;
-    const size_t red = (size_t)(2 * nvec / 32) * kWindowRows * 4;
-    const size_t normed = (size_t)N * 2;  // the whole normalised row
-    p->smem = w_bytes + s_bytes + red + normed;
-    return p->smem <= budget;
-}
-
 template <int NVEC_C, int NG_C>
 cudaError_t launch_shape(const DeviceInfo &di, const fd_step_layer *layers, int n_layers,
                          const void *x0, void *residual, float eps, int K, int N, int group,
@@ -526,30 +497,6 @@ cudaError_t launch_shape(const DeviceInfo &di, const fd_step_layer *layers, int 
 }
 
 }  // namespace
-
-// The decode shape: the down projection of K = 14336 (group 128), where the bulk-copy
-// GEMV also runs one CTA per SM (928 threads), so the two share one row partition for any
-// hidden and every output is bit-identical. hidden: one flush of the cross-warp sums per
-// layer (at most 64 rows per CTA).
-bool step_shape_supported(int hidden, int inter, int group) {
-    return inter == 14336 && group == 128 && hidden >= 8 && hidden <= 64 * 152;
-}
-
-// The add-RMSNorm row kernel's block for one row of `hidden`: the smallest vpt of 1, 2, 4
-// that keeps the block at <= 256 threads (threads rounded up to whole warps).
-bool step_rms_shape(int hidden, int *vpt, int *threads) {
-    const int nvec = hidden / 8;
-    for (int v : {1, 2, 4}) {
-        int t = (nvec + v - 1) / v;
-        t = (t + 31) / 32 * 32;
-        if (t <= 256) {
-            *vpt = v;
-            *threads = t;
-            return true;
-        }
-    }
-    return false;
-}
 
 cudaError_t launch_decode_step(const fd_step_layer *layers, int n_layers, const void *x0,
                                void *residual, float eps, int hidden, int inter, int group,

@@ -109,8 +109,7 @@ cudaError_t launch_gemv_fold_noalloc(const void *gate, const void *up, const voi
 // is outside its rules (K % 1024, N % 128, group % 64, (K / group) % 8).
 bool gemv_tc_supported(int M, int K, int N, int group);
 // The decode step as one persistent kernel (fd_decode_step.cu); *launched = false when the
-// shape has no kernel or no plan.
-bool step_shape_supported(int hidden, int inter, int group);
+// shape has no kernel or no plan (fd_step_plan.h).
 cudaError_t launch_decode_step(const fd_step_layer *layers, int n_layers, const void *x0,
                                void *residual, float eps, int hidden, int inter, int group,
                                void *scratch, cudaStream_t stream, bool *launched);
