@@ -272,9 +272,14 @@ def step_layer_table(layers, normed, y, device=None) -> torch.Tensor:
             _check_tensor(f"{name}[{i}]", t, torch.bfloat16)
             if t.numel() != hidden:
                 raise ValueError(f"{name}[{i}] must hold hidden={hidden} elements")
-        rows.append([l["gate"].data_ptr(), l["up"].data_ptr(), l["qweight"].data_ptr(),
-                     l["scales"].data_ptr(), l["rms_weight"].data_ptr(), n.data_ptr(),
-                     yy.data_ptr()])
+        ptrs = [l["gate"].data_ptr(), l["up"].data_ptr(), l["qweight"].data_ptr(),
+                l["scales"].data_ptr(), l["rms_weight"].data_ptr(), n.data_ptr(), yy.data_ptr()]
+        # the kernel reads these with 16-byte loads and bulk copies; the C ABI cannot check
+        # pointers that live in device memory, so they are checked here
+        for name, ptr in zip(("gate", "up", "qweight", "scales", "rms_weight", "normed", "y"), ptrs):
+            if ptr % 16:
+                raise ValueError(f"layers[{i}].{name} is not 16-byte aligned")
+        rows.append(ptrs)
     dev = device if device is not None else layers[0]["qweight"].device
     return torch.tensor(rows, dtype=torch.int64, device=dev)
 

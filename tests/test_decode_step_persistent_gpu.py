@@ -224,5 +224,23 @@ def bf16_float(bits):
     return b.view(np.float32)
 
 
+def test_layer_table_rejects_misaligned_tensors(cuda_device):
+    # the table's pointers are checked on the host (the C ABI cannot read device memory);
+    # nothing is launched
+    hidden, inter, group = 64, 256, 128
+    bf = torch.bfloat16
+    base = torch.zeros(inter + 8, dtype=bf, device="cuda")
+    layer = {"gate": base[:inter], "up": torch.zeros(inter, dtype=bf, device="cuda"),
+             "qweight": torch.zeros((hidden, inter // 8), dtype=torch.int32, device="cuda"),
+             "scales": torch.zeros((hidden, inter // group), dtype=bf, device="cuda"),
+             "rms_weight": torch.zeros(hidden, dtype=bf, device="cuda")}
+    normed = [torch.zeros((1, hidden), dtype=bf, device="cuda")]
+    y = [torch.zeros((1, hidden), dtype=bf, device="cuda")]
+    assert tuple(fd.step_layer_table([layer], normed, y).shape) == (1, 7)
+    layer["gate"] = base[1:inter + 1]  # 2 bytes past an aligned start
+    with pytest.raises(ValueError, match="16-byte aligned"):
+        fd.step_layer_table([layer], normed, y)
+
+
 def test_device_status_clean_after_the_persistent_steps(cuda_device):
     assert fd.device_status(clear=True) == 0

@@ -158,3 +158,4 @@ def test_plan_on_other_sm_counts(fdlib, sms):
             continue
         assert gst == _lib.FD_OK and g[7] == 1
         assert (p["grid"], p["rows_base"], p["rows_extra"]) == tuple(g[:3]), (sms, hidden)
+
