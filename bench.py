@@ -77,8 +77,9 @@ KERNEL_SOURCES = {
     "swiglu_w4a16_gemv_residual": ["csrc/fd_gemv_tma.cu", "csrc/fd_gemv_common.cuh", "csrc/fd_tma.cuh",
                                    "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
     # the tensor-core GEMV of batched decode (M >= 16)
-    "gemv_tc": ["csrc/fd_gemv_tc.cu", "csrc/fd_tc.cuh", "csrc/fd_gemv_common.cuh", "csrc/fd_tma.cuh",
-                "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],
+    "gemv_tc": ["csrc/fd_gemv_tc.cu", "csrc/fd_gemv_tc_plan.h", "csrc/fd_tc.cuh",
+                "csrc/fd_gemv_common.cuh", "csrc/fd_tma.cuh", "csrc/fd_w4_unpack.cuh",
+                "csrc/fd_internal.h"],
     # the decode step as one persistent kernel
     "decode_step": ["csrc/fd_decode_step.cu", "csrc/fd_gemv_common.cuh", "csrc/fd_tma.cuh",
                     "csrc/fd_w4_unpack.cuh", "csrc/fd_internal.h"],

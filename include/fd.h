@@ -479,6 +479,20 @@ int fd_debug_plan_gemv(const int *device, int M, int K, int N, int group, int pl
  */
 int fd_debug_plan_step(const int *device, int hidden, int inter, int group, int *plan);
 
+/*
+ * fd_debug_plan_tc - test support: the shared-memory plan of the tensor-core GEMV
+ * (fd_swiglu_w4a16_gemv at M >= 16) for its first launch (up to 128 activation rows),
+ * computed on the host without any CUDA call.
+ * smem_budget  dynamic shared memory a CTA may use (bytes).
+ * plan    int[10] out: the padded rows (the MMA's N), k per pipeline step, weight tiles,
+ *         gate/up stages, operand stages, scale columns per row, shared-memory offsets of the
+ *         gate/up ring, the operand ring and the scales (weights at 0), dynamic shared
+ *         memory per CTA.
+ * Returns FD_ERR_SHAPE for a non-positive size; FD_ERR_UNSUPPORTED when the tensor-core
+ * kernel does not run the shape or has no plan within the budget.
+ */
+int fd_debug_plan_tc(int M, int K, int N, int group, int smem_budget, int *plan);
+
 /* The cudaError_t value behind the calling thread's most recent FD_ERR_CUDA (0 if none).
  * Thread-local; not reset by successful calls. */
 int fd_last_cuda_error(void);

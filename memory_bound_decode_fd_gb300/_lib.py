@@ -57,6 +57,7 @@ SIGNATURES = {
     "fd_device_status": (_I, [_VP, _VP, _I]),
     "fd_decode_mlp_step": (_I, [_VP, _I, _VP, _VP, ctypes.c_float, _I, _I, _I, _VP, _VP]),
     "fd_debug_plan_step": (_I, [_VP, _I, _I, _I, _VP]),
+    "fd_debug_plan_tc": (_I, [_I, _I, _I, _I, _I, _VP]),
     "fd_nvfp4_scaled_mm": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _VP]),
     "fd_debug_plan_nvfp4": (_I, [_I, _I, _I, _I, _VP]),
     "fd_add_rmsnorm": (_I, [_VP, _VP, _VP, ctypes.c_float, _VP, _VP, _I, _I, _VP]),

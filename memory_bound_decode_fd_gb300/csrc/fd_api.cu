@@ -8,6 +8,7 @@
 
 #include "fd_copy.h"
 #include "fd_gemv_plan.h"
+#include "fd_gemv_tc_plan.h"
 #include "fd_internal.h"
 #include "fd_nvfp4_plan.h"
 #include "fd_step_plan.h"
@@ -361,6 +362,22 @@ int fd_debug_plan_gemv(const int *device, int M, int K, int N, int group, int pl
     const int v[9] = {p.grid, p.rows_base, p.rows_extra, p.S, p.w_rows, p.act_first_stage,
                       p.ring, p.per_sm, (int)p.smem};
     for (int i = 0; i < 9; ++i) plan[i] = v[i];
+    return FD_OK;
+}
+
+int fd_debug_plan_tc(int M, int K, int N, int group, int smem_budget, int *plan) {
+    if (!plan) return FD_ERR_NULL;
+    if (M <= 0 || K <= 0 || N <= 0 || group <= 0) return FD_ERR_SHAPE;
+    if (!gemv_tc_supported(M, K, N, group) || smem_budget <= 0) return FD_ERR_UNSUPPORTED;
+    // the first launch's row block (up to 128 activation rows)
+    const int npad = tc_npad(M < 128 ? M : 128);
+    int stepk = 0;
+    TcPlan p{};
+    if (!plan_tc(npad, K / kTcSplit, group, (size_t)smem_budget, &stepk, &p))
+        return FD_ERR_UNSUPPORTED;
+    const int v[10] = {npad, stepk, p.s_w, p.s_gu, p.s_op, p.sg, (int)p.off_gu, (int)p.off_op,
+                       (int)p.off_sc, (int)p.smem};
+    for (int i = 0; i < 10; ++i) plan[i] = v[i];
     return FD_OK;
 }
 

@@ -37,14 +37,12 @@
 #include <cudaTypedefs.h>
 
 #include "fd_gemv_common.cuh"
+#include "fd_gemv_tc_plan.h"
 #include "fd_tc.cuh"
 
 namespace fd {
 namespace {
 
-constexpr int kTcRows = 128;                 // weight rows per CTA (MMA M)
-constexpr int kTcGuBoxK = 64;                // k per gate/up tensor-map box (128 bytes)
-constexpr int kTcSplit = 4;                  // CTAs per cluster (K quarters)
 constexpr int kTcFirstWorker = 3;            // warps 0, 1, 2: weights, gate/up, MMA
 constexpr int kTcDequantWarps = 8;           // then the A-operand (weight) warps
 constexpr int kTcSiluWarps = 8;              // then the B-operand (activation) warps
@@ -53,13 +51,7 @@ constexpr int kTcThreads = (kTcFirstSilu + kTcSiluWarps) * 32;
 constexpr int kTcSiluThreads = kTcSiluWarps * 32;
 constexpr int kTcEpilogueThreads = kTcDequantWarps * 32;  // the dequant warps
 constexpr int kTcMaxStages = 16;
-constexpr int kTcWTileK = 256;               // k per weight tile (128 bytes of a row)
-constexpr uint32_t kWStageBytes = kTcRows * kTcWTileK / 2;  // int4 tile: 16384
 constexpr uint32_t kCoreBytes = 128;                       // 8 rows x 16 bytes
-
-// k per pipeline step: 128 for up to 64 activation rows (half the per-step handshakes per
-// weight byte), 64 for 128 rows (whose larger operand stages would not fit twice).
-__host__ __device__ constexpr int tc_step_k(int npad) { return npad <= 64 ? 128 : 64; }
 
 // Bias of the nibble trick: bf16 0x4300 | u is 128 + u, and u = q + 8.
 constexpr uint32_t kMagic136x2 = 0x43084308u;
@@ -501,65 +493,67 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base, uin
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-struct TcPlan {
-    int s_w, s_gu, s_op, sg;
-    uint32_t off_gu, off_op, off_sc, smem;
+// One kernel instantiation: its cached static shared memory and opt-in attribute.
+template <int NPAD, int STEPK>
+struct TcKernel {
+    static cudaError_t prepare(const DeviceInfo &di, size_t *budget) {
+        static std::atomic<int> static_smem_cache{-1};
+        static std::atomic<uint64_t> attr_done{0};
+        auto kern = gemv_tc_kernel<NPAD, STEPK>;
+        int static_smem = static_smem_cache.load(std::memory_order_relaxed);
+        if (static_smem < 0) {
+            cudaFuncAttributes fa;
+            cudaError_t err = cudaFuncGetAttributes(&fa, kern);
+            if (err != cudaSuccess) return err;
+            static_smem = (int)fa.sharedSizeBytes;
+            static_smem_cache.store(static_smem, std::memory_order_relaxed);
+        }
+        *budget = (size_t)di.max_smem_optin - (size_t)static_smem;
+        int dev = 0;
+        cudaError_t err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) return err;
+        const uint64_t bit = 1ull << (dev & 63);
+        if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)*budget);
+            if (err != cudaSuccess) return err;
+            attr_done.fetch_or(bit, std::memory_order_acq_rel);
+        }
+        return cudaSuccess;
+    }
+    static cudaError_t launch(const TcPlan &plan, const CUtensorMap &mw, const CUtensorMap &ms,
+                              const CUtensorMap &mg, const CUtensorMap &mu,
+                              const void *residual, void *out, int mc, int N, int group,
+                              int k_cta, cudaStream_t stream) {
+        return launch_kernel(gemv_tc_kernel<NPAD, STEPK>, dim3(kTcSplit, N / kTcRows),
+                             dim3(kTcThreads), plan.smem, stream, kTcSplit, mw, ms, mg, mu,
+                             static_cast<const uint16_t *>(residual), static_cast<uint16_t *>(out),
+                             mc, N, group, k_cta, plan.s_w, plan.s_gu, plan.s_op, plan.off_gu,
+                             plan.off_op, plan.off_sc, plan.sg);
+    }
 };
-
-// Shared-memory plan: a ring of int4 weight tiles (the HBM stream; 4 tiles, fewer where the
-// operand stages need the room), then as many gate/up and operand stages as fit (2..4 each).
-bool make_plan(int npad, int stepk, int k_cta, int group, size_t budget, TcPlan *p) {
-    const uint32_t gu_stage = 2u * (stepk / kTcGuBoxK) * npad * 128;
-    const uint32_t op_stage = (uint32_t)kTcRows * stepk * 2 + (uint32_t)npad * stepk * 2;
-    p->sg = ((k_cta + group - 1) / group + 7 + 7) & ~7;
-    if (p->sg > 256) return false;
-    const uint32_t sc_bytes = ((uint32_t)kTcRows * p->sg * 2 + 1023u) & ~1023u;
-    size_t avail = 0;
-    for (p->s_w = 4; p->s_w >= 2; --p->s_w) {
-        const size_t fixed = 1024 + (size_t)p->s_w * kWStageBytes + sc_bytes;
-        avail = budget > fixed ? budget - fixed : 0;
-        if (2 * (size_t)gu_stage + 2 * (size_t)op_stage <= avail) break;
-    }
-    if (p->s_w < 2) return false;
-    const uint32_t w_bytes = p->s_w * kWStageBytes;
-    int s_gu = 2, s_op = 2;
-    size_t used = 2 * (size_t)gu_stage + 2 * (size_t)op_stage;
-    for (bool grew = true; grew;) {
-        grew = false;
-        if (s_op < 4 && used + op_stage <= avail) { ++s_op; used += op_stage; grew = true; }
-        if (s_gu < 4 && used + gu_stage <= avail) { ++s_gu; used += gu_stage; grew = true; }
-    }
-    p->s_gu = s_gu;
-    p->s_op = s_op & ~1;  // two halves of equal size
-    p->off_gu = w_bytes;
-    p->off_op = p->off_gu + s_gu * gu_stage;
-    p->off_sc = p->off_op + s_op * op_stage;
-    p->smem = p->off_sc + sc_bytes + 1024;  // + alignment slack of the dynamic base
-    // the cluster reduction reuses the gate/up and operand rings
-    return (size_t)kTcSplit * npad * 32 * 4 <= (size_t)p->off_sc - p->off_gu;
-}
 
 template <int NPAD>
 cudaError_t launch_npad(const DeviceInfo &di, const void *gate, const void *up,
                         const void *qweight, const void *scales, const void *residual,
                         void *out, int mc, int K, int N, int group, cudaStream_t stream,
                         bool *launched) {
-    static std::atomic<uint64_t> attr_done{0};
-    static std::atomic<int> static_smem_cache{-1};
     constexpr int kStepK = tc_step_k(NPAD);
-    auto kern = gemv_tc_kernel<NPAD, kStepK>;
-    int static_smem = static_smem_cache.load(std::memory_order_relaxed);
-    if (static_smem < 0) {
-        cudaFuncAttributes fa;
-        cudaError_t err = cudaFuncGetAttributes(&fa, kern);
-        if (err != cudaSuccess) return err;
-        static_smem = (int)fa.sharedSizeBytes;
-        static_smem_cache.store(static_smem, std::memory_order_relaxed);
-    }
+    using Primary = TcKernel<NPAD, kStepK>;
+    using Fallback = TcKernel<NPAD, 64>;  // the same kernel at 64-k steps (see plan_tc)
     const int k_cta = K / kTcSplit;
+    size_t budget = 0;
+    cudaError_t err = Primary::prepare(di, &budget);
+    if (err != cudaSuccess) return err;
     TcPlan plan;
-    const size_t budget = (size_t)di.max_smem_optin - (size_t)static_smem;
-    if (!make_plan(NPAD, kStepK, k_cta, group, budget, &plan)) return cudaSuccess;  // not launched
+    int stepk = 0;
+    if (!plan_tc(NPAD, k_cta, group, budget, &stepk, &plan)) return cudaSuccess;  // not launched
+    if (stepk != kStepK) {
+        size_t b64 = 0;
+        err = Fallback::prepare(di, &b64);
+        if (err != cudaSuccess) return err;
+        if (b64 < plan.smem) return cudaSuccess;  // not launched
+    }
 
     CUtensorMap mw, ms, mg, mu;
     if (!encode_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, qweight, (uint64_t)K / 2, (uint64_t)N,
@@ -573,22 +567,10 @@ cudaError_t launch_npad(const DeviceInfo &di, const void *gate, const void *up,
                    (uint64_t)K * 2, kTcGuBoxK, NPAD, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
 
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)budget);
-        if (err != cudaSuccess) return err;
-        attr_done.fetch_or(bit, std::memory_order_acq_rel);
-    }
     *launched = true;
-    err = launch_kernel(kern, dim3(kTcSplit, N / kTcRows), dim3(kTcThreads), plan.smem, stream,
-                        kTcSplit, mw, ms, mg, mu, static_cast<const uint16_t *>(residual),
-                        static_cast<uint16_t *>(out), mc, N, group,
-                        k_cta, plan.s_w, plan.s_gu, plan.s_op, plan.off_gu, plan.off_op,
-                        plan.off_sc, plan.sg);
+    err = stepk == kStepK
+              ? Primary::launch(plan, mw, ms, mg, mu, residual, out, mc, N, group, k_cta, stream)
+              : Fallback::launch(plan, mw, ms, mg, mu, residual, out, mc, N, group, k_cta, stream);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }

@@ -75,6 +75,8 @@ TC_SHAPES = [
     (256, 1024, 256, 128),    # largest M
     (16, 16384, 128, 512),
     (20, 32768, 128, 64),     # largest K; 136-column scale window
+    (33, 32768, 128, 64),     # the same at 64 rows: 64-k steps (128-k stages do not fit)
+    (64, 32768, 256, 64),
 ]
 
 
