@@ -1,8 +1,10 @@
 // fd_copy.cu - one-kernel copy between device-accessible buffers, for the per-token I/O of
 // a decode step. On GB300 (Grace + Blackwell) pinned host memory is read and written by
-// the GPU over NVLink-C2C; a copy kernel spread over every SM moves a step's inputs
-// (1.85 MB for 32 layers of gate/up at MLP width 14336) several times faster than one
-// copy-engine transfer, which ran at ~68 GB/s here.
+// the GPU over NVLink-C2C. Alone, a copy-engine transfer of a step's 1.85 MB of inputs
+// (32 layers of gate/up at MLP width 14336) takes about as long as this kernel (10.7 vs
+// 13.1 us), but inside the captured step the kernels overlap their neighbours under
+// programmatic dependent launch: the step's end-to-end time measured 321 us with them
+// against 335 us with copy-engine transfers (memcpy nodes) for the same two copies.
 #include "fd_copy.h"
 #include "fd_internal.h"
 

@@ -156,8 +156,9 @@ class DecodeStep:
         device->host copy (new residual, last layer's y) on the step's stream: after the
         stream is synchronised, io.residual holds the new residual and io.out_x the output."""
         # The two transfers are fd_copy kernels: the GPU reads and writes the pinned host
-        # block over NVLink-C2C (one copy-engine transfer of the 1.85 MB input ran at
-        # ~68 GB/s on GB300). With capture_pinned(io) all of it is one graph launch.
+        # block over NVLink-C2C, overlapping the neighbouring kernels (measured on GB300:
+        # 321 us per step end to end, against 335 us with copy-engine transfers). With
+        # capture_pinned(io) all of it is one graph launch.
         with torch.cuda.stream(self.stream):
             if self.io_graph is not None and io.host is self._io_host:
                 self.io_graph.replay()
