@@ -452,6 +452,21 @@ const char *fd_status_string(int status);
 int fd_copy(void *dst, const void *src, size_t bytes, fd_stream_t stream);
 
 /*
+ * fd_copy_rows - the same for `rows` rows of `row_bytes` each, read at a pitch of
+ * src_pitch bytes and written at a pitch of dst_pitch bytes (a decode step's per-layer
+ * gate and up rows, which the step keeps interleaved). When a side is not accessible to a
+ * kernel the call falls back to one cudaMemcpy2DAsync.
+ * Requires  dst, src 16-byte aligned; row_bytes, dst_pitch, src_pitch multiples of 16 with
+ *           both pitches >= row_bytes; the two spans ((rows - 1) x pitch + row_bytes bytes
+ *           from each pointer) do not overlap. row_bytes == 0 or rows == 0 returns FD_OK at
+ *           once (no pointer read, nothing launched).
+ * Returns FD_OK; FD_ERR_NULL, FD_ERR_SHAPE, FD_ERR_ALIGN, FD_ERR_OVERLAP for bad arguments
+ * (nothing launched); FD_ERR_CUDA if the launch fails.
+ */
+int fd_copy_rows(void *dst, size_t dst_pitch, const void *src, size_t src_pitch,
+                 size_t row_bytes, size_t rows, fd_stream_t stream);
+
+/*
  * fd_debug_plan_gemv - test support: the launch plan the bulk-copy GEMV kernel would use,
  * computed on the host from given device facts, without any CUDA call.
  * device  int[6]: SM count, opt-in shared memory per CTA, shared memory per SM, shared

@@ -41,6 +41,7 @@ from .kernels import (  # noqa: F401
     GEMV_PATHS,
     add_rmsnorm,
     copy,
+    copy_rows,
     decode_mlp_step,
     decode_mlp_step_persistent,
     device_status,

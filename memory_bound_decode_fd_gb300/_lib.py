@@ -53,6 +53,8 @@ SIGNATURES = {
                                                      ctypes.c_float, _VP, _VP, _I, _I, _I, _VP]),
     "fd_w4a16_gate_up_gemv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "fd_copy": (_I, [_VP, _VP, ctypes.c_size_t, _VP]),
+    "fd_copy_rows": (_I, [_VP, ctypes.c_size_t, _VP, ctypes.c_size_t, ctypes.c_size_t,
+                          ctypes.c_size_t, _VP]),
     "fd_debug_plan_gemv": (_I, [_VP, _I, _I, _I, _I, _I, _VP]),
     "fd_device_status": (_I, [_VP, _VP, _I]),
     "fd_decode_mlp_step": (_I, [_VP, _I, _VP, _VP, ctypes.c_float, _I, _I, _I, _VP, _VP]),

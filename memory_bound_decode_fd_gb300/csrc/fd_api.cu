@@ -348,6 +348,22 @@ int fd_copy(void *dst, const void *src, size_t bytes, fd_stream_t stream) {
     return from_cuda(launch_copy(dst, src, bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int fd_copy_rows(void *dst, size_t dst_pitch, const void *src, size_t src_pitch,
+                 size_t row_bytes, size_t rows, fd_stream_t stream) {
+    if (row_bytes == 0 || rows == 0) return FD_OK;  // empty: nothing read or written
+    if (!dst || !src) return FD_ERR_NULL;
+    if (row_bytes % 16 != 0 || dst_pitch % 16 != 0 || src_pitch % 16 != 0 ||
+        dst_pitch < row_bytes || src_pitch < row_bytes)
+        return FD_ERR_SHAPE;
+    if (!aligned16(dst) || !aligned16(src)) return FD_ERR_ALIGN;
+    // the spans the rows lie in (conservative: no interleaving of the two is allowed)
+    if (overlaps(dst, (rows - 1) * dst_pitch + row_bytes, src, (rows - 1) * src_pitch + row_bytes))
+        return FD_ERR_OVERLAP;
+    if (fake_launch_failure()) return from_cuda(cudaErrorLaunchOutOfResources);
+    return from_cuda(launch_copy_rows(dst, dst_pitch, src, src_pitch, row_bytes, rows,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fd_debug_plan_gemv(const int *device, int M, int K, int N, int group, int plain, int *plan) {
     if (!device || !plan) return FD_ERR_NULL;
     if (M <= 0 || K <= 0 || N <= 0 || group <= 0 || K % 32 != 0 || K % group != 0)

@@ -472,6 +472,28 @@ def copy(dst: torch.Tensor, src: torch.Tensor, stream: torch.cuda.Stream | None 
     return dst
 
 
+def copy_rows(dst: torch.Tensor, src: torch.Tensor,
+              stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """dst <- src for two 2-D tensors of the same shape and dtype whose rows are contiguous
+    (unit inner stride) but may lie at any row stride, with one kernel (fd_copy_rows): either
+    side may be a CUDA tensor or host memory (pinned memory is read or written by the GPU
+    over NVLink-C2C; other host memory goes through one cudaMemcpy2DAsync)."""
+    if dst.dim() != 2 or src.dim() != 2 or dst.shape != src.shape or dst.dtype != src.dtype:
+        raise ValueError("copy_rows: dst and src must be 2-D tensors of the same shape and dtype")
+    if dst.stride(1) != 1 or src.stride(1) != 1:
+        raise ValueError("copy_rows: rows must be contiguous")
+    es = dst.element_size()
+    rows, row_bytes = dst.shape[0], dst.shape[1] * es
+    if not (dst.is_cuda or src.is_cuda):
+        raise ValueError("copy_rows: one side must be a CUDA tensor")
+    dev = _device_of(dst, src)
+    lib = _lib.load()
+    with _on_device(dev):
+        _lib.check(lib.fd_copy_rows(_ptr(dst), dst.stride(0) * es, _ptr(src), src.stride(0) * es,
+                                    row_bytes, rows, _stream_handle(stream, dev)))
+    return dst
+
+
 def add_rmsnorm(
     x: torch.Tensor,
     residual: torch.Tensor,

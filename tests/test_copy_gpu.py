@@ -1,7 +1,9 @@
 """fd_copy through the C ABI: device <-> device and pinned host <-> device, bit for bit,
 for one vector, a ragged count and a decode step's input block, without touching the
 bytes around the destination; and under programmatic dependent launch after a kernel
-that writes the source."""
+that writes the source. fd_copy_rows: rows at different pitches on both sides (the decode
+step's interleaved gate and up rows), from device, pinned and pageable host memory, with
+the bytes between the destination rows untouched."""
 
 import pytest
 import torch
@@ -57,3 +59,28 @@ def test_copy_with_pdl_after_a_writing_kernel(cuda_device):
         fd.set_pdl(prev)
     expect = (x.float() + r.float()).to(torch.bfloat16).cpu()
     assert torch.equal(host.view(torch.int16), expect.view(torch.int16))
+
+
+@pytest.mark.parametrize("rows,width,src_kind,dst_kind", [
+    (1, 8, "cuda", "cuda"),
+    (32, 14336, "pinned", "cuda"),    # a decode step's gate rows into the interleaved block
+    (32, 14336, "pageable", "cuda"),  # host memory a kernel cannot reach: cudaMemcpy2DAsync
+    (7, 24, "cuda", "pinned"),
+])
+def test_copy_rows_strided(cuda_device, rows, width, src_kind, dst_kind):
+    g = torch.Generator().manual_seed(rows * width)
+    src_full = torch.randint(-30000, 30000, (rows, 3 * width), dtype=torch.int16, generator=g)
+    src = src_full[:, width:2 * width]  # pitch 3 x width
+    if src_kind == "cuda":
+        src_full = src_full.cuda()
+        src = src_full[:, width:2 * width]
+    elif src_kind == "pinned":
+        src_full = src_full.pin_memory()
+        src = src_full[:, width:2 * width]
+    fill = torch.full((rows, 2, width), 0x5A5A, dtype=torch.int16)
+    buf = fill.cuda() if dst_kind == "cuda" else fill.pin_memory()
+    dst = buf[:, 0, :]  # pitch 2 x width: every other row of the buffer is a guard
+    fd.copy_rows(dst, src)
+    torch.cuda.synchronize()
+    assert torch.equal(dst.cpu(), src.cpu())
+    assert bool((buf[:, 1, :].cpu() == 0x5A5A).all())

@@ -158,6 +158,33 @@ def test_copy_rejects_bad_arguments_without_launching(fdlib, args, status):
     assert fdlib.fd_copy(*args, None) == status
 
 
+@pytest.mark.parametrize("args,status", [
+    # dst, dst_pitch, src, src_pitch, row_bytes, rows
+    ((None, 64, B, 64, 32, 4), _lib.FD_ERR_NULL),
+    ((A, 64, None, 64, 32, 4), _lib.FD_ERR_NULL),
+    ((A, 64, B, 64, 24, 4), _lib.FD_ERR_SHAPE),       # row not a multiple of 16 bytes
+    ((A, 40, B, 64, 32, 4), _lib.FD_ERR_SHAPE),       # pitch not a multiple of 16
+    ((A, 16, B, 64, 32, 4), _lib.FD_ERR_SHAPE),       # pitch below the row
+    ((A + 8, 64, B, 64, 32, 4), _lib.FD_ERR_ALIGN),
+    ((A, 64, B + 4, 64, 32, 4), _lib.FD_ERR_ALIGN),
+    ((A, 64, A + 32, 64, 32, 4), _lib.FD_ERR_OVERLAP),  # interleaved rows
+    ((A + 192, 64, A, 64, 32, 4), _lib.FD_ERR_OVERLAP),  # the last source row meets dst
+])
+def test_copy_rows_rejects_bad_arguments_without_launching(fdlib, args, status):
+    assert fdlib.fd_copy_rows(*args, None) == status
+
+
+def test_copy_rows_empty_and_failed_launch(fdlib):
+    assert fdlib.fd_copy_rows(None, 0, None, 0, 0, 4, None) == _lib.FD_OK
+    assert fdlib.fd_copy_rows(None, 0, None, 0, 32, 0, None) == _lib.FD_OK
+    prev = fdlib.fd_get_launch_flags()
+    assert fdlib.fd_set_launch_flags(prev | _lib.FD_LAUNCH_TEST_FAIL) == _lib.FD_OK
+    try:
+        assert fdlib.fd_copy_rows(A, 64, B, 64, 32, 4, None) == _lib.FD_ERR_CUDA
+    finally:
+        fdlib.fd_set_launch_flags(prev)
+
+
 def rms(lib, x=A, r=B, w=C, eps=1e-6, out=D, rout=E, rows=4, hidden=4096):
     return lib.fd_add_rmsnorm(x, r, w, ctypes.c_float(eps), out, rout, rows, hidden, None)
 
