@@ -112,12 +112,15 @@ __device__ __forceinline__ void fold_tail(const FoldArgs &fold, float ss, int N,
 // the per-row shared-memory offsets fold into instruction immediates.
 //
 // Shared memory: w_rows weight rows (stage s holds rows [sR, sR + R)), the scales of S
-// stages, then the per-warp partial sums. With one activation row (M == 1) the producer
-// first bulk-copies gate and up (2 * K * 2 bytes = 8 weight rows) into the last 8 weight
-// rows, ahead of the weight stream, so the consumers' activation reads do not queue
-// behind it (loaded from global memory instead, they arrived behind the weights and the
-// call took 10-25 % longer on GB300); stages from act_first_stage on are filled only
-// after every consumer warp has read its slice.
+// stages, then the per-warp partial sums. With one SwiGLU activation row (M == 1) the
+// producer first bulk-copies gate and up (2 * K * 2 bytes = 8 weight rows) into the last
+// 8 weight rows, ahead of the weight stream, so the consumers' activation reads do not
+// queue behind it (loaded from global memory instead, they arrived behind the weights and
+// the call took 10-25 % longer on GB300); stages from act_first_stage on are filled only
+// after every consumer warp has read its slice. The plain activation (x, K * 2 bytes) is
+// small enough to load straight from global memory, so for it the free stages' weight
+// chunks go out before the dependency wait instead (the gate/up GEMV measured 64 -> 69 %
+// of HBM with this on GB300).
 // FOLD: the next layer's add-RMSNorm in the tail (M = 1, SwiGLU form only); a separate
 // instantiation, so the other kernels' code is unchanged by it.
 template <int MB, int R, int NVEC_C, int NG_C, int LPS, bool PLAIN, bool FOLD>
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
     // gate then up, each K bf16 (4K bytes = 8 weight rows; PLAIN: x alone, 2K bytes = 4
     // rows), in the last weight rows (M == 1 only); stages from act_first_stage on are
     // filled only after its release
-    const bool act_in_smem = (M == 1);
+    const bool act_in_smem = (M == 1) && !PLAIN;
     const uint32_t act_bytes = (uint32_t)K * (PLAIN ? 2 : 4);
     uint16_t *act_smem =
         reinterpret_cast<uint16_t *>(smem + (size_t)w_rows * w_row_bytes - act_bytes);
@@ -214,22 +217,30 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
         fence_mbar_init();
         pol_w = weights_evict_first ? policy_evict_first() : policy_evict_last();
         pol_s = policy_evict_first();
-        // Nothing is issued before the dependency wait, although the weights never come
-        // from the previous kernel: the activation copy is what every consumer waits for
-        // first, and weight traffic issued ahead of it (copies into the ring or L2
-        // prefetches) delayed it and cost the 32-layer decode step 15-25 % in
-        // measurements on GB300.
-        grid_dep_wait();
-        grid_dep_launch();
-        if (act_in_smem) {
-            const uint32_t ab = (uint32_t)K * 2;
-            mbar_arrive_expect_tx(&act_full_bar, act_bytes);
-            const uint64_t pol_a = policy_evict_last();  // every CTA reads it
-            bulk_g2s(act_smem, gate, ab, &act_full_bar, pol_a);
-            if (!PLAIN) bulk_g2s(act_smem + K, up, ab, &act_full_bar, pol_a);
+        if constexpr (PLAIN) {
+            // The weights never come from the previous kernel, and the consumers read the
+            // small activation from global memory: the free stages' chunks go out before
+            // the dependency wait.
+            for (; pc < total && pc < S; ++pc) issue_chunk(pc);
+            grid_dep_wait();
+            grid_dep_launch();
+        } else {
+            // Nothing is issued before the dependency wait: the activation copy is what
+            // every consumer waits for first, and weight traffic issued ahead of it (copies
+            // into the ring or L2 prefetches) delayed it and cost the 32-layer decode step
+            // 15-25 % in measurements on GB300.
+            grid_dep_wait();
+            grid_dep_launch();
+            if (act_in_smem) {
+                const uint32_t ab = (uint32_t)K * 2;
+                mbar_arrive_expect_tx(&act_full_bar, act_bytes);
+                const uint64_t pol_a = policy_evict_last();  // every CTA reads it
+                bulk_g2s(act_smem, gate, ab, &act_full_bar, pol_a);
+                bulk_g2s(act_smem + K, up, ab, &act_full_bar, pol_a);
+            }
+            // stages that are free from the start: no waits
+            for (; pc < total && pc < act_first_stage; ++pc) issue_chunk(pc);
         }
-        // stages that are free from the start: no waits
-        for (; pc < total && pc < act_first_stage; ++pc) issue_chunk(pc);
     }
     __syncthreads();
 
