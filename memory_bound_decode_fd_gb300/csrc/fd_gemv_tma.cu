@@ -117,10 +117,11 @@ __device__ __forceinline__ void fold_tail(const FoldArgs &fold, float ss, int N,
 // 8 weight rows, ahead of the weight stream, so the consumers' activation reads do not
 // queue behind it (loaded from global memory instead, they arrived behind the weights and
 // the call took 10-25 % longer on GB300); stages from act_first_stage on are filled only
-// after every consumer warp has read its slice. The plain activation (x, K * 2 bytes) is
-// small enough to load straight from global memory, so for it the free stages' weight
-// chunks go out before the dependency wait instead (the gate/up GEMV measured 64 -> 69 %
-// of HBM with this on GB300).
+// after every consumer warp has read its slice. A small activation (at most 16 KB for the
+// call: the gate/up projection's x at K = 4096, gate and up up to K = 4096 at M = 1) is
+// loaded by the lanes straight from global memory instead, and the free stages' weight
+// chunks go out before the dependency wait (the gate/up GEMV measured 64 -> 69 % of HBM
+// with this on GB300; with 57 KB of gate/up the same order slowed the decode step).
 // FOLD: the next layer's add-RMSNorm in the tail (M = 1, SwiGLU form only); a separate
 // instantiation, so the other kernels' code is unchanged by it.
 template <int MB, int R, int NVEC_C, int NG_C, int LPS, bool PLAIN, bool FOLD>
@@ -161,7 +162,8 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
     // gate then up, each K bf16 (4K bytes = 8 weight rows; PLAIN: x alone, 2K bytes = 4
     // rows), in the last weight rows (M == 1 only); stages from act_first_stage on are
     // filled only after its release
-    const bool act_in_smem = (M == 1) && !PLAIN;
+    const bool direct_act = (long long)M * K * (PLAIN ? 2 : 4) <= 16384;
+    const bool act_in_smem = (M == 1) && !direct_act;
     const uint32_t act_bytes = (uint32_t)K * (PLAIN ? 2 : 4);
     uint16_t *act_smem =
         reinterpret_cast<uint16_t *>(smem + (size_t)w_rows * w_row_bytes - act_bytes);
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
         fence_mbar_init();
         pol_w = weights_evict_first ? policy_evict_first() : policy_evict_last();
         pol_s = policy_evict_first();
-        if constexpr (PLAIN) {
+        if (direct_act) {
             // The weights never come from the previous kernel, and the consumers read the
             // small activation from global memory: the free stages' chunks go out before
             // the dependency wait.
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(LPS == 2 ? 1024 : 512, 1)
                 mbar_arrive_expect_tx(&act_full_bar, act_bytes);
                 const uint64_t pol_a = policy_evict_last();  // every CTA reads it
                 bulk_g2s(act_smem, gate, ab, &act_full_bar, pol_a);
-                bulk_g2s(act_smem + K, up, ab, &act_full_bar, pol_a);
+                if (!PLAIN) bulk_g2s(act_smem + K, up, ab, &act_full_bar, pol_a);
             }
             // stages that are free from the start: no waits
             for (; pc < total && pc < act_first_stage; ++pc) issue_chunk(pc);

@@ -42,6 +42,8 @@ def run(d, gate_out=None, up_out=None):
 SHAPES = [
     # M, K, I, group
     (1, 4096, 1024, 128),    # the model width, fewer rows
+    (1, 8192, 256, 128),     # x of 16 KB: still read by the lanes directly
+    (1, 9216, 256, 128),     # x of 18 KB: bulk-copied into shared memory first
     (1, 1024, 300, 128),     # ragged rows per CTA
     (1, 4096, 2500, 64),
     (3, 4096, 500, 128),     # two activation rows per pass + one
