@@ -115,6 +115,13 @@ def test_persistent_edge_hidden(cuda_device, hidden):
     assert_same(persistent(d, layers), separate_chain(d, layers))
 
 
+def test_persistent_long_chain(cuda_device):
+    # 48 layers (the two h rows alternate 24 times each; 48 counters) at 8 rows per SM
+    d = inputs.decode_step_inputs(layers=48, hidden=1216, seed=15)
+    layers = device_layers(d)
+    assert_same(persistent(d, layers), separate_chain(d, layers))
+
+
 def test_persistent_rows_beyond_shared_memory_are_unsupported(cuda_device):
     # hidden 8192: 54 rows per CTA do not fit one CTA's shared memory; nothing is launched
     from memory_bound_decode_fd_gb300 import _lib
