@@ -84,3 +84,27 @@ def test_copy_rows_strided(cuda_device, rows, width, src_kind, dst_kind):
     torch.cuda.synchronize()
     assert torch.equal(dst.cpu(), src.cpu())
     assert bool((buf[:, 1, :].cpu() == 0x5A5A).all())
+
+
+def test_copy_rows_with_pdl_after_a_writing_kernel(cuda_device):
+    # the rows are written by the kernel just before (add_rmsnorm's residual_out, 4 rows);
+    # the strided copy must read them only after that kernel completes
+    rows, hidden = 4, 1024
+    x = torch.randn((rows, hidden), device="cuda").to(torch.bfloat16)
+    r = torch.randn((rows, hidden), device="cuda").to(torch.bfloat16)
+    w = torch.ones((hidden,), device="cuda", dtype=torch.bfloat16)
+    out, h = torch.empty_like(x), torch.empty_like(x)
+    host = torch.zeros((rows, 2, hidden), dtype=torch.bfloat16).pin_memory()
+    prev = fd.set_pdl(True)
+    try:
+        for _ in range(3):
+            h.zero_()
+            fd.add_rmsnorm(x, r, w, 1e-5, out=out, residual_out=h)
+            fd.copy_rows(host[:, 1, :], h)
+            torch.cuda.synchronize()
+            assert torch.equal(host[:, 1, :].view(torch.int16), h.cpu().view(torch.int16))
+    finally:
+        fd.set_pdl(prev)
+    expect = (x.float() + r.float()).to(torch.bfloat16).cpu()
+    assert torch.equal(host[:, 1, :].view(torch.int16), expect.view(torch.int16))
+    assert not host[:, 0, :].view(torch.int16).any()  # the rows between were not written

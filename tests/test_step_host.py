@@ -159,3 +159,20 @@ def test_plan_on_other_sm_counts(fdlib, sms):
         assert gst == _lib.FD_OK and g[7] == 1
         assert (p["grid"], p["rows_base"], p["rows_extra"]) == tuple(g[:3]), (sms, hidden)
 
+
+
+def test_copy_rows_binding_rejects_bad_tensors():
+    # checked before any CUDA call
+    import torch
+
+    from memory_bound_decode_fd_gb300 import kernels
+
+    a = torch.zeros((4, 16), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="same shape"):
+        kernels.copy_rows(a, torch.zeros((4, 8), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="same shape and dtype"):
+        kernels.copy_rows(a, torch.zeros((4, 16), dtype=torch.float32))
+    with pytest.raises(ValueError, match="contiguous"):
+        kernels.copy_rows(a, torch.zeros((16, 4), dtype=torch.bfloat16).t())
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        kernels.copy_rows(a, torch.zeros((4, 16), dtype=torch.bfloat16))
