@@ -234,9 +234,9 @@ int fd_swiglu_w4a16_gemv_add_rmsnorm_noalloc(const void *gate, const void *up,
  * layer's weight rows while the current layer finishes. Each CTA publishes h of its rows
  * as words tagged with the layer and counts in; every CTA, once all have counted in and it
  * has read the whole tagged row, computes the next add-RMSNorm over the whole row (the row
- * kernel's reduction order); a
- * CTA reads layer l+1's activations only when it holds the complete normed_{l+1} row, as
- * the chain's GEMV starts only after its add-RMSNorm has finished.
+ * kernel's reduction order). A CTA reads layer l+1's activations only when it holds the
+ * complete normed_{l+1} row, as the chain's GEMV starts only after its add-RMSNorm has
+ * finished.
  * layers      DEVICE array of n_layers fd_step_layer (below); the library does not read it on
  *             the host. Every pointer in it must be a device pointer, 16-byte aligned; the
  *             tensors have the layouts of fd_swiglu_w4a16_gemv (K = inter, N = hidden,
@@ -255,7 +255,9 @@ int fd_swiglu_w4a16_gemv_add_rmsnorm_noalloc(const void *gate, const void *up,
  * Returns FD_OK; FD_ERR_NULL, FD_ERR_SHAPE, FD_ERR_ALIGN, FD_ERR_OVERLAP (x0, residual,
  * scratch) for bad arguments, launching nothing; FD_ERR_UNSUPPORTED, launching nothing, for
  * another inter/group, a hidden above 64 rows per SM (9728) or above 8192 (the add-RMSNorm
- * row's 256 threads x 4 vectors), or rows that do not fit one CTA's shared memory;
+ * row's 256 threads x 4 vectors), or rows that do not fit one CTA's shared memory (all of
+ * a CTA's weight rows stay resident: at most 29 rows per SM, hidden <= 4408 on 152 SMs;
+ * fd_debug_plan_step gives the plan);
  * FD_ERR_CUDA if the launch fails (for example when the device cannot hold one CTA per SM at
  * once).
  * A wait that gives up (about a second) writes NaN outputs and sets
